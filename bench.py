@@ -1,0 +1,403 @@
+#!/usr/bin/env python3
+"""Benchmark of the PowerSGD compression step on one GB300 (per rank).
+
+A step is one pass of the whole compression over the ResNet-18-shaped
+workload (21 conv/fc gradient matrices + 41 vectors, 11.17 M parameters per
+worker, W = 4 simulated workers, rank 2): error feedback, P = sum M_w Q,
+Gram-Schmidt, Q_w = M_w^T Phat, Qbar, the decompressed update and the new
+error buffers, all in the library's step kernel.
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own
+replica of the workload (weak scaling; the method has no data exchange
+between the simulated workers of one GPU and the GPUs).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config c2]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "gradient GB/s compressed per PowerSGD step (1 GB300) and % of HBM roofline"
+UNIT = "GB/s"
+
+# DRAM bytes (read + write) of one step-kernel launch on the ResNet-18 workload,
+# from an ncu capture (see profiles/), valid only for the kernel sources whose
+# hash is recorded with it.
+NCU_TRAFFIC = {}  # {config: (sources_sha256_prefix, bytes_per_launch)}
+
+
+def kernel_sources_hash() -> str:
+    csrc = os.path.join(ROOT, "rank_gradient_compression_layer_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def config_of(name: str) -> workloads.Workload:
+    if name.startswith("c5r"):
+        return workloads.c5_rank_sweep(int(name[3:]))
+    return workloads.ALL[name]()
+
+
+def algorithmic_bytes(cfg: workloads.Workload, with_update: bool) -> dict:
+    """Minimum HBM bytes of one step.
+
+    Per matrix: every worker's gradient is read, its error buffer read and
+    written (3 n m floats per worker), plus the factors Phat (n r) and Qbar
+    (m r) written; with an update, U (n m) written once.  Per vector: W reads
+    and one write when an update is produced.
+    """
+    W, r = cfg.workers, cfg.rank
+    core = sum(W * 3 * n * m * 4 + 4 * (n + m) * r for n, m in cfg.matrices)
+    upd = sum(4 * n * m for n, m in cfg.matrices) if with_update else 0
+    vec = sum(4 * (W + 1) * n for n, _ in cfg.vectors) if with_update else 0
+    return {"core": core, "update": upd, "vectors": vec, "total": core + upd + vec}
+
+
+def compressed_bytes(cfg: workloads.Workload) -> int:
+    """Gradient bytes compressed per step: W x sum n m x 4."""
+    return cfg.workers * sum(n * m for n, m in cfg.matrices) * 4
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="psgd_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(name)
+        loaded = [s for s in sm if s > 0.5 * (max(sm) if sm else 1)]
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (timing only; no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, ws: int, device=None) -> float:
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline leg)
+# ---------------------------------------------------------------------------
+
+def time_oracle(cfg: workloads.Workload, steps: int, warmup: int, budget_s: float) -> dict:
+    """Times the float64 oracle on this host.  Each step runs on a bounded
+    sample of the workload's matrix layers (the largest prefix of the layer
+    list, in order, whose step fits the budget share), scaled to GB/s by the
+    bytes it compressed."""
+    from oracle import powersgd as O
+
+    layers_all = list(cfg.layers)
+    mats = [i for i, (n, m) in enumerate(layers_all) if m]
+    sig = {}
+    st = O.OracleState(layers_all, cfg.rank, cfg.workers, cfg.seed)
+    grads = workloads.gradients(cfg, 0, sig)
+    # size the sample: probe one full step
+    t0 = time.perf_counter()
+    st.step(grads, layers=mats)
+    full = time.perf_counter() - t0
+    per_step = budget_s / max(1, steps + warmup)
+    if full <= per_step:
+        sample = mats
+    else:
+        frac = per_step / full
+        tot = sum(layers_all[i][0] * layers_all[i][1] for i in mats)
+        sample, acc = [], 0
+        for i in mats:
+            if acc + layers_all[i][0] * layers_all[i][1] > frac * tot and sample:
+                break
+            sample.append(i)
+            acc += layers_all[i][0] * layers_all[i][1]
+    el = sum(layers_all[i][0] * layers_all[i][1] for i in sample)
+    for _ in range(warmup):
+        st.step(grads, layers=sample)
+    wall0, cpu0 = time.perf_counter(), time.process_time()
+    for _ in range(steps):
+        st.step(grads, layers=sample)
+    wall = time.perf_counter() - wall0
+    cpu = time.process_time() - cpu0
+    gbs = cfg.workers * el * 4 * steps / wall / 1e9
+    return {"value": gbs, "unit": UNIT, "cores": max(1, round(cpu / wall)), "kind": "oracle",
+            "host_cpus": os.cpu_count(), "ms_per_step": wall / steps * 1e3,
+            "sample": f"{len(sample)} of {len(mats)} matrix layers ({el} of {cfg.matrix_elements()} elements "
+                      f"per worker), W={cfg.workers}, r={cfg.rank}, float64 numpy, {steps} steps"}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def workload_desc(cfg: workloads.Workload) -> str:
+    return (f"{cfg.name}: {len(cfg.matrices)} matrices + {len(cfg.vectors)} vectors, "
+            f"{cfg.matrix_elements() + cfg.vector_elements()} params per worker, W={cfg.workers}, r={cfg.rank}")
+
+
+def fill_gradients(ctx, cfg, sets: int, device):
+    """`sets` rotating sets of W packed gradient buffers, generated on the device."""
+    import torch
+
+    out = []
+    for s in range(sets):
+        bufs = []
+        for w in range(cfg.workers):
+            buf = ctx.empty_buffer()
+            for li, (n, m) in enumerate(cfg.layers):
+                view = ctx.layer_view(buf, li)
+                if m:
+                    view.copy_(workloads.device_gradient_matrix(cfg, li, s, w, device))
+                else:
+                    g = torch.Generator(device=device)
+                    g.manual_seed(cfg.seed * 7777 + li * 31 + s * 7 + w)
+                    view.normal_(0.0, 1.0, generator=g)
+            bufs.append(buf)
+        out.append(bufs)
+    torch.cuda.synchronize()
+    return out
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+
+    from rank_gradient_compression_layer_gb300 import PowerSGD
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    cfg = config_of(args.config)
+    stream = torch.cuda.Stream(device=device)
+    ctx = PowerSGD(cfg.layers, cfg.rank, cfg.workers, seed=cfg.seed, stream=stream)
+    sets = 3
+    grads = fill_gradients(ctx, cfg, sets, device)
+    upd = ctx.empty_buffer()
+    ab = algorithmic_bytes(cfg, with_update=True)
+    comp = compressed_bytes(cfg)
+
+    # warm-up
+    for i in range(args.warmup):
+        ctx.step(grads[i % sets], upd)
+    ctx.sync()
+    barrier(ws)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(args.steps):
+            ctx.step(grads[i % sets], upd)
+            ev[i + 1].record(stream)
+    ctx.sync()
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    total_ms = max_over_ranks(total_ms, ws, device)
+    ms_per_step = total_ms / args.steps
+    value = comp * ws / (ms_per_step * 1e-3) / 1e9
+    launch_ms = statistics.mean(per)
+    peaks = measured_peaks()
+    achieved = ab["total"] / (launch_ms * 1e-3) / 1e9
+    h = kernel_sources_hash()
+    traffic = None
+    if args.config in NCU_TRAFFIC and NCU_TRAFFIC[args.config][0] == h:
+        traffic = NCU_TRAFFIC[args.config][1]
+
+    # end to end through the C ABI with host buffers (pinned), copies inside
+    e2e = run_e2e(ctx, cfg, args, ws, device)
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "parallelism": f"replicas x{ws} (W={cfg.workers} workers "
+                   "simulated per GPU)",
+                   "l2": "inputs larger than L2: 3 rotating gradient sets of "
+                         f"{comp / 1e6:.1f} MB + error buffers {comp / 1e6:.1f} MB per step",
+                   "seed": cfg.seed, "out_update": True},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
+                     else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": ab["total"], "kernel": "psgd::step_kernel<2>",
+                     "launch_ms": round(launch_ms, 5), "kernel_sources": h},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = time_oracle(cfg, steps=3, warmup=1, budget_s=args.cpu_budget)
+    ctx.close()
+    return out
+
+
+def run_e2e(ctx, cfg, args, ws, device):
+    import torch
+
+    host = [torch.empty(ctx.total, dtype=torch.float32).pin_memory() for _ in range(cfg.workers)]
+    src = fill_gradients(ctx, cfg, 1, device)[0]
+    for w in range(cfg.workers):
+        host[w].copy_(src[w].cpu())
+    msg = torch.empty(ctx.message_floats, dtype=torch.float32).pin_memory()
+    for _ in range(args.warmup):
+        ctx.step_host(host, msg)
+    steps = max(3, args.steps // 2)
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        ctx.step_host(host, msg)  # waits for its copies
+    dt = (time.perf_counter() - t0) / steps
+    dt = max_over_ranks(dt, ws, device)
+    comp = compressed_bytes(cfg)
+    return {"value": round(comp * ws / dt / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": cfg.workers * ctx.total * 4, "d2h_bytes_per_step": ctx.message_floats * 4,
+            "ms_per_step": round(dt * 1e3, 4), "steps": steps,
+            "api": "psgd_step_host (pinned host gradients in, compressed message Phat/Qbar out)"}
+
+
+def run_reference(args, ws, rank):
+    cfg = config_of(args.config)
+    if rank != 0:
+        return None
+    res = time_oracle(cfg, steps=args.steps, warmup=args.warmup, budget_s=args.cpu_budget)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(res["value"], 4), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "parallelism": "host cores", "seed": cfg.seed},
+        "cpu_baseline": {"value": round(res["value"], 4), "unit": UNIT, "cores": res["cores"], "kind": "oracle",
+                         "sample": res["sample"]},
+        "e2e": {"value": round(res["value"], 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "the reference arm is the float64 CPU oracle (the pages ship no code)",
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="c2")
+    ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for the CPU leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, ws, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    out = run_ours(args, ws, rank, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

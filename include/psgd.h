@@ -1,0 +1,185 @@
+/*
+ * psgd.h -- C ABI of the GB300 PowerSGD compression step (libpsgd.so).
+ *
+ * What it computes (PowerSGD review page, "PowerSGD: Practical Low-Rank
+ * Gradient Compression for Distributed Optimization", section 提案手法 /
+ * proposed method):  for every layer whose gradient is an n x m matrix and
+ * for W data-parallel workers w,
+ *     M_w   = G_w + E_w                       error feedback      (bullet 3)
+ *     P     = sum_w M_w Q                     first all-reduce    (bullets 1, 2)
+ *     Phat  = Gram-Schmidt(P)                 orthonormal columns (bullet 1)
+ *     Q_w   = M_w^T Phat                      power-iteration step
+ *     Qbar  = (1/W) sum_w Q_w                 second all-reduce   (bullet 2)
+ *     U     = Phat Qbar^T                     decompression       (bullet 5)
+ *     E_w  <- M_w - Phat Q_w^T                new error           (bullet 3)
+ *     Q    <- Qbar                            warm start of the next step (bullet 1)
+ * with P in R^{n x r} and Q in R^{m x r}, r small (bullet 4).  A 1-D tensor
+ * (a bias or a batch-norm vector) is averaged over the workers and sent whole.
+ * The W workers live on one GPU: each "all-reduce" is a sum over the worker
+ * axis inside the kernels.  All values are float32.
+ *
+ * Readings of points the page leaves open:
+ *   - P is a sum over workers, Qbar a mean, so U approximates the mean gradient;
+ *   - E_w uses the worker's own Q_w;
+ *   - Q starts as N(0,1) draws: splitmix64 keyed by (seed, layer) + Box-Muller
+ *     (see psgd_create);
+ *   - a column of P whose Gram-Schmidt remainder is zero gives a zero column.
+ *
+ * Layout of a packed gradient buffer (one per worker, float32, device memory):
+ * every layer l sits at element offset psgd_layer_info(..).offset, 16-byte
+ * aligned; a matrix layer is row-major n x ld with ld = m rounded up to a
+ * multiple of 4 (the ld - m padding columns are ignored on input and written
+ * as 0 on output); a vector layer is n contiguous floats.  The decompressed
+ * update (out_update) uses the same layout.
+ *
+ * Ownership: the caller owns the gradient buffers and out_update.  The library
+ * owns the error state, P, Q and all scratch, allocated by psgd_create and
+ * freed by psgd_destroy; it never frees caller memory.
+ *
+ * Errors: every call returns a psgd_status; nothing throws across the ABI.
+ * psgd_last_error() gives a message for the calling thread.  psgd_step is
+ * asynchronous on the context's stream; a device-side failure (a bounded wait
+ * that ran out) is reported as PSGD_ERR_TIMEOUT by the next synchronising call
+ * (psgd_sync or any psgd_get_*), after which the context only answers
+ * PSGD_ERR_STATE until destroyed.
+ *
+ * Thread safety: a context must not be used from two host threads at once.
+ * Two contexts are independent and may run concurrently on different streams.
+ */
+#ifndef PSGD_H_
+#define PSGD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct psgd_ctx psgd_ctx;
+
+typedef enum {
+  PSGD_OK = 0,
+  PSGD_ERR_INVALID = -1,  /* bad argument (null / misaligned pointer, bad size, rank) */
+  PSGD_ERR_OOM = -2,      /* device or pinned-host allocation failed */
+  PSGD_ERR_CUDA = -3,     /* a CUDA runtime call failed (message in psgd_last_error) */
+  PSGD_ERR_TIMEOUT = -4,  /* a bounded in-kernel wait ran out (see psgd_sync) */
+  PSGD_ERR_STATE = -5     /* the context hit an earlier device error and is unusable */
+} psgd_status;
+
+/* Cumulative counters of a context (exact integers except last_step_ms). */
+typedef struct {
+  int64_t steps;                        /* psgd_step calls completed (enqueued) */
+  int64_t floats_sent;                  /* per worker, summed over steps: sum (n+m) r + vector lengths */
+  int64_t floats_uncompressed;          /* per worker, summed over steps: sum n m + vector lengths */
+  int64_t floats_sent_per_step;         /* per worker, one step */
+  int64_t floats_uncompressed_per_step; /* per worker, one step */
+  int64_t matrix_elements;              /* per worker: sum over matrix layers of n*m */
+  int64_t vector_elements;              /* per worker: sum over vector layers of n */
+  int64_t buffer_elements;              /* floats in one packed gradient buffer (with padding) */
+  int64_t work_items;                   /* work items of one step (all layers, all phases) */
+  int32_t grid_ctas;                    /* CTAs of the step kernel */
+  int32_t kernel_rank;                  /* rank the kernels were compiled for (r rounded up to 1,2,4,8,16,32) */
+} psgd_stats;
+
+/* Optional knobs of psgd_create_ex (zero-initialise, then set what you need). */
+typedef struct {
+  int64_t spin_limit;   /* polls of a bounded in-kernel wait before it gives up (0: default, ~seconds) */
+  int32_t grid_ctas;    /* CTAs of the persistent step kernel (0: SMs x resident CTAs per SM) */
+  int32_t schedule;     /* 0: interleave layers (default), 1: phase by phase over all layers */
+} psgd_options;
+
+/*
+ * Create a context for num_layers layers.  Layer l is an n[l] x m[l] matrix,
+ * or a vector of length n[l] when m[l] == 0.  rank in [1, 32]; rank <= min(n, m)
+ * for every matrix; 1 <= num_workers <= 64.  The error buffers start at zero
+ * and each matrix layer's Q at N(0,1) draws from (seed, layer) (see the header
+ * comment).  cuda_stream (a cudaStream_t, may be NULL for the legacy default
+ * stream) is where every call of this context enqueues its work.  The current
+ * CUDA device at the time of the call is the context's device.
+ */
+int psgd_create(psgd_ctx** out, int num_layers, const int64_t* n, const int64_t* m,
+                int rank, int num_workers, uint64_t seed, void* cuda_stream);
+int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64_t* m,
+                   int rank, int num_workers, uint64_t seed, void* cuda_stream,
+                   const psgd_options* options);
+void psgd_destroy(psgd_ctx* ctx);
+
+/* Change the stream later calls enqueue on. */
+int psgd_set_stream(psgd_ctx* ctx, void* cuda_stream);
+
+/*
+ * One PowerSGD step (every row of the header comment, all layers) on the
+ * context's stream.  grad_ptrs: host array of num_workers DEVICE pointers, each
+ * to a packed gradient buffer (16-byte aligned) that stays valid until the step
+ * has run.  out_update: device packed buffer that receives U for matrix layers
+ * and the worker mean for vector layers, or NULL to skip both.  Asynchronous.
+ */
+int psgd_step(psgd_ctx* ctx, const float* const* grad_ptrs, float* out_update);
+
+/*
+ * The same step fed from HOST memory: copies each worker's packed buffer
+ * grad_host[w] (pinned host memory for an asynchronous copy) into device
+ * staging buffers owned by the context (allocated on first use), runs
+ * psgd_step, then copies the compressed message of every matrix layer
+ * (Phat then Qbar, each row-major, layers in order: sum (n+m) r floats) into
+ * msg_host and, when update_host is not NULL, the packed update into it.
+ * Waits for the copies before returning.
+ */
+int psgd_step_host(psgd_ctx* ctx, const float* const* grad_host, float* msg_host, float* update_host);
+
+/* Wait for the context's stream and report a device-side error, if any. */
+int psgd_sync(psgd_ctx* ctx);
+
+/*
+ * Read results of the last step of layer l (a matrix layer).  Each destination
+ * may be host or device memory (or NULL to skip it); the call waits for the
+ * copy.  P: n x r row-major (Phat, orthonormal columns).  Q: m x r row-major
+ * (Qbar, also the warm start of the next step).
+ */
+int psgd_get_PQ(psgd_ctx* ctx, int layer, float* P, float* Q);
+/* Q_w = M_w^T Phat of worker w in the last step: m x r row-major. */
+int psgd_get_Qw(psgd_ctx* ctx, int layer, int worker, float* Q);
+/* Error buffer E_w of layer l: dense n x m row-major (host or device memory). */
+int psgd_get_error(psgd_ctx* ctx, int layer, int worker, float* E);
+/*
+ * Overwrite the state of layer l: Q (m x r row-major, the next step's warm
+ * start) and, when E is not NULL, E[w] (dense n x m row-major) for every worker;
+ * E == NULL sets the errors to zero.  Host or device memory.  With
+ * psgd_get_PQ/psgd_get_error this checkpoints and restores a run bit-exactly.
+ */
+int psgd_set_state(psgd_ctx* ctx, int layer, const float* Q, const float* const* E);
+
+int psgd_get_stats(const psgd_ctx* ctx, psgd_stats* out);
+
+/* Placement of layer l in a packed buffer: element offset, n, m, row stride. */
+int psgd_layer_info(const psgd_ctx* ctx, int layer, int64_t* offset, int64_t* n, int64_t* m,
+                    int64_t* ld);
+
+/*
+ * Host-only helpers (no GPU needed).  psgd_plan_layout fills offset[l] and
+ * ld[l] (0 for vectors) of the packed layout and *total (floats per buffer).
+ * psgd_count_sent gives the floats one worker sends per step with and without
+ * compression: (n + m) r per matrix against n m, vectors whole either way.
+ */
+int psgd_plan_layout(int num_layers, const int64_t* n, const int64_t* m, int64_t* offset,
+                     int64_t* ld, int64_t* total);
+int psgd_count_sent(int num_layers, const int64_t* n, const int64_t* m, int rank,
+                    int64_t* compressed, int64_t* uncompressed);
+
+/*
+ * Self-test of the bounded wait used between phases of the step kernel: one
+ * CTA waits on a flag that nothing sets, gives up after spin_limit polls and
+ * records a timeout.  Writes the recorded status (PSGD_ERR_TIMEOUT expected)
+ * to *status.  Enqueued on cuda_stream and waited for.
+ */
+int psgd_selftest_wait(int64_t spin_limit, void* cuda_stream, int* status);
+
+const char* psgd_last_error(void);
+const char* psgd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSGD_H_ */

@@ -1,0 +1,274 @@
+"""ctypes binding of libpsgd.so (the C ABI in include/psgd.h).
+
+Argument marshalling only: every step of the compression runs in the
+library's CUDA kernels.  PyTorch provides device memory and streams.  There
+is no fallback: if the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpsgd.so")
+
+PSGD_OK = 0
+PSGD_ERR_INVALID = -1
+PSGD_ERR_OOM = -2
+PSGD_ERR_CUDA = -3
+PSGD_ERR_TIMEOUT = -4
+PSGD_ERR_STATE = -5
+
+# every symbol include/psgd.h declares
+EXPORTS = (
+    "psgd_create", "psgd_create_ex", "psgd_destroy", "psgd_set_stream", "psgd_step", "psgd_step_host",
+    "psgd_sync", "psgd_get_PQ", "psgd_get_Qw", "psgd_get_error", "psgd_set_state", "psgd_get_stats",
+    "psgd_layer_info", "psgd_plan_layout", "psgd_count_sent", "psgd_selftest_wait", "psgd_last_error",
+    "psgd_version",
+)
+
+
+class PsgdError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"psgd error {code}: {msg}")
+        self.code = code
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [
+        ("steps", ctypes.c_int64),
+        ("floats_sent", ctypes.c_int64),
+        ("floats_uncompressed", ctypes.c_int64),
+        ("floats_sent_per_step", ctypes.c_int64),
+        ("floats_uncompressed_per_step", ctypes.c_int64),
+        ("matrix_elements", ctypes.c_int64),
+        ("vector_elements", ctypes.c_int64),
+        ("buffer_elements", ctypes.c_int64),
+        ("work_items", ctypes.c_int64),
+        ("grid_ctas", ctypes.c_int32),
+        ("kernel_rank", ctypes.c_int32),
+    ]
+
+
+class Options(ctypes.Structure):
+    _fields_ = [
+        ("spin_limit", ctypes.c_int64),
+        ("grid_ctas", ctypes.c_int32),
+        ("schedule", ctypes.c_int32),
+    ]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+_P = ctypes.c_void_p
+_I64P = ctypes.POINTER(ctypes.c_int64)
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpsgd.so (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libpsgd.so not built (expected at {LIB_PATH}); run the package's build()")
+    L = ctypes.CDLL(LIB_PATH)
+    sig = {
+        "psgd_create": ([ctypes.POINTER(_P), ctypes.c_int, _I64P, _I64P, ctypes.c_int, ctypes.c_int,
+                         ctypes.c_uint64, _P], ctypes.c_int),
+        "psgd_create_ex": ([ctypes.POINTER(_P), ctypes.c_int, _I64P, _I64P, ctypes.c_int, ctypes.c_int,
+                            ctypes.c_uint64, _P, ctypes.POINTER(Options)], ctypes.c_int),
+        "psgd_destroy": ([_P], None),
+        "psgd_set_stream": ([_P, _P], ctypes.c_int),
+        "psgd_step": ([_P, ctypes.POINTER(_P), _P], ctypes.c_int),
+        "psgd_step_host": ([_P, ctypes.POINTER(_P), _P, _P], ctypes.c_int),
+        "psgd_sync": ([_P], ctypes.c_int),
+        "psgd_get_PQ": ([_P, ctypes.c_int, _P, _P], ctypes.c_int),
+        "psgd_get_Qw": ([_P, ctypes.c_int, ctypes.c_int, _P], ctypes.c_int),
+        "psgd_get_error": ([_P, ctypes.c_int, ctypes.c_int, _P], ctypes.c_int),
+        "psgd_set_state": ([_P, ctypes.c_int, _P, ctypes.POINTER(_P)], ctypes.c_int),
+        "psgd_get_stats": ([_P, ctypes.POINTER(Stats)], ctypes.c_int),
+        "psgd_layer_info": ([_P, ctypes.c_int, _I64P, _I64P, _I64P, _I64P], ctypes.c_int),
+        "psgd_plan_layout": ([ctypes.c_int, _I64P, _I64P, _I64P, _I64P, _I64P], ctypes.c_int),
+        "psgd_count_sent": ([ctypes.c_int, _I64P, _I64P, ctypes.c_int, _I64P, _I64P], ctypes.c_int),
+        "psgd_selftest_wait": ([ctypes.c_int64, _P, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
+        "psgd_last_error": ([], ctypes.c_char_p),
+        "psgd_version": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = L
+    return L
+
+
+def _check(rc: int) -> None:
+    if rc != PSGD_OK:
+        raise PsgdError(rc, lib().psgd_last_error().decode(errors="replace"))
+
+
+def _i64(values: Sequence[int]):
+    return (ctypes.c_int64 * len(values))(*[int(v) for v in values])
+
+
+def _shapes(shapes: Sequence[Tuple[int, int]]):
+    return _i64([s[0] for s in shapes]), _i64([s[1] for s in shapes])
+
+
+# ----------------------------------------------------------- host-only -----
+
+def psgd_plan_layout(shapes: Sequence[Tuple[int, int]]) -> Tuple[List[int], List[int], int]:
+    """(offsets, row strides, floats per packed buffer); needs no GPU."""
+    n, m = _shapes(shapes)
+    L = len(shapes)
+    off, ld, tot = (ctypes.c_int64 * L)(), (ctypes.c_int64 * L)(), ctypes.c_int64()
+    _check(lib().psgd_plan_layout(L, n, m, off, ld, ctypes.byref(tot)))
+    return list(off), list(ld), tot.value
+
+
+def psgd_count_sent(shapes: Sequence[Tuple[int, int]], rank: int) -> Tuple[int, int]:
+    """Floats one worker sends per step (compressed, uncompressed); needs no GPU."""
+    n, m = _shapes(shapes)
+    c, u = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().psgd_count_sent(len(shapes), n, m, rank, ctypes.byref(c), ctypes.byref(u)))
+    return c.value, u.value
+
+
+def psgd_selftest_wait(spin_limit: int, stream=None) -> int:
+    st = ctypes.c_int()
+    _check(lib().psgd_selftest_wait(int(spin_limit), _stream_ptr(stream), ctypes.byref(st)))
+    return st.value
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+# ------------------------------------------------------------- context -----
+
+class PowerSGD:
+    """One compression context: layer shapes, rank r, W simulated workers.
+
+    ``shapes`` lists (n, m) per layer; m == 0 marks a vector (averaged, not
+    compressed).  Gradients are passed as packed float32 device buffers (see
+    ``layout``/``pack``), one per worker.
+    """
+
+    def __init__(self, shapes: Sequence[Tuple[int, int]], rank: int, workers: int, seed: int = 0,
+                 stream=None, spin_limit: int = 0, grid_ctas: int = 0, schedule: int = 0):
+        import torch
+
+        if not torch.cuda.is_available():
+            raise RuntimeError("PowerSGD needs a CUDA device")
+        self.shapes = [(int(a), int(b)) for a, b in shapes]
+        self.rank, self.workers, self.seed = int(rank), int(workers), int(seed)
+        self.device = torch.device("cuda", torch.cuda.current_device())
+        self._stream = stream
+        n, m = _shapes(self.shapes)
+        opt = Options(int(spin_limit), int(grid_ctas), int(schedule))
+        h = _P()
+        _check(lib().psgd_create_ex(ctypes.byref(h), len(self.shapes), n, m, self.rank, self.workers,
+                                    ctypes.c_uint64(self.seed), _stream_ptr(stream), ctypes.byref(opt)))
+        self._h = h
+        self.offsets, self.lds, self.total = psgd_plan_layout(self.shapes)
+
+    # -- lifetime
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().psgd_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_stream(self, stream) -> None:
+        self._stream = stream
+        _check(lib().psgd_set_stream(self._h, _stream_ptr(stream)))
+
+    # -- packed layout helpers (plain tensor copies, outside the step)
+    def empty_buffer(self):
+        import torch
+        return torch.zeros(self.total, dtype=torch.float32, device=self.device)
+
+    def layer_view(self, buf, layer: int):
+        n, m = self.shapes[layer]
+        off, ld = self.offsets[layer], self.lds[layer]
+        if m == 0:
+            return buf[off:off + n]
+        return buf[off:off + n * ld].view(n, ld)[:, :m]
+
+    def pack(self, tensors: Sequence, out=None):
+        """Copy per-layer gradients ((n, m) or (n,)) into one packed buffer."""
+        buf = self.empty_buffer() if out is None else out
+        for li, t in enumerate(tensors):
+            self.layer_view(buf, li).copy_(t)
+        return buf
+
+    def unpack(self, buf) -> List:
+        return [self.layer_view(buf, li) for li in range(len(self.shapes))]
+
+    # -- the step
+    def step(self, grads: Sequence, out_update=None) -> None:
+        if len(grads) != self.workers:
+            raise ValueError(f"expected {self.workers} gradient buffers, got {len(grads)}")
+        ptrs = (_P * self.workers)(*[_ptr(g) for g in grads])
+        _check(lib().psgd_step(self._h, ptrs, _ptr(out_update)))
+
+    def step_host(self, grads_host: Sequence, msg_host, update_host=None) -> None:
+        ptrs = (_P * self.workers)(*[_ptr(g) for g in grads_host])
+        _check(lib().psgd_step_host(self._h, ptrs, _ptr(msg_host), _ptr(update_host)))
+
+    def sync(self) -> None:
+        _check(lib().psgd_sync(self._h))
+
+    # -- state access
+    def get_PQ(self, layer: int):
+        import torch
+        n, m = self.shapes[layer]
+        P = torch.empty(n, self.rank, dtype=torch.float32, device=self.device)
+        Q = torch.empty(m, self.rank, dtype=torch.float32, device=self.device)
+        _check(lib().psgd_get_PQ(self._h, layer, _ptr(P), _ptr(Q)))
+        return P, Q
+
+    def get_Qw(self, layer: int, worker: int):
+        import torch
+        n, m = self.shapes[layer]
+        Q = torch.empty(m, self.rank, dtype=torch.float32, device=self.device)
+        _check(lib().psgd_get_Qw(self._h, layer, worker, _ptr(Q)))
+        return Q
+
+    def get_error(self, layer: int, worker: int):
+        import torch
+        n, m = self.shapes[layer]
+        E = torch.empty(n, m, dtype=torch.float32, device=self.device)
+        _check(lib().psgd_get_error(self._h, layer, worker, _ptr(E)))
+        return E
+
+    def set_state(self, layer: int, Q, E: Optional[Sequence] = None) -> None:
+        Q = Q.contiguous()
+        if E is not None:
+            E = [e.contiguous() for e in E]
+            arr = (_P * self.workers)(*[_ptr(e) for e in E])
+        else:
+            arr = None
+        _check(lib().psgd_set_state(self._h, layer, _ptr(Q), arr))
+
+    def stats(self) -> dict:
+        s = Stats()
+        _check(lib().psgd_get_stats(self._h, ctypes.byref(s)))
+        return {f: getattr(s, f) for f, _ in Stats._fields_}
+
+    @property
+    def message_floats(self) -> int:
+        return sum((n + m) * self.rank for n, m in self.shapes if m)

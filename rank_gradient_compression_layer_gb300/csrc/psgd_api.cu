@@ -1,0 +1,716 @@
+// Host side of libpsgd.so: the C ABI declared in include/psgd.h.
+//
+// psgd_create plans the packed layout and the work items of one step, owns
+// every device buffer of the state, and initialises Q.  psgd_step fills a
+// StepArgs and launches the persistent step kernel for the context's padded
+// rank; nothing else runs on the host per step.
+#define PSGD_SIDE_KERNELS 1
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include "../../include/psgd.h"
+#include "psgd_dispatch.h"
+#include "psgd_kernels.cuh"
+
+using namespace psgd;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[1024];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  const int code = (e == cudaErrorMemoryAllocation) ? PSGD_ERR_OOM : PSGD_ERR_CUDA;
+  return fail(code, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CUDA_TRY(x)                                    \
+  do {                                                 \
+    cudaError_t e_ = (x);                              \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #x);   \
+  } while (0)
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int padded_rank(int r) {
+  int rp = 1;
+  while (rp < r) rp *= 2;
+  return rp;
+}
+
+const KernelSet* kernels_for(int rp) {
+  switch (rp) {
+    case 1: return &kKernelsR1;
+    case 2: return &kKernelsR2;
+    case 4: return &kKernelsR4;
+    case 8: return &kKernelsR8;
+    case 16: return &kKernelsR16;
+    case 32: return &kKernelsR32;
+    default: return nullptr;
+  }
+}
+
+int check_layers(int num_layers, const int64_t* n, const int64_t* m) {
+  if (num_layers < 1) return fail(PSGD_ERR_INVALID, "num_layers must be >= 1 (got %d)", num_layers);
+  if (!n || !m) return fail(PSGD_ERR_INVALID, "n and m must not be NULL");
+  for (int l = 0; l < num_layers; ++l) {
+    if (n[l] < 1 || n[l] > (int64_t)1 << 30)
+      return fail(PSGD_ERR_INVALID, "layer %d: n = %lld out of range [1, 2^30]", l, (long long)n[l]);
+    if (m[l] < 0 || m[l] > (int64_t)1 << 30)
+      return fail(PSGD_ERR_INVALID, "layer %d: m = %lld out of range [0, 2^30]", l, (long long)m[l]);
+    if (m[l] > 0 && n[l] * m[l] > ((int64_t)1 << 40))
+      return fail(PSGD_ERR_INVALID, "layer %d: n*m too large", l);
+  }
+  return PSGD_OK;
+}
+
+// Packed layout: 16-byte aligned layers, matrix rows padded to a multiple of 4.
+void layout(int num_layers, const int64_t* n, const int64_t* m, int64_t* off, int64_t* ld, int64_t* total) {
+  int64_t pos = 0;
+  for (int l = 0; l < num_layers; ++l) {
+    off[l] = pos;
+    if (m[l] > 0) {
+      ld[l] = (m[l] + 3) & ~(int64_t)3;
+      pos += n[l] * ld[l];
+    } else {
+      ld[l] = 0;
+      pos += (n[l] + 3) & ~(int64_t)3;
+    }
+  }
+  *total = pos;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+// Packs Phat (n x r out of n x RP) and Qbar (m x r out of ld x RP) of every
+// matrix layer into one contiguous message: the floats a worker would send.
+struct PackEntry {
+  int64_t src_p, src_q, dst;
+  int32_t n, m;
+};
+
+__global__ void pack_msg_kernel(float* dst, const float* Phat, const float* Qbar, const PackEntry* ent, int r,
+                                int rp) {
+  const PackEntry e = ent[blockIdx.y];
+  const int64_t np = (int64_t)e.n * r, nq = (int64_t)e.m * r;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < np + nq;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float v;
+    if (i < np)
+      v = Phat[e.src_p + (i / r) * rp + (i % r)];
+    else
+      v = Qbar[e.src_q + ((i - np) / r) * rp + ((i - np) % r)];
+    dst[e.dst + i] = v;
+  }
+}
+
+}  // namespace
+
+struct psgd_ctx {
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  int num_layers = 0, rank = 0, rp = 0, W = 0;
+  uint64_t seed = 0;
+  const KernelSet* ks = nullptr;
+  std::vector<int64_t> n, m, off, ld;
+  std::vector<int> mat_of;  // layer -> matrix index or -1
+  std::vector<LayerDev> hl;
+  std::vector<VecDev> hv;
+  std::vector<Item> items;
+  std::vector<PackEntry> pack;
+  int64_t total = 0, q_total = 0, p_total = 0, gram_total = 0, rinv_total = 0, qpart_total = 0;
+  int64_t n_counters = 0, n_flags = 0, msg_floats = 0;
+  // device state and scratch
+  float *B = nullptr, *P = nullptr, *Phat = nullptr, *Qbar = nullptr, *Qw = nullptr, *qpart = nullptr;
+  double *gram = nullptr, *rinv = nullptr;
+  unsigned *counters = nullptr, *flags = nullptr;
+  Ctl* ctl = nullptr;
+  LayerDev* d_layers = nullptr;
+  VecDev* d_vecs = nullptr;
+  Item* d_items = nullptr;
+  PackEntry* d_pack = nullptr;
+  // lazily allocated: error read-back scratch, host-path staging
+  float* e_scratch = nullptr;
+  int64_t e_scratch_elems = 0;
+  float *stage_G = nullptr, *stage_U = nullptr, *stage_msg = nullptr;
+  // launch
+  int grid = 0;
+  size_t smem = 0;
+  int64_t spin_limit = 0;
+  int schedule = 0;
+  unsigned epoch = 0;
+  int has_prev = 0;
+  bool broken = false;
+  // stats
+  int64_t steps = 0, sent_step = 0, unc_step = 0, mat_el = 0, vec_el = 0;
+};
+
+namespace {
+
+void free_all(psgd_ctx* c) {
+  void* ptrs[] = {c->B, c->P, c->Phat, c->Qbar, c->Qw, c->qpart, c->gram, c->rinv, c->counters, c->flags,
+                  c->ctl, c->d_layers, c->d_vecs, c->d_items, c->d_pack, c->e_scratch, c->stage_G,
+                  c->stage_U, c->stage_msg};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+}
+
+template <class T>
+int dalloc(T** p, int64_t count, const char* what) {
+  if (count <= 0) count = 1;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), (size_t)count * sizeof(T));
+  if (e != cudaSuccess) {
+    *p = nullptr;
+    return cuda_fail(e, what);
+  }
+  return PSGD_OK;
+}
+
+// Tiling of one matrix layer for padded rank rp and W workers.
+void plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp, int W) {
+  L.n = (int32_t)n;
+  L.m = (int32_t)m;
+  L.ld = (int32_t)ld;
+  L.F = (int32_t)(ld / 4);
+  L.S = (int32_t)ceil_div(L.F, kSeg);
+  L.tail = (int32_t)(m - 4 * (L.F - 1));
+  const int rs1 = rp <= 4 ? 8 : (rp == 8 ? 4 : (rp == 16 ? 2 : 1));
+  const int rsu = rp <= 8 ? 8 : 4;
+  auto rho = [&](int rs) {
+    int r = (int)std::min<int64_t>(8, ceil_div(kWarps, L.S));
+    r = (int)std::min<int64_t>(r, ceil_div(n, rs));
+    return std::max(1, r);
+  };
+  L.rs1 = rs1;
+  L.rho1 = rho(rs1);
+  L.r1 = rs1 * L.rho1;
+  L.t1 = (int32_t)ceil_div(n, L.r1);
+  L.g1 = (int32_t)ceil_div(L.t1, kGramGroup);
+  L.rph = rp <= 8 ? 256 : (rp == 16 ? 128 : 64);
+  L.tph = (int32_t)ceil_div(n, L.rph);
+  L.r3 = (int32_t)std::min<int64_t>(n, 2048);
+  L.t3r = (int32_t)ceil_div(n, L.r3);
+  L.rsu = rsu;
+  L.rhou = rho(rsu);
+  L.ru = rsu * L.rhou;
+  L.tu = (int32_t)ceil_div(n, L.ru);
+  (void)W;
+}
+
+void emit_p1(std::vector<Item>& v, int li, const LayerDev& L) {
+  for (int t = 0; t < L.t1; ++t) v.push_back({kItemP1, li, t, 0});
+}
+void emit_ph(std::vector<Item>& v, int li, const LayerDev& L) {
+  for (int t = 0; t < L.tph; ++t) v.push_back({kItemPH, li, t, 0});
+}
+void emit_p3(std::vector<Item>& v, int li, const LayerDev& L, int W) {
+  for (int rt = 0; rt < L.t3r; ++rt)
+    for (int s = 0; s < L.S; ++s)
+      for (int w = 0; w < W; ++w) v.push_back({kItemP3, li, rt, s * W + w});
+}
+void emit_u(std::vector<Item>& v, int li, const LayerDev& L) {
+  for (int t = 0; t < L.tu; ++t) v.push_back({kItemU, li, t, 0});
+}
+
+// Work-item order.  Every item that waits on a layer's flag comes after all
+// the items that publish it, so the in-order queue always drains.
+void build_items(psgd_ctx* c) {
+  std::vector<Item>& v = c->items;
+  v.clear();
+  for (int vi = 0; vi < (int)c->hv.size(); ++vi)
+    for (int t = 0; t < (int)ceil_div(c->hv[vi].n, kVChunk); ++t) v.push_back({kItemV, vi, t, 0});
+  const int nm = (int)c->hl.size();
+  if (c->schedule == 1) {
+    for (int li = 0; li < nm; ++li) emit_p1(v, li, c->hl[li]);
+    for (int li = 0; li < nm; ++li) emit_ph(v, li, c->hl[li]);
+    for (int li = 0; li < nm; ++li) emit_p3(v, li, c->hl[li], c->W);
+    for (int li = 0; li < nm; ++li) emit_u(v, li, c->hl[li]);
+    return;
+  }
+  // interleaved: largest layers first; a layer's later phases trail its P1 by
+  // one (PH, P3) and two (U) layers so that their waits are short
+  std::vector<int> order(nm);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+    return (int64_t)c->hl[x].n * c->hl[x].m > (int64_t)c->hl[y].n * c->hl[y].m;
+  });
+  for (int k = 0; k < nm + 2; ++k) {
+    if (k < nm) emit_p1(v, order[k], c->hl[order[k]]);
+    if (k - 1 >= 0 && k - 1 < nm) {
+      emit_ph(v, order[k - 1], c->hl[order[k - 1]]);
+      emit_p3(v, order[k - 1], c->hl[order[k - 1]], c->W);
+    }
+    if (k - 2 >= 0 && k - 2 < nm) emit_u(v, order[k - 2], c->hl[order[k - 2]]);
+  }
+}
+
+int ctx_ok(const psgd_ctx* c) {
+  if (!c) return fail(PSGD_ERR_INVALID, "context is NULL");
+  if (c->broken) return fail(PSGD_ERR_STATE, "context hit an earlier device error; destroy it");
+  return PSGD_OK;
+}
+
+int matrix_layer(const psgd_ctx* c, int layer, const LayerDev** L) {
+  if (layer < 0 || layer >= c->num_layers) return fail(PSGD_ERR_INVALID, "layer %d out of range", layer);
+  const int mi = c->mat_of[layer];
+  if (mi < 0) return fail(PSGD_ERR_INVALID, "layer %d is a vector layer", layer);
+  *L = &c->hl[mi];
+  return PSGD_OK;
+}
+
+int sync_and_check(psgd_ctx* c) {
+  CUDA_TRY(cudaStreamSynchronize(c->stream));
+  Ctl h;
+  CUDA_TRY(cudaMemcpy(&h, c->ctl, sizeof(Ctl), cudaMemcpyDeviceToHost));
+  if (h.status != 0) {
+    c->broken = true;
+    return fail(PSGD_ERR_TIMEOUT, "a bounded wait in the step kernel ran out (work item %d)", h.where);
+  }
+  return PSGD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* psgd_last_error(void) { return g_err.c_str(); }
+
+const char* psgd_version(void) { return "psgd 0.1 (sm_103a)"; }
+
+int psgd_plan_layout(int num_layers, const int64_t* n, const int64_t* m, int64_t* offset, int64_t* ld,
+                     int64_t* total) {
+  int rc = check_layers(num_layers, n, m);
+  if (rc) return rc;
+  if (!offset || !ld || !total) return fail(PSGD_ERR_INVALID, "output pointers must not be NULL");
+  layout(num_layers, n, m, offset, ld, total);
+  return PSGD_OK;
+}
+
+int psgd_count_sent(int num_layers, const int64_t* n, const int64_t* m, int rank, int64_t* compressed,
+                    int64_t* uncompressed) {
+  int rc = check_layers(num_layers, n, m);
+  if (rc) return rc;
+  if (rank < 1) return fail(PSGD_ERR_INVALID, "rank must be >= 1");
+  if (!compressed || !uncompressed) return fail(PSGD_ERR_INVALID, "output pointers must not be NULL");
+  int64_t cs = 0, us = 0;
+  for (int l = 0; l < num_layers; ++l) {
+    if (m[l] == 0) {
+      cs += n[l];
+      us += n[l];
+    } else {
+      cs += (n[l] + m[l]) * rank;
+      us += n[l] * m[l];
+    }
+  }
+  *compressed = cs;
+  *uncompressed = us;
+  return PSGD_OK;
+}
+
+int psgd_create(psgd_ctx** out, int num_layers, const int64_t* n, const int64_t* m, int rank, int num_workers,
+                uint64_t seed, void* cuda_stream) {
+  return psgd_create_ex(out, num_layers, n, m, rank, num_workers, seed, cuda_stream, nullptr);
+}
+
+int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64_t* m, int rank,
+                   int num_workers, uint64_t seed, void* cuda_stream, const psgd_options* opt) {
+  if (!out) return fail(PSGD_ERR_INVALID, "out must not be NULL");
+  *out = nullptr;
+  int rc = check_layers(num_layers, n, m);
+  if (rc) return rc;
+  if (rank < 1 || rank > 32) return fail(PSGD_ERR_INVALID, "rank must be in [1, 32] (got %d)", rank);
+  if (num_workers < 1 || num_workers > kMaxWorkers)
+    return fail(PSGD_ERR_INVALID, "num_workers must be in [1, %d] (got %d)", kMaxWorkers, num_workers);
+  for (int l = 0; l < num_layers; ++l)
+    if (m[l] > 0 && (rank > n[l] || rank > m[l]))
+      return fail(PSGD_ERR_INVALID, "layer %d: rank %d exceeds min(n, m) = %lld", l, rank,
+                  (long long)std::min(n[l], m[l]));
+
+  psgd_ctx* c = new psgd_ctx();
+  c->stream = static_cast<cudaStream_t>(cuda_stream);
+  c->num_layers = num_layers;
+  c->rank = rank;
+  c->rp = padded_rank(rank);
+  c->W = num_workers;
+  c->seed = seed;
+  c->ks = kernels_for(c->rp);
+  c->spin_limit = (opt && opt->spin_limit > 0) ? opt->spin_limit : ((int64_t)1 << 22);
+  c->schedule = opt ? opt->schedule : 0;
+  if (cudaGetDevice(&c->device) != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return fail(PSGD_ERR_CUDA, "no CUDA device");
+  }
+  c->n.assign(n, n + num_layers);
+  c->m.assign(m, m + num_layers);
+  c->off.resize(num_layers);
+  c->ld.resize(num_layers);
+  layout(num_layers, n, m, c->off.data(), c->ld.data(), &c->total);
+  c->mat_of.assign(num_layers, -1);
+
+  const int rp = c->rp;
+  const int NG = rp * (rp + 1) / 2;
+  int max_r1 = 1, max_ru = 1;
+  for (int l = 0; l < num_layers; ++l) {
+    if (m[l] == 0) {
+      c->hv.push_back({c->off[l], (int32_t)n[l], 0});
+      c->vec_el += n[l];
+      c->sent_step += n[l];
+      c->unc_step += n[l];
+      continue;
+    }
+    LayerDev L;
+    std::memset(&L, 0, sizeof(L));
+    plan_matrix(L, n[l], m[l], c->ld[l], rp, c->W);
+    L.off = c->off[l];
+    L.index = l;
+    L.p_off = c->p_total;
+    c->p_total += n[l] * rp;
+    L.q_off = c->q_total;
+    c->q_total += c->ld[l] * rp;
+    L.gram_off = c->gram_total;
+    c->gram_total += (int64_t)(L.t1 + L.g1) * NG;
+    L.rinv_off = c->rinv_total;
+    c->rinv_total += (int64_t)rp * rp;
+    L.qpart_off = c->qpart_total;
+    c->qpart_total += (int64_t)L.t3r * c->W * c->ld[l] * rp;
+    L.cnt_off = (int32_t)c->n_counters;
+    c->n_counters += 3 + L.g1 + L.S;
+    L.flag_off = (int32_t)c->n_flags;
+    c->n_flags += 3;
+    max_r1 = std::max(max_r1, (int)L.r1);
+    max_ru = std::max(max_ru, (int)L.ru);
+    c->pack.push_back({L.p_off, L.q_off, c->msg_floats, L.n, L.m});
+    c->msg_floats += (n[l] + m[l]) * rank;
+    c->mat_of[l] = (int)c->hl.size();
+    c->hl.push_back(L);
+    c->mat_el += n[l] * m[l];
+    c->sent_step += (n[l] + m[l]) * rank;
+    c->unc_step += n[l] * m[l];
+  }
+  build_items(c);
+
+  const int W = c->W;
+  rc = PSGD_OK;
+#define ALLOC(p, cnt) \
+  if (!rc) rc = dalloc(&c->p, (cnt), #p)
+  ALLOC(B, (int64_t)W * c->total);
+  ALLOC(P, c->p_total);
+  ALLOC(Phat, c->p_total);
+  ALLOC(Qbar, c->q_total);
+  ALLOC(Qw, (int64_t)W * c->q_total);
+  ALLOC(qpart, c->qpart_total);
+  ALLOC(gram, c->gram_total);
+  ALLOC(rinv, c->rinv_total);
+  ALLOC(counters, c->n_counters);
+  ALLOC(flags, c->n_flags);
+  ALLOC(ctl, 1);
+  ALLOC(d_layers, (int64_t)c->hl.size());
+  ALLOC(d_vecs, (int64_t)c->hv.size());
+  ALLOC(d_items, (int64_t)c->items.size());
+  ALLOC(d_pack, (int64_t)c->pack.size());
+#undef ALLOC
+  if (rc) {
+    free_all(c);
+    delete c;
+    return rc;
+  }
+  auto setup = [&]() -> int {
+    cudaStream_t s = c->stream;
+    CUDA_TRY(cudaMemsetAsync(c->B, 0, (size_t)W * c->total * sizeof(float), s));
+    CUDA_TRY(cudaMemsetAsync(c->Phat, 0, (size_t)std::max<int64_t>(c->p_total, 1) * sizeof(float), s));
+    CUDA_TRY(cudaMemsetAsync(c->Qbar, 0, (size_t)std::max<int64_t>(c->q_total, 1) * sizeof(float), s));
+    CUDA_TRY(cudaMemsetAsync(c->Qw, 0, (size_t)std::max<int64_t>(W * c->q_total, 1) * sizeof(float), s));
+    CUDA_TRY(cudaMemsetAsync(c->counters, 0, (size_t)std::max<int64_t>(c->n_counters, 1) * sizeof(unsigned), s));
+    CUDA_TRY(cudaMemsetAsync(c->flags, 0, (size_t)std::max<int64_t>(c->n_flags, 1) * sizeof(unsigned), s));
+    CUDA_TRY(cudaMemsetAsync(c->ctl, 0, sizeof(Ctl), s));
+    if (!c->hl.empty())
+      CUDA_TRY(cudaMemcpyAsync(c->d_layers, c->hl.data(), c->hl.size() * sizeof(LayerDev),
+                               cudaMemcpyHostToDevice, s));
+    if (!c->hv.empty())
+      CUDA_TRY(cudaMemcpyAsync(c->d_vecs, c->hv.data(), c->hv.size() * sizeof(VecDev), cudaMemcpyHostToDevice, s));
+    if (!c->items.empty())
+      CUDA_TRY(cudaMemcpyAsync(c->d_items, c->items.data(), c->items.size() * sizeof(Item),
+                               cudaMemcpyHostToDevice, s));
+    if (!c->pack.empty())
+      CUDA_TRY(cudaMemcpyAsync(c->d_pack, c->pack.data(), c->pack.size() * sizeof(PackEntry),
+                               cudaMemcpyHostToDevice, s));
+    if (!c->hl.empty()) {
+      dim3 grid(64, (unsigned)c->hl.size());
+      q_init_kernel<<<grid, 256, 0, s>>>(c->Qbar, c->d_layers, c->rank, c->rp, c->seed);
+      CUDA_TRY(cudaGetLastError());
+    }
+    // launch geometry of the step kernel
+    c->smem = c->ks->smem_bytes(max_r1, max_ru);
+    int per_sm = 0;
+    CUDA_TRY(c->ks->prepare(c->smem, &per_sm));
+    if (per_sm < 1) return fail(PSGD_ERR_CUDA, "step kernel does not fit on an SM (smem %zu)", c->smem);
+    int sms = 0;
+    CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device));
+    int64_t g = (opt && opt->grid_ctas > 0) ? opt->grid_ctas : (int64_t)sms * per_sm;
+    g = std::min<int64_t>(g, std::max<int64_t>((int64_t)c->items.size(), 1));
+    c->grid = (int)g;
+    CUDA_TRY(cudaStreamSynchronize(s));
+    return PSGD_OK;
+  };
+  rc = setup();
+  if (rc) {
+    cudaStreamSynchronize(c->stream);
+    free_all(c);
+    delete c;
+    return rc;
+  }
+  *out = c;
+  return PSGD_OK;
+}
+
+void psgd_destroy(psgd_ctx* c) {
+  if (!c) return;
+  cudaStreamSynchronize(c->stream);
+  free_all(c);
+  delete c;
+}
+
+int psgd_set_stream(psgd_ctx* c, void* cuda_stream) {
+  if (!c) return fail(PSGD_ERR_INVALID, "context is NULL");
+  c->stream = static_cast<cudaStream_t>(cuda_stream);
+  return PSGD_OK;
+}
+
+int psgd_step(psgd_ctx* c, const float* const* grad_ptrs, float* out_update) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  if (!grad_ptrs) return fail(PSGD_ERR_INVALID, "grad_ptrs must not be NULL");
+  StepArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int w = 0; w < c->W; ++w) {
+    if (!grad_ptrs[w]) return fail(PSGD_ERR_INVALID, "grad_ptrs[%d] is NULL", w);
+    if (!aligned16(grad_ptrs[w])) return fail(PSGD_ERR_INVALID, "grad_ptrs[%d] is not 16-byte aligned", w);
+    a.G[w] = grad_ptrs[w];
+  }
+  if (out_update && !aligned16(out_update)) return fail(PSGD_ERR_INVALID, "out_update is not 16-byte aligned");
+  if (++c->epoch == 0) ++c->epoch;
+  a.U = out_update;
+  a.B = c->B;
+  a.total = c->total;
+  a.P = c->P;
+  a.Phat = c->Phat;
+  a.Qbar = c->Qbar;
+  a.Qw = c->Qw;
+  a.q_total = c->q_total;
+  a.gram = c->gram;
+  a.rinv = c->rinv;
+  a.qpart = c->qpart;
+  a.counters = c->counters;
+  a.flags = c->flags;
+  a.ctl = c->ctl;
+  a.layers = c->d_layers;
+  a.vecs = c->d_vecs;
+  a.items = c->d_items;
+  a.num_items = (int32_t)c->items.size();
+  a.W = c->W;
+  a.epoch = c->epoch;
+  a.has_prev = c->has_prev;
+  a.spin_limit = c->spin_limit;
+  cudaError_t e = c->ks->step(a, c->grid, c->smem, c->stream);
+  if (e != cudaSuccess) return cuda_fail(e, "step kernel launch");
+  c->has_prev = 1;
+  c->steps += 1;
+  return PSGD_OK;
+}
+
+int psgd_sync(psgd_ctx* c) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  return sync_and_check(c);
+}
+
+int psgd_step_host(psgd_ctx* c, const float* const* grad_host, float* msg_host, float* update_host) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  if (!grad_host || !msg_host) return fail(PSGD_ERR_INVALID, "grad_host and msg_host must not be NULL");
+  const int W = c->W;
+  if (!c->stage_G) {
+    rc = dalloc(&c->stage_G, (int64_t)W * c->total, "stage_G");
+    if (!rc) rc = dalloc(&c->stage_U, c->total, "stage_U");
+    if (!rc) rc = dalloc(&c->stage_msg, c->msg_floats, "stage_msg");
+    if (rc) return rc;
+  }
+  std::vector<const float*> dptr(W);
+  for (int w = 0; w < W; ++w) {
+    if (!grad_host[w]) return fail(PSGD_ERR_INVALID, "grad_host[%d] is NULL", w);
+    dptr[w] = c->stage_G + (int64_t)w * c->total;
+    CUDA_TRY(cudaMemcpyAsync(const_cast<float*>(dptr[w]), grad_host[w], (size_t)c->total * sizeof(float),
+                             cudaMemcpyHostToDevice, c->stream));
+  }
+  rc = psgd_step(c, dptr.data(), update_host ? c->stage_U : nullptr);
+  if (rc) return rc;
+  if (!c->pack.empty()) {
+    dim3 grid(32, (unsigned)c->pack.size());
+    pack_msg_kernel<<<grid, 256, 0, c->stream>>>(c->stage_msg, c->Phat, c->Qbar, c->d_pack, c->rank, c->rp);
+    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(cudaMemcpyAsync(msg_host, c->stage_msg, (size_t)c->msg_floats * sizeof(float),
+                             cudaMemcpyDeviceToHost, c->stream));
+  }
+  if (update_host)
+    CUDA_TRY(cudaMemcpyAsync(update_host, c->stage_U, (size_t)c->total * sizeof(float), cudaMemcpyDeviceToHost,
+                             c->stream));
+  return sync_and_check(c);
+}
+
+int psgd_get_PQ(psgd_ctx* c, int layer, float* P, float* Q) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  const LayerDev* L;
+  if ((rc = matrix_layer(c, layer, &L))) return rc;
+  const size_t rb = (size_t)c->rank * sizeof(float), pb = (size_t)c->rp * sizeof(float);
+  if (P) CUDA_TRY(cudaMemcpy2DAsync(P, rb, c->Phat + L->p_off, pb, rb, L->n, cudaMemcpyDefault, c->stream));
+  if (Q) CUDA_TRY(cudaMemcpy2DAsync(Q, rb, c->Qbar + L->q_off, pb, rb, L->m, cudaMemcpyDefault, c->stream));
+  return sync_and_check(c);
+}
+
+int psgd_get_Qw(psgd_ctx* c, int layer, int worker, float* Q) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  const LayerDev* L;
+  if ((rc = matrix_layer(c, layer, &L))) return rc;
+  if (worker < 0 || worker >= c->W) return fail(PSGD_ERR_INVALID, "worker %d out of range", worker);
+  if (!Q) return fail(PSGD_ERR_INVALID, "Q must not be NULL");
+  const size_t rb = (size_t)c->rank * sizeof(float), pb = (size_t)c->rp * sizeof(float);
+  CUDA_TRY(cudaMemcpy2DAsync(Q, rb, c->Qw + (int64_t)worker * c->q_total + L->q_off, pb, rb, L->m,
+                             cudaMemcpyDefault, c->stream));
+  return sync_and_check(c);
+}
+
+int psgd_get_error(psgd_ctx* c, int layer, int worker, float* E) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  const LayerDev* L;
+  if ((rc = matrix_layer(c, layer, &L))) return rc;
+  if (worker < 0 || worker >= c->W) return fail(PSGD_ERR_INVALID, "worker %d out of range", worker);
+  if (!E) return fail(PSGD_ERR_INVALID, "E must not be NULL");
+  const int64_t nm = (int64_t)L->n * L->m;
+  float* dst = E;
+  const bool dev = is_device_ptr(E);
+  if (!dev) {
+    if (c->e_scratch_elems < nm) {
+      if (c->e_scratch) cudaFree(c->e_scratch);
+      c->e_scratch = nullptr;
+      c->e_scratch_elems = 0;
+      if ((rc = dalloc(&c->e_scratch, nm, "error scratch"))) return rc;
+      c->e_scratch_elems = nm;
+    }
+    dst = c->e_scratch;
+  }
+  const float* Bw = c->B + (int64_t)worker * c->total + L->off;
+  const float* Qw = c->Qw + (int64_t)worker * c->q_total + L->q_off;
+  CUDA_TRY(c->ks->error(dst, Bw, c->Phat + L->p_off, Qw, L->n, L->m, L->ld, c->stream));
+  if (!dev) CUDA_TRY(cudaMemcpyAsync(E, dst, (size_t)nm * sizeof(float), cudaMemcpyDeviceToHost, c->stream));
+  return sync_and_check(c);
+}
+
+int psgd_set_state(psgd_ctx* c, int layer, const float* Q, const float* const* E) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  const LayerDev* L;
+  if ((rc = matrix_layer(c, layer, &L))) return rc;
+  if (!Q) return fail(PSGD_ERR_INVALID, "Q must not be NULL");
+  cudaStream_t s = c->stream;
+  const size_t rb = (size_t)c->rank * sizeof(float), pb = (size_t)c->rp * sizeof(float);
+  CUDA_TRY(cudaMemsetAsync(c->Qbar + L->q_off, 0, (size_t)L->ld * c->rp * sizeof(float), s));
+  CUDA_TRY(cudaMemcpy2DAsync(c->Qbar + L->q_off, pb, Q, rb, rb, L->m, cudaMemcpyDefault, s));
+  CUDA_TRY(cudaMemsetAsync(c->Phat + L->p_off, 0, (size_t)L->n * c->rp * sizeof(float), s));
+  for (int w = 0; w < c->W; ++w) {
+    float* Bw = c->B + (int64_t)w * c->total + L->off;
+    CUDA_TRY(cudaMemsetAsync(c->Qw + (int64_t)w * c->q_total + L->q_off, 0, (size_t)L->ld * c->rp * sizeof(float), s));
+    CUDA_TRY(cudaMemsetAsync(Bw, 0, (size_t)L->n * L->ld * sizeof(float), s));
+    if (E) {
+      if (!E[w]) return fail(PSGD_ERR_INVALID, "E[%d] is NULL", w);
+      CUDA_TRY(cudaMemcpy2DAsync(Bw, (size_t)L->ld * sizeof(float), E[w], (size_t)L->m * sizeof(float),
+                                 (size_t)L->m * sizeof(float), L->n, cudaMemcpyDefault, s));
+    }
+  }
+  return sync_and_check(c);
+}
+
+int psgd_get_stats(const psgd_ctx* c, psgd_stats* out) {
+  if (!c || !out) return fail(PSGD_ERR_INVALID, "NULL argument");
+  std::memset(out, 0, sizeof(*out));
+  out->steps = c->steps;
+  out->floats_sent_per_step = c->sent_step;
+  out->floats_uncompressed_per_step = c->unc_step;
+  out->floats_sent = c->sent_step * c->steps;
+  out->floats_uncompressed = c->unc_step * c->steps;
+  out->matrix_elements = c->mat_el;
+  out->vector_elements = c->vec_el;
+  out->buffer_elements = c->total;
+  out->work_items = (int64_t)c->items.size();
+  out->grid_ctas = c->grid;
+  out->kernel_rank = c->rp;
+  return PSGD_OK;
+}
+
+int psgd_layer_info(const psgd_ctx* c, int layer, int64_t* offset, int64_t* n, int64_t* m, int64_t* ld) {
+  if (!c) return fail(PSGD_ERR_INVALID, "context is NULL");
+  if (layer < 0 || layer >= c->num_layers) return fail(PSGD_ERR_INVALID, "layer %d out of range", layer);
+  if (offset) *offset = c->off[layer];
+  if (n) *n = c->n[layer];
+  if (m) *m = c->m[layer];
+  if (ld) *ld = c->ld[layer];
+  return PSGD_OK;
+}
+
+int psgd_selftest_wait(int64_t spin_limit, void* cuda_stream, int* status) {
+  if (!status) return fail(PSGD_ERR_INVALID, "status must not be NULL");
+  if (spin_limit < 1) return fail(PSGD_ERR_INVALID, "spin_limit must be >= 1");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  unsigned* flag = nullptr;
+  Ctl* ctl = nullptr;
+  int rc = dalloc(&flag, 1, "selftest flag");
+  if (!rc) rc = dalloc(&ctl, 1, "selftest ctl");
+  if (!rc) {
+    auto run = [&]() -> int {
+      CUDA_TRY(cudaMemsetAsync(flag, 0, sizeof(unsigned), s));
+      CUDA_TRY(cudaMemsetAsync(ctl, 0, sizeof(Ctl), s));
+      wait_selftest_kernel<<<1, kThreads, 0, s>>>(flag, ctl, spin_limit);
+      CUDA_TRY(cudaGetLastError());
+      Ctl h;
+      CUDA_TRY(cudaMemcpyAsync(&h, ctl, sizeof(Ctl), cudaMemcpyDeviceToHost, s));
+      CUDA_TRY(cudaStreamSynchronize(s));
+      *status = h.status;
+      return PSGD_OK;
+    };
+    rc = run();
+  }
+  if (flag) cudaFree(flag);
+  if (ctl) cudaFree(ctl);
+  return rc;
+}
+
+}  // extern "C"
