@@ -87,7 +87,28 @@ typedef struct {
   int64_t spin_limit;   /* polls of a bounded in-kernel wait before it gives up (0: default, ~seconds) */
   int32_t grid_ctas;    /* CTAs of the persistent step kernel (0: SMs x resident CTAs per SM) */
   int32_t schedule;     /* 0: interleave layers (default), 1: phase by phase over all layers */
+  int32_t trace;        /* 1: record per-work-item timings of every step (psgd_get_trace) */
+  int32_t reserved;
 } psgd_options;
+
+/* One traced work item of the last step (see psgd_get_trace). */
+typedef struct {
+  uint32_t item;   /* position in the step's work queue */
+  uint16_t sm;     /* SM that ran it */
+  uint16_t warp;   /* warp slot (CTA * warps per CTA + warp) */
+  uint64_t t0;     /* start, GPU global timer (ns) */
+  uint64_t tw;     /* its dependency wait (if any) ended */
+  uint64_t t1;     /* end */
+} psgd_trace_rec;
+
+/* Kind of one work item: 0 project (P = M Q, error add), 1 orthonormalise
+ * rows, 2 back-project (Q = M^T Phat), 3 decompress (U), 4 vector mean. */
+typedef struct {
+  int32_t kind;
+  int32_t layer;
+  int32_t a;
+  int32_t b;
+} psgd_item_desc;
 
 /*
  * Create a context for num_layers layers.  Layer l is an n[l] x m[l] matrix,
@@ -151,6 +172,14 @@ int psgd_get_error(psgd_ctx* ctx, int layer, int worker, float* E);
 int psgd_set_state(psgd_ctx* ctx, int layer, const float* Q, const float* const* E);
 
 int psgd_get_stats(const psgd_ctx* ctx, psgd_stats* out);
+
+/*
+ * Timing records of the last step of a context created with options.trace = 1:
+ * copies min(capacity, work_items) records (host memory) and the matching
+ * work-item descriptions (desc may be NULL); *count receives the number
+ * copied.  Waits for the stream.  PSGD_ERR_INVALID when tracing is off.
+ */
+int psgd_get_trace(psgd_ctx* ctx, psgd_trace_rec* recs, psgd_item_desc* desc, int64_t capacity, int64_t* count);
 
 /* Placement of layer l in a packed buffer: element offset, n, m, row stride. */
 int psgd_layer_info(const psgd_ctx* ctx, int layer, int64_t* offset, int64_t* n, int64_t* m,

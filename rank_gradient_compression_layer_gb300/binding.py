@@ -25,7 +25,7 @@ EXPORTS = (
     "psgd_create", "psgd_create_ex", "psgd_destroy", "psgd_set_stream", "psgd_step", "psgd_step_host",
     "psgd_sync", "psgd_get_PQ", "psgd_get_Qw", "psgd_get_error", "psgd_set_state", "psgd_get_stats",
     "psgd_layer_info", "psgd_plan_layout", "psgd_count_sent", "psgd_selftest_wait", "psgd_last_error",
-    "psgd_version",
+    "psgd_version", "psgd_get_trace",
 )
 
 
@@ -56,7 +56,21 @@ class Options(ctypes.Structure):
         ("spin_limit", ctypes.c_int64),
         ("grid_ctas", ctypes.c_int32),
         ("schedule", ctypes.c_int32),
+        ("trace", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
+
+
+class TraceRec(ctypes.Structure):
+    _fields_ = [("item", ctypes.c_uint32), ("sm", ctypes.c_uint16), ("warp", ctypes.c_uint16),
+                ("t0", ctypes.c_uint64), ("tw", ctypes.c_uint64), ("t1", ctypes.c_uint64)]
+
+
+class ItemDesc(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("layer", ctypes.c_int32), ("a", ctypes.c_int32), ("b", ctypes.c_int32)]
+
+
+ITEM_KINDS = ("project", "orthonormalise", "back_project", "decompress", "vector_mean")
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -94,6 +108,8 @@ def lib() -> ctypes.CDLL:
         "psgd_selftest_wait": ([ctypes.c_int64, _P, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
         "psgd_last_error": ([], ctypes.c_char_p),
         "psgd_version": ([], ctypes.c_char_p),
+        "psgd_get_trace": ([_P, ctypes.POINTER(TraceRec), ctypes.POINTER(ItemDesc), ctypes.c_int64, _I64P],
+                           ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -163,7 +179,7 @@ class PowerSGD:
     """
 
     def __init__(self, shapes: Sequence[Tuple[int, int]], rank: int, workers: int, seed: int = 0,
-                 stream=None, spin_limit: int = 0, grid_ctas: int = 0, schedule: int = 0):
+                 stream=None, spin_limit: int = 0, grid_ctas: int = 0, schedule: int = 0, trace: bool = False):
         import torch
 
         if not torch.cuda.is_available():
@@ -173,7 +189,7 @@ class PowerSGD:
         self.device = torch.device("cuda", torch.cuda.current_device())
         self._stream = stream
         n, m = _shapes(self.shapes)
-        opt = Options(int(spin_limit), int(grid_ctas), int(schedule))
+        opt = Options(int(spin_limit), int(grid_ctas), int(schedule), int(bool(trace)), 0)
         h = _P()
         _check(lib().psgd_create_ex(ctypes.byref(h), len(self.shapes), n, m, self.rank, self.workers,
                                     ctypes.c_uint64(self.seed), _stream_ptr(stream), ctypes.byref(opt)))
@@ -233,9 +249,13 @@ class PowerSGD:
         _check(lib().psgd_sync(self._h))
 
     # -- state access
+    def _shape(self, layer: int):
+        # out-of-range layers are passed through so that the library reports them
+        return self.shapes[layer] if 0 <= layer < len(self.shapes) else (1, 1)
+
     def get_PQ(self, layer: int):
         import torch
-        n, m = self.shapes[layer]
+        n, m = self._shape(layer)
         P = torch.empty(n, self.rank, dtype=torch.float32, device=self.device)
         Q = torch.empty(m, self.rank, dtype=torch.float32, device=self.device)
         _check(lib().psgd_get_PQ(self._h, layer, _ptr(P), _ptr(Q)))
@@ -243,14 +263,14 @@ class PowerSGD:
 
     def get_Qw(self, layer: int, worker: int):
         import torch
-        n, m = self.shapes[layer]
+        n, m = self._shape(layer)
         Q = torch.empty(m, self.rank, dtype=torch.float32, device=self.device)
         _check(lib().psgd_get_Qw(self._h, layer, worker, _ptr(Q)))
         return Q
 
     def get_error(self, layer: int, worker: int):
         import torch
-        n, m = self.shapes[layer]
+        n, m = self._shape(layer)
         E = torch.empty(n, m, dtype=torch.float32, device=self.device)
         _check(lib().psgd_get_error(self._h, layer, worker, _ptr(E)))
         return E
@@ -268,6 +288,17 @@ class PowerSGD:
         s = Stats()
         _check(lib().psgd_get_stats(self._h, ctypes.byref(s)))
         return {f: getattr(s, f) for f, _ in Stats._fields_}
+
+    def trace(self) -> List[dict]:
+        """Per-work-item timings of the last step (context created with trace=True)."""
+        cap = self.stats()["work_items"]
+        recs = (TraceRec * cap)()
+        desc = (ItemDesc * cap)()
+        cnt = ctypes.c_int64()
+        _check(lib().psgd_get_trace(self._h, recs, desc, cap, ctypes.byref(cnt)))
+        return [{"item": r.item, "sm": r.sm, "warp": r.warp, "t0": r.t0, "tw": r.tw, "t1": r.t1,
+                 "kind": ITEM_KINDS[d.kind], "layer": d.layer, "a": d.a, "b": d.b}
+                for r, d in zip(recs[:cnt.value], desc[:cnt.value])]
 
     @property
     def message_floats(self) -> int:

@@ -144,10 +144,12 @@ struct psgd_ctx {
   std::vector<VecDev> hv;
   std::vector<Item> items;
   std::vector<PackEntry> pack;
-  int64_t total = 0, q_total = 0, p_total = 0, gram_total = 0, rinv_total = 0, qpart_total = 0;
+  int64_t total = 0, q_total = 0, p_total = 0, gram_total = 0, rinv_total = 0, qpart_total = 0,
+          ppart_total = 0;
   int64_t n_counters = 0, n_flags = 0, msg_floats = 0;
   // device state and scratch
-  float *B = nullptr, *P = nullptr, *Phat = nullptr, *Qbar = nullptr, *Qw = nullptr, *qpart = nullptr;
+  float *B = nullptr, *P = nullptr, *Phat = nullptr, *Qbar = nullptr, *Qw = nullptr, *qpart = nullptr,
+        *ppart = nullptr;
   double *gram = nullptr, *rinv = nullptr;
   unsigned *counters = nullptr, *flags = nullptr;
   Ctl* ctl = nullptr;
@@ -159,6 +161,7 @@ struct psgd_ctx {
   float* e_scratch = nullptr;
   int64_t e_scratch_elems = 0;
   float *stage_G = nullptr, *stage_U = nullptr, *stage_msg = nullptr;
+  TraceRec* trace = nullptr;
   // launch
   int grid = 0;
   size_t smem = 0;
@@ -174,9 +177,9 @@ struct psgd_ctx {
 namespace {
 
 void free_all(psgd_ctx* c) {
-  void* ptrs[] = {c->B, c->P, c->Phat, c->Qbar, c->Qw, c->qpart, c->gram, c->rinv, c->counters, c->flags,
+  void* ptrs[] = {c->B, c->P, c->Phat, c->Qbar, c->Qw, c->qpart, c->ppart, c->gram, c->rinv, c->counters, c->flags,
                   c->ctl, c->d_layers, c->d_vecs, c->d_items, c->d_pack, c->e_scratch, c->stage_G,
-                  c->stage_U, c->stage_msg};
+                  c->stage_U, c->stage_msg, c->trace};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -192,39 +195,47 @@ int dalloc(T** p, int64_t count, const char* what) {
   return PSGD_OK;
 }
 
-// Tiling of one matrix layer for padded rank rp and W workers.
-void plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp, int W) {
+// Tiling of one matrix layer for padded rank rp and W workers.  Each work
+// item is one warp's share of a phase.  Returns the number of counters the
+// layer needs and sets its counter offsets relative to cnt_off.
+int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp, int W, const KernelSet& ks) {
   L.n = (int32_t)n;
   L.m = (int32_t)m;
   L.ld = (int32_t)ld;
   L.F = (int32_t)(ld / 4);
   L.S = (int32_t)ceil_div(L.F, kSeg);
   L.tail = (int32_t)(m - 4 * (L.F - 1));
-  const int rs1 = rp <= 4 ? 8 : (rp == 8 ? 4 : (rp == 16 ? 2 : 1));
-  const int rsu = rp <= 8 ? 8 : 4;
-  auto rho = [&](int rs) {
-    int r = (int)std::min<int64_t>(8, ceil_div(kWarps, L.S));
-    r = (int)std::min<int64_t>(r, ceil_div(n, rs));
-    return std::max(1, r);
-  };
-  L.rs1 = rs1;
-  L.rho1 = rho(rs1);
-  L.r1 = rs1 * L.rho1;
-  L.t1 = (int32_t)ceil_div(n, L.r1);
-  L.g1 = (int32_t)ceil_div(L.t1, kGramGroup);
-  L.rph = rp <= 8 ? 256 : (rp == 16 ? 128 : 64);
-  L.tph = (int32_t)ceil_div(n, L.rph);
-  L.r3 = (int32_t)std::min<int64_t>(n, 2048);
+  // P1: rs1 rows x nf4 float4 columns per item
+  L.r1 = ks.rs1;
+  L.gs1 = ks.nf4;
+  L.nsg1 = (int32_t)ceil_div(L.F, ks.nf4);
+  L.nrb = (int32_t)ceil_div(n, L.r1);
+  L.g1 = (int32_t)ceil_div(L.nrb, kGramGroup);
+  L.tph = (int32_t)ceil_div(n, 32);
+  // P3: one segment of one worker over r3 rows (a multiple of the 16-row
+  // stage), at most 16 row tiles so that the Q partial sums stay short
+  int64_t r3 = std::max<int64_t>(std::max(256, 32 * rp), (ceil_div(n, 16) + 15) / 16 * 16);
+  L.r3 = (int32_t)std::min<int64_t>(n, r3);
   L.t3r = (int32_t)ceil_div(n, L.r3);
-  L.rsu = rsu;
-  L.rhou = rho(rsu);
-  L.ru = rsu * L.rhou;
-  L.tu = (int32_t)ceil_div(n, L.ru);
-  (void)W;
+  // U: rsu rows x gsu segments
+  L.rsu = ks.rsu;
+  L.gsu = ks.gsu;
+  L.nrbu = (int32_t)ceil_div(n, L.rsu);
+  L.nsgu = (int32_t)ceil_div(L.F, (int64_t)L.gsu * kSeg);
+  // counters
+  L.c_gram = 0;
+  L.c_grp = 1;
+  L.c_ph = 1 + L.g1;
+  L.c_qf = 2 + L.g1;
+  L.c_qs = 3 + L.g1;
+  L.c_p3 = L.c_qs + L.S;
+  L.c_rb = L.c_p3 + L.S * W;
+  return (int64_t)L.c_rb + (L.nsg1 > 1 ? L.nrb : 0);
 }
 
 void emit_p1(std::vector<Item>& v, int li, const LayerDev& L) {
-  for (int t = 0; t < L.t1; ++t) v.push_back({kItemP1, li, t, 0});
+  for (int rb = 0; rb < L.nrb; ++rb)
+    for (int sg = 0; sg < L.nsg1; ++sg) v.push_back({kItemP1, li, rb, sg});
 }
 void emit_ph(std::vector<Item>& v, int li, const LayerDev& L) {
   for (int t = 0; t < L.tph; ++t) v.push_back({kItemPH, li, t, 0});
@@ -235,12 +246,18 @@ void emit_p3(std::vector<Item>& v, int li, const LayerDev& L, int W) {
       for (int w = 0; w < W; ++w) v.push_back({kItemP3, li, rt, s * W + w});
 }
 void emit_u(std::vector<Item>& v, int li, const LayerDev& L) {
-  for (int t = 0; t < L.tu; ++t) v.push_back({kItemU, li, t, 0});
+  for (int rb = 0; rb < L.nrbu; ++rb)
+    for (int sg = 0; sg < L.nsgu; ++sg) v.push_back({kItemU, li, rb, sg});
 }
 
 // Work-item order.  Every item that waits on a layer's flag comes after all
 // the items that publish it, so the in-order queue always drains.
-void build_items(psgd_ctx* c) {
+//   schedule 1: phase by phase over all layers (P1 all, PH all, P3 all, U all);
+//   schedule 0: layers largest first; a layer's PH and P3 items follow its P1
+//   items once `lag` further P1 items have been queued (enough to keep every
+//   warp busy while its Gram-Schmidt completes), and its U items follow
+//   another `lag` P1 items later.  Remaining phases drain in layer order.
+void build_items(psgd_ctx* c, int64_t lag) {
   std::vector<Item>& v = c->items;
   v.clear();
   for (int vi = 0; vi < (int)c->hv.size(); ++vi)
@@ -253,21 +270,57 @@ void build_items(psgd_ctx* c) {
     for (int li = 0; li < nm; ++li) emit_u(v, li, c->hl[li]);
     return;
   }
-  // interleaved: largest layers first; a layer's later phases trail its P1 by
-  // one (PH, P3) and two (U) layers so that their waits are short
   std::vector<int> order(nm);
   std::iota(order.begin(), order.end(), 0);
   std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
     return (int64_t)c->hl[x].n * c->hl[x].m > (int64_t)c->hl[y].n * c->hl[y].m;
   });
-  for (int k = 0; k < nm + 2; ++k) {
-    if (k < nm) emit_p1(v, order[k], c->hl[order[k]]);
-    if (k - 1 >= 0 && k - 1 < nm) {
-      emit_ph(v, order[k - 1], c->hl[order[k - 1]]);
-      emit_p3(v, order[k - 1], c->hl[order[k - 1]], c->W);
+  struct Pending {
+    int li;
+    int64_t at;  // P1 items queued when the next phase was last queued
+    int next;    // 1: PH + P3 due, 2: U due
+  };
+  std::vector<Pending> pend;
+  int64_t p1 = 0;
+  auto drain = [&](bool all) {
+    for (size_t k = 0; k < pend.size();) {
+      Pending& q = pend[k];
+      if (!all && p1 < q.at + lag) {
+        ++k;
+        continue;
+      }
+      if (q.next == 1) {
+        emit_ph(v, q.li, c->hl[q.li]);
+        emit_p3(v, q.li, c->hl[q.li], c->W);
+        q.next = 2;
+        q.at = p1;
+        if (!all) {
+          ++k;
+          continue;
+        }
+      }
+      emit_u(v, q.li, c->hl[q.li]);
+      pend.erase(pend.begin() + k);
     }
-    if (k - 2 >= 0 && k - 2 < nm) emit_u(v, order[k - 2], c->hl[order[k - 2]]);
+  };
+  for (int k = 0; k < nm; ++k) {
+    const LayerDev& L = c->hl[order[k]];
+    for (int rb = 0; rb < L.nrb; ++rb)
+      for (int sg = 0; sg < L.nsg1; ++sg) {
+        v.push_back({kItemP1, order[k], rb, sg});
+        ++p1;
+        if ((p1 & 63) == 0) drain(false);
+      }
+    pend.push_back({order[k], p1, 1});
   }
+  // the tail: the remaining layers' later phases, phase by phase
+  for (Pending& q : pend)
+    if (q.next == 1) {
+      emit_ph(v, q.li, c->hl[q.li]);
+      emit_p3(v, q.li, c->hl[q.li], c->W);
+      q.next = 2;
+    }
+  for (Pending& q : pend) emit_u(v, q.li, c->hl[q.li]);
 }
 
 int ctx_ok(const psgd_ctx* c) {
@@ -376,7 +429,6 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
 
   const int rp = c->rp;
   const int NG = rp * (rp + 1) / 2;
-  int max_r1 = 1, max_ru = 1;
   for (int l = 0; l < num_layers; ++l) {
     if (m[l] == 0) {
       c->hv.push_back({c->off[l], (int32_t)n[l], 0});
@@ -387,25 +439,25 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     }
     LayerDev L;
     std::memset(&L, 0, sizeof(L));
-    plan_matrix(L, n[l], m[l], c->ld[l], rp, c->W);
+    const int64_t ncnt = plan_matrix(L, n[l], m[l], c->ld[l], rp, c->W, *c->ks);
     L.off = c->off[l];
     L.index = l;
     L.p_off = c->p_total;
-    c->p_total += n[l] * rp;
+    c->p_total += (n[l] * rp + 3) & ~(int64_t)3;  // 16-byte aligned per layer (bulk copies)
     L.q_off = c->q_total;
     c->q_total += c->ld[l] * rp;
     L.gram_off = c->gram_total;
-    c->gram_total += (int64_t)(L.t1 + L.g1) * NG;
+    c->gram_total += (int64_t)(L.nrb + L.g1) * NG;
     L.rinv_off = c->rinv_total;
-    c->rinv_total += (int64_t)rp * rp;
+    c->rinv_total += (int64_t)2 * rp * rp + rp;
     L.qpart_off = c->qpart_total;
     c->qpart_total += (int64_t)L.t3r * c->W * c->ld[l] * rp;
+    L.ppart_off = c->ppart_total;
+    if (L.nsg1 > 1) c->ppart_total += (int64_t)L.nrb * L.nsg1 * L.r1 * rp;
     L.cnt_off = (int32_t)c->n_counters;
-    c->n_counters += 3 + L.g1 + L.S;
+    c->n_counters += ncnt;
     L.flag_off = (int32_t)c->n_flags;
     c->n_flags += 3;
-    max_r1 = std::max(max_r1, (int)L.r1);
-    max_ru = std::max(max_ru, (int)L.ru);
     c->pack.push_back({L.p_off, L.q_off, c->msg_floats, L.n, L.m});
     c->msg_floats += (n[l] + m[l]) * rank;
     c->mat_of[l] = (int)c->hl.size();
@@ -414,7 +466,22 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     c->sent_step += (n[l] + m[l]) * rank;
     c->unc_step += n[l] * m[l];
   }
-  build_items(c);
+  // launch geometry of the step kernel (needed to size the schedule's lag)
+  c->smem = c->ks->smem_bytes();
+  int per_sm = 0, sms = 0;
+  {
+    cudaError_t e = c->ks->prepare(c->smem, &per_sm);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (e != cudaSuccess || per_sm < 1) {
+      cudaGetLastError();
+      delete c;
+      return e != cudaSuccess ? cuda_fail(e, "step kernel set-up")
+                              : fail(PSGD_ERR_CUDA, "step kernel does not fit on an SM (smem %zu)", c->smem);
+    }
+  }
+  c->grid = (opt && opt->grid_ctas > 0) ? opt->grid_ctas : sms * per_sm;
+  build_items(c, 2LL * c->grid * kWarps);
+  c->grid = (int)std::min<int64_t>(c->grid, std::max<int64_t>((int64_t)c->items.size(), 1));
 
   const int W = c->W;
   rc = PSGD_OK;
@@ -422,10 +489,11 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   if (!rc) rc = dalloc(&c->p, (cnt), #p)
   ALLOC(B, (int64_t)W * c->total);
   ALLOC(P, c->p_total);
-  ALLOC(Phat, c->p_total);
+  ALLOC(Phat, c->p_total + 64);  // slack: Phat rows are bulk-copied in 16-byte units
   ALLOC(Qbar, c->q_total);
   ALLOC(Qw, (int64_t)W * c->q_total);
   ALLOC(qpart, c->qpart_total);
+  ALLOC(ppart, c->ppart_total);
   ALLOC(gram, c->gram_total);
   ALLOC(rinv, c->rinv_total);
   ALLOC(counters, c->n_counters);
@@ -435,6 +503,7 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   ALLOC(d_vecs, (int64_t)c->hv.size());
   ALLOC(d_items, (int64_t)c->items.size());
   ALLOC(d_pack, (int64_t)c->pack.size());
+  if (opt && opt->trace) ALLOC(trace, (int64_t)c->items.size());
 #undef ALLOC
   if (rc) {
     free_all(c);
@@ -444,7 +513,7 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   auto setup = [&]() -> int {
     cudaStream_t s = c->stream;
     CUDA_TRY(cudaMemsetAsync(c->B, 0, (size_t)W * c->total * sizeof(float), s));
-    CUDA_TRY(cudaMemsetAsync(c->Phat, 0, (size_t)std::max<int64_t>(c->p_total, 1) * sizeof(float), s));
+    CUDA_TRY(cudaMemsetAsync(c->Phat, 0, (size_t)(c->p_total + 64) * sizeof(float), s));
     CUDA_TRY(cudaMemsetAsync(c->Qbar, 0, (size_t)std::max<int64_t>(c->q_total, 1) * sizeof(float), s));
     CUDA_TRY(cudaMemsetAsync(c->Qw, 0, (size_t)std::max<int64_t>(W * c->q_total, 1) * sizeof(float), s));
     CUDA_TRY(cudaMemsetAsync(c->counters, 0, (size_t)std::max<int64_t>(c->n_counters, 1) * sizeof(unsigned), s));
@@ -466,16 +535,6 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
       q_init_kernel<<<grid, 256, 0, s>>>(c->Qbar, c->d_layers, c->rank, c->rp, c->seed);
       CUDA_TRY(cudaGetLastError());
     }
-    // launch geometry of the step kernel
-    c->smem = c->ks->smem_bytes(max_r1, max_ru);
-    int per_sm = 0;
-    CUDA_TRY(c->ks->prepare(c->smem, &per_sm));
-    if (per_sm < 1) return fail(PSGD_ERR_CUDA, "step kernel does not fit on an SM (smem %zu)", c->smem);
-    int sms = 0;
-    CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device));
-    int64_t g = (opt && opt->grid_ctas > 0) ? opt->grid_ctas : (int64_t)sms * per_sm;
-    g = std::min<int64_t>(g, std::max<int64_t>((int64_t)c->items.size(), 1));
-    c->grid = (int)g;
     CUDA_TRY(cudaStreamSynchronize(s));
     return PSGD_OK;
   };
@@ -527,6 +586,7 @@ int psgd_step(psgd_ctx* c, const float* const* grad_ptrs, float* out_update) {
   a.gram = c->gram;
   a.rinv = c->rinv;
   a.qpart = c->qpart;
+  a.ppart = c->ppart;
   a.counters = c->counters;
   a.flags = c->flags;
   a.ctl = c->ctl;
@@ -538,6 +598,7 @@ int psgd_step(psgd_ctx* c, const float* const* grad_ptrs, float* out_update) {
   a.epoch = c->epoch;
   a.has_prev = c->has_prev;
   a.spin_limit = c->spin_limit;
+  a.trace = c->trace;
   cudaError_t e = c->ks->step(a, c->grid, c->smem, c->stream);
   if (e != cudaSuccess) return cuda_fail(e, "step kernel launch");
   c->has_prev = 1;
@@ -673,6 +734,21 @@ int psgd_get_stats(const psgd_ctx* c, psgd_stats* out) {
   out->work_items = (int64_t)c->items.size();
   out->grid_ctas = c->grid;
   out->kernel_rank = c->rp;
+  return PSGD_OK;
+}
+
+int psgd_get_trace(psgd_ctx* c, psgd_trace_rec* recs, psgd_item_desc* desc, int64_t capacity, int64_t* count) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  if (!c->trace) return fail(PSGD_ERR_INVALID, "tracing is off (psgd_options.trace)");
+  if (!recs || !count || capacity < 0) return fail(PSGD_ERR_INVALID, "recs and count must not be NULL");
+  static_assert(sizeof(psgd_trace_rec) == sizeof(TraceRec), "trace record layout");
+  static_assert(sizeof(psgd_item_desc) == sizeof(Item), "item layout");
+  const int64_t nrec = std::min<int64_t>(capacity, (int64_t)c->items.size());
+  if ((rc = sync_and_check(c))) return rc;
+  CUDA_TRY(cudaMemcpy(recs, c->trace, (size_t)nrec * sizeof(TraceRec), cudaMemcpyDeviceToHost));
+  if (desc) std::memcpy(desc, c->items.data(), (size_t)nrec * sizeof(Item));
+  *count = nrec;
   return PSGD_OK;
 }
 

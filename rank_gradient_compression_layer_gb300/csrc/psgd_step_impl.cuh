@@ -25,7 +25,7 @@ cudaError_t launch_error(float* E, const float* B, const float* Phat, const floa
   return cudaGetLastError();
 }
 
-size_t smem_bytes(int max_r1, int max_ru) { return step_smem_bytes<kRP>(max_r1, max_ru); }
+size_t smem_bytes() { return step_smem_bytes<kRP>(); }
 
 cudaError_t prepare(size_t smem, int* ctas_per_sm) {
   cudaError_t e = cudaFuncSetAttribute(step_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -35,6 +35,8 @@ cudaError_t prepare(size_t smem, int* ctas_per_sm) {
 
 }  // namespace
 
-extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {kRP, launch_step, launch_error, smem_bytes, prepare};
+extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {kRP,          launch_step,   launch_error, smem_bytes,
+                                                       Cfg<kRP>::R1, Cfg<kRP>::NF4, Cfg<kRP>::RSU,
+                                                       Cfg<kRP>::GSU, prepare};
 
 }  // namespace psgd

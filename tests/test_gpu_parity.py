@@ -36,7 +36,7 @@ def _run_config(cfg, steps, check_every=1, check_e=True, **kw):
             ref = st.step(grads)
             if t == 0 or (t + 1) % check_every == 0 or t == steps - 1:
                 tol = TOL1 if t == 0 else TOLN
-                worst, bad = compare_step(run, ref, st, tol, check_e=check_e)
+                worst, bad = compare_step(run, ref, st, tol, check_e=check_e, grads=grads)
                 worst_all.append(worst)
                 assert not bad, f"step {t}: {sorted(bad.items(), key=lambda kv: -kv[1])[:5]}"
         s = run.ctx.stats()
