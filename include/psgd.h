@@ -38,10 +38,11 @@
  *
  * Errors: every call returns a psgd_status; nothing throws across the ABI.
  * psgd_last_error() gives a message for the calling thread.  psgd_step is
- * asynchronous on the context's stream; a device-side failure (a bounded wait
- * that ran out) is reported as PSGD_ERR_TIMEOUT by the next synchronising call
- * (psgd_sync or any psgd_get_*), after which the context only answers
- * PSGD_ERR_STATE until destroyed.
+ * asynchronous on the context's stream (four kernel launches, no host
+ * synchronisation); a CUDA error raised while it runs is reported by the next
+ * synchronising call (psgd_sync or any psgd_get_*), after which the context
+ * only answers PSGD_ERR_STATE until destroyed.  No kernel of this library
+ * waits on another kernel or on another CTA, so a step cannot hang.
  *
  * Thread safety: a context must not be used from two host threads at once.
  * Two contexts are independent and may run concurrently on different streams.
@@ -63,13 +64,12 @@ typedef enum {
   PSGD_ERR_INVALID = -1,  /* bad argument (null / misaligned pointer, bad size, rank) */
   PSGD_ERR_OOM = -2,      /* device or pinned-host allocation failed */
   PSGD_ERR_CUDA = -3,     /* a CUDA runtime call failed (message in psgd_last_error) */
-  PSGD_ERR_TIMEOUT = -4,  /* a bounded in-kernel wait ran out (see psgd_sync) */
-  PSGD_ERR_STATE = -5     /* the context hit an earlier device error and is unusable */
+  PSGD_ERR_STATE = -5     /* the context hit an earlier CUDA error and is unusable */
 } psgd_status;
 
-/* Cumulative counters of a context (exact integers except last_step_ms). */
+/* Cumulative counters of a context (exact integers). */
 typedef struct {
-  int64_t steps;                        /* psgd_step calls completed (enqueued) */
+  int64_t steps;                        /* psgd_step calls enqueued */
   int64_t floats_sent;                  /* per worker, summed over steps: sum (n+m) r + vector lengths */
   int64_t floats_uncompressed;          /* per worker, summed over steps: sum n m + vector lengths */
   int64_t floats_sent_per_step;         /* per worker, one step */
@@ -77,38 +77,16 @@ typedef struct {
   int64_t matrix_elements;              /* per worker: sum over matrix layers of n*m */
   int64_t vector_elements;              /* per worker: sum over vector layers of n */
   int64_t buffer_elements;              /* floats in one packed gradient buffer (with padding) */
-  int64_t work_items;                   /* work items of one step (all layers, all phases) */
-  int32_t grid_ctas;                    /* CTAs of the step kernel */
+  int64_t tiles[4];                     /* CTAs of the project, orthonormalise, back-project, decompress kernels */
   int32_t kernel_rank;                  /* rank the kernels were compiled for (r rounded up to 1,2,4,8,16,32) */
+  int32_t launches_per_step;            /* kernels one psgd_step enqueues (with an update) */
 } psgd_stats;
 
 /* Optional knobs of psgd_create_ex (zero-initialise, then set what you need). */
 typedef struct {
-  int64_t spin_limit;   /* polls of a bounded in-kernel wait before it gives up (0: default, ~seconds) */
-  int32_t grid_ctas;    /* CTAs of the persistent step kernel (0: SMs x resident CTAs per SM) */
-  int32_t schedule;     /* 0: interleave layers (default), 1: phase by phase over all layers */
-  int32_t trace;        /* 1: record per-work-item timings of every step (psgd_get_trace) */
-  int32_t reserved;
+  int32_t timing;       /* 1: time every phase of every step with CUDA events (psgd_get_phase_times) */
+  int32_t reserved[3];
 } psgd_options;
-
-/* One traced work item of the last step (see psgd_get_trace). */
-typedef struct {
-  uint32_t item;   /* position in the step's work queue */
-  uint16_t sm;     /* SM that ran it */
-  uint16_t warp;   /* warp slot (CTA * warps per CTA + warp) */
-  uint64_t t0;     /* start, GPU global timer (ns) */
-  uint64_t tw;     /* its dependency wait (if any) ended */
-  uint64_t t1;     /* end */
-} psgd_trace_rec;
-
-/* Kind of one work item: 0 project (P = M Q, error add), 1 orthonormalise
- * rows, 2 back-project (Q = M^T Phat), 3 decompress (U), 4 vector mean. */
-typedef struct {
-  int32_t kind;
-  int32_t layer;
-  int32_t a;
-  int32_t b;
-} psgd_item_desc;
 
 /*
  * Create a context for num_layers layers.  Layer l is an n[l] x m[l] matrix,
@@ -174,12 +152,11 @@ int psgd_set_state(psgd_ctx* ctx, int layer, const float* Q, const float* const*
 int psgd_get_stats(const psgd_ctx* ctx, psgd_stats* out);
 
 /*
- * Timing records of the last step of a context created with options.trace = 1:
- * copies min(capacity, work_items) records (host memory) and the matching
- * work-item descriptions (desc may be NULL); *count receives the number
- * copied.  Waits for the stream.  PSGD_ERR_INVALID when tracing is off.
+ * Device time of each phase of the last step, in milliseconds: project,
+ * orthonormalise, back-project, decompress (ms[4]).  Needs options.timing = 1;
+ * waits for the stream.
  */
-int psgd_get_trace(psgd_ctx* ctx, psgd_trace_rec* recs, psgd_item_desc* desc, int64_t capacity, int64_t* count);
+int psgd_get_phase_times(psgd_ctx* ctx, float* ms);
 
 /* Placement of layer l in a packed buffer: element offset, n, m, row stride. */
 int psgd_layer_info(const psgd_ctx* ctx, int layer, int64_t* offset, int64_t* n, int64_t* m,
@@ -195,14 +172,6 @@ int psgd_plan_layout(int num_layers, const int64_t* n, const int64_t* m, int64_t
                      int64_t* ld, int64_t* total);
 int psgd_count_sent(int num_layers, const int64_t* n, const int64_t* m, int rank,
                     int64_t* compressed, int64_t* uncompressed);
-
-/*
- * Self-test of the bounded wait used between phases of the step kernel: one
- * CTA waits on a flag that nothing sets, gives up after spin_limit polls and
- * records a timeout.  Writes the recorded status (PSGD_ERR_TIMEOUT expected)
- * to *status.  Enqueued on cuda_stream and waited for.
- */
-int psgd_selftest_wait(int64_t spin_limit, void* cuda_stream, int* status);
 
 const char* psgd_last_error(void);
 const char* psgd_version(void);

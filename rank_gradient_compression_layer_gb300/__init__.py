@@ -4,7 +4,7 @@ The compute lives in ``libpsgd.so`` (hand-written CUDA for sm_103a, C ABI in
 ``include/psgd.h``); this package only builds it and binds it with ctypes.
 """
 from .binding import (  # noqa: F401
-    EXPORTS, LIB_PATH, PSGD_ERR_CUDA, PSGD_ERR_INVALID, PSGD_ERR_OOM, PSGD_ERR_STATE, PSGD_ERR_TIMEOUT,
-    PSGD_OK, PowerSGD, PsgdError, lib, psgd_count_sent, psgd_plan_layout, psgd_selftest_wait,
+    EXPORTS, LIB_PATH, PHASES, PSGD_ERR_CUDA, PSGD_ERR_INVALID, PSGD_ERR_OOM, PSGD_ERR_STATE, PSGD_OK,
+    PowerSGD, PsgdError, lib, psgd_count_sent, psgd_plan_layout,
 )
 from .build import build  # noqa: F401

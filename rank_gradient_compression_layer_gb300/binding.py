@@ -17,16 +17,17 @@ PSGD_OK = 0
 PSGD_ERR_INVALID = -1
 PSGD_ERR_OOM = -2
 PSGD_ERR_CUDA = -3
-PSGD_ERR_TIMEOUT = -4
 PSGD_ERR_STATE = -5
 
 # every symbol include/psgd.h declares
 EXPORTS = (
     "psgd_create", "psgd_create_ex", "psgd_destroy", "psgd_set_stream", "psgd_step", "psgd_step_host",
     "psgd_sync", "psgd_get_PQ", "psgd_get_Qw", "psgd_get_error", "psgd_set_state", "psgd_get_stats",
-    "psgd_layer_info", "psgd_plan_layout", "psgd_count_sent", "psgd_selftest_wait", "psgd_last_error",
-    "psgd_version", "psgd_get_trace",
+    "psgd_layer_info", "psgd_plan_layout", "psgd_count_sent", "psgd_last_error", "psgd_version",
+    "psgd_get_phase_times",
 )
+
+PHASES = ("project", "orthonormalise", "back_project", "decompress")
 
 
 class PsgdError(RuntimeError):
@@ -45,32 +46,14 @@ class Stats(ctypes.Structure):
         ("matrix_elements", ctypes.c_int64),
         ("vector_elements", ctypes.c_int64),
         ("buffer_elements", ctypes.c_int64),
-        ("work_items", ctypes.c_int64),
-        ("grid_ctas", ctypes.c_int32),
+        ("tiles", ctypes.c_int64 * 4),
         ("kernel_rank", ctypes.c_int32),
+        ("launches_per_step", ctypes.c_int32),
     ]
 
 
 class Options(ctypes.Structure):
-    _fields_ = [
-        ("spin_limit", ctypes.c_int64),
-        ("grid_ctas", ctypes.c_int32),
-        ("schedule", ctypes.c_int32),
-        ("trace", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
-    ]
-
-
-class TraceRec(ctypes.Structure):
-    _fields_ = [("item", ctypes.c_uint32), ("sm", ctypes.c_uint16), ("warp", ctypes.c_uint16),
-                ("t0", ctypes.c_uint64), ("tw", ctypes.c_uint64), ("t1", ctypes.c_uint64)]
-
-
-class ItemDesc(ctypes.Structure):
-    _fields_ = [("kind", ctypes.c_int32), ("layer", ctypes.c_int32), ("a", ctypes.c_int32), ("b", ctypes.c_int32)]
-
-
-ITEM_KINDS = ("project", "orthonormalise", "back_project", "decompress", "vector_mean")
+    _fields_ = [("timing", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -105,11 +88,9 @@ def lib() -> ctypes.CDLL:
         "psgd_layer_info": ([_P, ctypes.c_int, _I64P, _I64P, _I64P, _I64P], ctypes.c_int),
         "psgd_plan_layout": ([ctypes.c_int, _I64P, _I64P, _I64P, _I64P, _I64P], ctypes.c_int),
         "psgd_count_sent": ([ctypes.c_int, _I64P, _I64P, ctypes.c_int, _I64P, _I64P], ctypes.c_int),
-        "psgd_selftest_wait": ([ctypes.c_int64, _P, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
         "psgd_last_error": ([], ctypes.c_char_p),
         "psgd_version": ([], ctypes.c_char_p),
-        "psgd_get_trace": ([_P, ctypes.POINTER(TraceRec), ctypes.POINTER(ItemDesc), ctypes.c_int64, _I64P],
-                           ctypes.c_int),
+        "psgd_get_phase_times": ([_P, ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -151,12 +132,6 @@ def psgd_count_sent(shapes: Sequence[Tuple[int, int]], rank: int) -> Tuple[int, 
     return c.value, u.value
 
 
-def psgd_selftest_wait(spin_limit: int, stream=None) -> int:
-    st = ctypes.c_int()
-    _check(lib().psgd_selftest_wait(int(spin_limit), _stream_ptr(stream), ctypes.byref(st)))
-    return st.value
-
-
 def _stream_ptr(stream) -> Optional[int]:
     if stream is None:
         import torch
@@ -179,7 +154,7 @@ class PowerSGD:
     """
 
     def __init__(self, shapes: Sequence[Tuple[int, int]], rank: int, workers: int, seed: int = 0,
-                 stream=None, spin_limit: int = 0, grid_ctas: int = 0, schedule: int = 0, trace: bool = False):
+                 stream=None, timing: bool = False):
         import torch
 
         if not torch.cuda.is_available():
@@ -189,7 +164,7 @@ class PowerSGD:
         self.device = torch.device("cuda", torch.cuda.current_device())
         self._stream = stream
         n, m = _shapes(self.shapes)
-        opt = Options(int(spin_limit), int(grid_ctas), int(schedule), int(bool(trace)), 0)
+        opt = Options(int(bool(timing)))
         h = _P()
         _check(lib().psgd_create_ex(ctypes.byref(h), len(self.shapes), n, m, self.rank, self.workers,
                                     ctypes.c_uint64(self.seed), _stream_ptr(stream), ctypes.byref(opt)))
@@ -287,18 +262,15 @@ class PowerSGD:
     def stats(self) -> dict:
         s = Stats()
         _check(lib().psgd_get_stats(self._h, ctypes.byref(s)))
-        return {f: getattr(s, f) for f, _ in Stats._fields_}
+        out = {f: getattr(s, f) for f, _ in Stats._fields_}
+        out["tiles"] = dict(zip(PHASES, list(s.tiles)))
+        return out
 
-    def trace(self) -> List[dict]:
-        """Per-work-item timings of the last step (context created with trace=True)."""
-        cap = self.stats()["work_items"]
-        recs = (TraceRec * cap)()
-        desc = (ItemDesc * cap)()
-        cnt = ctypes.c_int64()
-        _check(lib().psgd_get_trace(self._h, recs, desc, cap, ctypes.byref(cnt)))
-        return [{"item": r.item, "sm": r.sm, "warp": r.warp, "t0": r.t0, "tw": r.tw, "t1": r.t1,
-                 "kind": ITEM_KINDS[d.kind], "layer": d.layer, "a": d.a, "b": d.b}
-                for r, d in zip(recs[:cnt.value], desc[:cnt.value])]
+    def phase_times(self) -> dict:
+        """Device milliseconds of each phase of the last step (context created with timing=True)."""
+        ms = (ctypes.c_float * 4)()
+        _check(lib().psgd_get_phase_times(self._h, ms))
+        return dict(zip(PHASES, list(ms)))
 
     @property
     def message_floats(self) -> int:

@@ -1,9 +1,10 @@
 // Host side of libpsgd.so: the C ABI declared in include/psgd.h.
 //
-// psgd_create plans the packed layout and the work items of one step, owns
-// every device buffer of the state, and initialises Q.  psgd_step fills a
-// StepArgs and launches the persistent step kernel for the context's padded
-// rank; nothing else runs on the host per step.
+// psgd_create plans the packed layout and the tiles of the four phase kernels
+// (project, orthonormalise, back-project, decompress), owns every device
+// buffer of the state and initialises Q.  psgd_step fills a StepArgs and
+// enqueues the four kernels on the context's stream; nothing else runs on the
+// host per step.
 #define PSGD_SIDE_KERNELS 1
 
 #include <cuda_runtime.h>
@@ -12,7 +13,6 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
-#include <numeric>
 #include <string>
 #include <vector>
 
@@ -41,10 +41,10 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(code, "%s: %s", what, cudaGetErrorString(e));
 }
 
-#define CUDA_TRY(x)                                    \
-  do {                                                 \
-    cudaError_t e_ = (x);                              \
-    if (e_ != cudaSuccess) return cuda_fail(e_, #x);   \
+#define CUDA_TRY(x)                                  \
+  do {                                               \
+    cudaError_t e_ = (x);                            \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #x); \
   } while (0)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -142,32 +142,27 @@ struct psgd_ctx {
   std::vector<int> mat_of;  // layer -> matrix index or -1
   std::vector<LayerDev> hl;
   std::vector<VecDev> hv;
-  std::vector<Item> items;
+  std::vector<Tile> tiles[kPhases];
   std::vector<PackEntry> pack;
   int64_t total = 0, q_total = 0, p_total = 0, gram_total = 0, rinv_total = 0, qpart_total = 0,
           ppart_total = 0;
-  int64_t n_counters = 0, n_flags = 0, msg_floats = 0;
+  int64_t n_counters = 0, msg_floats = 0;
   // device state and scratch
   float *B = nullptr, *P = nullptr, *Phat = nullptr, *Qbar = nullptr, *Qw = nullptr, *qpart = nullptr,
         *ppart = nullptr;
   double *gram = nullptr, *rinv = nullptr;
-  unsigned *counters = nullptr, *flags = nullptr;
-  Ctl* ctl = nullptr;
+  unsigned* counters = nullptr;
   LayerDev* d_layers = nullptr;
   VecDev* d_vecs = nullptr;
-  Item* d_items = nullptr;
+  Tile* d_tiles[kPhases] = {nullptr, nullptr, nullptr, nullptr};
   PackEntry* d_pack = nullptr;
   // lazily allocated: error read-back scratch, host-path staging
   float* e_scratch = nullptr;
   int64_t e_scratch_elems = 0;
   float *stage_G = nullptr, *stage_U = nullptr, *stage_msg = nullptr;
-  TraceRec* trace = nullptr;
-  // launch
-  int grid = 0;
-  size_t smem = 0;
-  int64_t spin_limit = 0;
-  int schedule = 0;
-  unsigned epoch = 0;
+  // optional phase timing
+  bool timing = false;
+  cudaEvent_t ev[kPhases + 1] = {nullptr, nullptr, nullptr, nullptr, nullptr};
   int has_prev = 0;
   bool broken = false;
   // stats
@@ -177,11 +172,13 @@ struct psgd_ctx {
 namespace {
 
 void free_all(psgd_ctx* c) {
-  void* ptrs[] = {c->B, c->P, c->Phat, c->Qbar, c->Qw, c->qpart, c->ppart, c->gram, c->rinv, c->counters, c->flags,
-                  c->ctl, c->d_layers, c->d_vecs, c->d_items, c->d_pack, c->e_scratch, c->stage_G,
-                  c->stage_U, c->stage_msg, c->trace};
+  void* ptrs[] = {c->B, c->P, c->Phat, c->Qbar, c->Qw, c->qpart, c->ppart, c->gram, c->rinv, c->counters,
+                  c->d_layers, c->d_vecs, c->d_tiles[0], c->d_tiles[1], c->d_tiles[2], c->d_tiles[3], c->d_pack,
+                  c->e_scratch, c->stage_G, c->stage_U, c->stage_msg};
   for (void* p : ptrs)
     if (p) cudaFree(p);
+  for (cudaEvent_t e : c->ev)
+    if (e) cudaEventDestroy(e);
 }
 
 template <class T>
@@ -195,9 +192,9 @@ int dalloc(T** p, int64_t count, const char* what) {
   return PSGD_OK;
 }
 
-// Tiling of one matrix layer for padded rank rp and W workers.  Each work
-// item is one warp's share of a phase.  Returns the number of counters the
-// layer needs and sets its counter offsets relative to cnt_off.
+// Tiling of one matrix layer for padded rank rp and W workers.  Returns the
+// number of counters the layer needs and sets its counter offsets relative
+// to cnt_off.
 int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp, int W, const KernelSet& ks) {
   L.n = (int32_t)n;
   L.m = (int32_t)m;
@@ -205,127 +202,42 @@ int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp, int W
   L.F = (int32_t)(ld / 4);
   L.S = (int32_t)ceil_div(L.F, kSeg);
   L.tail = (int32_t)(m - 4 * (L.F - 1));
-  // P1: rs1 rows x nf4 float4 columns per item
-  L.r1 = ks.rs1;
-  L.gs1 = ks.nf4;
-  L.nsg1 = (int32_t)ceil_div(L.F, ks.nf4);
-  L.nrb = (int32_t)ceil_div(n, L.r1);
+  L.nrb = (int32_t)ceil_div(n, ks.r1);
   L.g1 = (int32_t)ceil_div(L.nrb, kGramGroup);
-  L.tph = (int32_t)ceil_div(n, 32);
-  // P3: one segment of one worker over r3 rows (a multiple of the 16-row
-  // stage), at most 16 row tiles so that the Q partial sums stay short
-  int64_t r3 = std::max<int64_t>(std::max(256, 32 * rp), (ceil_div(n, 16) + 15) / 16 * 16);
+  // back-project: at most 16 row tiles (the Q partial sums stay short), at
+  // least 256 rows per tile
+  const int64_t r3 = std::max<int64_t>(std::max(256, 32 * rp), ceil_div(n, 16));
   L.r3 = (int32_t)std::min<int64_t>(n, r3);
   L.t3r = (int32_t)ceil_div(n, L.r3);
-  // U: rsu rows x gsu segments
-  L.rsu = ks.rsu;
-  L.gsu = ks.gsu;
-  L.nrbu = (int32_t)ceil_div(n, L.rsu);
-  L.nsgu = (int32_t)ceil_div(L.F, (int64_t)L.gsu * kSeg);
-  // counters
   L.c_gram = 0;
   L.c_grp = 1;
-  L.c_ph = 1 + L.g1;
-  L.c_qf = 2 + L.g1;
-  L.c_qs = 3 + L.g1;
+  L.c_qs = 1 + L.g1;
   L.c_p3 = L.c_qs + L.S;
   L.c_rb = L.c_p3 + L.S * W;
-  return (int64_t)L.c_rb + (L.nsg1 > 1 ? L.nrb : 0);
+  return (int64_t)L.c_rb + (L.S > 1 ? L.nrb : 0);
 }
 
-void emit_p1(std::vector<Item>& v, int li, const LayerDev& L) {
-  for (int rb = 0; rb < L.nrb; ++rb)
-    for (int sg = 0; sg < L.nsg1; ++sg) v.push_back({kItemP1, li, rb, sg});
-}
-void emit_ph(std::vector<Item>& v, int li, const LayerDev& L) {
-  for (int t = 0; t < L.tph; ++t) v.push_back({kItemPH, li, t, 0});
-}
-void emit_p3(std::vector<Item>& v, int li, const LayerDev& L, int W) {
-  for (int rt = 0; rt < L.t3r; ++rt)
-    for (int s = 0; s < L.S; ++s)
-      for (int w = 0; w < W; ++w) v.push_back({kItemP3, li, rt, s * W + w});
-}
-void emit_u(std::vector<Item>& v, int li, const LayerDev& L) {
-  for (int rb = 0; rb < L.nrbu; ++rb)
-    for (int sg = 0; sg < L.nsgu; ++sg) v.push_back({kItemU, li, rb, sg});
-}
-
-// Work-item order.  Every item that waits on a layer's flag comes after all
-// the items that publish it, so the in-order queue always drains.
-//   schedule 1: phase by phase over all layers (P1 all, PH all, P3 all, U all);
-//   schedule 0: layers largest first; a layer's PH and P3 items follow its P1
-//   items once `lag` further P1 items have been queued (enough to keep every
-//   warp busy while its Gram-Schmidt completes), and its U items follow
-//   another `lag` P1 items later.  Remaining phases drain in layer order.
-void build_items(psgd_ctx* c, int64_t lag) {
-  std::vector<Item>& v = c->items;
-  v.clear();
-  for (int vi = 0; vi < (int)c->hv.size(); ++vi)
-    for (int t = 0; t < (int)ceil_div(c->hv[vi].n, kVChunk); ++t) v.push_back({kItemV, vi, t, 0});
+void build_tiles(psgd_ctx* c) {
+  for (auto& v : c->tiles) v.clear();
   const int nm = (int)c->hl.size();
-  if (c->schedule == 1) {
-    for (int li = 0; li < nm; ++li) emit_p1(v, li, c->hl[li]);
-    for (int li = 0; li < nm; ++li) emit_ph(v, li, c->hl[li]);
-    for (int li = 0; li < nm; ++li) emit_p3(v, li, c->hl[li], c->W);
-    for (int li = 0; li < nm; ++li) emit_u(v, li, c->hl[li]);
-    return;
-  }
-  std::vector<int> order(nm);
-  std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
-    return (int64_t)c->hl[x].n * c->hl[x].m > (int64_t)c->hl[y].n * c->hl[y].m;
-  });
-  struct Pending {
-    int li;
-    int64_t at;  // P1 items queued when the next phase was last queued
-    int next;    // 1: PH + P3 due, 2: U due
-  };
-  std::vector<Pending> pend;
-  int64_t p1 = 0;
-  auto drain = [&](bool all) {
-    for (size_t k = 0; k < pend.size();) {
-      Pending& q = pend[k];
-      if (!all && p1 < q.at + lag) {
-        ++k;
-        continue;
-      }
-      if (q.next == 1) {
-        emit_ph(v, q.li, c->hl[q.li]);
-        emit_p3(v, q.li, c->hl[q.li], c->W);
-        q.next = 2;
-        q.at = p1;
-        if (!all) {
-          ++k;
-          continue;
-        }
-      }
-      emit_u(v, q.li, c->hl[q.li]);
-      pend.erase(pend.begin() + k);
-    }
-  };
-  for (int k = 0; k < nm; ++k) {
-    const LayerDev& L = c->hl[order[k]];
+  for (int li = 0; li < nm; ++li) {
+    const LayerDev& L = c->hl[li];
     for (int rb = 0; rb < L.nrb; ++rb)
-      for (int sg = 0; sg < L.nsg1; ++sg) {
-        v.push_back({kItemP1, order[k], rb, sg});
-        ++p1;
-        if ((p1 & 63) == 0) drain(false);
-      }
-    pend.push_back({order[k], p1, 1});
+      for (int s = 0; s < L.S; ++s) c->tiles[kProject].push_back({li, rb, s, 0});
+    for (int t = 0; t < (int)ceil_div(L.n, kPHThreads); ++t) c->tiles[kOrthonormalise].push_back({li, t, 0, 0});
+    for (int rt = 0; rt < L.t3r; ++rt)
+      for (int s = 0; s < L.S; ++s)
+        for (int w = 0; w < c->W; ++w) c->tiles[kBackProject].push_back({li, rt, s, w});
+    for (int rb = 0; rb < (int)ceil_div(L.n, c->ks->ru); ++rb)
+      for (int s = 0; s < L.S; ++s) c->tiles[kDecompress].push_back({li, rb, s, 0});
   }
-  // the tail: the remaining layers' later phases, phase by phase
-  for (Pending& q : pend)
-    if (q.next == 1) {
-      emit_ph(v, q.li, c->hl[q.li]);
-      emit_p3(v, q.li, c->hl[q.li], c->W);
-      q.next = 2;
-    }
-  for (Pending& q : pend) emit_u(v, q.li, c->hl[q.li]);
+  for (int vi = 0; vi < (int)c->hv.size(); ++vi)
+    for (int t = 0; t < (int)ceil_div(c->hv[vi].n, kVChunk); ++t) c->tiles[kDecompress].push_back({vi, t, 0, 1});
 }
 
 int ctx_ok(const psgd_ctx* c) {
   if (!c) return fail(PSGD_ERR_INVALID, "context is NULL");
-  if (c->broken) return fail(PSGD_ERR_STATE, "context hit an earlier device error; destroy it");
+  if (c->broken) return fail(PSGD_ERR_STATE, "context hit an earlier CUDA error; destroy it");
   return PSGD_OK;
 }
 
@@ -338,12 +250,10 @@ int matrix_layer(const psgd_ctx* c, int layer, const LayerDev** L) {
 }
 
 int sync_and_check(psgd_ctx* c) {
-  CUDA_TRY(cudaStreamSynchronize(c->stream));
-  Ctl h;
-  CUDA_TRY(cudaMemcpy(&h, c->ctl, sizeof(Ctl), cudaMemcpyDeviceToHost));
-  if (h.status != 0) {
+  cudaError_t e = cudaStreamSynchronize(c->stream);
+  if (e != cudaSuccess) {
     c->broken = true;
-    return fail(PSGD_ERR_TIMEOUT, "a bounded wait in the step kernel ran out (work item %d)", h.where);
+    return cuda_fail(e, "step");
   }
   return PSGD_OK;
 }
@@ -354,7 +264,7 @@ extern "C" {
 
 const char* psgd_last_error(void) { return g_err.c_str(); }
 
-const char* psgd_version(void) { return "psgd 0.1 (sm_103a)"; }
+const char* psgd_version(void) { return "psgd 0.2 (sm_103a)"; }
 
 int psgd_plan_layout(int num_layers, const int64_t* n, const int64_t* m, int64_t* offset, int64_t* ld,
                      int64_t* total) {
@@ -413,8 +323,7 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   c->W = num_workers;
   c->seed = seed;
   c->ks = kernels_for(c->rp);
-  c->spin_limit = (opt && opt->spin_limit > 0) ? opt->spin_limit : ((int64_t)1 << 22);
-  c->schedule = opt ? opt->schedule : 0;
+  c->timing = opt && opt->timing;
   if (cudaGetDevice(&c->device) != cudaSuccess) {
     cudaGetLastError();
     delete c;
@@ -443,21 +352,19 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     L.off = c->off[l];
     L.index = l;
     L.p_off = c->p_total;
-    c->p_total += (n[l] * rp + 3) & ~(int64_t)3;  // 16-byte aligned per layer (bulk copies)
+    c->p_total += (n[l] * rp + 3) & ~(int64_t)3;
     L.q_off = c->q_total;
     c->q_total += c->ld[l] * rp;
     L.gram_off = c->gram_total;
     c->gram_total += (int64_t)(L.nrb + L.g1) * NG;
     L.rinv_off = c->rinv_total;
-    c->rinv_total += (int64_t)2 * rp * rp + rp;
+    c->rinv_total += (int64_t)rp * rp + rp;
     L.qpart_off = c->qpart_total;
     c->qpart_total += (int64_t)L.t3r * c->W * c->ld[l] * rp;
     L.ppart_off = c->ppart_total;
-    if (L.nsg1 > 1) c->ppart_total += (int64_t)L.nrb * L.nsg1 * L.r1 * rp;
+    if (L.S > 1) c->ppart_total += (int64_t)L.nrb * L.S * c->ks->r1 * rp;
     L.cnt_off = (int32_t)c->n_counters;
     c->n_counters += ncnt;
-    L.flag_off = (int32_t)c->n_flags;
-    c->n_flags += 3;
     c->pack.push_back({L.p_off, L.q_off, c->msg_floats, L.n, L.m});
     c->msg_floats += (n[l] + m[l]) * rank;
     c->mat_of[l] = (int)c->hl.size();
@@ -466,22 +373,7 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     c->sent_step += (n[l] + m[l]) * rank;
     c->unc_step += n[l] * m[l];
   }
-  // launch geometry of the step kernel (needed to size the schedule's lag)
-  c->smem = c->ks->smem_bytes();
-  int per_sm = 0, sms = 0;
-  {
-    cudaError_t e = c->ks->prepare(c->smem, &per_sm);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
-    if (e != cudaSuccess || per_sm < 1) {
-      cudaGetLastError();
-      delete c;
-      return e != cudaSuccess ? cuda_fail(e, "step kernel set-up")
-                              : fail(PSGD_ERR_CUDA, "step kernel does not fit on an SM (smem %zu)", c->smem);
-    }
-  }
-  c->grid = (opt && opt->grid_ctas > 0) ? opt->grid_ctas : sms * per_sm;
-  build_items(c, 2LL * c->grid * kWarps);
-  c->grid = (int)std::min<int64_t>(c->grid, std::max<int64_t>((int64_t)c->items.size(), 1));
+  build_tiles(c);
 
   const int W = c->W;
   rc = PSGD_OK;
@@ -489,7 +381,7 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   if (!rc) rc = dalloc(&c->p, (cnt), #p)
   ALLOC(B, (int64_t)W * c->total);
   ALLOC(P, c->p_total);
-  ALLOC(Phat, c->p_total + 64);  // slack: Phat rows are bulk-copied in 16-byte units
+  ALLOC(Phat, c->p_total);
   ALLOC(Qbar, c->q_total);
   ALLOC(Qw, (int64_t)W * c->q_total);
   ALLOC(qpart, c->qpart_total);
@@ -497,13 +389,10 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   ALLOC(gram, c->gram_total);
   ALLOC(rinv, c->rinv_total);
   ALLOC(counters, c->n_counters);
-  ALLOC(flags, c->n_flags);
-  ALLOC(ctl, 1);
   ALLOC(d_layers, (int64_t)c->hl.size());
   ALLOC(d_vecs, (int64_t)c->hv.size());
-  ALLOC(d_items, (int64_t)c->items.size());
+  for (int ph = 0; ph < kPhases; ++ph) ALLOC(d_tiles[ph], (int64_t)c->tiles[ph].size());
   ALLOC(d_pack, (int64_t)c->pack.size());
-  if (opt && opt->trace) ALLOC(trace, (int64_t)c->items.size());
 #undef ALLOC
   if (rc) {
     free_all(c);
@@ -512,21 +401,23 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   }
   auto setup = [&]() -> int {
     cudaStream_t s = c->stream;
+    CUDA_TRY(c->ks->prepare());
+    if (c->timing)
+      for (auto& e : c->ev) CUDA_TRY(cudaEventCreate(&e));
     CUDA_TRY(cudaMemsetAsync(c->B, 0, (size_t)W * c->total * sizeof(float), s));
-    CUDA_TRY(cudaMemsetAsync(c->Phat, 0, (size_t)(c->p_total + 64) * sizeof(float), s));
+    CUDA_TRY(cudaMemsetAsync(c->Phat, 0, (size_t)std::max<int64_t>(c->p_total, 1) * sizeof(float), s));
     CUDA_TRY(cudaMemsetAsync(c->Qbar, 0, (size_t)std::max<int64_t>(c->q_total, 1) * sizeof(float), s));
     CUDA_TRY(cudaMemsetAsync(c->Qw, 0, (size_t)std::max<int64_t>(W * c->q_total, 1) * sizeof(float), s));
     CUDA_TRY(cudaMemsetAsync(c->counters, 0, (size_t)std::max<int64_t>(c->n_counters, 1) * sizeof(unsigned), s));
-    CUDA_TRY(cudaMemsetAsync(c->flags, 0, (size_t)std::max<int64_t>(c->n_flags, 1) * sizeof(unsigned), s));
-    CUDA_TRY(cudaMemsetAsync(c->ctl, 0, sizeof(Ctl), s));
     if (!c->hl.empty())
       CUDA_TRY(cudaMemcpyAsync(c->d_layers, c->hl.data(), c->hl.size() * sizeof(LayerDev),
                                cudaMemcpyHostToDevice, s));
     if (!c->hv.empty())
       CUDA_TRY(cudaMemcpyAsync(c->d_vecs, c->hv.data(), c->hv.size() * sizeof(VecDev), cudaMemcpyHostToDevice, s));
-    if (!c->items.empty())
-      CUDA_TRY(cudaMemcpyAsync(c->d_items, c->items.data(), c->items.size() * sizeof(Item),
-                               cudaMemcpyHostToDevice, s));
+    for (int ph = 0; ph < kPhases; ++ph)
+      if (!c->tiles[ph].empty())
+        CUDA_TRY(cudaMemcpyAsync(c->d_tiles[ph], c->tiles[ph].data(), c->tiles[ph].size() * sizeof(Tile),
+                                 cudaMemcpyHostToDevice, s));
     if (!c->pack.empty())
       CUDA_TRY(cudaMemcpyAsync(c->d_pack, c->pack.data(), c->pack.size() * sizeof(PackEntry),
                                cudaMemcpyHostToDevice, s));
@@ -574,7 +465,6 @@ int psgd_step(psgd_ctx* c, const float* const* grad_ptrs, float* out_update) {
     a.G[w] = grad_ptrs[w];
   }
   if (out_update && !aligned16(out_update)) return fail(PSGD_ERR_INVALID, "out_update is not 16-byte aligned");
-  if (++c->epoch == 0) ++c->epoch;
   a.U = out_update;
   a.B = c->B;
   a.total = c->total;
@@ -588,19 +478,23 @@ int psgd_step(psgd_ctx* c, const float* const* grad_ptrs, float* out_update) {
   a.qpart = c->qpart;
   a.ppart = c->ppart;
   a.counters = c->counters;
-  a.flags = c->flags;
-  a.ctl = c->ctl;
   a.layers = c->d_layers;
   a.vecs = c->d_vecs;
-  a.items = c->d_items;
-  a.num_items = (int32_t)c->items.size();
   a.W = c->W;
-  a.epoch = c->epoch;
   a.has_prev = c->has_prev;
-  a.spin_limit = c->spin_limit;
-  a.trace = c->trace;
-  cudaError_t e = c->ks->step(a, c->grid, c->smem, c->stream);
-  if (e != cudaSuccess) return cuda_fail(e, "step kernel launch");
+  const int phases = out_update ? kPhases : kPhases - 1;  // the decompress phase only writes U
+  if (c->timing) CUDA_TRY(cudaEventRecord(c->ev[0], c->stream));
+  for (int ph = 0; ph < kPhases; ++ph) {
+    if (ph < phases) {
+      a.tiles = c->d_tiles[ph];
+      cudaError_t e = c->ks->launch(ph, a, (int)c->tiles[ph].size(), c->stream);
+      if (e != cudaSuccess) {
+        c->broken = true;
+        return cuda_fail(e, "phase kernel launch");
+      }
+    }
+    if (c->timing) CUDA_TRY(cudaEventRecord(c->ev[ph + 1], c->stream));
+  }
   c->has_prev = 1;
   c->steps += 1;
   return PSGD_OK;
@@ -610,6 +504,16 @@ int psgd_sync(psgd_ctx* c) {
   int rc = ctx_ok(c);
   if (rc) return rc;
   return sync_and_check(c);
+}
+
+int psgd_get_phase_times(psgd_ctx* c, float* ms) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  if (!ms) return fail(PSGD_ERR_INVALID, "ms must not be NULL");
+  if (!c->timing) return fail(PSGD_ERR_INVALID, "phase timing is off (psgd_options.timing)");
+  if ((rc = sync_and_check(c))) return rc;
+  for (int ph = 0; ph < kPhases; ++ph) CUDA_TRY(cudaEventElapsedTime(&ms[ph], c->ev[ph], c->ev[ph + 1]));
+  return PSGD_OK;
 }
 
 int psgd_step_host(psgd_ctx* c, const float* const* grad_host, float* msg_host, float* update_host) {
@@ -702,6 +606,9 @@ int psgd_set_state(psgd_ctx* c, int layer, const float* Q, const float* const* E
   const LayerDev* L;
   if ((rc = matrix_layer(c, layer, &L))) return rc;
   if (!Q) return fail(PSGD_ERR_INVALID, "Q must not be NULL");
+  if (E)
+    for (int w = 0; w < c->W; ++w)
+      if (!E[w]) return fail(PSGD_ERR_INVALID, "E[%d] is NULL", w);
   cudaStream_t s = c->stream;
   const size_t rb = (size_t)c->rank * sizeof(float), pb = (size_t)c->rp * sizeof(float);
   CUDA_TRY(cudaMemsetAsync(c->Qbar + L->q_off, 0, (size_t)L->ld * c->rp * sizeof(float), s));
@@ -711,11 +618,9 @@ int psgd_set_state(psgd_ctx* c, int layer, const float* Q, const float* const* E
     float* Bw = c->B + (int64_t)w * c->total + L->off;
     CUDA_TRY(cudaMemsetAsync(c->Qw + (int64_t)w * c->q_total + L->q_off, 0, (size_t)L->ld * c->rp * sizeof(float), s));
     CUDA_TRY(cudaMemsetAsync(Bw, 0, (size_t)L->n * L->ld * sizeof(float), s));
-    if (E) {
-      if (!E[w]) return fail(PSGD_ERR_INVALID, "E[%d] is NULL", w);
+    if (E)
       CUDA_TRY(cudaMemcpy2DAsync(Bw, (size_t)L->ld * sizeof(float), E[w], (size_t)L->m * sizeof(float),
                                  (size_t)L->m * sizeof(float), L->n, cudaMemcpyDefault, s));
-    }
   }
   return sync_and_check(c);
 }
@@ -731,24 +636,9 @@ int psgd_get_stats(const psgd_ctx* c, psgd_stats* out) {
   out->matrix_elements = c->mat_el;
   out->vector_elements = c->vec_el;
   out->buffer_elements = c->total;
-  out->work_items = (int64_t)c->items.size();
-  out->grid_ctas = c->grid;
+  for (int ph = 0; ph < kPhases; ++ph) out->tiles[ph] = (int64_t)c->tiles[ph].size();
   out->kernel_rank = c->rp;
-  return PSGD_OK;
-}
-
-int psgd_get_trace(psgd_ctx* c, psgd_trace_rec* recs, psgd_item_desc* desc, int64_t capacity, int64_t* count) {
-  int rc = ctx_ok(c);
-  if (rc) return rc;
-  if (!c->trace) return fail(PSGD_ERR_INVALID, "tracing is off (psgd_options.trace)");
-  if (!recs || !count || capacity < 0) return fail(PSGD_ERR_INVALID, "recs and count must not be NULL");
-  static_assert(sizeof(psgd_trace_rec) == sizeof(TraceRec), "trace record layout");
-  static_assert(sizeof(psgd_item_desc) == sizeof(Item), "item layout");
-  const int64_t nrec = std::min<int64_t>(capacity, (int64_t)c->items.size());
-  if ((rc = sync_and_check(c))) return rc;
-  CUDA_TRY(cudaMemcpy(recs, c->trace, (size_t)nrec * sizeof(TraceRec), cudaMemcpyDeviceToHost));
-  if (desc) std::memcpy(desc, c->items.data(), (size_t)nrec * sizeof(Item));
-  *count = nrec;
+  out->launches_per_step = kPhases;
   return PSGD_OK;
 }
 
@@ -760,33 +650,6 @@ int psgd_layer_info(const psgd_ctx* c, int layer, int64_t* offset, int64_t* n, i
   if (m) *m = c->m[layer];
   if (ld) *ld = c->ld[layer];
   return PSGD_OK;
-}
-
-int psgd_selftest_wait(int64_t spin_limit, void* cuda_stream, int* status) {
-  if (!status) return fail(PSGD_ERR_INVALID, "status must not be NULL");
-  if (spin_limit < 1) return fail(PSGD_ERR_INVALID, "spin_limit must be >= 1");
-  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  unsigned* flag = nullptr;
-  Ctl* ctl = nullptr;
-  int rc = dalloc(&flag, 1, "selftest flag");
-  if (!rc) rc = dalloc(&ctl, 1, "selftest ctl");
-  if (!rc) {
-    auto run = [&]() -> int {
-      CUDA_TRY(cudaMemsetAsync(flag, 0, sizeof(unsigned), s));
-      CUDA_TRY(cudaMemsetAsync(ctl, 0, sizeof(Ctl), s));
-      wait_selftest_kernel<<<1, kThreads, 0, s>>>(flag, ctl, spin_limit);
-      CUDA_TRY(cudaGetLastError());
-      Ctl h;
-      CUDA_TRY(cudaMemcpyAsync(&h, ctl, sizeof(Ctl), cudaMemcpyDeviceToHost, s));
-      CUDA_TRY(cudaStreamSynchronize(s));
-      *status = h.status;
-      return PSGD_OK;
-    };
-    rc = run();
-  }
-  if (flag) cudaFree(flag);
-  if (ctl) cudaFree(ctl);
-  return rc;
 }
 
 }  // extern "C"

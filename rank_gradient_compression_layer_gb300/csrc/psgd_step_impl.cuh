@@ -1,4 +1,4 @@
-// Instantiation of the step kernels for one padded rank (PSGD_RP).
+// Instantiation of the phase kernels for one padded rank (PSGD_RP).
 #include "psgd_dispatch.h"
 #include "psgd_kernels.cuh"
 
@@ -9,9 +9,33 @@ namespace psgd {
 namespace {
 
 constexpr int kRP = PSGD_RP;
+constexpr size_t kP3Dyn = (size_t)(kP3Threads / 32) * 32 * 4 * kRP * sizeof(float);
+constexpr size_t kSegQ = (size_t)kSeg * 4 * kRP * sizeof(float);
+constexpr size_t kP1DynMax = kSegQ + Cfg<kRP>::QW_STAGE_BYTES;
 
-cudaError_t launch_step(const StepArgs& a, int grid, size_t smem, cudaStream_t s) {
-  step_kernel<kRP><<<grid, kThreads, smem, s>>>(a);
+cudaError_t launch(int phase, const StepArgs& a, int tiles, cudaStream_t s) {
+  if (tiles <= 0) return cudaSuccess;
+  switch (phase) {
+    case kProject: {
+      const int warps = a.W < Cfg<kRP>::P1_WARPS ? a.W : Cfg<kRP>::P1_WARPS;
+      // the Q rows of a segment, plus every worker's Q_w' rows when they fit
+      const size_t qw = (size_t)a.W * kSegQ;
+      const size_t dyn = kSegQ + ((a.has_prev && qw <= (size_t)Cfg<kRP>::QW_STAGE_BYTES) ? qw : 0);
+      p1_kernel<kRP><<<tiles, 32 * warps, dyn, s>>>(a);
+      break;
+    }
+    case kOrthonormalise:
+      ph_kernel<kRP><<<tiles, kPHThreads, 0, s>>>(a);
+      break;
+    case kBackProject:
+      p3_kernel<kRP><<<tiles, kP3Threads, kP3Dyn, s>>>(a);
+      break;
+    case kDecompress:
+      u_kernel<kRP><<<tiles, kUThreads, 0, s>>>(a);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
@@ -25,18 +49,16 @@ cudaError_t launch_error(float* E, const float* B, const float* Phat, const floa
   return cudaGetLastError();
 }
 
-size_t smem_bytes() { return step_smem_bytes<kRP>(); }
-
-cudaError_t prepare(size_t smem, int* ctas_per_sm) {
-  cudaError_t e = cudaFuncSetAttribute(step_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, step_kernel<kRP>, kThreads, smem);
+cudaError_t prepare() {
+  cudaError_t e = cudaFuncSetAttribute(p3_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP3Dyn);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(p1_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP1DynMax);
+  return e;
 }
 
 }  // namespace
 
-extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {kRP,          launch_step,   launch_error, smem_bytes,
-                                                       Cfg<kRP>::R1, Cfg<kRP>::NF4, Cfg<kRP>::RSU,
-                                                       Cfg<kRP>::GSU, prepare};
+extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {kRP, launch, launch_error, prepare, Cfg<kRP>::R1,
+                                                       Cfg<kRP>::RU};
 
 }  // namespace psgd
