@@ -45,6 +45,7 @@ struct Cfg {
   static constexpr int R1 = 16;
   static constexpr int P1_WARPS = 8;                        // at most (more workers loop)
   static constexpr int QW_STAGE_BYTES = 32 * 1024;          // Q_w' rows staged when they fit
+  static constexpr int P1_MINB = RP <= 4 ? 4 : 1;           // 256-thread CTAs per SM the registers must allow
   // back-project: row tiles staged by chunks of R3C Phat rows, 8 warps
   static constexpr int R3C = 256;
   static constexpr int UNR3 = RP <= 4 ? 16 : 8;
@@ -197,7 +198,7 @@ __device__ void gram_tail(const StepArgs& a, const LayerDev& L, int rb, const fl
 // segment and, when W x RP is small enough, every worker's Q_w' rows live in
 // shared memory, so the registers hold the loads in flight.
 template <int RP>
-__global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS) p1_kernel(const StepArgs a) {
+__global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_kernel(const StepArgs a) {
   constexpr int RSB = Cfg<RP>::RSB;
   constexpr int R1 = Cfg<RP>::R1;
   constexpr int NW = Cfg<RP>::P1_WARPS;
@@ -222,30 +223,36 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS) p1_kernel(const StepAr
   const bool stage_qw = prev && a.W * SEGQ * 4 <= Cfg<RP>::QW_STAGE_BYTES;
   float* s_q = s_dyn;
   float* s_qw = s_dyn + SEGQ;
-  // stage Q and Q_w' (read-only in this kernel) and the previous Phat rows
+  // stage Q and Q_w' (read-only in this kernel) and the previous Phat rows.
+  // Shared layout is lane-minor: Q[4 L + j][k] sits at (j RP + k) 32 + L, so
+  // the 32 lanes of a warp read 32 consecutive words (no bank conflict).
   {
     const int64_t e0 = L.q_off + (int64_t)seg * SEGQ;
-    const int n4 = ncol4 * RP;  // float4 per segment slice
-    for (int i = threadIdx.x; i < n4; i += blockDim.x)
-      reinterpret_cast<float4*>(s_q)[i] = __ldg(reinterpret_cast<const float4*>(a.Qbar + e0) + i);
+    const int ne = ncol4 * 4 * RP;  // floats of the segment's Q slice
+    for (int e = threadIdx.x; e < ne; e += blockDim.x) {
+      const int col = e / RP, k = e - col * RP;
+      s_q[((col & 3) * RP + k) * kSeg + (col >> 2)] = __ldg(a.Qbar + e0 + e);
+    }
     if (stage_qw)
-      for (int i = threadIdx.x; i < a.W * n4; i += blockDim.x) {
-        const int w = i / n4, q = i - w * n4;
-        reinterpret_cast<float4*>(s_qw + w * SEGQ)[q] =
-            __ldg(reinterpret_cast<const float4*>(a.Qw + (int64_t)w * a.q_total + e0) + q);
+      for (int i = threadIdx.x; i < a.W * ne; i += blockDim.x) {
+        const int w = i / ne, e = i - w * ne;
+        const int col = e / RP, k = e - col * RP;
+        s_qw[w * SEGQ + ((col & 3) * RP + k) * kSeg + (col >> 2)] = __ldg(a.Qw + (int64_t)w * a.q_total + e0 + e);
       }
     for (int i = threadIdx.x; i < R1 * RP; i += blockDim.x)
       s_pp[i] = (prev && i < rcnt * RP) ? __ldg(a.Phat + L.p_off + (int64_t)row0 * RP + i) : 0.f;
   }
   __syncthreads();
-  const float* q = s_q + lane * 4 * RP;  // this lane's 4 Q rows
+  const float* q = s_q + lane;  // Q[4 lane + j][k] = q[(j RP + k) 32]
 
   bool first = true;
   for (int w = warp; w < a.W; w += nwarps) {
     const float* Gw = a.G[w] + L.off + 4 * c;
     float* Bw = a.B + (int64_t)w * a.total + L.off + 4 * c;
-    const float* qw = stage_qw ? s_qw + w * SEGQ + lane * 4 * RP
-                               : a.Qw + (int64_t)w * a.q_total + L.q_off + (int64_t)(4 * c) * RP;
+    // Q_w'[4 lane + j][k] = qw[(j RP + k) qs]: lane-minor in shared memory,
+    // row-major in global memory when not staged
+    const float* qw = stage_qw ? s_qw + w * SEGQ + lane : a.Qw + (int64_t)w * a.q_total + L.q_off + (int64_t)(4 * c) * RP;
+    const int qs = stage_qw ? kSeg : 1;
     for (int sb = 0; sb < rcnt; sb += RSB) {
       const int rn = min(RSB, rcnt - sb);
       float4 g[RSB], b[RSB];
@@ -275,10 +282,10 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS) p1_kernel(const StepAr
 #pragma unroll
             for (int k = 0; k < RP; ++k) {
               const float p = s_pp[(sb + i) * RP + k];
-              e0 = fmaf(-p, qw[k], e0);
-              e1 = fmaf(-p, qw[RP + k], e1);
-              e2 = fmaf(-p, qw[2 * RP + k], e2);
-              e3 = fmaf(-p, qw[3 * RP + k], e3);
+              e0 = fmaf(-p, qw[k * qs], e0);
+              e1 = fmaf(-p, qw[(RP + k) * qs], e1);
+              e2 = fmaf(-p, qw[(2 * RP + k) * qs], e2);
+              e3 = fmaf(-p, qw[(3 * RP + k) * qs], e3);
             }
           }
           float m0 = g[i].x + e0, m1 = g[i].y + e1, m2 = g[i].z + e2, m3 = g[i].w + e3;
@@ -290,10 +297,10 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS) p1_kernel(const StepAr
           *reinterpret_cast<float4*>(Bw + (int64_t)(row0 + sb + i) * L.ld) = make_float4(m0, m1, m2, m3);
 #pragma unroll
           for (int k = 0; k < RP; ++k) {
-            float s = m0 * q[k];
-            s = fmaf(m1, q[RP + k], s);
-            s = fmaf(m2, q[2 * RP + k], s);
-            s = fmaf(m3, q[3 * RP + k], s);
+            float s = m0 * q[k * kSeg];
+            s = fmaf(m1, q[(RP + k) * kSeg], s);
+            s = fmaf(m2, q[(2 * RP + k) * kSeg], s);
+            s = fmaf(m3, q[(3 * RP + k) * kSeg], s);
             acc[i][k] = s;
           }
         }
