@@ -217,6 +217,9 @@ int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp, int W
   return (int64_t)L.c_rb + (L.S > 1 ? L.nrb : 0);
 }
 
+// Tiles of every phase.  Back-project walks the layers and rows in the
+// reverse of the project order, so it first reads the error buffers the
+// project phase wrote last, while they are still in L2.
 void build_tiles(psgd_ctx* c) {
   for (auto& v : c->tiles) v.clear();
   const int nm = (int)c->hl.size();
@@ -224,12 +227,16 @@ void build_tiles(psgd_ctx* c) {
     const LayerDev& L = c->hl[li];
     for (int rb = 0; rb < L.nrb; ++rb)
       for (int s = 0; s < L.S; ++s) c->tiles[kProject].push_back({li, rb, s, 0});
-    for (int t = 0; t < (int)ceil_div(L.n, kPHThreads); ++t) c->tiles[kOrthonormalise].push_back({li, t, 0, 0});
-    for (int rt = 0; rt < L.t3r; ++rt)
-      for (int s = 0; s < L.S; ++s)
-        for (int w = 0; w < c->W; ++w) c->tiles[kBackProject].push_back({li, rt, s, w});
+    if (!c->ks->fuse_ph)
+      for (int t = 0; t < (int)ceil_div(L.n, kPHThreads); ++t) c->tiles[kOrthonormalise].push_back({li, t, 0, 0});
     for (int rb = 0; rb < (int)ceil_div(L.n, c->ks->ru); ++rb)
       for (int s = 0; s < L.S; ++s) c->tiles[kDecompress].push_back({li, rb, s, 0});
+  }
+  for (int li = nm - 1; li >= 0; --li) {
+    const LayerDev& L = c->hl[li];
+    for (int rt = L.t3r - 1; rt >= 0; --rt)
+      for (int s = L.S - 1; s >= 0; --s)
+        for (int w = 0; w < c->W; ++w) c->tiles[kBackProject].push_back({li, rt, s, w});
   }
   for (int vi = 0; vi < (int)c->hv.size(); ++vi)
     for (int t = 0; t < (int)ceil_div(c->hv[vi].n, kVChunk); ++t) c->tiles[kDecompress].push_back({vi, t, 0, 1});
@@ -638,7 +645,7 @@ int psgd_get_stats(const psgd_ctx* c, psgd_stats* out) {
   out->buffer_elements = c->total;
   for (int ph = 0; ph < kPhases; ++ph) out->tiles[ph] = (int64_t)c->tiles[ph].size();
   out->kernel_rank = c->rp;
-  out->launches_per_step = kPhases;
+  out->launches_per_step = c->ks->fuse_ph ? kPhases - 1 : kPhases;
   return PSGD_OK;
 }
 

@@ -22,6 +22,8 @@ struct KernelSet {
   cudaError_t (*prepare)();
   // tile geometry: project rows per tile, decompress rows per tile
   int r1, ru;
+  // back-project tiles form the Phat rows (no orthonormalise launch)
+  bool fuse_ph;
 };
 
 extern const KernelSet kKernelsR1, kKernelsR2, kKernelsR4, kKernelsR8, kKernelsR16, kKernelsR32;

@@ -10,7 +10,8 @@
 //                   (float64); the CTA that completes a layer sums the Gram
 //                   (fixed order), factors A = R^T R (Cholesky, float64) and
 //                   stores R: Phat = P R^-1 is the Gram-Schmidt basis of P.
-//   orthonormalise  Phat rows: forward substitution Phat R = P (float64).
+//   orthonormalise  Phat rows: forward substitution Phat R = P (float64); for
+//                   r <= 8 done by the back-project tiles themselves.
 //   back-project    partial Q_w = M_w^T Phat over a row tile of one segment
 //                   and one worker; the CTA that completes (segment, worker)
 //                   sums the partials (fixed order) into Q_w, and the one that
@@ -42,12 +43,15 @@ struct Cfg {
   // project: tiles of R1 rows x one segment x all workers; a warp per worker,
   // RSB rows per pass
   static constexpr int RSB = RP <= 4 ? 4 : (RP == 8 ? 2 : 1);
-  static constexpr int R1 = 16;
+  static constexpr int R1 = RP <= 8 ? 32 : 16;
   static constexpr int P1_WARPS = 8;                        // at most (more workers loop)
   static constexpr int QW_STAGE_BYTES = 32 * 1024;          // Q_w' rows staged when they fit
-  static constexpr int P1_MINB = RP <= 4 ? 4 : 1;           // 256-thread CTAs per SM the registers must allow
-  // back-project: row tiles staged by chunks of R3C Phat rows, 8 warps
+  static constexpr int P1_MINB = RP <= 2 ? 4 : (RP == 4 ? 3 : 1);          // 256-thread CTAs per SM the registers must allow
+  // back-project: row tiles staged by chunks of R3C Phat rows, 8 warps; for
+  // small ranks the tile forms its Phat rows itself (float64 forward
+  // substitution) instead of a separate orthonormalise launch
   static constexpr int R3C = 256;
+  static constexpr bool FUSE_PH = false;
   static constexpr int UNR3 = RP <= 4 ? 16 : 8;
   // decompress: RU rows x one segment per CTA of 256 threads
   static constexpr int RU = 64;
@@ -75,6 +79,39 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
   return v;
+}
+
+// Sums each of N values (N a power of two, 1..32) over the 32 lanes of a
+// warp with N - 1 + 5 - log2(N) shuffles: every level of the butterfly hands
+// half of the still-unsummed values to the partner lane, until each lane
+// holds one value, then the remaining levels sum that value.  Afterwards the
+// total of value j is held by lane j << (5 - log2 N) (and its group).
+// Returns the lane's value index.  Deterministic: each total is formed by one
+// fixed expression tree.
+template <int N>
+__device__ __forceinline__ int warp_reduce_multi(float (&v)[N], float& out) {
+  static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "N must be a power of two <= 32");
+  const int lane = threadIdx.x & 31;
+  constexpr int LOGN = N == 1 ? 0 : (N == 2 ? 1 : (N == 4 ? 2 : (N == 8 ? 3 : (N == 16 ? 4 : 5))));
+  int idx = 0;
+#pragma unroll
+  for (int l = 0; l < LOGN; ++l) {
+    const int o = 16 >> l;
+    const int c = N >> l;  // values still held
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < c / 2; ++i) {
+      const float send = up ? v[i] : v[i + c / 2];
+      const float keep = up ? v[i + c / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFull, send, o);
+    }
+    idx = (idx << 1) | (up ? 1 : 0);
+  }
+  float x = v[0];
+#pragma unroll
+  for (int o = 16 >> LOGN; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+  out = x;
+  return idx;
 }
 
 // (i, j), i <= j, of upper-triangle entry e in row-major order.
@@ -243,16 +280,28 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
       s_pp[i] = (prev && i < rcnt * RP) ? __ldg(a.Phat + L.p_off + (int64_t)row0 * RP + i) : 0.f;
   }
   __syncthreads();
-  const float* q = s_q + lane;  // Q[4 lane + j][k] = q[(j RP + k) 32]
+  // this lane's 4 Q rows, held in registers for the whole tile
+  float qv[4][RP];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int k = 0; k < RP; ++k) qv[j][k] = s_q[(j * RP + k) * kSeg + lane];
 
   bool first = true;
   for (int w = warp; w < a.W; w += nwarps) {
     const float* Gw = a.G[w] + L.off + 4 * c;
     float* Bw = a.B + (int64_t)w * a.total + L.off + 4 * c;
-    // Q_w'[4 lane + j][k] = qw[(j RP + k) qs]: lane-minor in shared memory,
-    // row-major in global memory when not staged
-    const float* qw = stage_qw ? s_qw + w * SEGQ + lane : a.Qw + (int64_t)w * a.q_total + L.q_off + (int64_t)(4 * c) * RP;
-    const int qs = stage_qw ? kSeg : 1;
+    // this worker's Q_w' rows for the lane's columns (registers)
+    float qw[4][RP];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int k = 0; k < RP; ++k)
+        qw[j][k] = !prev ? 0.f
+                         : (stage_qw ? s_qw[w * SEGQ + (j * RP + k) * kSeg + lane]
+                                     : (act ? __ldg(a.Qw + (int64_t)w * a.q_total + L.q_off +
+                                                    (int64_t)(4 * c + j) * RP + k)
+                                            : 0.f));
     for (int sb = 0; sb < rcnt; sb += RSB) {
       const int rn = min(RSB, rcnt - sb);
       float4 g[RSB], b[RSB];
@@ -267,11 +316,9 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
           b[i] = zero4();
         }
       }
-      float acc[RSB][RP];
+      float acc[RSB * RP];
 #pragma unroll
-      for (int i = 0; i < RSB; ++i)
-#pragma unroll
-        for (int k = 0; k < RP; ++k) acc[i][k] = 0.f;
+      for (int i = 0; i < RSB * RP; ++i) acc[i] = 0.f;
 #pragma unroll
       for (int i = 0; i < RSB; ++i) {
         if (act && i < rn) {
@@ -282,10 +329,10 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
 #pragma unroll
             for (int k = 0; k < RP; ++k) {
               const float p = s_pp[(sb + i) * RP + k];
-              e0 = fmaf(-p, qw[k * qs], e0);
-              e1 = fmaf(-p, qw[(RP + k) * qs], e1);
-              e2 = fmaf(-p, qw[(2 * RP + k) * qs], e2);
-              e3 = fmaf(-p, qw[(3 * RP + k) * qs], e3);
+              e0 = fmaf(-p, qw[0][k], e0);
+              e1 = fmaf(-p, qw[1][k], e1);
+              e2 = fmaf(-p, qw[2][k], e2);
+              e3 = fmaf(-p, qw[3][k], e3);
             }
           }
           float m0 = g[i].x + e0, m1 = g[i].y + e1, m2 = g[i].z + e2, m3 = g[i].w + e3;
@@ -297,26 +344,23 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
           *reinterpret_cast<float4*>(Bw + (int64_t)(row0 + sb + i) * L.ld) = make_float4(m0, m1, m2, m3);
 #pragma unroll
           for (int k = 0; k < RP; ++k) {
-            float s = m0 * q[k * kSeg];
-            s = fmaf(m1, q[(RP + k) * kSeg], s);
-            s = fmaf(m2, q[(2 * RP + k) * kSeg], s);
-            s = fmaf(m3, q[(3 * RP + k) * kSeg], s);
-            acc[i][k] = s;
+            float t = m0 * qv[0][k];
+            t = fmaf(m1, qv[1][k], t);
+            t = fmaf(m2, qv[2][k], t);
+            t = fmaf(m3, qv[3][k], t);
+            acc[i * RP + k] = t;
           }
         }
       }
-      // this worker's rows, reduced over the lanes (fixed butterfly); a warp
-      // with several workers adds them in worker order
-#pragma unroll
-      for (int i = 0; i < RSB; ++i)
-#pragma unroll
-        for (int k = 0; k < RP; ++k) {
-          const float v = warp_sum(acc[i][k]);
-          if (lane == 0 && i < rn) {
-            float& dst = s_red[warp][(sb + i) * RP + k];
-            dst = first ? v : dst + v;
-          }
-        }
+      // this worker's rows, summed over the lanes; a warp with several
+      // workers adds them in worker order
+      float tot;
+      const int j = warp_reduce_multi<RSB * RP>(acc, tot);
+      constexpr int SH = 5 - (RSB * RP == 1 ? 0 : (RSB * RP == 2 ? 1 : (RSB * RP == 4 ? 2 : (RSB * RP == 8 ? 3 : (RSB * RP == 16 ? 4 : 5)))));
+      if ((lane & ((1 << SH) - 1)) == 0 && j < rn * RP) {
+        float& dst = s_red[warp][sb * RP + j];
+        dst = first ? tot : dst + tot;
+      }
     }
     first = false;
   }
@@ -448,7 +492,33 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
   for (int r0 = 0; r0 < nrows; r0 += R3C) {
     const int rn = min(R3C, nrows - r0);
     __syncthreads();
-    for (int i = threadIdx.x; i < rn * RP; i += blockDim.x) s_ph[i] = a.Phat[L.p_off + (int64_t)(row0 + r0) * RP + i];
+    if constexpr (Cfg<RP>::FUSE_PH) {
+      // Phat rows = P rows R^-1 by forward substitution (float64); the tile of
+      // segment 0, worker 0 also stores them
+      const double* Rr = a.rinv + L.rinv_off;
+      const bool store = (seg == 0 && w == 0);
+      for (int i = threadIdx.x; i < rn; i += blockDim.x) {
+        const int64_t row = row0 + r0 + i;
+        double x[RP];
+#pragma unroll
+        for (int k = 0; k < RP; ++k) x[k] = (double)a.P[L.p_off + row * RP + k];
+#pragma unroll
+        for (int k = 0; k < RP; ++k) {
+          double sum = x[k];
+#pragma unroll
+          for (int j = 0; j < k; ++j) sum = fma(-x[j], __ldg(Rr + j * RP + k), sum);
+          x[k] = sum * __ldg(Rr + RP * RP + k);
+        }
+#pragma unroll
+        for (int k = 0; k < RP; ++k) {
+          const float v = (float)x[k];
+          s_ph[i * RP + k] = v;
+          if (store) a.Phat[L.p_off + row * RP + k] = v;
+        }
+      }
+    } else {
+      for (int i = threadIdx.x; i < rn * RP; i += blockDim.x) s_ph[i] = a.Phat[L.p_off + (int64_t)(row0 + r0) * RP + i];
+    }
     __syncthreads();
     // warps take interleaved groups of UNR rows of the chunk
     for (int i0 = warp * UNR; i0 < rn; i0 += NW * UNR) {

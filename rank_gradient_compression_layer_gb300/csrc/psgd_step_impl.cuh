@@ -58,7 +58,7 @@ cudaError_t prepare() {
 
 }  // namespace
 
-extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {kRP, launch, launch_error, prepare, Cfg<kRP>::R1,
-                                                       Cfg<kRP>::RU};
+extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {kRP,          launch,       launch_error,      prepare,
+                                                       Cfg<kRP>::R1, Cfg<kRP>::RU, Cfg<kRP>::FUSE_PH};
 
 }  // namespace psgd

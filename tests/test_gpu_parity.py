@@ -250,7 +250,7 @@ def test_phase_timing():
         assert set(t) == {"project", "orthonormalise", "back_project", "decompress"}
         assert all(v >= 0.0 for v in t.values()) and t["project"] > 0.0
         s = run.ctx.stats()
-        assert s["launches_per_step"] == 4 and s["tiles"]["project"] > 0
+        assert s["launches_per_step"] in (3, 4) and s["tiles"]["project"] > 0
     finally:
         run.close()
 
