@@ -55,6 +55,9 @@ def kernel_sources_hash() -> str:
 def config_of(name: str) -> workloads.Workload:
     if name.startswith("c5r"):
         return workloads.c5_rank_sweep(int(name[3:]))
+    if name.startswith("c2x"):  # the ResNet-18 set repeated k times (a larger model of the same shapes)
+        base = workloads.c2_resnet18()
+        return workloads.scaled(base, list(base.layers) * int(name[3:]), name=f"resnet18x{name[3:]}_r2_w4")
     return workloads.ALL[name]()
 
 

@@ -80,12 +80,15 @@ typedef struct {
   int64_t tiles[4];                     /* CTAs of the project, orthonormalise, back-project, decompress kernels */
   int32_t kernel_rank;                  /* rank the kernels were compiled for (r rounded up to 1,2,4,8,16,32) */
   int32_t launches_per_step;            /* kernels one psgd_step enqueues (with an update) */
+  int32_t tile_rows[3];                 /* rows per tile: project, back-project (least), decompress */
+  int32_t reserved;
 } psgd_stats;
 
 /* Optional knobs of psgd_create_ex (zero-initialise, then set what you need). */
 typedef struct {
   int32_t timing;       /* 1: time every phase of every step with CUDA events (psgd_get_phase_times) */
-  int32_t reserved[3];
+  int32_t project_rows; /* rows per project tile (0: chosen so the grid holds several waves of CTAs) */
+  int32_t reserved[2];
 } psgd_options;
 
 /*
@@ -152,9 +155,10 @@ int psgd_set_state(psgd_ctx* ctx, int layer, const float* Q, const float* const*
 int psgd_get_stats(const psgd_ctx* ctx, psgd_stats* out);
 
 /*
- * Device time of each phase of the last step, in milliseconds: project,
- * orthonormalise, back-project, decompress (ms[4]).  Needs options.timing = 1;
- * waits for the stream.
+ * Device time of each phase, in milliseconds, averaged over the steps since
+ * the previous call (the last 256 at most): project, orthonormalise,
+ * back-project, decompress (ms[4]).  Needs options.timing = 1; waits for the
+ * stream.  Each timed step records five CUDA events on the stream.
  */
 int psgd_get_phase_times(psgd_ctx* ctx, float* ms);
 

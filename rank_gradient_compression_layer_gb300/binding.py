@@ -49,11 +49,13 @@ class Stats(ctypes.Structure):
         ("tiles", ctypes.c_int64 * 4),
         ("kernel_rank", ctypes.c_int32),
         ("launches_per_step", ctypes.c_int32),
+        ("tile_rows", ctypes.c_int32 * 3),
+        ("reserved", ctypes.c_int32),
     ]
 
 
 class Options(ctypes.Structure):
-    _fields_ = [("timing", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+    _fields_ = [("timing", ctypes.c_int32), ("project_rows", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -154,7 +156,7 @@ class PowerSGD:
     """
 
     def __init__(self, shapes: Sequence[Tuple[int, int]], rank: int, workers: int, seed: int = 0,
-                 stream=None, timing: bool = False):
+                 stream=None, timing: bool = False, project_rows: int = 0):
         import torch
 
         if not torch.cuda.is_available():
@@ -164,7 +166,7 @@ class PowerSGD:
         self.device = torch.device("cuda", torch.cuda.current_device())
         self._stream = stream
         n, m = _shapes(self.shapes)
-        opt = Options(int(bool(timing)))
+        opt = Options(int(bool(timing)), int(project_rows))
         h = _P()
         _check(lib().psgd_create_ex(ctypes.byref(h), len(self.shapes), n, m, self.rank, self.workers,
                                     ctypes.c_uint64(self.seed), _stream_ptr(stream), ctypes.byref(opt)))
@@ -264,6 +266,7 @@ class PowerSGD:
         _check(lib().psgd_get_stats(self._h, ctypes.byref(s)))
         out = {f: getattr(s, f) for f, _ in Stats._fields_}
         out["tiles"] = dict(zip(PHASES, list(s.tiles)))
+        out["tile_rows"] = list(s.tile_rows)
         return out
 
     def phase_times(self) -> dict:

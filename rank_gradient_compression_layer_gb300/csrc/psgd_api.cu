@@ -160,9 +160,11 @@ struct psgd_ctx {
   float* e_scratch = nullptr;
   int64_t e_scratch_elems = 0;
   float *stage_G = nullptr, *stage_U = nullptr, *stage_msg = nullptr;
-  // optional phase timing
+  // optional phase timing: one set of kPhases + 1 events per step, in a ring
   bool timing = false;
-  cudaEvent_t ev[kPhases + 1] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  std::vector<cudaEvent_t> ev;  // kTimedSteps x (kPhases + 1)
+  int64_t timed_since = 0;      // steps recorded since the last psgd_get_phase_times
+  int tile_rows[3] = {0, 0, 0};  // project rows, least back-project rows, decompress rows
   int has_prev = 0;
   bool broken = false;
   // stats
@@ -179,6 +181,7 @@ void free_all(psgd_ctx* c) {
     if (p) cudaFree(p);
   for (cudaEvent_t e : c->ev)
     if (e) cudaEventDestroy(e);
+  c->ev.clear();
 }
 
 template <class T>
@@ -192,21 +195,31 @@ int dalloc(T** p, int64_t count, const char* what) {
   return PSGD_OK;
 }
 
+// Per-context tile sizes.  The phase grids must hold several waves of
+// resident CTAs, or the last, partly filled wave leaves HBM idle: rows per
+// tile shrink (down to a floor) until every phase has >= kWaves waves.
+struct TileRows {
+  int r1 = 32, r3min = 256, ru = 64;
+};
+
+constexpr int kWaves = 4;
+
 // Tiling of one matrix layer for padded rank rp and W workers.  Returns the
 // number of counters the layer needs and sets its counter offsets relative
 // to cnt_off.
-int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp, int W, const KernelSet& ks) {
+int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp, int W, const TileRows& tr) {
   L.n = (int32_t)n;
   L.m = (int32_t)m;
   L.ld = (int32_t)ld;
   L.F = (int32_t)(ld / 4);
   L.S = (int32_t)ceil_div(L.F, kSeg);
   L.tail = (int32_t)(m - 4 * (L.F - 1));
-  L.nrb = (int32_t)ceil_div(n, ks.r1);
+  L.r1 = tr.r1;
+  L.nrb = (int32_t)ceil_div(n, L.r1);
+  L.ru = tr.ru;
   L.g1 = (int32_t)ceil_div(L.nrb, kGramGroup);
-  // back-project: at most 16 row tiles (the Q partial sums stay short), at
-  // least 256 rows per tile
-  const int64_t r3 = std::max<int64_t>(std::max(256, 32 * rp), ceil_div(n, 16));
+  // back-project: at most 16 row tiles (the Q partial sums stay short)
+  const int64_t r3 = std::max<int64_t>(std::max(tr.r3min, 8 * rp), ceil_div(n, 16));
   L.r3 = (int32_t)std::min<int64_t>(n, r3);
   L.t3r = (int32_t)ceil_div(n, L.r3);
   L.c_gram = 0;
@@ -215,6 +228,44 @@ int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp, int W
   L.c_p3 = L.c_qs + L.S;
   L.c_rb = L.c_p3 + L.S * W;
   return (int64_t)L.c_rb + (L.S > 1 ? L.nrb : 0);
+}
+
+// Chooses the tile rows of a layer set so that each phase grid is at least
+// kWaves waves of resident CTAs (or the rows reach their floor); decompress
+// tiles keep their size (their cost is the per-tile set-up, not the tail).
+int choose_tile_rows(const std::vector<int64_t>& n, const std::vector<int64_t>& m, int rp, int W,
+                     const KernelSet& ks, int device, TileRows* tr) {
+  int sms = 0, c1 = 0, c3 = 0, cu = 0;
+  CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
+  CUDA_TRY(ks.occupancy(kProject, W, &c1));
+  CUDA_TRY(ks.occupancy(kBackProject, W, &c3));
+  CUDA_TRY(ks.occupancy(kDecompress, W, &cu));
+  auto count = [&](int r1, int r3min, int ru, int64_t* t1, int64_t* t3, int64_t* tu) {
+    *t1 = *t3 = *tu = 0;
+    for (size_t l = 0; l < n.size(); ++l) {
+      if (m[l] == 0) continue;
+      const int64_t S = ceil_div(ceil_div(m[l], 4), kSeg);
+      const int64_t r3 = std::min<int64_t>(n[l], std::max<int64_t>(std::max(r3min, 8 * rp), ceil_div(n[l], 16)));
+      *t1 += ceil_div(n[l], r1) * S;
+      *t3 += ceil_div(n[l], r3) * S * W;
+      *tu += ceil_div(n[l], ru) * S;
+    }
+  };
+  int64_t t1, t3, tu;
+  TileRows r;
+  r.r1 = ks.r1;
+  r.ru = ks.ru;
+  count(r.r1, r.r3min, r.ru, &t1, &t3, &tu);
+  while (t1 < (int64_t)kWaves * c1 * sms && r.r1 > ks.rsb) {
+    r.r1 /= 2;
+    count(r.r1, r.r3min, r.ru, &t1, &t3, &tu);
+  }
+  while (t3 < (int64_t)kWaves * c3 * sms && r.r3min > 32) {
+    r.r3min /= 2;
+    count(r.r1, r.r3min, r.ru, &t1, &t3, &tu);
+  }
+  *tr = r;
+  return PSGD_OK;
 }
 
 // Tiles of every phase.  Back-project walks the layers and rows in the
@@ -229,7 +280,7 @@ void build_tiles(psgd_ctx* c) {
       for (int s = 0; s < L.S; ++s) c->tiles[kProject].push_back({li, rb, s, 0});
     if (!c->ks->fuse_ph)
       for (int t = 0; t < (int)ceil_div(L.n, kPHThreads); ++t) c->tiles[kOrthonormalise].push_back({li, t, 0, 0});
-    for (int rb = 0; rb < (int)ceil_div(L.n, c->ks->ru); ++rb)
+    for (int rb = 0; rb < (int)ceil_div(L.n, L.ru); ++rb)
       for (int s = 0; s < L.S; ++s) c->tiles[kDecompress].push_back({li, rb, s, 0});
   }
   for (int li = nm - 1; li >= 0; --li) {
@@ -241,6 +292,8 @@ void build_tiles(psgd_ctx* c) {
   for (int vi = 0; vi < (int)c->hv.size(); ++vi)
     for (int t = 0; t < (int)ceil_div(c->hv[vi].n, kVChunk); ++t) c->tiles[kDecompress].push_back({vi, t, 0, 1});
 }
+
+constexpr int kTimedSteps = 256;  // steps whose phase times one psgd_get_phase_times can average
 
 int ctx_ok(const psgd_ctx* c) {
   if (!c) return fail(PSGD_ERR_INVALID, "context is NULL");
@@ -345,6 +398,21 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
 
   const int rp = c->rp;
   const int NG = rp * (rp + 1) / 2;
+  TileRows tr;
+  if ((rc = choose_tile_rows(c->n, c->m, rp, c->W, *c->ks, c->device, &tr))) {
+    delete c;
+    return rc;
+  }
+  if (opt && opt->project_rows > 0) {
+    if (opt->project_rows > c->ks->r1 || opt->project_rows % c->ks->rsb != 0) {
+      delete c;
+      return fail(PSGD_ERR_INVALID, "project_rows must be a multiple of %d and <= %d", c->ks->rsb, c->ks->r1);
+    }
+    tr.r1 = opt->project_rows;
+  }
+  c->tile_rows[0] = tr.r1;
+  c->tile_rows[1] = tr.r3min;
+  c->tile_rows[2] = tr.ru;
   for (int l = 0; l < num_layers; ++l) {
     if (m[l] == 0) {
       c->hv.push_back({c->off[l], (int32_t)n[l], 0});
@@ -355,7 +423,7 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     }
     LayerDev L;
     std::memset(&L, 0, sizeof(L));
-    const int64_t ncnt = plan_matrix(L, n[l], m[l], c->ld[l], rp, c->W, *c->ks);
+    const int64_t ncnt = plan_matrix(L, n[l], m[l], c->ld[l], rp, c->W, tr);
     L.off = c->off[l];
     L.index = l;
     L.p_off = c->p_total;
@@ -409,8 +477,10 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   auto setup = [&]() -> int {
     cudaStream_t s = c->stream;
     CUDA_TRY(c->ks->prepare());
-    if (c->timing)
+    if (c->timing) {
+      c->ev.assign((size_t)kTimedSteps * (kPhases + 1), nullptr);
       for (auto& e : c->ev) CUDA_TRY(cudaEventCreate(&e));
+    }
     CUDA_TRY(cudaMemsetAsync(c->B, 0, (size_t)W * c->total * sizeof(float), s));
     CUDA_TRY(cudaMemsetAsync(c->Phat, 0, (size_t)std::max<int64_t>(c->p_total, 1) * sizeof(float), s));
     CUDA_TRY(cudaMemsetAsync(c->Qbar, 0, (size_t)std::max<int64_t>(c->q_total, 1) * sizeof(float), s));
@@ -490,7 +560,12 @@ int psgd_step(psgd_ctx* c, const float* const* grad_ptrs, float* out_update) {
   a.W = c->W;
   a.has_prev = c->has_prev;
   const int phases = out_update ? kPhases : kPhases - 1;  // the decompress phase only writes U
-  if (c->timing) CUDA_TRY(cudaEventRecord(c->ev[0], c->stream));
+  cudaEvent_t* ev = nullptr;
+  if (c->timing) {
+    ev = &c->ev[(size_t)(c->timed_since % kTimedSteps) * (kPhases + 1)];
+    c->timed_since += 1;
+    CUDA_TRY(cudaEventRecord(ev[0], c->stream));
+  }
   for (int ph = 0; ph < kPhases; ++ph) {
     if (ph < phases) {
       a.tiles = c->d_tiles[ph];
@@ -500,7 +575,7 @@ int psgd_step(psgd_ctx* c, const float* const* grad_ptrs, float* out_update) {
         return cuda_fail(e, "phase kernel launch");
       }
     }
-    if (c->timing) CUDA_TRY(cudaEventRecord(c->ev[ph + 1], c->stream));
+    if (ev) CUDA_TRY(cudaEventRecord(ev[ph + 1], c->stream));
   }
   c->has_prev = 1;
   c->steps += 1;
@@ -518,8 +593,21 @@ int psgd_get_phase_times(psgd_ctx* c, float* ms) {
   if (rc) return rc;
   if (!ms) return fail(PSGD_ERR_INVALID, "ms must not be NULL");
   if (!c->timing) return fail(PSGD_ERR_INVALID, "phase timing is off (psgd_options.timing)");
+  if (c->timed_since == 0) return fail(PSGD_ERR_INVALID, "no step since the last call");
   if ((rc = sync_and_check(c))) return rc;
-  for (int ph = 0; ph < kPhases; ++ph) CUDA_TRY(cudaEventElapsedTime(&ms[ph], c->ev[ph], c->ev[ph + 1]));
+  const int64_t nsteps = std::min<int64_t>(c->timed_since, kTimedSteps);
+  const int64_t first = c->timed_since - nsteps;
+  for (int ph = 0; ph < kPhases; ++ph) ms[ph] = 0.f;
+  for (int64_t t = first; t < c->timed_since; ++t) {
+    const cudaEvent_t* ev = &c->ev[(size_t)(t % kTimedSteps) * (kPhases + 1)];
+    for (int ph = 0; ph < kPhases; ++ph) {
+      float x = 0.f;
+      CUDA_TRY(cudaEventElapsedTime(&x, ev[ph], ev[ph + 1]));
+      ms[ph] += x;
+    }
+  }
+  for (int ph = 0; ph < kPhases; ++ph) ms[ph] /= (float)nsteps;
+  c->timed_since = 0;
   return PSGD_OK;
 }
 
@@ -645,6 +733,7 @@ int psgd_get_stats(const psgd_ctx* c, psgd_stats* out) {
   out->buffer_elements = c->total;
   for (int ph = 0; ph < kPhases; ++ph) out->tiles[ph] = (int64_t)c->tiles[ph].size();
   out->kernel_rank = c->rp;
+  for (int i = 0; i < 3; ++i) out->tile_rows[i] = c->tile_rows[i];
   out->launches_per_step = c->ks->fuse_ph ? kPhases - 1 : kPhases;
   return PSGD_OK;
 }

@@ -20,8 +20,11 @@ struct KernelSet {
                        cudaStream_t s);
   // one-time set-up (shared memory limits)
   cudaError_t (*prepare)();
-  // tile geometry: project rows per tile, decompress rows per tile
-  int r1, ru;
+  // resident CTAs per SM of a phase kernel for W workers
+  cudaError_t (*occupancy)(int phase, int W, int* ctas_per_sm);
+  // tile geometry: most project rows per tile, most decompress rows per tile,
+  // rows per project pass
+  int r1, ru, rsb;
   // back-project tiles form the Phat rows (no orthonormalise launch)
   bool fuse_ph;
 };

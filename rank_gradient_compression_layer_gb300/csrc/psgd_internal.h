@@ -32,7 +32,8 @@ struct LayerDev {
   int32_t S;         // segments of kSeg float4 per row
   int32_t tail;      // valid floats in the last float4 of a row (1..4)
   int32_t index;     // position of the layer in the caller's layer list
-  int32_t nrb;       // project row blocks (R1 rows each)
+  int32_t r1, nrb;   // project rows per tile (<= Cfg::R1), row blocks
+  int32_t ru;        // decompress rows per tile (<= Cfg::RU)
   int32_t g1;        // Gram groups (kGramGroup row blocks each)
   int32_t r3, t3r;   // back-project rows per tile, row tiles
   int64_t p_off;      // P and Phat: n x RP (16-byte aligned)

@@ -248,8 +248,8 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
   const Tile t = a.tiles[blockIdx.x];
   const LayerDev& L = a.layers[t.layer];
   const int rb = t.a, seg = t.b;
-  const int row0 = rb * R1;
-  const int rcnt = min(R1, L.n - row0);
+  const int row0 = rb * L.r1;
+  const int rcnt = min(L.r1, L.n - row0);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int c = seg * kSeg + lane;  // this lane's float4 column
   const bool act = c < L.F;
@@ -584,8 +584,8 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
     return;
   }
   const LayerDev& L = a.layers[t.layer];
-  const int row0 = t.a * RU, seg = t.b;
-  const int rcnt = min(RU, L.n - row0);
+  const int row0 = t.a * L.ru, seg = t.b;
+  const int rcnt = min(L.ru, L.n - row0);
   for (int i = threadIdx.x; i < rcnt * RP; i += blockDim.x) s_ph[i] = __ldg(a.Phat + L.p_off + (int64_t)row0 * RP + i);
   __syncthreads();
   const int lane = threadIdx.x & 31, sub = threadIdx.x >> 5;  // 8 rows in flight per pass

@@ -56,9 +56,26 @@ cudaError_t prepare() {
   return e;
 }
 
+cudaError_t occupancy(int phase, int W, int* ctas) {
+  switch (phase) {
+    case kProject: {
+      const int warps = W < Cfg<kRP>::P1_WARPS ? W : Cfg<kRP>::P1_WARPS;
+      const size_t qw = (size_t)W * kSegQ;
+      const size_t dyn = kSegQ + (qw <= (size_t)Cfg<kRP>::QW_STAGE_BYTES ? qw : 0);
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p1_kernel<kRP>, 32 * warps, dyn);
+    }
+    case kBackProject:
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p3_kernel<kRP>, kP3Threads, kP3Dyn);
+    case kDecompress:
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, u_kernel<kRP>, kUThreads, 0);
+    default:
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, ph_kernel<kRP>, kPHThreads, 0);
+  }
+}
+
 }  // namespace
 
-extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {kRP,          launch,       launch_error,      prepare,
-                                                       Cfg<kRP>::R1, Cfg<kRP>::RU, Cfg<kRP>::FUSE_PH};
+extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {
+    kRP, launch, launch_error, prepare, occupancy, Cfg<kRP>::R1, Cfg<kRP>::RU, Cfg<kRP>::RSB, Cfg<kRP>::FUSE_PH};
 
 }  // namespace psgd
