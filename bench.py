@@ -37,9 +37,9 @@ import workloads  # noqa: E402
 METRIC = "gradient GB/s compressed per PowerSGD step (1 GB300) and % of HBM roofline"
 UNIT = "GB/s"
 
-# DRAM bytes (read + write) of one step-kernel launch on the ResNet-18 workload,
-# from an ncu capture (see profiles/), valid only for the kernel sources whose
-# hash is recorded with it.
+# DRAM bytes (read + write) of one project-kernel launch per workload, from an
+# ncu capture (see profiles/), valid only for the kernel sources whose hash is
+# recorded with it.
 NCU_TRAFFIC = {}  # {config: (sources_sha256_prefix, bytes_per_launch)}
 
 
@@ -261,42 +261,46 @@ def run_ours(args, ws, rank, local):
     torch.cuda.set_device(device)
     cfg = config_of(args.config)
     stream = torch.cuda.Stream(device=device)
-    ctx = PowerSGD(cfg.layers, cfg.rank, cfg.workers, seed=cfg.seed, stream=stream)
+    ctx = PowerSGD(cfg.layers, cfg.rank, cfg.workers, seed=cfg.seed, stream=stream, timing=True)
     sets = 3
     grads = fill_gradients(ctx, cfg, sets, device)
     upd = ctx.empty_buffer()
     ab = algorithmic_bytes(cfg, with_update=True)
     comp = compressed_bytes(cfg)
+    st = ctx.stats()
 
     # warm-up
     for i in range(args.warmup):
         ctx.step(grads[i % sets], upd)
     ctx.sync()
+    ctx.phase_times()  # restart the per-phase averages at the timed region
     barrier(ws)
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
     sampler.start()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        ev[0].record(stream)
-        for i in range(args.steps):
-            ctx.step(grads[i % sets], upd)
-            ev[i + 1].record(stream)
+    ev0.record(stream)
+    for i in range(args.steps):
+        ctx.step(grads[i % sets], upd)
+    ev1.record(stream)
     ctx.sync()
     torch.cuda.synchronize()
     barrier(ws)
     clocks = sampler.stop()
-    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
+    phases = ctx.phase_times()  # device ms per phase, averaged over the timed steps
+    total_ms = ev0.elapsed_time(ev1)
     total_ms = max_over_ranks(total_ms, ws, device)
     ms_per_step = total_ms / args.steps
     value = comp * ws / (ms_per_step * 1e-3) / 1e9
-    launch_ms = statistics.mean(per)
     peaks = measured_peaks()
-    achieved = ab["total"] / (launch_ms * 1e-3) / 1e9
+    project_ms = phases["project"]
+    project_bytes = ab["core"]  # read G, read E, write E of every worker (+ the factors)
+    achieved = project_bytes / (project_ms * 1e-3) / 1e9
+    step_achieved = ab["total"] / (ms_per_step * 1e-3) / 1e9
     h = kernel_sources_hash()
     traffic = None
     if args.config in NCU_TRAFFIC and NCU_TRAFFIC[args.config][0] == h:
@@ -313,15 +317,19 @@ def run_ours(args, ws, rank, local):
                    "simulated per GPU)",
                    "l2": "inputs larger than L2: 3 rotating gradient sets of "
                          f"{comp / 1e6:.1f} MB + error buffers {comp / 1e6:.1f} MB per step",
-                   "seed": cfg.seed, "out_update": True},
+                   "seed": cfg.seed, "out_update": True, "tile_rows": st["tile_rows"]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
+                     "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
                      else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": ab["total"], "kernel": "psgd::step_kernel<2>",
-                     "launch_ms": round(launch_ms, 5), "kernel_sources": h},
+                     "kernel": f"psgd::p1_kernel<{st['kernel_rank']}> (project: error add, E write, P = M Q)",
+                     "algorithmic_bytes_per_launch": project_bytes, "launch_ms": round(project_ms, 5),
+                     "kernel_sources": h},
+        "step_roofline": {"achieved": round(step_achieved, 1), "frac": round(step_achieved / peaks["hbm_gbs"], 4),
+                          "algorithmic_bytes_per_step": ab["total"],
+                          "phase_ms": {k: round(v, 5) for k, v in phases.items()}},
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * st["launches_per_step"],
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -233,30 +233,32 @@ def gradients(w: Workload, step: int, signals: dict | None = None) -> List[List[
 # --------------------------------------------------------------------------
 
 def device_gradient_matrix(w: Workload, layer: int, step: int, worker: int, device, out=None):
-    """One matrix gradient generated with torch on ``device`` (float32).
+    """One matrix gradient generated on ``device`` (float32).
 
     Same recipe as :func:`gradients` (low-rank signal with orthonormal factors
-    plus Gaussian noise), drawn with torch's seeded generator so that the
-    multi-GB configurations need no host round trip.  Returns a (n, m) tensor,
-    or writes into ``out`` (a (n, m) view) when given.
+    plus Gaussian noise): the thin factors come from a seeded numpy QR (small,
+    n x k and m x k), the n x m noise is drawn on the device with torch's
+    seeded generator, so the multi-GB configurations need no large host round
+    trip.  Returns a (n, m) tensor, or writes into ``out`` (a (n, m) view).
     """
     import torch
 
     n, m = w.layers[layer]
-    sig = torch.as_tensor(np.asarray(w.sigma(n, m), dtype=np.float64), device=device, dtype=torch.float32)
-    k = min(sig.numel(), n, m)
-    g = torch.Generator(device=device)
-    g.manual_seed((w.seed * 1_000_003 + layer) & 0x7FFFFFFFFFFF)
-    U, _ = torch.linalg.qr(torch.randn(n, k, generator=g, device=device))
-    V, _ = torch.linalg.qr(torch.randn(m, k, generator=g, device=device))
-    S = (U * sig[:k]) @ V.T
-    s_fro = float(torch.linalg.norm(sig[:k]))
-    g.manual_seed(((w.seed * 1_000_003 + layer) * 7919 + step * 131 + worker + 1) & 0x7FFFFFFFFFFF)
+    sig = np.asarray(w.sigma(n, m), dtype=np.float64)
+    k = min(len(sig), n, m)
+    g = _rng(w.seed, 5, layer)
+    U, _ = np.linalg.qr(g.standard_normal((n, k)))
+    V, _ = np.linalg.qr(g.standard_normal((m, k)))
+    Ud = torch.as_tensor((U * sig[:k]).astype(np.float32), device=device)
+    Vd = torch.as_tensor(V.astype(np.float32), device=device)
+    s_fro = float(np.linalg.norm(sig[:k]))
+    gen = torch.Generator(device=device)
+    gen.manual_seed(((w.seed * 1_000_003 + layer) * 7919 + step * 131 + worker + 1) & 0x7FFFFFFFFFFF)
     std = w.noise_rel * s_fro / math.sqrt(n * m) if w.noise == "gaussian_rel" else w.noise_abs
     if out is None:
         out = torch.empty(n, m, device=device, dtype=torch.float32)
-    out.normal_(0.0, std, generator=g)
-    out.add_(S)
+    out.normal_(0.0, std, generator=gen)
+    out.add_(Ud @ Vd.T)
     return out
 
 
