@@ -173,6 +173,14 @@ def barrier(ws: int):
         dist.barrier()
 
 
+def replica_throughput(comp_bytes: float, steps: int, local_ms: float, ws: int, device=None):
+    """(ms per step, whole-job GB/s) of ws replicas that each compressed
+    comp_bytes per step: the job lasts as long as its slowest rank."""
+    total_ms = max_over_ranks(local_ms, ws, device)
+    ms_per_step = total_ms / steps
+    return ms_per_step, comp_bytes * ws / (ms_per_step * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing (the reference arm and the cpu_baseline leg)
 # ---------------------------------------------------------------------------
@@ -292,10 +300,7 @@ def run_ours(args, ws, rank, local):
     barrier(ws)
     clocks = sampler.stop()
     phases = ctx.phase_times()  # device ms per phase, averaged over the timed steps
-    total_ms = ev0.elapsed_time(ev1)
-    total_ms = max_over_ranks(total_ms, ws, device)
-    ms_per_step = total_ms / args.steps
-    value = comp * ws / (ms_per_step * 1e-3) / 1e9
+    ms_per_step, value = replica_throughput(comp, args.steps, ev0.elapsed_time(ev1), ws, device)
     peaks = measured_peaks()
     project_ms = phases["project"]
     project_bytes = ab["core"]  # read G, read E, write E of every worker (+ the factors)

@@ -273,6 +273,10 @@ def test_splitmix64_stream_matches_counter_form():
         return z
     for v in [0, 1, 12345, O.MASK64, 0x0123456789ABCDEF]:
         assert unmix(O.splitmix64_mix(v)) == v
+    # the first outputs of the generator's public reference code (Vigna's
+    # splitmix64.c) seeded with 0
+    assert O.splitmix64_stream(0, 4) == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4,
+                                         0x06C45D188009454F, 0xF88BB8A8724C81EC]
     assert O.uniform_open0(0) == 2.0 ** -53
     assert O.uniform_open0(O.MASK64) == 1.0
 
