@@ -167,6 +167,70 @@ int psgd_layer_info(const psgd_ctx* ctx, int layer, int64_t* offset, int64_t* n,
                     int64_t* ld);
 
 /*
+ * psgd_step_noalloc -- one step of ONE matrix layer that allocates nothing.
+ *
+ * The method itself has no such call; it exists for callers that cannot let
+ * a library allocate device memory: a framework that sizes one arena for all
+ * of its device memory at start-up (a library cudaMalloc would sit outside
+ * the arena and may fail once the arena owns the GPU), or a training loop
+ * that must not call cudaMalloc/cudaFree between steps because those calls
+ * can synchronise the whole device.  psgd_create allocates the state and
+ * scratch of a context; this call takes the state from the caller and keeps
+ * its scratch in one fixed device array of PSGD_NOALLOC_SCRATCH_BYTES that is
+ * part of the library's device image.  Neither it nor anything it calls
+ * allocates memory (host or device).
+ *
+ * The arithmetic is the step of the header comment for one n x m layer and
+ * W = num_workers workers, run by the same kernels and tiling as psgd_step on
+ * a one-layer context, so both give the same results.
+ *
+ * Arguments (all device pointers 16-byte aligned, float32, row-major,
+ * ld = m rounded up to a multiple of 4, r = rank):
+ *   rank        1, 2, 4, 8, 16 or 32, and <= min(n, m);  1 <= num_workers <= 64
+ *   grad_ptrs   host array of W device pointers, each an n x ld gradient
+ *               (the ld - m padding columns are ignored)
+ *   B           device, W x n x ld, caller-owned error state:
+ *                 has_prev == 0: B_w is the error E_w to add (zeros at the
+ *                                start); Phat and Qw are not read;
+ *                 has_prev != 0: B_w, Phat and Qw are what the previous call
+ *                                left, and E_w = B_w - Phat Qw_w^T.
+ *               On return B_w holds M_w, so the new error is B_w - Phat Qw_w^T.
+ *   Phat        device, n x r: out, the orthonormal P (state for the next call)
+ *   Qbar        device, ld x r: in, the warm-start Q (rows m..ld-1 must be
+ *               zero); out, Qbar = mean_w Q_w (the next call's warm start;
+ *               padding rows stay zero)
+ *   Qw          device, W x ld x r: out, Q_w of every worker (state)
+ *   out_update  device, n x ld: out, U = Phat Qbar^T (padding columns 0), or NULL
+ *   has_prev    0 on the first call of a run, 1 after that (see B)
+ *   cuda_stream where the work is enqueued (a cudaStream_t, NULL = legacy default)
+ * Asynchronous: returns after enqueueing (five kernel launches, four without
+ * out_update); a device error shows at the caller's next synchronisation.
+ *
+ * Limits and errors: PSGD_ERR_INVALID, with nothing enqueued, for a bad
+ * argument or a layer whose scratch would exceed PSGD_NOALLOC_SCRATCH_BYTES
+ * (8 MiB; the bulk is W x (row tiles, at most 16) x ld x r x 4 bytes of
+ * partial Q_w plus (row blocks) x ld x 32 x r bytes of partial P rows, the
+ * tile counts chosen by occupancy as for a context: the largest ResNet-18
+ * layer, 512 x 4608 at r = 2 with 4 workers, fits, an 8192 x 8192 layer at
+ * r = 4 with 8 workers does not -- use a context for those);
+ * PSGD_ERR_CUDA when a CUDA call fails.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) and sets the kernels' shared-memory limits; make that
+ * first call before any stream capture.  Later calls only enqueue work.
+ *
+ * Concurrency: every call on a device uses the same scratch array.  Two calls
+ * whose work overlaps on the device (different streams, or host threads,
+ * without ordering between them) race on it and give wrong results; order
+ * them on one stream or with events.  The counters in the scratch are cleared
+ * by every call itself before its kernels run.
+ */
+#define PSGD_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers,
+                      const float* const* grad_ptrs, float* B, float* Phat, float* Qbar,
+                      float* Qw, float* out_update, int has_prev, void* cuda_stream);
+
+/*
  * Host-only helpers (no GPU needed).  psgd_plan_layout fills offset[l] and
  * ld[l] (0 for vectors) of the packed layout and *total (floats per buffer).
  * psgd_count_sent gives the floats one worker sends per step with and without

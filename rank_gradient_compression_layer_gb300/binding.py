@@ -24,7 +24,7 @@ EXPORTS = (
     "psgd_create", "psgd_create_ex", "psgd_destroy", "psgd_set_stream", "psgd_step", "psgd_step_host",
     "psgd_sync", "psgd_get_PQ", "psgd_get_Qw", "psgd_get_error", "psgd_set_state", "psgd_get_stats",
     "psgd_layer_info", "psgd_plan_layout", "psgd_count_sent", "psgd_last_error", "psgd_version",
-    "psgd_get_phase_times",
+    "psgd_get_phase_times", "psgd_step_noalloc",
 )
 
 PHASES = ("project", "orthonormalise", "back_project", "decompress")
@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
         "psgd_last_error": ([], ctypes.c_char_p),
         "psgd_version": ([], ctypes.c_char_p),
         "psgd_get_phase_times": ([_P, ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
+        "psgd_step_noalloc": ([ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_P),
+                               _P, _P, _P, _P, _P, ctypes.c_int, _P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -278,3 +280,22 @@ class PowerSGD:
     @property
     def message_floats(self) -> int:
         return sum((n + m) * self.rank for n, m in self.shapes if m)
+
+
+# ------------------------------------------------------ no-allocation step --
+
+def step_noalloc(n: int, m: int, rank: int, grads: Sequence, B, Phat, Qbar, Qw, out_update=None,
+                 has_prev: bool = False, stream=None) -> None:
+    """One step of one n x m layer with caller-owned state; nothing is allocated.
+
+    ``grads`` holds one (n, ld) float32 device tensor per worker (ld = m
+    rounded up to 4); ``B`` (W, n, ld), ``Phat`` (n, rank), ``Qbar`` (ld,
+    rank) and ``Qw`` (W, ld, rank) are the state tensors and ``out_update``
+    an (n, ld) tensor or None; see psgd_step_noalloc in include/psgd.h for
+    what each holds before and after.  Asynchronous on ``stream`` (torch's
+    current stream by default).
+    """
+    W = len(grads)
+    arr = (_P * W)(*[_ptr(g) for g in grads])
+    _check(lib().psgd_step_noalloc(int(n), int(m), int(rank), W, arr, _ptr(B), _ptr(Phat), _ptr(Qbar), _ptr(Qw),
+                                   _ptr(out_update), 1 if has_prev else 0, _stream_ptr(stream)))
