@@ -170,6 +170,26 @@ def compress(M: Sequence[np.ndarray], Q: np.ndarray) -> Compressed:
 
 
 # --------------------------------------------------------------------------
+# The optimiser update after the step (section 提案手法, bullet 5: the
+# decompressed P Q^T drives a momentum SGD update, "EF-SGD with momentum")
+# --------------------------------------------------------------------------
+
+def momentum_update(x: np.ndarray, mom: np.ndarray, U: np.ndarray, lr: float, beta: float):
+    """One momentum-SGD update of the parameters ``x`` by the decompressed ``U``.
+
+    The page names the optimiser without its formula.  Reading taken:
+    heavy-ball momentum ``mom <- beta * mom + U`` and a Nesterov-style step
+    ``x <- x - lr * (U + mom)`` with the new ``mom``.  Element-wise, so it is
+    the same for a matrix layer's U and a vector layer's worker mean.
+    Returns ``(x_new, mom_new)`` in float64.
+    """
+    U = np.asarray(U, dtype=np.float64)
+    mom_new = beta * np.asarray(mom, dtype=np.float64) + U
+    x_new = np.asarray(x, dtype=np.float64) - lr * (U + mom_new)
+    return x_new, mom_new
+
+
+# --------------------------------------------------------------------------
 # The step with error feedback and warm start, over a whole layer set
 # --------------------------------------------------------------------------
 

@@ -288,6 +288,41 @@ def test_zero_gradient_step():
     assert all(np.all(E == 0) for E in st.E[0])
 
 
+def check_momentum_update(update):
+    rng = np.random.default_rng(9)
+    x0, U = rng.standard_normal((5, 3)), rng.standard_normal((5, 3))
+    lr = 0.1
+    # beta = 0: the step is x - 2 lr U and the momentum is U
+    x1, m1 = update(x0, np.zeros_like(x0), U, lr, 0.0)
+    np.testing.assert_allclose(m1, U, rtol=1e-15)
+    np.testing.assert_allclose(x1, x0 - 2 * lr * U, rtol=1e-14, atol=1e-15)
+    # constant U from zero momentum: closed forms of the geometric sums
+    beta, k = 0.9, 7
+    x, m = x0.copy(), np.zeros_like(x0)
+    for _ in range(k):
+        x, m = update(x, m, U, lr, beta)
+    np.testing.assert_allclose(m, U * (1 - beta ** k) / (1 - beta), rtol=1e-13)
+    summed = (k - beta * (1 - beta ** k) / (1 - beta)) / (1 - beta)  # sum of the k momenta / U
+    np.testing.assert_allclose(x, x0 - lr * U * (k + summed), rtol=1e-13, atol=1e-14)
+
+
+def test_momentum_update_closed_forms():
+    check_momentum_update(O.momentum_update)
+
+
+@pytest.mark.parametrize("kind", ["heavy_ball_step", "old_momentum_in_step", "sign"])
+def test_planted_momentum_mistakes_are_caught(kind):
+    def mutant(x, mom, U, lr, beta):
+        m_new = beta * mom + U
+        if kind == "heavy_ball_step":
+            return x - lr * m_new, m_new
+        if kind == "old_momentum_in_step":
+            return x - lr * (U + mom), m_new
+        return x + lr * (U + m_new), m_new
+    with pytest.raises(AssertionError):
+        check_momentum_update(mutant)
+
+
 # ------------------------------------------------- planted mistakes -----
 
 def _mutant_compress(kind):
