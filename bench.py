@@ -61,18 +61,21 @@ def config_of(name: str) -> workloads.Workload:
     return workloads.ALL[name]()
 
 
-def algorithmic_bytes(cfg: workloads.Workload, with_update: bool) -> dict:
+def algorithmic_bytes(cfg: workloads.Workload, with_update: bool, momentum: bool = False) -> dict:
     """Minimum HBM bytes of one step.
 
     Per matrix: every worker's gradient is read, its error buffer read and
     written (3 n m floats per worker), plus the factors Phat (n r) and Qbar
-    (m r) written; with an update, U (n m) written once.  Per vector: W reads
-    and one write when an update is produced.
+    (m r) written; with an update, U (n m) written once; with the fused
+    momentum update instead, params and momentum read and written (4 n m).
+    Per vector: W reads, plus one write (update) or two reads and two writes
+    (momentum update).
     """
     W, r = cfg.workers, cfg.rank
     core = sum(W * 3 * n * m * 4 + 4 * (n + m) * r for n, m in cfg.matrices)
-    upd = sum(4 * n * m for n, m in cfg.matrices) if with_update else 0
-    vec = sum(4 * (W + 1) * n for n, _ in cfg.vectors) if with_update else 0
+    per = 4 if momentum else (1 if with_update else 0)
+    upd = sum(4 * per * n * m for n, m in cfg.matrices)
+    vec = sum(4 * (W + per) * n for n, _ in cfg.vectors) if per else 0
     return {"core": core, "update": upd, "vectors": vec, "total": core + upd + vec}
 
 
@@ -273,13 +276,24 @@ def run_ours(args, ws, rank, local):
     sets = 3
     grads = fill_gradients(ctx, cfg, sets, device)
     upd = ctx.empty_buffer()
-    ab = algorithmic_bytes(cfg, with_update=True)
+    if args.momentum:
+        # the fused momentum-SGD update replaces the update write
+        params, mom = ctx.empty_buffer(), ctx.empty_buffer()
+        params.zero_()
+        mom.zero_()
+
+        def one_step(g):
+            ctx.step_momentum(g, params, mom, 1e-3, 0.9)
+    else:
+        def one_step(g):
+            ctx.step(g, upd)
+    ab = algorithmic_bytes(cfg, with_update=True, momentum=args.momentum)
     comp = compressed_bytes(cfg)
     st = ctx.stats()
 
     # warm-up
     for i in range(args.warmup):
-        ctx.step(grads[i % sets], upd)
+        one_step(grads[i % sets])
     ctx.sync()
     ctx.phase_times()  # restart the per-phase averages at the timed region
     barrier(ws)
@@ -293,7 +307,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     ev0.record(stream)
     for i in range(args.steps):
-        ctx.step(grads[i % sets], upd)
+        one_step(grads[i % sets])
     ev1.record(stream)
     ctx.sync()
     torch.cuda.synchronize()
@@ -322,7 +336,8 @@ def run_ours(args, ws, rank, local):
                    "simulated per GPU)",
                    "l2": "inputs larger than L2: 3 rotating gradient sets of "
                          f"{comp / 1e6:.1f} MB + error buffers {comp / 1e6:.1f} MB per step",
-                   "seed": cfg.seed, "out_update": True, "tile_rows": st["tile_rows"]},
+                   "seed": cfg.seed, "out_update": not args.momentum,
+                   "fused_momentum_update": bool(args.momentum), "tile_rows": st["tile_rows"]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                      "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
@@ -393,6 +408,8 @@ def main():
     ap.add_argument("--config", default="c2")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for the CPU leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--momentum", action="store_true",
+                    help="time psgd_step_momentum (step + fused momentum-SGD update) instead of psgd_step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

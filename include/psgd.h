@@ -120,6 +120,23 @@ int psgd_set_stream(psgd_ctx* ctx, void* cuda_stream);
 int psgd_step(psgd_ctx* ctx, const float* const* grad_ptrs, float* out_update);
 
 /*
+ * One step followed by the optimiser update it drives (PowerSGD review page,
+ * proposed method, bullet 5: the decompressed update feeds momentum SGD,
+ * "EF-SGD with momentum").  The page gives no formula; the reading taken is
+ * heavy-ball momentum with a Nesterov-style step, element-wise on every
+ * layer (U = Phat Qbar^T for a matrix, the worker mean for a vector):
+ *     momentum <- beta * momentum + U
+ *     params   <- params - lr * (U + momentum)
+ * params and momentum: device packed buffers (the gradient layout, 16-byte
+ * aligned), read and written in place by the decompress kernel; their row
+ * padding is left as it is.  out_update: as in psgd_step (may be NULL: the
+ * update then never goes to memory).  lr and beta must be finite.
+ * Asynchronous like psgd_step.
+ */
+int psgd_step_momentum(psgd_ctx* ctx, const float* const* grad_ptrs, float* params, float* momentum,
+                       float lr, float beta, float* out_update);
+
+/*
  * The same step fed from HOST memory: copies each worker's packed buffer
  * grad_host[w] (pinned host memory for an asynchronous copy) into device
  * staging buffers owned by the context (allocated on first use), runs

@@ -24,7 +24,7 @@ EXPORTS = (
     "psgd_create", "psgd_create_ex", "psgd_destroy", "psgd_set_stream", "psgd_step", "psgd_step_host",
     "psgd_sync", "psgd_get_PQ", "psgd_get_Qw", "psgd_get_error", "psgd_set_state", "psgd_get_stats",
     "psgd_layer_info", "psgd_plan_layout", "psgd_count_sent", "psgd_last_error", "psgd_version",
-    "psgd_get_phase_times", "psgd_step_noalloc",
+    "psgd_get_phase_times", "psgd_step_noalloc", "psgd_step_momentum",
 )
 
 PHASES = ("project", "orthonormalise", "back_project", "decompress")
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
         "psgd_set_stream": ([_P, _P], ctypes.c_int),
         "psgd_step": ([_P, ctypes.POINTER(_P), _P], ctypes.c_int),
         "psgd_step_host": ([_P, ctypes.POINTER(_P), _P, _P], ctypes.c_int),
+        "psgd_step_momentum": ([_P, ctypes.POINTER(_P), _P, _P, ctypes.c_float, ctypes.c_float, _P], ctypes.c_int),
         "psgd_sync": ([_P], ctypes.c_int),
         "psgd_get_PQ": ([_P, ctypes.c_int, _P, _P], ctypes.c_int),
         "psgd_get_Qw": ([_P, ctypes.c_int, ctypes.c_int, _P], ctypes.c_int),
@@ -219,6 +220,17 @@ class PowerSGD:
             raise ValueError(f"expected {self.workers} gradient buffers, got {len(grads)}")
         ptrs = (_P * self.workers)(*[_ptr(g) for g in grads])
         _check(lib().psgd_step(self._h, ptrs, _ptr(out_update)))
+
+    def step_momentum(self, grads: Sequence, params, momentum, lr: float, beta: float, out_update=None) -> None:
+        """One step, then momentum <- beta momentum + U; params <- params - lr (U + momentum).
+
+        ``params`` and ``momentum`` are packed device buffers, updated in place.
+        """
+        if len(grads) != self.workers:
+            raise ValueError(f"expected {self.workers} gradient buffers, got {len(grads)}")
+        ptrs = (_P * self.workers)(*[_ptr(g) for g in grads])
+        _check(lib().psgd_step_momentum(self._h, ptrs, _ptr(params), _ptr(momentum), float(lr), float(beta),
+                                        _ptr(out_update)))
 
     def step_host(self, grads_host: Sequence, msg_host, update_host=None) -> None:
         ptrs = (_P * self.workers)(*[_ptr(g) for g in grads_host])

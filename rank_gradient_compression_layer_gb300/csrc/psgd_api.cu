@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -438,7 +439,14 @@ int psgd_set_stream(psgd_ctx* c, void* cuda_stream) {
   return PSGD_OK;
 }
 
-int psgd_step(psgd_ctx* c, const float* const* grad_ptrs, float* out_update) {
+}  // extern "C"
+
+namespace {
+
+// One step; when X is not NULL the decompress phase also applies the
+// momentum-SGD update to X and Mom.
+int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, float* X, float* Mom, float lr,
+              float beta) {
   int rc = ctx_ok(c);
   if (rc) return rc;
   if (!grad_ptrs) return fail(PSGD_ERR_INVALID, "grad_ptrs must not be NULL");
@@ -467,7 +475,12 @@ int psgd_step(psgd_ctx* c, const float* const* grad_ptrs, float* out_update) {
   a.vecs = c->d_vecs;
   a.W = c->W;
   a.has_prev = c->has_prev;
-  const int phases = out_update ? kPhases : kPhases - 1;  // the decompress phase only writes U
+  a.X = X;
+  a.Mom = Mom;
+  a.lr = lr;
+  a.beta = beta;
+  // the decompress phase only writes U and the optional update
+  const int phases = (out_update || X) ? kPhases : kPhases - 1;
   cudaEvent_t* ev = nullptr;
   if (c->timing) {
     ev = &c->ev[(size_t)(c->timed_since % kTimedSteps) * (kPhases + 1)];
@@ -488,6 +501,23 @@ int psgd_step(psgd_ctx* c, const float* const* grad_ptrs, float* out_update) {
   c->has_prev = 1;
   c->steps += 1;
   return PSGD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int psgd_step(psgd_ctx* c, const float* const* grad_ptrs, float* out_update) {
+  return step_impl(c, grad_ptrs, out_update, nullptr, nullptr, 0.f, 0.f);
+}
+
+int psgd_step_momentum(psgd_ctx* c, const float* const* grad_ptrs, float* params, float* momentum, float lr,
+                       float beta, float* out_update) {
+  if (!params || !momentum) return fail(PSGD_ERR_INVALID, "params and momentum must not be NULL");
+  if (!aligned16(params) || !aligned16(momentum))
+    return fail(PSGD_ERR_INVALID, "params and momentum must be 16-byte aligned");
+  if (!std::isfinite(lr) || !std::isfinite(beta)) return fail(PSGD_ERR_INVALID, "lr and beta must be finite");
+  return step_impl(c, grad_ptrs, out_update, params, momentum, lr, beta);
 }
 
 int psgd_sync(psgd_ctx* c) {

@@ -77,6 +77,12 @@ struct StepArgs {
   const Tile* tiles;            // this phase's tiles
   int32_t W;
   int32_t has_prev;             // 0 before the first step: no correction term
+  // optional momentum-SGD update fused into the decompress phase (packed
+  // layout like U): Mom <- beta Mom + U, X <- X - lr (U + Mom); X == nullptr: off
+  float* X;
+  float* Mom;
+  float lr;
+  float beta;
 };
 
 }  // namespace psgd

@@ -233,12 +233,172 @@ __device__ void gram_tail(const StepArgs& a, const LayerDev& L, int rb, const fl
 // A CTA owns R1 rows x one segment (128 columns) of one layer and all W
 // workers; warp v handles workers v, v + 8, ...  The warm-start Q rows of the
 // segment and, when W x RP is small enough, every worker's Q_w' rows live in
-// shared memory, so the registers hold the loads in flight.
+// shared memory; each lane holds its 4 columns' Q rows in registers.
+
+// Per-tile geometry and flags of the project phase.
+struct P1Tile {
+  int rb, seg, row0, rcnt, lane, warp, nwarps, c, ncol4;
+  bool act, tailc, prev, stage_qw;
+};
+
+template <int RP>
+__device__ __forceinline__ P1Tile p1_tile(const StepArgs& a, const Tile& t, const LayerDev& L) {
+  constexpr int SEGQ = kSeg * 4 * RP;
+  P1Tile T;
+  T.rb = t.a;
+  T.seg = t.b;
+  T.row0 = T.rb * L.r1;
+  T.rcnt = min(L.r1, L.n - T.row0);
+  T.lane = threadIdx.x & 31;
+  T.warp = threadIdx.x >> 5;
+  T.nwarps = blockDim.x >> 5;
+  T.c = T.seg * kSeg + T.lane;  // this lane's float4 column
+  T.act = T.c < L.F;
+  T.tailc = T.act && (T.c == L.F - 1) && (L.tail < 4);
+  T.prev = a.has_prev != 0;
+  T.ncol4 = min(kSeg, L.F - T.seg * kSeg);
+  T.stage_qw = T.prev && a.W * SEGQ * 4 <= Cfg<RP>::QW_STAGE_BYTES;
+  return T;
+}
+
+// Stage Q and Q_w' (read-only in this kernel) and the previous Phat rows.
+// Shared layout is lane-minor: Q[4 L + j][k] sits at (j RP + k) 32 + L, so
+// the 32 lanes of a warp read 32 consecutive words (no bank conflict).
+template <int RP>
+__device__ __forceinline__ void p1_stage(const StepArgs& a, const LayerDev& L, const P1Tile& T, float* s_q,
+                                         float* s_qw, float* s_pp) {
+  constexpr int SEGQ = kSeg * 4 * RP;
+  constexpr int R1 = Cfg<RP>::R1;
+  const int64_t e0 = L.q_off + (int64_t)T.seg * SEGQ;
+  const int ne = T.ncol4 * 4 * RP;  // floats of the segment's Q slice
+  for (int e = threadIdx.x; e < ne; e += blockDim.x) {
+    const int col = e / RP, k = e - col * RP;
+    s_q[((col & 3) * RP + k) * kSeg + (col >> 2)] = __ldg(a.Qbar + e0 + e);
+  }
+  if (T.stage_qw)
+    for (int i = threadIdx.x; i < a.W * ne; i += blockDim.x) {
+      const int w = i / ne, e = i - w * ne;
+      const int col = e / RP, k = e - col * RP;
+      s_qw[w * SEGQ + ((col & 3) * RP + k) * kSeg + (col >> 2)] = __ldg(a.Qw + (int64_t)w * a.q_total + e0 + e);
+    }
+  for (int i = threadIdx.x; i < R1 * RP; i += blockDim.x)
+    s_pp[i] = (T.prev && i < T.rcnt * RP) ? __ldg(a.Phat + L.p_off + (int64_t)T.row0 * RP + i) : 0.f;
+}
+
+// Worker w's Q_w' rows for the lane's 4 columns (zero before the first step).
+template <int RP>
+__device__ __forceinline__ void p1_load_qw(const StepArgs& a, const LayerDev& L, const P1Tile& T, const float* s_qw,
+                                           int w, float (&qw)[4][RP]) {
+  constexpr int SEGQ = kSeg * 4 * RP;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int k = 0; k < RP; ++k)
+      qw[j][k] = !T.prev ? 0.f
+                         : (T.stage_qw ? s_qw[w * SEGQ + (j * RP + k) * kSeg + T.lane]
+                                       : (T.act ? __ldg(a.Qw + (int64_t)w * a.q_total + L.q_off +
+                                                        (int64_t)(4 * T.c + j) * RP + k)
+                                                : 0.f));
+}
+
+// The arithmetic of one pass over rn <= RSB rows of one worker, starting at
+// tile row sb: the error E = B - Phat' Q_w'^T (k ascending, the same chain
+// as the error read-back kernel), M = G + E stored to B, and the lane's
+// share of the rows' P partials in acc.
+template <int RP>
+__device__ __forceinline__ void p1_rows(const LayerDev& L, const P1Tile& T, const float4 (&g)[Cfg<RP>::RSB],
+                                        const float4 (&b)[Cfg<RP>::RSB], int sb, int rn, const float* s_pp,
+                                        const float (&qv)[4][RP], const float (&qw)[4][RP], float* Bw,
+                                        float (&acc)[Cfg<RP>::RSB * RP]) {
+  constexpr int RSB = Cfg<RP>::RSB;
+#pragma unroll
+  for (int i = 0; i < RSB * RP; ++i) acc[i] = 0.f;
+#pragma unroll
+  for (int i = 0; i < RSB; ++i) {
+    if (T.act && i < rn) {
+      float e0 = b[i].x, e1 = b[i].y, e2 = b[i].z, e3 = b[i].w;
+      if (T.prev) {
+#pragma unroll
+        for (int k = 0; k < RP; ++k) {
+          const float p = s_pp[(sb + i) * RP + k];
+          e0 = fmaf(-p, qw[0][k], e0);
+          e1 = fmaf(-p, qw[1][k], e1);
+          e2 = fmaf(-p, qw[2][k], e2);
+          e3 = fmaf(-p, qw[3][k], e3);
+        }
+      }
+      float m0 = g[i].x + e0, m1 = g[i].y + e1, m2 = g[i].z + e2, m3 = g[i].w + e3;
+      if (T.tailc) {
+        if (L.tail < 2) m1 = 0.f;
+        if (L.tail < 3) m2 = 0.f;
+        m3 = 0.f;
+      }
+      *reinterpret_cast<float4*>(Bw + (int64_t)(T.row0 + sb + i) * L.ld) = make_float4(m0, m1, m2, m3);
+#pragma unroll
+      for (int k = 0; k < RP; ++k) {
+        float t = m0 * qv[0][k];
+        t = fmaf(m1, qv[1][k], t);
+        t = fmaf(m2, qv[2][k], t);
+        t = fmaf(m3, qv[3][k], t);
+        acc[i * RP + k] = t;
+      }
+    }
+  }
+}
+
+// The pass's P partials summed over the lanes into s_red_w (first worker of
+// the warp: stored, later workers: added, so in worker order).
+template <int RP>
+__device__ __forceinline__ void p1_reduce(const P1Tile& T, float (&acc)[Cfg<RP>::RSB * RP], int sb, int rn,
+                                          float* s_red_w, bool first) {
+  constexpr int RSB = Cfg<RP>::RSB;
+  float tot;
+  const int j = warp_reduce_multi<RSB * RP>(acc, tot);
+  constexpr int SH = 5 - (RSB * RP == 1 ? 0 : (RSB * RP == 2 ? 1 : (RSB * RP == 4 ? 2 : (RSB * RP == 8 ? 3 : (RSB * RP == 16 ? 4 : 5)))));
+  if ((T.lane & ((1 << SH) - 1)) == 0 && j < rn * RP) {
+    float& dst = s_red_w[sb * RP + j];
+    dst = first ? tot : dst + tot;
+  }
+}
+
+// The tile's P rows (fixed-order sum over the warps, then over the segments
+// of the row block by its last CTA), P written, then the Gram tail.
+template <int RP>
+__device__ __forceinline__ void p1_finish(const StepArgs& a, const LayerDev& L, const P1Tile& T,
+                                          const float (*s_red)[Cfg<RP>::R1 * RP], float* s_prow, double* s_gram,
+                                          int* s_flag) {
+  constexpr int R1 = Cfg<RP>::R1;
+  for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) {
+    float s = 0.f;
+    for (int v = 0; v < T.nwarps; ++v) s += s_red[v][idx];
+    s_prow[idx] = s;
+  }
+  __syncthreads();
+  if (L.S > 1) {
+    float* pp = a.ppart + L.ppart_off + ((int64_t)T.rb * L.S + T.seg) * R1 * RP;
+    for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) pp[idx] = s_prow[idx];
+    if (!cta_arrive_last(a.counters + L.cnt_off + L.c_rb + T.rb, (unsigned)L.S, s_flag)) return;
+    const float* pb = a.ppart + L.ppart_off + (int64_t)T.rb * L.S * R1 * RP;
+    for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) {
+      float s = 0.f;
+      for (int qq = 0; qq < L.S; ++qq) s += __ldcg(pb + (int64_t)qq * R1 * RP + idx);
+      s_prow[idx] = s;
+    }
+    __syncthreads();
+  }
+  for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x)
+    a.P[L.p_off + (int64_t)T.row0 * RP + idx] = s_prow[idx];
+  gram_tail<RP>(a, L, T.rb, s_prow, T.rcnt, s_gram, s_flag);
+}
+
+// Each pass's RSB rows of G and B are loaded into registers (streaming
+// loads), then used.
 template <int RP>
 __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_kernel(const StepArgs a) {
   constexpr int RSB = Cfg<RP>::RSB;
   constexpr int R1 = Cfg<RP>::R1;
   constexpr int NW = Cfg<RP>::P1_WARPS;
+  constexpr int SEGQ = kSeg * 4 * RP;
   extern __shared__ __align__(16) float s_dyn[];      // Q rows, then Q_w' rows of every worker (staged)
   __shared__ float s_pp[R1 * RP];                     // previous Phat rows of the tile
   __shared__ float s_red[NW][R1 * RP];                // per-warp P partials
@@ -247,68 +407,31 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
   __shared__ int s_flag;
   const Tile t = a.tiles[blockIdx.x];
   const LayerDev& L = a.layers[t.layer];
-  const int rb = t.a, seg = t.b;
-  const int row0 = rb * L.r1;
-  const int rcnt = min(L.r1, L.n - row0);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int c = seg * kSeg + lane;  // this lane's float4 column
-  const bool act = c < L.F;
-  const bool tailc = act && (c == L.F - 1) && (L.tail < 4);
-  const bool prev = a.has_prev != 0;
-  const int ncol4 = min(kSeg, L.F - seg * kSeg);
-  constexpr int SEGQ = kSeg * 4 * RP;  // floats of one segment's Q rows
-  const bool stage_qw = prev && a.W * SEGQ * 4 <= Cfg<RP>::QW_STAGE_BYTES;
+  const P1Tile T = p1_tile<RP>(a, t, L);
   float* s_q = s_dyn;
   float* s_qw = s_dyn + SEGQ;
-  // stage Q and Q_w' (read-only in this kernel) and the previous Phat rows.
-  // Shared layout is lane-minor: Q[4 L + j][k] sits at (j RP + k) 32 + L, so
-  // the 32 lanes of a warp read 32 consecutive words (no bank conflict).
-  {
-    const int64_t e0 = L.q_off + (int64_t)seg * SEGQ;
-    const int ne = ncol4 * 4 * RP;  // floats of the segment's Q slice
-    for (int e = threadIdx.x; e < ne; e += blockDim.x) {
-      const int col = e / RP, k = e - col * RP;
-      s_q[((col & 3) * RP + k) * kSeg + (col >> 2)] = __ldg(a.Qbar + e0 + e);
-    }
-    if (stage_qw)
-      for (int i = threadIdx.x; i < a.W * ne; i += blockDim.x) {
-        const int w = i / ne, e = i - w * ne;
-        const int col = e / RP, k = e - col * RP;
-        s_qw[w * SEGQ + ((col & 3) * RP + k) * kSeg + (col >> 2)] = __ldg(a.Qw + (int64_t)w * a.q_total + e0 + e);
-      }
-    for (int i = threadIdx.x; i < R1 * RP; i += blockDim.x)
-      s_pp[i] = (prev && i < rcnt * RP) ? __ldg(a.Phat + L.p_off + (int64_t)row0 * RP + i) : 0.f;
-  }
+  p1_stage<RP>(a, L, T, s_q, s_qw, s_pp);
   __syncthreads();
   // this lane's 4 Q rows, held in registers for the whole tile
   float qv[4][RP];
 #pragma unroll
   for (int j = 0; j < 4; ++j)
 #pragma unroll
-    for (int k = 0; k < RP; ++k) qv[j][k] = s_q[(j * RP + k) * kSeg + lane];
+    for (int k = 0; k < RP; ++k) qv[j][k] = s_q[(j * RP + k) * kSeg + T.lane];
 
   bool first = true;
-  for (int w = warp; w < a.W; w += nwarps) {
-    const float* Gw = a.G[w] + L.off + 4 * c;
-    float* Bw = a.B + (int64_t)w * a.total + L.off + 4 * c;
-    // this worker's Q_w' rows for the lane's columns (registers)
+  for (int w = T.warp; w < a.W; w += T.nwarps) {
+    const float* Gw = a.G[w] + L.off + 4 * T.c;
+    float* Bw = a.B + (int64_t)w * a.total + L.off + 4 * T.c;
     float qw[4][RP];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int k = 0; k < RP; ++k)
-        qw[j][k] = !prev ? 0.f
-                         : (stage_qw ? s_qw[w * SEGQ + (j * RP + k) * kSeg + lane]
-                                     : (act ? __ldg(a.Qw + (int64_t)w * a.q_total + L.q_off +
-                                                    (int64_t)(4 * c + j) * RP + k)
-                                            : 0.f));
-    for (int sb = 0; sb < rcnt; sb += RSB) {
-      const int rn = min(RSB, rcnt - sb);
+    p1_load_qw<RP>(a, L, T, s_qw, w, qw);
+    for (int sb = 0; sb < T.rcnt; sb += RSB) {
+      const int rn = min(RSB, T.rcnt - sb);
       float4 g[RSB], b[RSB];
 #pragma unroll
       for (int i = 0; i < RSB; ++i) {
-        if (act && i < rn) {
-          const int64_t o = (int64_t)(row0 + sb + i) * L.ld;
+        if (T.act && i < rn) {
+          const int64_t o = (int64_t)(T.row0 + sb + i) * L.ld;
           g[i] = __ldcs(reinterpret_cast<const float4*>(Gw + o));
           b[i] = __ldcs(reinterpret_cast<const float4*>(Bw + o));
         } else {
@@ -317,75 +440,13 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
         }
       }
       float acc[RSB * RP];
-#pragma unroll
-      for (int i = 0; i < RSB * RP; ++i) acc[i] = 0.f;
-#pragma unroll
-      for (int i = 0; i < RSB; ++i) {
-        if (act && i < rn) {
-          // E_w = B_w - Phat' Q_w'^T, k ascending (the same chain as the
-          // error read-back kernel)
-          float e0 = b[i].x, e1 = b[i].y, e2 = b[i].z, e3 = b[i].w;
-          if (prev) {
-#pragma unroll
-            for (int k = 0; k < RP; ++k) {
-              const float p = s_pp[(sb + i) * RP + k];
-              e0 = fmaf(-p, qw[0][k], e0);
-              e1 = fmaf(-p, qw[1][k], e1);
-              e2 = fmaf(-p, qw[2][k], e2);
-              e3 = fmaf(-p, qw[3][k], e3);
-            }
-          }
-          float m0 = g[i].x + e0, m1 = g[i].y + e1, m2 = g[i].z + e2, m3 = g[i].w + e3;
-          if (tailc) {
-            if (L.tail < 2) m1 = 0.f;
-            if (L.tail < 3) m2 = 0.f;
-            m3 = 0.f;
-          }
-          *reinterpret_cast<float4*>(Bw + (int64_t)(row0 + sb + i) * L.ld) = make_float4(m0, m1, m2, m3);
-#pragma unroll
-          for (int k = 0; k < RP; ++k) {
-            float t = m0 * qv[0][k];
-            t = fmaf(m1, qv[1][k], t);
-            t = fmaf(m2, qv[2][k], t);
-            t = fmaf(m3, qv[3][k], t);
-            acc[i * RP + k] = t;
-          }
-        }
-      }
-      // this worker's rows, summed over the lanes; a warp with several
-      // workers adds them in worker order
-      float tot;
-      const int j = warp_reduce_multi<RSB * RP>(acc, tot);
-      constexpr int SH = 5 - (RSB * RP == 1 ? 0 : (RSB * RP == 2 ? 1 : (RSB * RP == 4 ? 2 : (RSB * RP == 8 ? 3 : (RSB * RP == 16 ? 4 : 5)))));
-      if ((lane & ((1 << SH) - 1)) == 0 && j < rn * RP) {
-        float& dst = s_red[warp][sb * RP + j];
-        dst = first ? tot : dst + tot;
-      }
+      p1_rows<RP>(L, T, g, b, sb, rn, s_pp, qv, qw, Bw, acc);
+      p1_reduce<RP>(T, acc, sb, rn, s_red[T.warp], first);
     }
     first = false;
   }
   __syncthreads();
-  // the tile's P rows: fixed-order sum over the warps
-  for (int idx = threadIdx.x; idx < rcnt * RP; idx += blockDim.x) {
-    float s = 0.f;
-    for (int v = 0; v < nwarps; ++v) s += s_red[v][idx];
-    s_prow[idx] = s;
-  }
-  __syncthreads();
-  if (L.S > 1) {
-    float* pp = a.ppart + L.ppart_off + ((int64_t)rb * L.S + seg) * R1 * RP;
-    for (int idx = threadIdx.x; idx < rcnt * RP; idx += blockDim.x) pp[idx] = s_prow[idx];
-    if (!cta_arrive_last(a.counters + L.cnt_off + L.c_rb + rb, (unsigned)L.S, &s_flag)) return;
-    const float* pb = a.ppart + L.ppart_off + (int64_t)rb * L.S * R1 * RP;
-    for (int idx = threadIdx.x; idx < rcnt * RP; idx += blockDim.x) {
-      float s = 0.f;
-      for (int qq = 0; qq < L.S; ++qq) s += __ldcg(pb + (int64_t)qq * R1 * RP + idx);
-      s_prow[idx] = s;
-    }
-    __syncthreads();
-  }
-  for (int idx = threadIdx.x; idx < rcnt * RP; idx += blockDim.x) a.P[L.p_off + (int64_t)row0 * RP + idx] = s_prow[idx];
-  gram_tail<RP>(a, L, rb, s_prow, rcnt, s_gram, &s_flag);
+  p1_finish<RP>(a, L, T, s_red, s_prow, s_gram, &s_flag);
 }
 
 // ----------------------------------------------------------------------------
@@ -567,6 +628,27 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
 // ----------------------------------------------------------------------------
 // decompress: rows of Phat Qbar^T; vector layers: worker mean
 // ----------------------------------------------------------------------------
+
+// Momentum-SGD update of one element by the decompressed u:
+// mom <- beta mom + u, x <- x - lr (u + mom).
+__device__ __forceinline__ void momentum1(float& x, float& mom, float u, float lr, float beta) {
+  mom = fmaf(beta, mom, u);
+  x = fmaf(-lr, u + mom, x);
+}
+
+// The same for the float4 at p of X and Mom; elements at or past `valid`
+// (row padding) are left as they are.
+__device__ __forceinline__ void momentum4(float* X, float* Mom, int64_t p, float4 u, int valid, float lr,
+                                          float beta) {
+  float4 x = __ldcs(reinterpret_cast<const float4*>(X + p));
+  float4 m = __ldcs(reinterpret_cast<const float4*>(Mom + p));
+  momentum1(x.x, m.x, u.x, lr, beta);
+  if (valid > 1) momentum1(x.y, m.y, u.y, lr, beta);
+  if (valid > 2) momentum1(x.z, m.z, u.z, lr, beta);
+  if (valid > 3) momentum1(x.w, m.w, u.w, lr, beta);
+  __stcs(reinterpret_cast<float4*>(X + p), x);
+  __stcs(reinterpret_cast<float4*>(Mom + p), m);
+}
 template <int RP>
 __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
   constexpr int RU = Cfg<RP>::RU;
@@ -579,7 +661,14 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
     for (int i = base + (int)threadIdx.x; i < end; i += blockDim.x) {
       float s = 0.f;
       for (int w = 0; w < a.W; ++w) s += __ldcs(a.G[w] + V.off + i);
-      a.U[V.off + i] = s / (float)a.W;
+      const float u = s / (float)a.W;
+      if (a.U) a.U[V.off + i] = u;
+      if (a.X) {
+        float x = a.X[V.off + i], mom = a.Mom[V.off + i];
+        momentum1(x, mom, u, a.lr, a.beta);
+        a.X[V.off + i] = x;
+        a.Mom[V.off + i] = mom;
+      }
     }
     return;
   }
@@ -610,7 +699,8 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
       for (int i = 0; i < 4 * RP; ++i) flat[i] = __ldg(qs + i);
     }
   }
-  float* Ub = a.U + L.off + 4 * c;
+  const int valid = (c == L.F - 1) ? L.tail : 4;
+  const int64_t col = L.off + 4 * c;
 #pragma unroll 4
   for (int r = sub; r < rcnt; r += kUThreads / 32) {
     float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
@@ -622,7 +712,9 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
       u2 = fmaf(p, qv[2][k], u2);
       u3 = fmaf(p, qv[3][k], u3);
     }
-    __stcs(reinterpret_cast<float4*>(Ub + (int64_t)(row0 + r) * L.ld), make_float4(u0, u1, u2, u3));
+    const int64_t pos = col + (int64_t)(row0 + r) * L.ld;
+    if (a.U) __stcs(reinterpret_cast<float4*>(a.U + pos), make_float4(u0, u1, u2, u3));
+    if (a.X) momentum4(a.X, a.Mom, pos, make_float4(u0, u1, u2, u3), valid, a.lr, a.beta);
   }
 }
 

@@ -13,15 +13,18 @@ constexpr size_t kP3Dyn = (size_t)(kP3Threads / 32) * 32 * 4 * kRP * sizeof(floa
 constexpr size_t kSegQ = (size_t)kSeg * 4 * kRP * sizeof(float);
 constexpr size_t kP1DynMax = kSegQ + Cfg<kRP>::QW_STAGE_BYTES;
 
+size_t p1_dyn(int W, bool has_prev) {
+  // the Q rows of a segment, plus every worker's Q_w' rows when they fit
+  const size_t qw = (size_t)W * kSegQ;
+  return kSegQ + ((has_prev && qw <= (size_t)Cfg<kRP>::QW_STAGE_BYTES) ? qw : 0);
+}
+
 cudaError_t launch(int phase, const StepArgs& a, int tiles, cudaStream_t s) {
   if (tiles <= 0) return cudaSuccess;
   switch (phase) {
     case kProject: {
       const int warps = a.W < Cfg<kRP>::P1_WARPS ? a.W : Cfg<kRP>::P1_WARPS;
-      // the Q rows of a segment, plus every worker's Q_w' rows when they fit
-      const size_t qw = (size_t)a.W * kSegQ;
-      const size_t dyn = kSegQ + ((a.has_prev && qw <= (size_t)Cfg<kRP>::QW_STAGE_BYTES) ? qw : 0);
-      p1_kernel<kRP><<<tiles, 32 * warps, dyn, s>>>(a);
+      p1_kernel<kRP><<<tiles, 32 * warps, p1_dyn(a.W, a.has_prev != 0), s>>>(a);
       break;
     }
     case kOrthonormalise:
@@ -60,9 +63,7 @@ cudaError_t occupancy(int phase, int W, int* ctas) {
   switch (phase) {
     case kProject: {
       const int warps = W < Cfg<kRP>::P1_WARPS ? W : Cfg<kRP>::P1_WARPS;
-      const size_t qw = (size_t)W * kSegQ;
-      const size_t dyn = kSegQ + (qw <= (size_t)Cfg<kRP>::QW_STAGE_BYTES ? qw : 0);
-      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p1_kernel<kRP>, 32 * warps, dyn);
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p1_kernel<kRP>, 32 * warps, p1_dyn(W, true));
     }
     case kBackProject:
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p3_kernel<kRP>, kP3Threads, kP3Dyn);
@@ -76,6 +77,7 @@ cudaError_t occupancy(int phase, int W, int* ctas) {
 }  // namespace
 
 extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {
-    kRP, launch, launch_error, prepare, occupancy, Cfg<kRP>::R1, Cfg<kRP>::RU, Cfg<kRP>::RSB, Cfg<kRP>::FUSE_PH};
+    kRP, launch, launch_error, prepare, occupancy, Cfg<kRP>::R1, Cfg<kRP>::RU, Cfg<kRP>::RSB,
+    Cfg<kRP>::FUSE_PH};
 
 }  // namespace psgd

@@ -273,3 +273,4 @@ def test_invalid_arguments_are_rejected():
         ctx.close()
     with pytest.raises(PsgdError):
         PowerSGD([(16, 8)], 9, 2)  # rank > min(n, m)
+
