@@ -129,11 +129,14 @@ __device__ __forceinline__ void tri_index(int e, int rp, int& i, int& j) {
 // Whole CTA: make the CTA's global writes visible, count one arrival on *cnt
 // and return true (in every thread) when this was arrival number `total`.
 // The last arriver resets the counter for the next launch and may then read
-// everything the other arrivers wrote (with .cg loads).
+// everything the other arrivers wrote (with .cg loads).  The barrier orders
+// every thread's writes before thread 0's fence, whose cumulativity makes
+// them visible at GPU scope before the arrival; one fence per CTA, not one
+// per thread.
 __device__ __forceinline__ bool cta_arrive_last(unsigned* cnt, unsigned total, int* s_flag) {
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();
     const unsigned old = atom_add_acq_rel(cnt, 1u);
     const bool last = (old == total - 1);
     if (last) *cnt = 0u;
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
   __shared__ double s_gram[RP * RP];
   __shared__ int s_flag;
   const Tile t = a.tiles[blockIdx.x];
-  const LayerDev& L = a.layers[t.layer];
+  const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
   const P1Tile T = p1_tile<RP>(a, t, L);
   float* s_q = s_dyn;
   float* s_qw = s_dyn + SEGQ;
@@ -456,7 +459,7 @@ template <int RP>
 __global__ void __launch_bounds__(kPHThreads) ph_kernel(const StepArgs a) {
   __shared__ double s_r[RP * RP + RP];
   const Tile t = a.tiles[blockIdx.x];
-  const LayerDev& L = a.layers[t.layer];
+  const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
   for (int e = threadIdx.x; e < RP * RP + RP; e += blockDim.x) s_r[e] = a.rinv[L.rinv_off + e];
   __syncthreads();
   const int row = t.a * kPHThreads + threadIdx.x;
@@ -537,7 +540,7 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
   extern __shared__ __align__(16) float s_red[];  // NW x 32 x 4 x RP
   __shared__ int s_flag;
   const Tile t = a.tiles[blockIdx.x];
-  const LayerDev& L = a.layers[t.layer];
+  const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
   const int rt = t.a, seg = t.b, w = t.c;
   const int row0 = rt * L.r3;
   const int nrows = min(L.r3, L.n - row0);
@@ -672,7 +675,7 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
     }
     return;
   }
-  const LayerDev& L = a.layers[t.layer];
+  const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
   const int row0 = t.a * L.ru, seg = t.b;
   const int rcnt = min(L.ru, L.n - row0);
   for (int i = threadIdx.x; i < rcnt * RP; i += blockDim.x) s_ph[i] = __ldg(a.Phat + L.p_off + (int64_t)row0 * RP + i);
