@@ -45,7 +45,6 @@ struct Cfg {
   static constexpr int RSB = RP <= 4 ? 4 : (RP == 8 ? 2 : 1);
   static constexpr int R1 = RP <= 8 ? 32 : 16;
   static constexpr int P1_WARPS = 8;                        // at most (more workers loop)
-  static constexpr int QW_STAGE_BYTES = 32 * 1024;          // Q_w' rows staged when they fit
   static constexpr int P1_MINB = RP <= 2 ? 4 : (RP == 4 ? 3 : 1);          // 256-thread CTAs per SM the registers must allow
   // back-project: row tiles staged by chunks of R3C Phat rows, 8 warps; for
   // small ranks the tile forms its Phat rows itself (float64 forward
@@ -234,19 +233,17 @@ __device__ void gram_tail(const StepArgs& a, const LayerDev& L, int rb, const fl
 // ----------------------------------------------------------------------------
 //
 // A CTA owns R1 rows x one segment (128 columns) of one layer and all W
-// workers; warp v handles workers v, v + 8, ...  The warm-start Q rows of the
-// segment and, when W x RP is small enough, every worker's Q_w' rows live in
-// shared memory; each lane holds its 4 columns' Q rows in registers.
+// workers; warp v handles workers v, v + 8, ...  Each lane holds its 4
+// columns' rows of Q and of its worker's Q_w' in registers.
 
 // Per-tile geometry and flags of the project phase.
 struct P1Tile {
-  int rb, seg, row0, rcnt, lane, warp, nwarps, c, ncol4;
-  bool act, tailc, prev, stage_qw;
+  int rb, seg, row0, rcnt, lane, warp, nwarps, c;
+  bool act, tailc, prev;
 };
 
 template <int RP>
 __device__ __forceinline__ P1Tile p1_tile(const StepArgs& a, const Tile& t, const LayerDev& L) {
-  constexpr int SEGQ = kSeg * 4 * RP;
   P1Tile T;
   T.rb = t.a;
   T.seg = t.b;
@@ -259,58 +256,38 @@ __device__ __forceinline__ P1Tile p1_tile(const StepArgs& a, const Tile& t, cons
   T.act = T.c < L.F;
   T.tailc = T.act && (T.c == L.F - 1) && (L.tail < 4);
   T.prev = a.has_prev != 0;
-  T.ncol4 = min(kSeg, L.F - T.seg * kSeg);
-  T.stage_qw = T.prev && a.W * SEGQ * 4 <= Cfg<RP>::QW_STAGE_BYTES;
   return T;
 }
 
-// Stage Q and Q_w' (read-only in this kernel) and the previous Phat rows.
-// Shared layout is lane-minor: Q[4 L + j][k] sits at (j RP + k) 32 + L, so
-// the 32 lanes of a warp read 32 consecutive words (no bank conflict).
+// The RP values of rows 4c .. 4c + 3 of an ld x RP factor (Q or Q_w'),
+// which sit contiguously: RP float4 loads per lane, coalesced over the warp.
 template <int RP>
-__device__ __forceinline__ void p1_stage(const StepArgs& a, const LayerDev& L, const P1Tile& T, float* s_q,
-                                         float* s_qw, float* s_pp) {
-  constexpr int SEGQ = kSeg * 4 * RP;
-  constexpr int R1 = Cfg<RP>::R1;
-  const int64_t e0 = L.q_off + (int64_t)T.seg * SEGQ;
-  const int ne = T.ncol4 * 4 * RP;  // floats of the segment's Q slice
-  for (int e = threadIdx.x; e < ne; e += blockDim.x) {
-    const int col = e / RP, k = e - col * RP;
-    s_q[((col & 3) * RP + k) * kSeg + (col >> 2)] = __ldg(a.Qbar + e0 + e);
+__device__ __forceinline__ void p1_load_q(const float* Qrows, const P1Tile& T, bool zero, float (&q)[4][RP]) {
+  float* flat = &q[0][0];
+  if (zero || !T.act) {
+#pragma unroll
+    for (int i = 0; i < 4 * RP; ++i) flat[i] = 0.f;
+    return;
   }
-  if (T.stage_qw)
-    for (int i = threadIdx.x; i < a.W * ne; i += blockDim.x) {
-      const int w = i / ne, e = i - w * ne;
-      const int col = e / RP, k = e - col * RP;
-      s_qw[w * SEGQ + ((col & 3) * RP + k) * kSeg + (col >> 2)] = __ldg(a.Qw + (int64_t)w * a.q_total + e0 + e);
-    }
-  for (int i = threadIdx.x; i < R1 * RP; i += blockDim.x)
-    s_pp[i] = (T.prev && i < T.rcnt * RP) ? __ldg(a.Phat + L.p_off + (int64_t)T.row0 * RP + i) : 0.f;
-}
-
-// Worker w's Q_w' rows for the lane's 4 columns (zero before the first step).
-template <int RP>
-__device__ __forceinline__ void p1_load_qw(const StepArgs& a, const LayerDev& L, const P1Tile& T, const float* s_qw,
-                                           int w, float (&qw)[4][RP]) {
-  constexpr int SEGQ = kSeg * 4 * RP;
+  const float4* src = reinterpret_cast<const float4*>(Qrows + (int64_t)(4 * T.c) * RP);
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int k = 0; k < RP; ++k)
-      qw[j][k] = !T.prev ? 0.f
-                         : (T.stage_qw ? s_qw[w * SEGQ + (j * RP + k) * kSeg + T.lane]
-                                       : (T.act ? __ldg(a.Qw + (int64_t)w * a.q_total + L.q_off +
-                                                        (int64_t)(4 * T.c + j) * RP + k)
-                                                : 0.f));
+  for (int i = 0; i < RP; ++i) {
+    const float4 v = __ldg(src + i);
+    flat[4 * i] = v.x;
+    flat[4 * i + 1] = v.y;
+    flat[4 * i + 2] = v.z;
+    flat[4 * i + 3] = v.w;
+  }
 }
 
 // The arithmetic of one pass over rn <= RSB rows of one worker, starting at
 // tile row sb: the error E = B - Phat' Q_w'^T (k ascending, the same chain
-// as the error read-back kernel), M = G + E stored to B, and the lane's
-// share of the rows' P partials in acc.
+// as the error read-back kernel; the previous Phat rows are warp-uniform
+// loads), M = G + E stored to B, and the lane's share of the rows' P
+// partials in acc.
 template <int RP>
 __device__ __forceinline__ void p1_rows(const LayerDev& L, const P1Tile& T, const float4 (&g)[Cfg<RP>::RSB],
-                                        const float4 (&b)[Cfg<RP>::RSB], int sb, int rn, const float* s_pp,
+                                        const float4 (&b)[Cfg<RP>::RSB], int sb, int rn, const float* Pprev,
                                         const float (&qv)[4][RP], const float (&qw)[4][RP], float* Bw,
                                         float (&acc)[Cfg<RP>::RSB * RP]) {
   constexpr int RSB = Cfg<RP>::RSB;
@@ -323,7 +300,7 @@ __device__ __forceinline__ void p1_rows(const LayerDev& L, const P1Tile& T, cons
       if (T.prev) {
 #pragma unroll
         for (int k = 0; k < RP; ++k) {
-          const float p = s_pp[(sb + i) * RP + k];
+          const float p = __ldg(Pprev + (sb + i) * RP + k);
           e0 = fmaf(-p, qw[0][k], e0);
           e1 = fmaf(-p, qw[1][k], e1);
           e2 = fmaf(-p, qw[2][k], e2);
@@ -395,39 +372,32 @@ __device__ __forceinline__ void p1_finish(const StepArgs& a, const LayerDev& L, 
 }
 
 // Each pass's RSB rows of G and B are loaded into registers (streaming
-// loads), then used.
+// loads), then used.  Every warp starts on its own: its lanes load their
+// Q and Q_w' rows straight into registers, so the only barrier of a tile is
+// the final cross-warp sum.
 template <int RP>
 __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_kernel(const StepArgs a) {
   constexpr int RSB = Cfg<RP>::RSB;
   constexpr int R1 = Cfg<RP>::R1;
   constexpr int NW = Cfg<RP>::P1_WARPS;
-  constexpr int SEGQ = kSeg * 4 * RP;
-  extern __shared__ __align__(16) float s_dyn[];      // Q rows, then Q_w' rows of every worker (staged)
-  __shared__ float s_pp[R1 * RP];                     // previous Phat rows of the tile
   __shared__ float s_red[NW][R1 * RP];                // per-warp P partials
   __shared__ float s_prow[R1 * RP];
   __shared__ double s_gram[RP * RP];
   __shared__ int s_flag;
   const Tile t = a.tiles[blockIdx.x];
-  const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
+  const LayerDev L = a.layers[t.layer];  // by value: stores to B cannot alias it
   const P1Tile T = p1_tile<RP>(a, t, L);
-  float* s_q = s_dyn;
-  float* s_qw = s_dyn + SEGQ;
-  p1_stage<RP>(a, L, T, s_q, s_qw, s_pp);
-  __syncthreads();
+  const float* Pprev = a.Phat + L.p_off + (int64_t)T.row0 * RP;  // previous Phat rows of the tile
   // this lane's 4 Q rows, held in registers for the whole tile
   float qv[4][RP];
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int k = 0; k < RP; ++k) qv[j][k] = s_q[(j * RP + k) * kSeg + T.lane];
+  p1_load_q<RP>(a.Qbar + L.q_off, T, false, qv);
 
   bool first = true;
   for (int w = T.warp; w < a.W; w += T.nwarps) {
     const float* Gw = a.G[w] + L.off + 4 * T.c;
     float* Bw = a.B + (int64_t)w * a.total + L.off + 4 * T.c;
     float qw[4][RP];
-    p1_load_qw<RP>(a, L, T, s_qw, w, qw);
+    p1_load_q<RP>(a.Qw + (int64_t)w * a.q_total + L.q_off, T, !T.prev, qw);
     for (int sb = 0; sb < T.rcnt; sb += RSB) {
       const int rn = min(RSB, T.rcnt - sb);
       float4 g[RSB], b[RSB];
@@ -443,7 +413,7 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
         }
       }
       float acc[RSB * RP];
-      p1_rows<RP>(L, T, g, b, sb, rn, s_pp, qv, qw, Bw, acc);
+      p1_rows<RP>(L, T, g, b, sb, rn, Pprev, qv, qw, Bw, acc);
       p1_reduce<RP>(T, acc, sb, rn, s_red[T.warp], first);
     }
     first = false;

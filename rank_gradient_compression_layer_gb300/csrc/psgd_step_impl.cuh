@@ -10,21 +10,13 @@ namespace {
 
 constexpr int kRP = PSGD_RP;
 constexpr size_t kP3Dyn = (size_t)(kP3Threads / 32) * 32 * 4 * kRP * sizeof(float);
-constexpr size_t kSegQ = (size_t)kSeg * 4 * kRP * sizeof(float);
-constexpr size_t kP1DynMax = kSegQ + Cfg<kRP>::QW_STAGE_BYTES;
-
-size_t p1_dyn(int W, bool has_prev) {
-  // the Q rows of a segment, plus every worker's Q_w' rows when they fit
-  const size_t qw = (size_t)W * kSegQ;
-  return kSegQ + ((has_prev && qw <= (size_t)Cfg<kRP>::QW_STAGE_BYTES) ? qw : 0);
-}
 
 cudaError_t launch(int phase, const StepArgs& a, int tiles, cudaStream_t s) {
   if (tiles <= 0) return cudaSuccess;
   switch (phase) {
     case kProject: {
       const int warps = a.W < Cfg<kRP>::P1_WARPS ? a.W : Cfg<kRP>::P1_WARPS;
-      p1_kernel<kRP><<<tiles, 32 * warps, p1_dyn(a.W, a.has_prev != 0), s>>>(a);
+      p1_kernel<kRP><<<tiles, 32 * warps, 0, s>>>(a);
       break;
     }
     case kOrthonormalise:
@@ -54,8 +46,6 @@ cudaError_t launch_error(float* E, const float* B, const float* Phat, const floa
 
 cudaError_t prepare() {
   cudaError_t e = cudaFuncSetAttribute(p3_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP3Dyn);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(p1_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP1DynMax);
   return e;
 }
 
@@ -63,7 +53,7 @@ cudaError_t occupancy(int phase, int W, int* ctas) {
   switch (phase) {
     case kProject: {
       const int warps = W < Cfg<kRP>::P1_WARPS ? W : Cfg<kRP>::P1_WARPS;
-      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p1_kernel<kRP>, 32 * warps, p1_dyn(W, true));
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p1_kernel<kRP>, 32 * warps, 0);
     }
     case kBackProject:
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p3_kernel<kRP>, kP3Threads, kP3Dyn);
