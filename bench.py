@@ -40,7 +40,11 @@ UNIT = "GB/s"
 # DRAM bytes (read + write) of one project-kernel launch per workload, from an
 # ncu capture (see profiles/), valid only for the kernel sources whose hash is
 # recorded with it.
-NCU_TRAFFIC = {}  # {config: (sources_sha256_prefix, bytes_per_launch)}
+NCU_TRAFFIC = {  # {config: (sources_sha256_prefix, bytes_per_launch)}
+    # ResNet-18 set, r = 2, W = 4: mean of two project launches, 365.7 MB read +
+    # 125.8 MB written (profiles/bench_all_configs.md)
+    "c2": ("77489d7555fb16b0", 491524992),
+}
 
 
 def kernel_sources_hash() -> str:

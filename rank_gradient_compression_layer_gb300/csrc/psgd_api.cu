@@ -187,8 +187,7 @@ void build_tiles(psgd_ctx* c) {
     const LayerDev& L = c->hl[li];
     for (int rb = 0; rb < L.nrb; ++rb)
       for (int s = 0; s < L.S; ++s) c->tiles[kProject].push_back({li, rb, s, 0});
-    if (!c->ks->fuse_ph)
-      for (int t = 0; t < (int)ceil_div(L.n, kPHThreads); ++t) c->tiles[kOrthonormalise].push_back({li, t, 0, 0});
+    for (int t = 0; t < (int)ceil_div(L.n, kPHThreads); ++t) c->tiles[kOrthonormalise].push_back({li, t, 0, 0});
     for (int rb = 0; rb < (int)ceil_div(L.n, L.ru); ++rb)
       for (int s = 0; s < L.S; ++s) c->tiles[kDecompress].push_back({li, rb, s, 0});
   }
@@ -672,7 +671,7 @@ int psgd_get_stats(const psgd_ctx* c, psgd_stats* out) {
   for (int ph = 0; ph < kPhases; ++ph) out->tiles[ph] = (int64_t)c->tiles[ph].size();
   out->kernel_rank = c->rp;
   for (int i = 0; i < 3; ++i) out->tile_rows[i] = c->tile_rows[i];
-  out->launches_per_step = c->ks->fuse_ph ? kPhases - 1 : kPhases;
+  out->launches_per_step = kPhases;
   return PSGD_OK;
 }
 

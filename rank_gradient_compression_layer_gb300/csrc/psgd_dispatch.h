@@ -25,8 +25,6 @@ struct KernelSet {
   // tile geometry: most project rows per tile, most decompress rows per tile,
   // rows per project pass
   int r1, ru, rsb;
-  // back-project tiles form the Phat rows (no orthonormalise launch)
-  bool fuse_ph;
 };
 
 extern const KernelSet kKernelsR1, kKernelsR2, kKernelsR4, kKernelsR8, kKernelsR16, kKernelsR32;

@@ -43,14 +43,11 @@ struct Cfg {
   // project: tiles of R1 rows x one segment x all workers; a warp per worker,
   // RSB rows per pass
   static constexpr int RSB = RP <= 4 ? 4 : (RP == 8 ? 2 : 1);
-  static constexpr int R1 = RP <= 8 ? 32 : 16;
+  static constexpr int R1 = 32;
   static constexpr int P1_WARPS = 8;                        // at most (more workers loop)
   static constexpr int P1_MINB = RP <= 2 ? 4 : (RP == 4 ? 3 : 1);          // 256-thread CTAs per SM the registers must allow
-  // back-project: row tiles staged by chunks of R3C Phat rows, 8 warps; for
-  // small ranks the tile forms its Phat rows itself (float64 forward
-  // substitution) instead of a separate orthonormalise launch
+  // back-project: row tiles staged by chunks of R3C Phat rows, 8 warps
   static constexpr int R3C = 256;
-  static constexpr bool FUSE_PH = false;
   static constexpr int UNR3 = RP <= 4 ? 16 : 8;
   // decompress: RU rows x one segment per CTA of 256 threads
   static constexpr int RU = 64;
@@ -341,19 +338,13 @@ __device__ __forceinline__ void p1_reduce(const P1Tile& T, float (&acc)[Cfg<RP>:
   }
 }
 
-// The tile's P rows (fixed-order sum over the warps, then over the segments
-// of the row block by its last CTA), P written, then the Gram tail.
+// The tile's P rows are complete in s_prow (visible to the CTA): for a layer
+// of several segments the row block's last CTA sums the segments' rows (fixed
+// order); then P is written and the Gram tail runs.
 template <int RP>
-__device__ __forceinline__ void p1_finish(const StepArgs& a, const LayerDev& L, const P1Tile& T,
-                                          const float (*s_red)[Cfg<RP>::R1 * RP], float* s_prow, double* s_gram,
-                                          int* s_flag) {
+__device__ __forceinline__ void p1_rows_done(const StepArgs& a, const LayerDev& L, const P1Tile& T, float* s_prow,
+                                             double* s_gram, int* s_flag) {
   constexpr int R1 = Cfg<RP>::R1;
-  for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) {
-    float s = 0.f;
-    for (int v = 0; v < T.nwarps; ++v) s += s_red[v][idx];
-    s_prow[idx] = s;
-  }
-  __syncthreads();
   if (L.S > 1) {
     float* pp = a.ppart + L.ppart_off + ((int64_t)T.rb * L.S + T.seg) * R1 * RP;
     for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) pp[idx] = s_prow[idx];
@@ -369,6 +360,20 @@ __device__ __forceinline__ void p1_finish(const StepArgs& a, const LayerDev& L, 
   for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x)
     a.P[L.p_off + (int64_t)T.row0 * RP + idx] = s_prow[idx];
   gram_tail<RP>(a, L, T.rb, s_prow, T.rcnt, s_gram, s_flag);
+}
+
+// The tile's P rows: fixed-order sum over the warps, then p1_rows_done.
+template <int RP>
+__device__ __forceinline__ void p1_finish(const StepArgs& a, const LayerDev& L, const P1Tile& T,
+                                          const float (*s_red)[Cfg<RP>::R1 * RP], float* s_prow, double* s_gram,
+                                          int* s_flag) {
+  for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) {
+    float s = 0.f;
+    for (int v = 0; v < T.nwarps; ++v) s += s_red[v][idx];
+    s_prow[idx] = s;
+  }
+  __syncthreads();
+  p1_rows_done<RP>(a, L, T, s_prow, s_gram, s_flag);
 }
 
 // Each pass's RSB rows of G and B are loaded into registers (streaming
@@ -526,33 +531,7 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
   for (int r0 = 0; r0 < nrows; r0 += R3C) {
     const int rn = min(R3C, nrows - r0);
     __syncthreads();
-    if constexpr (Cfg<RP>::FUSE_PH) {
-      // Phat rows = P rows R^-1 by forward substitution (float64); the tile of
-      // segment 0, worker 0 also stores them
-      const double* Rr = a.rinv + L.rinv_off;
-      const bool store = (seg == 0 && w == 0);
-      for (int i = threadIdx.x; i < rn; i += blockDim.x) {
-        const int64_t row = row0 + r0 + i;
-        double x[RP];
-#pragma unroll
-        for (int k = 0; k < RP; ++k) x[k] = (double)a.P[L.p_off + row * RP + k];
-#pragma unroll
-        for (int k = 0; k < RP; ++k) {
-          double sum = x[k];
-#pragma unroll
-          for (int j = 0; j < k; ++j) sum = fma(-x[j], __ldg(Rr + j * RP + k), sum);
-          x[k] = sum * __ldg(Rr + RP * RP + k);
-        }
-#pragma unroll
-        for (int k = 0; k < RP; ++k) {
-          const float v = (float)x[k];
-          s_ph[i * RP + k] = v;
-          if (store) a.Phat[L.p_off + row * RP + k] = v;
-        }
-      }
-    } else {
-      for (int i = threadIdx.x; i < rn * RP; i += blockDim.x) s_ph[i] = a.Phat[L.p_off + (int64_t)(row0 + r0) * RP + i];
-    }
+    for (int i = threadIdx.x; i < rn * RP; i += blockDim.x) s_ph[i] = a.Phat[L.p_off + (int64_t)(row0 + r0) * RP + i];
     __syncthreads();
     // warps take interleaved groups of UNR rows of the chunk
     for (int i0 = warp * UNR; i0 < rn; i0 += NW * UNR) {
@@ -688,6 +667,214 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
     const int64_t pos = col + (int64_t)(row0 + r) * L.ld;
     if (a.U) __stcs(reinterpret_cast<float4*>(a.U + pos), make_float4(u0, u1, u2, u3));
     if (a.X) momentum4(a.X, a.Mom, pos, make_float4(u0, u1, u2, u3), valid, a.lr, a.beta);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// r >= 16: register-tiled project and decompress
+// ----------------------------------------------------------------------------
+//
+// At r >= 16 the lane-per-4-columns project and decompress kernels would
+// hold 8 r floats of Q rows per lane; these kernels instead spread the
+// r-wide dot products so that each value loaded from shared memory feeds
+// several fused multiply-adds.  (The back-project kernel serves every rank.)
+
+constexpr int kTThreads = 256;  // threads of a tiled project or decompress CTA
+
+// Project, r >= 16.  A CTA owns up to 32 rows x one segment (128 columns) and
+// loops over the workers.  Thread (row i = tid / 8, column group cg = tid % 8)
+// owns the float4 columns cg, cg + 8, cg + 16, cg + 24 of its row (16
+// columns; each of the 8 threads of a row reads a different 16 bytes, so the
+// loads of a warp are coalesced and the shared-memory reads conflict-free).
+// Per worker: E = B - Phat' Q_w'^T for its 16 elements (fmaf chains, k
+// ascending, as in the error read-back kernel), M = G + E stored to B, and
+// its share of the P row, sum_c M[i][c] Q[c][k], accumulated over the workers
+// in registers; the 8 column groups of a row are summed with a butterfly
+// over their 8 lanes at the end.  Q and Q_w' are staged transposed
+// ([k][column]) so a thread reads its 4 float4 columns at fixed k.
+template <int RP>
+__global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
+  constexpr int TR = 32;
+  constexpr int SC = kSeg * 4;  // columns of a segment
+  static_assert(Cfg<RP>::R1 == TR, "the tiled project kernel covers 32 rows");
+  extern __shared__ __align__(16) float s_t[];
+  float* s_qT = s_t;              // Q rows of the segment, transposed: [RP][SC]
+  float* s_qwT = s_qT + RP * SC;  // Q_w' rows of the current worker, transposed: [RP][SC]
+  float* s_pp = s_qwT + RP * SC;  // previous Phat rows of the tile: [TR][RP]
+  __shared__ float s_prow[TR * RP];
+  __shared__ double s_gram[RP * RP];
+  __shared__ int s_flag;
+  const Tile t = a.tiles[blockIdx.x];
+  const LayerDev L = a.layers[t.layer];  // by value
+  const P1Tile T = p1_tile<RP>(a, t, L);
+  const int i = threadIdx.x >> 3, cg = threadIdx.x & 7;
+  const bool row_ok = i < T.rcnt;
+  const int c40 = T.seg * kSeg + cg;  // float4 column of v = 0; v-th is c40 + 8 v
+  const int64_t q0 = L.q_off + (int64_t)T.seg * SC * RP;
+  const int segcols = min(SC, L.ld - T.seg * SC);
+  // staging: column fastest, so consecutive threads store to consecutive words
+  for (int e = threadIdx.x; e < RP * SC; e += blockDim.x) {
+    const int k = e / SC, c = e - k * SC;
+    s_qT[e] = c < segcols ? __ldg(a.Qbar + q0 + (int64_t)c * RP + k) : 0.f;
+  }
+  for (int e = threadIdx.x; e < TR * RP; e += blockDim.x)
+    s_pp[e] = (T.prev && e < T.rcnt * RP) ? __ldg(a.Phat + L.p_off + (int64_t)T.row0 * RP + e) : 0.f;
+  float pacc[RP];
+#pragma unroll
+  for (int k = 0; k < RP; ++k) pacc[k] = 0.f;
+  for (int w = 0; w < a.W; ++w) {
+    __syncthreads();  // the previous worker's Q_w' rows are no longer read
+    if (T.prev) {
+      const float* qw = a.Qw + (int64_t)w * a.q_total + q0;
+      for (int e = threadIdx.x; e < RP * SC; e += blockDim.x) {
+        const int k = e / SC, c = e - k * SC;
+        s_qwT[e] = c < segcols ? __ldg(qw + (int64_t)c * RP + k) : 0.f;
+      }
+    }
+    __syncthreads();
+    const float* Gw = a.G[w] + L.off + (int64_t)(T.row0 + i) * L.ld;
+    float* Bw = a.B + (int64_t)w * a.total + L.off + (int64_t)(T.row0 + i) * L.ld;
+    float g[16], m[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int c4 = c40 + 8 * v;
+      float4 gv = zero4(), bv = zero4();
+      if (row_ok && c4 < L.F) {
+        gv = __ldcs(reinterpret_cast<const float4*>(Gw) + c4);
+        bv = __ldcs(reinterpret_cast<const float4*>(Bw) + c4);
+      }
+      g[4 * v] = gv.x; g[4 * v + 1] = gv.y; g[4 * v + 2] = gv.z; g[4 * v + 3] = gv.w;
+      m[4 * v] = bv.x; m[4 * v + 1] = bv.y; m[4 * v + 2] = bv.z; m[4 * v + 3] = bv.w;
+    }
+    if (T.prev) {
+#pragma unroll 4
+      for (int k = 0; k < RP; ++k) {
+        const float p = s_pp[i * RP + k];
+        const float4* qk = reinterpret_cast<const float4*>(s_qwT + k * SC) + cg;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const float4 q = qk[8 * v];
+          m[4 * v] = fmaf(-p, q.x, m[4 * v]);
+          m[4 * v + 1] = fmaf(-p, q.y, m[4 * v + 1]);
+          m[4 * v + 2] = fmaf(-p, q.z, m[4 * v + 2]);
+          m[4 * v + 3] = fmaf(-p, q.w, m[4 * v + 3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int c4 = c40 + 8 * v;
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int col = 4 * c4 + x;
+        m[4 * v + x] = (col < L.m) ? g[4 * v + x] + m[4 * v + x] : 0.f;
+      }
+      if (row_ok && c4 < L.F)
+        reinterpret_cast<float4*>(Bw)[c4] = make_float4(m[4 * v], m[4 * v + 1], m[4 * v + 2], m[4 * v + 3]);
+    }
+    // P partial: for each rank, the thread's 16 columns in order; workers in order
+#pragma unroll 4
+    for (int k = 0; k < RP; ++k) {
+      const float4* qk = reinterpret_cast<const float4*>(s_qT + k * SC) + cg;
+      float acc = pacc[k];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const float4 q = qk[8 * v];
+        acc = fmaf(m[4 * v], q.x, acc);
+        acc = fmaf(m[4 * v + 1], q.y, acc);
+        acc = fmaf(m[4 * v + 2], q.z, acc);
+        acc = fmaf(m[4 * v + 3], q.w, acc);
+      }
+      pacc[k] = acc;
+    }
+  }
+  // sum the 8 column groups of each row (lanes 8 (i % 4) + cg): a fixed
+  // butterfly that leaves lane cg with ranks [base, base + RP / 8)
+  {
+    int base = 0;
+#pragma unroll
+    for (int l = 0; l < 3; ++l) {
+      const int o = 4 >> l;             // lane bit 2, 1, 0 of cg
+      const int half = RP >> (l + 1);   // values still held / 2
+      const bool up = (cg & o) != 0;
+#pragma unroll
+      for (int x = 0; x < half; ++x) {
+        const float send = up ? pacc[x] : pacc[x + half];
+        const float keep = up ? pacc[x + half] : pacc[x];
+        pacc[x] = keep + __shfl_xor_sync(kFull, send, o);
+      }
+      if (up) base += half;
+    }
+    if (row_ok)
+#pragma unroll
+      for (int x = 0; x < RP / 8; ++x) s_prow[i * RP + base + x] = pacc[x];
+  }
+  __syncthreads();
+  p1_rows_done<RP>(a, L, T, s_prow, s_gram, &s_flag);
+}
+
+// Decompress, r >= 16: thread = one column of the segment (its Q rows, RP
+// floats, in registers), rows walked with the Phat rows broadcast from
+// shared memory; vector layers as in u_kernel.
+template <int RP>
+__global__ void __launch_bounds__(kSeg * 4) ut_kernel(const StepArgs a) {
+  constexpr int RU = Cfg<RP>::RU;
+  __shared__ __align__(16) float s_ph[RU * RP];
+  const Tile t = a.tiles[blockIdx.x];
+  if (t.c == 1) {  // vector layer: U = mean_w G_w
+    const VecDev V = a.vecs[t.layer];
+    const int base = t.a * kVChunk;
+    const int end = min(V.n, base + kVChunk);
+    for (int i = base + (int)threadIdx.x; i < end; i += blockDim.x) {
+      float s = 0.f;
+      for (int w = 0; w < a.W; ++w) s += __ldcs(a.G[w] + V.off + i);
+      const float u = s / (float)a.W;
+      if (a.U) a.U[V.off + i] = u;
+      if (a.X) {
+        float x = a.X[V.off + i], mom = a.Mom[V.off + i];
+        momentum1(x, mom, u, a.lr, a.beta);
+        a.X[V.off + i] = x;
+        a.Mom[V.off + i] = mom;
+      }
+    }
+    return;
+  }
+  const LayerDev L = a.layers[t.layer];  // by value
+  const int row0 = t.a * L.ru, seg = t.b;
+  const int rcnt = min(L.ru, L.n - row0);
+  for (int i = threadIdx.x; i < rcnt * RP; i += blockDim.x) s_ph[i] = __ldg(a.Phat + L.p_off + (int64_t)row0 * RP + i);
+  __syncthreads();
+  const int col = seg * kSeg * 4 + threadIdx.x;
+  if (col >= L.ld) return;
+  float q[RP];
+  {
+    const float4* qs = reinterpret_cast<const float4*>(a.Qbar + L.q_off + (int64_t)col * RP);
+#pragma unroll
+    for (int k4 = 0; k4 < RP / 4; ++k4) {
+      const float4 v = __ldg(qs + k4);
+      q[4 * k4] = v.x; q[4 * k4 + 1] = v.y; q[4 * k4 + 2] = v.z; q[4 * k4 + 3] = v.w;
+    }
+  }
+  const bool valid = col < L.m;
+  for (int r = 0; r < rcnt; ++r) {
+    const float4* ph = reinterpret_cast<const float4*>(s_ph + r * RP);
+    float u = 0.f;
+#pragma unroll
+    for (int k4 = 0; k4 < RP / 4; ++k4) {
+      const float4 p = ph[k4];
+      u = fmaf(p.x, q[4 * k4], u);
+      u = fmaf(p.y, q[4 * k4 + 1], u);
+      u = fmaf(p.z, q[4 * k4 + 2], u);
+      u = fmaf(p.w, q[4 * k4 + 3], u);
+    }
+    const int64_t pos = L.off + (int64_t)(row0 + r) * L.ld + col;
+    if (a.U) __stcs(a.U + pos, u);
+    if (a.X && valid) {
+      float x = a.X[pos], mom = a.Mom[pos];
+      momentum1(x, mom, u, a.lr, a.beta);
+      a.X[pos] = x;
+      a.Mom[pos] = mom;
+    }
   }
 }
 

@@ -135,7 +135,7 @@ extern "C" int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers
   L.ppart_off = 0;
   L.cnt_off = 0;
   sp.ntiles[kProject] = (int)((int64_t)L.nrb * L.S);
-  sp.ntiles[kOrthonormalise] = ks->fuse_ph ? 0 : (int)ceil_div(n, kPHThreads);
+  sp.ntiles[kOrthonormalise] = (int)ceil_div(n, kPHThreads);
   sp.ntiles[kBackProject] = (int)((int64_t)L.t3r * L.S * W);
   sp.ntiles[kDecompress] = (int)(ceil_div(n, L.ru) * L.S);
   const int NG = rp * (rp + 1) / 2;

@@ -11,12 +11,21 @@ namespace {
 constexpr int kRP = PSGD_RP;
 constexpr size_t kP3Dyn = (size_t)(kP3Threads / 32) * 32 * 4 * kRP * sizeof(float);
 
+#if PSGD_RP >= 16
+// r >= 16: the register-tiled kernels
+constexpr size_t kP1TDyn = (size_t)(2 * kRP * kSeg * 4 + 32 * kRP) * sizeof(float);
+#endif
+
 cudaError_t launch(int phase, const StepArgs& a, int tiles, cudaStream_t s) {
   if (tiles <= 0) return cudaSuccess;
   switch (phase) {
     case kProject: {
+#if PSGD_RP >= 16
+      p1t_kernel<kRP><<<tiles, kTThreads, kP1TDyn, s>>>(a);
+#else
       const int warps = a.W < Cfg<kRP>::P1_WARPS ? a.W : Cfg<kRP>::P1_WARPS;
       p1_kernel<kRP><<<tiles, 32 * warps, 0, s>>>(a);
+#endif
       break;
     }
     case kOrthonormalise:
@@ -26,7 +35,11 @@ cudaError_t launch(int phase, const StepArgs& a, int tiles, cudaStream_t s) {
       p3_kernel<kRP><<<tiles, kP3Threads, kP3Dyn, s>>>(a);
       break;
     case kDecompress:
+#if PSGD_RP >= 16
+      ut_kernel<kRP><<<tiles, kSeg * 4, 0, s>>>(a);
+#else
       u_kernel<kRP><<<tiles, kUThreads, 0, s>>>(a);
+#endif
       break;
     default:
       return cudaErrorInvalidValue;
@@ -46,11 +59,23 @@ cudaError_t launch_error(float* E, const float* B, const float* Phat, const floa
 
 cudaError_t prepare() {
   cudaError_t e = cudaFuncSetAttribute(p3_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP3Dyn);
+#if PSGD_RP >= 16
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(p1t_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP1TDyn);
+#endif
   return e;
 }
 
 cudaError_t occupancy(int phase, int W, int* ctas) {
   switch (phase) {
+#if PSGD_RP >= 16
+    case kProject:
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p1t_kernel<kRP>, kTThreads, kP1TDyn);
+    case kBackProject:
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p3_kernel<kRP>, kP3Threads, kP3Dyn);
+    case kDecompress:
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, ut_kernel<kRP>, kSeg * 4, 0);
+#else
     case kProject: {
       const int warps = W < Cfg<kRP>::P1_WARPS ? W : Cfg<kRP>::P1_WARPS;
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p1_kernel<kRP>, 32 * warps, 0);
@@ -59,6 +84,7 @@ cudaError_t occupancy(int phase, int W, int* ctas) {
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p3_kernel<kRP>, kP3Threads, kP3Dyn);
     case kDecompress:
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, u_kernel<kRP>, kUThreads, 0);
+#endif
     default:
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, ph_kernel<kRP>, kPHThreads, 0);
   }
@@ -67,7 +93,6 @@ cudaError_t occupancy(int phase, int W, int* ctas) {
 }  // namespace
 
 extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {
-    kRP, launch, launch_error, prepare, occupancy, Cfg<kRP>::R1, Cfg<kRP>::RU, Cfg<kRP>::RSB,
-    Cfg<kRP>::FUSE_PH};
+    kRP, launch, launch_error, prepare, occupancy, Cfg<kRP>::R1, Cfg<kRP>::RU, Cfg<kRP>::RSB};
 
 }  // namespace psgd
