@@ -323,6 +323,57 @@ def test_planted_momentum_mistakes_are_caught(kind):
         check_momentum_update(mutant)
 
 
+def check_unbiased(compress):
+    rng = np.random.default_rng(13)
+    n, m, W = 10, 6, 2
+    G = [rng.standard_normal((n, m)) for _ in range(W)]
+    Gbar = sum(G) / W
+    # a Q with Q Q^T = r I exactly (r = m, Q = sqrt(r) I): U is the mean gradient
+    _, U = compress(G, math.sqrt(m) * np.eye(m))
+    np.testing.assert_allclose(U, Gbar, rtol=0, atol=1e-12)
+    # unbiasedness: the mean of U over many fresh N(0,1) draws of Q approaches
+    # the mean gradient within a few standard errors
+    r, K = 2, 4000
+    Us = np.stack([compress(G, O.q_init(O.step_seed(99, t), 0, m, r).astype(np.float64))[1] for t in range(K)])
+    se = Us.std(axis=0) / math.sqrt(K)
+    assert np.max(np.abs(Us.mean(axis=0) - Gbar) / se) < 5.0
+    # and a single draw is far from it (the estimate is noisy, not exact)
+    assert np.linalg.norm(Us[0] - Gbar) > 0.1 * np.linalg.norm(Gbar)
+
+
+def test_unbiased_variant():
+    check_unbiased(O.unbiased_compress)
+    # fresh Q per step: distinct steps, same seed -> distinct draws; deterministic
+    a = O.q_init(O.step_seed(5, 0), 1, 7, 2)
+    assert not np.allclose(a, O.q_init(O.step_seed(5, 1), 1, 7, 2))
+    np.testing.assert_array_equal(a, O.q_init(O.step_seed(5, 0), 1, 7, 2))
+    # only P travels: n r per matrix, vectors whole
+    layers = workloads.resnet18_cifar_layers()
+    assert O.unbiased_data_sent(layers, 2) == 2 * sum(n for n, m in layers if m) + sum(n for n, m in layers if not m)
+    # the layer-set step averages vectors and compresses matrices with step t's Q
+    rng = np.random.default_rng(3)
+    lay = [(8, 5), (4, 0)]
+    grads = [[rng.standard_normal((8, 5)), rng.standard_normal(4)] for _ in range(3)]
+    out = O.unbiased_step(grads, lay, 2, seed=7, step=4)
+    Q = O.q_init(O.step_seed(7, 4), 0, 5, 2).astype(np.float64)
+    np.testing.assert_allclose(out.Qbar[0], Q, atol=0)
+    np.testing.assert_allclose(out.U[1], sum(g[1] for g in grads) / 3, atol=1e-15)
+
+
+@pytest.mark.parametrize("kind", ["no_rank_scale", "sum_not_mean", "off_scale"])
+def test_planted_unbiased_mistakes_are_caught(kind):
+    def mutant(G, Q):
+        W, r = len(G), Q.shape[1]
+        P = sum(np.asarray(g, dtype=np.float64) @ Q for g in G)
+        if kind == "no_rank_scale":
+            return P, P @ Q.T / W
+        if kind == "sum_not_mean":
+            return P, P @ Q.T / r
+        return P, (P @ Q.T / (W * r)) * (1.0 + 1e-3)
+    with pytest.raises(AssertionError):
+        check_unbiased(mutant)
+
+
 # ------------------------------------------------- planted mistakes -----
 
 def _mutant_compress(kind):
