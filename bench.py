@@ -83,6 +83,16 @@ def algorithmic_bytes(cfg: workloads.Workload, with_update: bool, momentum: bool
     return {"core": core, "update": upd, "vectors": vec, "total": core + upd + vec}
 
 
+def unbiased_bytes(cfg: workloads.Workload) -> dict:
+    """Minimum HBM bytes of one step of the unbiased variant: every worker's
+    gradient read once, P (n r) written, U (n m) written; vectors as above."""
+    W, r = cfg.workers, cfg.rank
+    core = sum(W * n * m * 4 + 4 * n * r for n, m in cfg.matrices)
+    upd = sum(4 * n * m for n, m in cfg.matrices)
+    vec = sum(4 * (W + 1) * n for n, _ in cfg.vectors)
+    return {"core": core, "update": upd, "vectors": vec, "total": core + upd + vec}
+
+
 def compressed_bytes(cfg: workloads.Workload) -> int:
     """Gradient bytes compressed per step: W x sum n m x 4."""
     return cfg.workers * sum(n * m for n, m in cfg.matrices) * 4
@@ -276,7 +286,8 @@ def run_ours(args, ws, rank, local):
     torch.cuda.set_device(device)
     cfg = config_of(args.config)
     stream = torch.cuda.Stream(device=device)
-    ctx = PowerSGD(cfg.layers, cfg.rank, cfg.workers, seed=cfg.seed, stream=stream, timing=True)
+    ctx = PowerSGD(cfg.layers, cfg.rank, cfg.workers, seed=cfg.seed, stream=stream, timing=True,
+                   unbiased=args.unbiased)
     sets = 3
     grads = fill_gradients(ctx, cfg, sets, device)
     upd = ctx.empty_buffer()
@@ -291,7 +302,7 @@ def run_ours(args, ws, rank, local):
     else:
         def one_step(g):
             ctx.step(g, upd)
-    ab = algorithmic_bytes(cfg, with_update=True, momentum=args.momentum)
+    ab = unbiased_bytes(cfg) if args.unbiased else algorithmic_bytes(cfg, with_update=True, momentum=args.momentum)
     comp = compressed_bytes(cfg)
     st = ctx.stats()
 
@@ -321,12 +332,12 @@ def run_ours(args, ws, rank, local):
     ms_per_step, value = replica_throughput(comp, args.steps, ev0.elapsed_time(ev1), ws, device)
     peaks = measured_peaks()
     project_ms = phases["project"]
-    project_bytes = ab["core"]  # read G, read E, write E of every worker (+ the factors)
+    project_bytes = ab["core"]  # read G, read E, write E of every worker (+ the factors); unbiased: read G
     achieved = project_bytes / (project_ms * 1e-3) / 1e9
     step_achieved = ab["total"] / (ms_per_step * 1e-3) / 1e9
     h = kernel_sources_hash()
     traffic = None
-    if args.config in NCU_TRAFFIC and NCU_TRAFFIC[args.config][0] == h:
+    if not args.unbiased and not args.momentum and args.config in NCU_TRAFFIC and NCU_TRAFFIC[args.config][0] == h:
         traffic = NCU_TRAFFIC[args.config][1]
 
     # end to end through the C ABI with host buffers (pinned), copies inside
@@ -341,12 +352,14 @@ def run_ours(args, ws, rank, local):
                    "l2": "inputs larger than L2: 3 rotating gradient sets of "
                          f"{comp / 1e6:.1f} MB + error buffers {comp / 1e6:.1f} MB per step",
                    "seed": cfg.seed, "out_update": not args.momentum,
-                   "fused_momentum_update": bool(args.momentum), "tile_rows": st["tile_rows"]},
+                   "fused_momentum_update": bool(args.momentum), "variant": "unbiased" if args.unbiased else "powersgd",
+                   "tile_rows": st["tile_rows"]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                      "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
                      else "fallback 6.8 TB/s",
-                     "kernel": f"psgd::p1_kernel<{st['kernel_rank']}> (project: error add, E write, P = M Q)",
+                     "kernel": (f"psgd::p1_kernel<{st['kernel_rank']}> (project: P = G Q)" if args.unbiased else
+                                f"psgd::p1_kernel<{st['kernel_rank']}> (project: error add, E write, P = M Q)"),
                      "algorithmic_bytes_per_launch": project_bytes, "launch_ms": round(project_ms, 5),
                      "kernel_sources": h},
         "step_roofline": {"achieved": round(step_achieved, 1), "frac": round(step_achieved / peaks["hbm_gbs"], 4),
@@ -412,6 +425,8 @@ def main():
     ap.add_argument("--config", default="c2")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for the CPU leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unbiased", action="store_true",
+                    help="time the unbiased rank-r variant (fresh shared Q per step, no error feedback)")
     ap.add_argument("--momentum", action="store_true",
                     help="time psgd_step_momentum (step + fused momentum-SGD update) instead of psgd_step")
     args = ap.parse_args()

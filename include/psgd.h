@@ -29,7 +29,8 @@
  * every layer l sits at element offset psgd_layer_info(..).offset, 16-byte
  * aligned; a matrix layer is row-major n x ld with ld = m rounded up to a
  * multiple of 4 (the ld - m padding columns are ignored on input and written
- * as 0 on output); a vector layer is n contiguous floats.  The decompressed
+ * as 0 on output); a vector layer is n contiguous floats (the floats after it,
+ * up to the next layer, are neither read nor written).  The decompressed
  * update (out_update) uses the same layout.
  *
  * Ownership: the caller owns the gradient buffers and out_update.  The library
@@ -88,8 +89,24 @@ typedef struct {
 typedef struct {
   int32_t timing;       /* 1: time every phase of every step with CUDA events (psgd_get_phase_times) */
   int32_t project_rows; /* rows per project tile (0: chosen so the grid holds several waves of CTAs) */
-  int32_t reserved[2];
+  int32_t unbiased;     /* 1: the unbiased rank-r variant (see below) instead of PowerSGD */
+  int32_t reserved;
 } psgd_options;
+
+/*
+ * The unbiased rank-r variant (options.unbiased = 1).  The PowerSGD review
+ * page (main findings, bullet 4) sets PowerSGD's biased, error-fed compressor
+ * against an unbiased rank-r one without defining it; the reading taken is
+ * the random-projection estimate.  Every step draws a fresh Q (m x r, N(0,1))
+ * from a seed all workers share -- the draw of psgd_create with the seed
+ * replaced by the splitmix64 output of seed + (t + 1) * 0x9E3779B97F4A7C15 for
+ * step t (the t-th psgd_step of the context, from 0) -- and computes
+ *     P = sum_w G_w Q   (the one all-reduce: only P is sent, n r floats)
+ *     U = P Q^T / (W r) (unbiased: E[Q Q^T] = r I)
+ * with no error feedback, no warm start and no orthonormalisation.  In this
+ * variant psgd_get_PQ returns P and the step's Q, psgd_get_error returns
+ * zeros, and psgd_get_Qw and psgd_set_state answer PSGD_ERR_INVALID.
+ */
 
 /*
  * Create a context for num_layers layers.  Layer l is an n[l] x m[l] matrix,

@@ -55,7 +55,8 @@ class Stats(ctypes.Structure):
 
 
 class Options(ctypes.Structure):
-    _fields_ = [("timing", ctypes.c_int32), ("project_rows", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
+    _fields_ = [("timing", ctypes.c_int32), ("project_rows", ctypes.c_int32), ("unbiased", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -159,7 +160,7 @@ class PowerSGD:
     """
 
     def __init__(self, shapes: Sequence[Tuple[int, int]], rank: int, workers: int, seed: int = 0,
-                 stream=None, timing: bool = False, project_rows: int = 0):
+                 stream=None, timing: bool = False, project_rows: int = 0, unbiased: bool = False):
         import torch
 
         if not torch.cuda.is_available():
@@ -169,7 +170,7 @@ class PowerSGD:
         self.device = torch.device("cuda", torch.cuda.current_device())
         self._stream = stream
         n, m = _shapes(self.shapes)
-        opt = Options(int(bool(timing)), int(project_rows))
+        opt = Options(int(bool(timing)), int(project_rows), int(bool(unbiased)))
         h = _P()
         _check(lib().psgd_create_ex(ctypes.byref(h), len(self.shapes), n, m, self.rank, self.workers,
                                     ctypes.c_uint64(self.seed), _stream_ptr(stream), ctypes.byref(opt)))

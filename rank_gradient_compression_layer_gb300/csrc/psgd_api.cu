@@ -81,6 +81,15 @@ void layout(int num_layers, const int64_t* n, const int64_t* m, int64_t* off, in
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Seed of step t's fresh Q in the unbiased variant: the splitmix64 output
+// function (Steele, Lea & Flood 2014) of seed + (t + 1) * golden gamma.
+uint64_t step_seed(uint64_t seed, int64_t step) {
+  uint64_t z = seed + (uint64_t)(step + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
 bool is_device_ptr(const void* p) {
   cudaPointerAttributes at;
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
@@ -148,6 +157,7 @@ struct psgd_ctx {
   int64_t timed_since = 0;      // steps recorded since the last psgd_get_phase_times
   int tile_rows[3] = {0, 0, 0};  // project rows, least back-project rows, decompress rows
   int has_prev = 0;
+  bool unbiased = false;  // psgd_options.unbiased: fresh shared Q per step, no error feedback
   bool broken = false;
   // stats
   int64_t steps = 0, sent_step = 0, unc_step = 0, mat_el = 0, vec_el = 0;
@@ -292,6 +302,7 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   c->seed = seed;
   c->ks = kernels_for(c->rp);
   c->timing = opt && opt->timing;
+  c->unbiased = opt && opt->unbiased;
   if (cudaGetDevice(&c->device) != cudaSuccess) {
     cudaGetLastError();
     delete c;
@@ -348,12 +359,14 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     if (L.S > 1) c->ppart_total += (int64_t)L.nrb * L.S * c->ks->r1 * rp;
     L.cnt_off = (int32_t)c->n_counters;
     c->n_counters += ncnt;
-    c->pack.push_back({L.p_off, L.q_off, c->msg_floats, L.n, L.m});
-    c->msg_floats += (n[l] + m[l]) * rank;
+    // the message: Phat and Qbar; the unbiased variant sends P alone
+    const int64_t sent = c->unbiased ? n[l] * rank : (n[l] + m[l]) * rank;
+    c->pack.push_back({L.p_off, L.q_off, c->msg_floats, L.n, c->unbiased ? 0 : L.m});
+    c->msg_floats += sent;
     c->mat_of[l] = (int)c->hl.size();
     c->hl.push_back(L);
     c->mat_el += n[l] * m[l];
-    c->sent_step += (n[l] + m[l]) * rank;
+    c->sent_step += sent;
     c->unc_step += n[l] * m[l];
   }
   build_tiles(c);
@@ -478,6 +491,8 @@ int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, flo
   a.Mom = Mom;
   a.lr = lr;
   a.beta = beta;
+  a.unbiased = c->unbiased ? 1 : 0;
+  a.u_scale = 1.0f / ((float)c->W * (float)c->rank);
   // the decompress phase only writes U and the optional update
   const int phases = (out_update || X) ? kPhases : kPhases - 1;
   cudaEvent_t* ev = nullptr;
@@ -486,8 +501,19 @@ int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, flo
     c->timed_since += 1;
     CUDA_TRY(cudaEventRecord(ev[0], c->stream));
   }
+  if (c->unbiased && !c->hl.empty()) {
+    // this step's Q: N(0,1) draws from the step's seed, shared by all workers
+    dim3 grid(64, (unsigned)c->hl.size());
+    q_init_kernel<<<grid, 256, 0, c->stream>>>(c->Qbar, c->d_layers, c->rank, c->rp, step_seed(c->seed, c->steps));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      c->broken = true;
+      return cuda_fail(e, "Q draw launch");
+    }
+  }
   for (int ph = 0; ph < kPhases; ++ph) {
-    if (ph < phases) {
+    const bool skip = c->unbiased && (ph == kOrthonormalise || ph == kBackProject);
+    if (ph < phases && !skip) {
       a.tiles = c->d_tiles[ph];
       cudaError_t e = c->ks->launch(ph, a, (int)c->tiles[ph].size(), c->stream);
       if (e != cudaSuccess) {
@@ -570,7 +596,8 @@ int psgd_step_host(psgd_ctx* c, const float* const* grad_host, float* msg_host, 
   if (rc) return rc;
   if (!c->pack.empty()) {
     dim3 grid(32, (unsigned)c->pack.size());
-    pack_msg_kernel<<<grid, 256, 0, c->stream>>>(c->stage_msg, c->Phat, c->Qbar, c->d_pack, c->rank, c->rp);
+    pack_msg_kernel<<<grid, 256, 0, c->stream>>>(c->stage_msg, c->unbiased ? c->P : c->Phat, c->Qbar, c->d_pack,
+                                                 c->rank, c->rp);
     CUDA_TRY(cudaGetLastError());
     CUDA_TRY(cudaMemcpyAsync(msg_host, c->stage_msg, (size_t)c->msg_floats * sizeof(float),
                              cudaMemcpyDeviceToHost, c->stream));
@@ -587,7 +614,7 @@ int psgd_get_PQ(psgd_ctx* c, int layer, float* P, float* Q) {
   const LayerDev* L;
   if ((rc = matrix_layer(c, layer, &L))) return rc;
   const size_t rb = (size_t)c->rank * sizeof(float), pb = (size_t)c->rp * sizeof(float);
-  if (P) CUDA_TRY(cudaMemcpy2DAsync(P, rb, c->Phat + L->p_off, pb, rb, L->n, cudaMemcpyDefault, c->stream));
+  if (P) CUDA_TRY(cudaMemcpy2DAsync(P, rb, (c->unbiased ? c->P : c->Phat) + L->p_off, pb, rb, L->n, cudaMemcpyDefault, c->stream));
   if (Q) CUDA_TRY(cudaMemcpy2DAsync(Q, rb, c->Qbar + L->q_off, pb, rb, L->m, cudaMemcpyDefault, c->stream));
   return sync_and_check(c);
 }
@@ -599,6 +626,7 @@ int psgd_get_Qw(psgd_ctx* c, int layer, int worker, float* Q) {
   if ((rc = matrix_layer(c, layer, &L))) return rc;
   if (worker < 0 || worker >= c->W) return fail(PSGD_ERR_INVALID, "worker %d out of range", worker);
   if (!Q) return fail(PSGD_ERR_INVALID, "Q must not be NULL");
+  if (c->unbiased) return fail(PSGD_ERR_INVALID, "the unbiased variant forms no Q_w");
   const size_t rb = (size_t)c->rank * sizeof(float), pb = (size_t)c->rp * sizeof(float);
   CUDA_TRY(cudaMemcpy2DAsync(Q, rb, c->Qw + (int64_t)worker * c->q_total + L->q_off, pb, rb, L->m,
                              cudaMemcpyDefault, c->stream));
@@ -615,6 +643,14 @@ int psgd_get_error(psgd_ctx* c, int layer, int worker, float* E) {
   const int64_t nm = (int64_t)L->n * L->m;
   float* dst = E;
   const bool dev = is_device_ptr(E);
+  if (c->unbiased) {  // no error feedback: the error is zero
+    if (dev) {
+      CUDA_TRY(cudaMemsetAsync(E, 0, (size_t)nm * sizeof(float), c->stream));
+      return sync_and_check(c);
+    }
+    std::memset(E, 0, (size_t)nm * sizeof(float));
+    return PSGD_OK;
+  }
   if (!dev) {
     if (c->e_scratch_elems < nm) {
       if (c->e_scratch) cudaFree(c->e_scratch);
@@ -638,6 +674,7 @@ int psgd_set_state(psgd_ctx* c, int layer, const float* Q, const float* const* E
   const LayerDev* L;
   if ((rc = matrix_layer(c, layer, &L))) return rc;
   if (!Q) return fail(PSGD_ERR_INVALID, "Q must not be NULL");
+  if (c->unbiased) return fail(PSGD_ERR_INVALID, "the unbiased variant keeps no state");
   if (E)
     for (int w = 0; w < c->W; ++w)
       if (!E[w]) return fail(PSGD_ERR_INVALID, "E[%d] is NULL", w);
@@ -671,7 +708,8 @@ int psgd_get_stats(const psgd_ctx* c, psgd_stats* out) {
   for (int ph = 0; ph < kPhases; ++ph) out->tiles[ph] = (int64_t)c->tiles[ph].size();
   out->kernel_rank = c->rp;
   for (int i = 0; i < 3; ++i) out->tile_rows[i] = c->tile_rows[i];
-  out->launches_per_step = kPhases;
+  out->launches_per_step = kPhases;  // the unbiased variant: Q draw, project, decompress
+  if (c->unbiased) out->launches_per_step = 3;
   return PSGD_OK;
 }
 

@@ -83,6 +83,10 @@ struct StepArgs {
   float* Mom;
   float lr;
   float beta;
+  // unbiased variant: M = G (no error feedback, B untouched), P kept as is
+  // (no Gram tail, no back-project), U = u_scale P Q^T with Q the step's draw
+  int32_t unbiased;
+  float u_scale;
 };
 
 }  // namespace psgd

@@ -50,7 +50,7 @@ struct Cfg {
   static constexpr int R3C = 256;
   static constexpr int UNR3 = RP <= 4 ? 16 : 8;
   // decompress: RU rows x one segment per CTA of 256 threads
-  static constexpr int RU = 64;
+  static constexpr int RU = 128;
 };
 
 constexpr int kP3Threads = 256;
@@ -236,7 +236,7 @@ __device__ void gram_tail(const StepArgs& a, const LayerDev& L, int rb, const fl
 // Per-tile geometry and flags of the project phase.
 struct P1Tile {
   int rb, seg, row0, rcnt, lane, warp, nwarps, c;
-  bool act, tailc, prev;
+  bool act, tailc, prev, ub;  // ub: unbiased variant (M = G, B untouched)
 };
 
 template <int RP>
@@ -252,7 +252,8 @@ __device__ __forceinline__ P1Tile p1_tile(const StepArgs& a, const Tile& t, cons
   T.c = T.seg * kSeg + T.lane;  // this lane's float4 column
   T.act = T.c < L.F;
   T.tailc = T.act && (T.c == L.F - 1) && (L.tail < 4);
-  T.prev = a.has_prev != 0;
+  T.ub = a.unbiased != 0;
+  T.prev = a.has_prev != 0 && !T.ub;
   return T;
 }
 
@@ -310,7 +311,7 @@ __device__ __forceinline__ void p1_rows(const LayerDev& L, const P1Tile& T, cons
         if (L.tail < 3) m2 = 0.f;
         m3 = 0.f;
       }
-      *reinterpret_cast<float4*>(Bw + (int64_t)(T.row0 + sb + i) * L.ld) = make_float4(m0, m1, m2, m3);
+      if (!T.ub) *reinterpret_cast<float4*>(Bw + (int64_t)(T.row0 + sb + i) * L.ld) = make_float4(m0, m1, m2, m3);
 #pragma unroll
       for (int k = 0; k < RP; ++k) {
         float t = m0 * qv[0][k];
@@ -359,6 +360,7 @@ __device__ __forceinline__ void p1_rows_done(const StepArgs& a, const LayerDev& 
   }
   for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x)
     a.P[L.p_off + (int64_t)T.row0 * RP + idx] = s_prow[idx];
+  if (T.ub) return;  // the unbiased variant sends P as it is
   gram_tail<RP>(a, L, T.rb, s_prow, T.rcnt, s_gram, s_flag);
 }
 
@@ -411,7 +413,7 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
         if (T.act && i < rn) {
           const int64_t o = (int64_t)(T.row0 + sb + i) * L.ld;
           g[i] = __ldcs(reinterpret_cast<const float4*>(Gw + o));
-          b[i] = __ldcs(reinterpret_cast<const float4*>(Bw + o));
+          b[i] = T.ub ? zero4() : __ldcs(reinterpret_cast<const float4*>(Bw + o));
         } else {
           g[i] = zero4();
           b[i] = zero4();
@@ -627,7 +629,8 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
   const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
   const int row0 = t.a * L.ru, seg = t.b;
   const int rcnt = min(L.ru, L.n - row0);
-  for (int i = threadIdx.x; i < rcnt * RP; i += blockDim.x) s_ph[i] = __ldg(a.Phat + L.p_off + (int64_t)row0 * RP + i);
+  const float* Psrc = a.unbiased ? a.P : a.Phat;
+  for (int i = threadIdx.x; i < rcnt * RP; i += blockDim.x) s_ph[i] = __ldg(Psrc + L.p_off + (int64_t)row0 * RP + i);
   __syncthreads();
   const int lane = threadIdx.x & 31, sub = threadIdx.x >> 5;  // 8 rows in flight per pass
   const int c = seg * kSeg + lane;
@@ -664,6 +667,12 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
       u2 = fmaf(p, qv[2][k], u2);
       u3 = fmaf(p, qv[3][k], u3);
     }
+    if (a.unbiased) {
+      u0 *= a.u_scale;
+      u1 *= a.u_scale;
+      u2 *= a.u_scale;
+      u3 *= a.u_scale;
+    }
     const int64_t pos = col + (int64_t)(row0 + r) * L.ld;
     if (a.U) __stcs(reinterpret_cast<float4*>(a.U + pos), make_float4(u0, u1, u2, u3));
     if (a.X) momentum4(a.X, a.Mom, pos, make_float4(u0, u1, u2, u3), valid, a.lr, a.beta);
@@ -671,17 +680,17 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
 }
 
 // ----------------------------------------------------------------------------
-// r >= 16: register-tiled project and decompress
+// r >= 8: register-tiled project and decompress
 // ----------------------------------------------------------------------------
 //
-// At r >= 16 the lane-per-4-columns project and decompress kernels would
+// At r >= 8 the lane-per-4-columns project and decompress kernels would
 // hold 8 r floats of Q rows per lane; these kernels instead spread the
 // r-wide dot products so that each value loaded from shared memory feeds
 // several fused multiply-adds.  (The back-project kernel serves every rank.)
 
 constexpr int kTThreads = 256;  // threads of a tiled project or decompress CTA
 
-// Project, r >= 16.  A CTA owns up to 32 rows x one segment (128 columns) and
+// Project, r >= 8.  A CTA owns up to 32 rows x one segment (128 columns) and
 // loops over the workers.  Thread (row i = tid / 8, column group cg = tid % 8)
 // owns the float4 columns cg, cg + 8, cg + 16, cg + 24 of its row (16
 // columns; each of the 8 threads of a row reads a different 16 bytes, so the
@@ -741,7 +750,7 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
       float4 gv = zero4(), bv = zero4();
       if (row_ok && c4 < L.F) {
         gv = __ldcs(reinterpret_cast<const float4*>(Gw) + c4);
-        bv = __ldcs(reinterpret_cast<const float4*>(Bw) + c4);
+        if (!T.ub) bv = __ldcs(reinterpret_cast<const float4*>(Bw) + c4);
       }
       g[4 * v] = gv.x; g[4 * v + 1] = gv.y; g[4 * v + 2] = gv.z; g[4 * v + 3] = gv.w;
       m[4 * v] = bv.x; m[4 * v + 1] = bv.y; m[4 * v + 2] = bv.z; m[4 * v + 3] = bv.w;
@@ -769,7 +778,7 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
         const int col = 4 * c4 + x;
         m[4 * v + x] = (col < L.m) ? g[4 * v + x] + m[4 * v + x] : 0.f;
       }
-      if (row_ok && c4 < L.F)
+      if (row_ok && c4 < L.F && !T.ub)
         reinterpret_cast<float4*>(Bw)[c4] = make_float4(m[4 * v], m[4 * v + 1], m[4 * v + 2], m[4 * v + 3]);
     }
     // P partial: for each rank, the thread's 16 columns in order; workers in order
@@ -813,7 +822,7 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
   p1_rows_done<RP>(a, L, T, s_prow, s_gram, &s_flag);
 }
 
-// Decompress, r >= 16: thread = one column of the segment (its Q rows, RP
+// Decompress, r >= 8: thread = one column of the segment (its Q rows, RP
 // floats, in registers), rows walked with the Phat rows broadcast from
 // shared memory; vector layers as in u_kernel.
 template <int RP>
@@ -842,7 +851,8 @@ __global__ void __launch_bounds__(kSeg * 4) ut_kernel(const StepArgs a) {
   const LayerDev L = a.layers[t.layer];  // by value
   const int row0 = t.a * L.ru, seg = t.b;
   const int rcnt = min(L.ru, L.n - row0);
-  for (int i = threadIdx.x; i < rcnt * RP; i += blockDim.x) s_ph[i] = __ldg(a.Phat + L.p_off + (int64_t)row0 * RP + i);
+  const float* Psrc = a.unbiased ? a.P : a.Phat;
+  for (int i = threadIdx.x; i < rcnt * RP; i += blockDim.x) s_ph[i] = __ldg(Psrc + L.p_off + (int64_t)row0 * RP + i);
   __syncthreads();
   const int col = seg * kSeg * 4 + threadIdx.x;
   if (col >= L.ld) return;
@@ -867,6 +877,7 @@ __global__ void __launch_bounds__(kSeg * 4) ut_kernel(const StepArgs a) {
       u = fmaf(p.z, q[4 * k4 + 2], u);
       u = fmaf(p.w, q[4 * k4 + 3], u);
     }
+    if (a.unbiased) u *= a.u_scale;
     const int64_t pos = L.off + (int64_t)(row0 + r) * L.ld + col;
     if (a.U) __stcs(a.U + pos, u);
     if (a.X && valid) {

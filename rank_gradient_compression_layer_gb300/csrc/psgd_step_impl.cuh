@@ -11,8 +11,8 @@ namespace {
 constexpr int kRP = PSGD_RP;
 constexpr size_t kP3Dyn = (size_t)(kP3Threads / 32) * 32 * 4 * kRP * sizeof(float);
 
-#if PSGD_RP >= 16
-// r >= 16: the register-tiled kernels
+#if PSGD_RP >= 8
+// r >= 8: the register-tiled kernels
 constexpr size_t kP1TDyn = (size_t)(2 * kRP * kSeg * 4 + 32 * kRP) * sizeof(float);
 #endif
 
@@ -20,7 +20,7 @@ cudaError_t launch(int phase, const StepArgs& a, int tiles, cudaStream_t s) {
   if (tiles <= 0) return cudaSuccess;
   switch (phase) {
     case kProject: {
-#if PSGD_RP >= 16
+#if PSGD_RP >= 8
       p1t_kernel<kRP><<<tiles, kTThreads, kP1TDyn, s>>>(a);
 #else
       const int warps = a.W < Cfg<kRP>::P1_WARPS ? a.W : Cfg<kRP>::P1_WARPS;
@@ -35,7 +35,7 @@ cudaError_t launch(int phase, const StepArgs& a, int tiles, cudaStream_t s) {
       p3_kernel<kRP><<<tiles, kP3Threads, kP3Dyn, s>>>(a);
       break;
     case kDecompress:
-#if PSGD_RP >= 16
+#if PSGD_RP >= 8
       ut_kernel<kRP><<<tiles, kSeg * 4, 0, s>>>(a);
 #else
       u_kernel<kRP><<<tiles, kUThreads, 0, s>>>(a);
@@ -59,7 +59,7 @@ cudaError_t launch_error(float* E, const float* B, const float* Phat, const floa
 
 cudaError_t prepare() {
   cudaError_t e = cudaFuncSetAttribute(p3_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP3Dyn);
-#if PSGD_RP >= 16
+#if PSGD_RP >= 8
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(p1t_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP1TDyn);
 #endif
@@ -68,7 +68,7 @@ cudaError_t prepare() {
 
 cudaError_t occupancy(int phase, int W, int* ctas) {
   switch (phase) {
-#if PSGD_RP >= 16
+#if PSGD_RP >= 8
     case kProject:
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, p1t_kernel<kRP>, kTThreads, kP1TDyn);
     case kBackProject:
