@@ -46,9 +46,8 @@ struct Cfg {
   static constexpr int R1 = 32;
   static constexpr int P1_WARPS = 8;                        // at most (more workers loop)
   static constexpr int P1_MINB = RP <= 2 ? 4 : (RP == 4 ? 3 : 1);          // 256-thread CTAs per SM the registers must allow
-  // back-project: row tiles staged by chunks of R3C Phat rows, 8 warps
-  static constexpr int R3C = 256;
-  static constexpr int UNR3 = RP <= 4 ? 16 : 8;
+  // back-project: 8 warps over interleaved groups of UNR3 rows
+  static constexpr int UNR3 = RP <= 2 ? 16 : 8;  // rows a warp loads at once (r = 4: 8 is faster)
   // decompress: RU rows x one segment per CTA of 256 threads
   static constexpr int RU = 128;
 };
@@ -510,10 +509,9 @@ __device__ void qf_segment_worker(const StepArgs& a, const LayerDev& L, int seg,
 
 template <int RP>
 __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
-  constexpr int R3C = Cfg<RP>::R3C;
   constexpr int UNR = Cfg<RP>::UNR3;
   constexpr int NW = kP3Threads / 32;
-  __shared__ float s_ph[R3C * RP];                // a chunk of Phat rows
+  __shared__ float s_ph[NW][UNR * RP];            // each warp's Phat rows of its current group
   extern __shared__ __align__(16) float s_red[];  // NW x 32 x 4 x RP
   __shared__ int s_flag;
   const Tile t = a.tiles[blockIdx.x];
@@ -525,34 +523,35 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
   const int c = seg * kSeg + lane;
   const bool act = c < L.F;
   const float* Bw = a.B + (int64_t)w * a.total + L.off + 4 * c;
+  const float* Ph = a.Phat + L.p_off + (int64_t)row0 * RP;
+  float* s_mine = s_ph[warp];
   float acc[4][RP];
 #pragma unroll
   for (int j = 0; j < 4; ++j)
 #pragma unroll
     for (int k = 0; k < RP; ++k) acc[j][k] = 0.f;
-  for (int r0 = 0; r0 < nrows; r0 += R3C) {
-    const int rn = min(R3C, nrows - r0);
-    __syncthreads();
-    for (int i = threadIdx.x; i < rn * RP; i += blockDim.x) s_ph[i] = a.Phat[L.p_off + (int64_t)(row0 + r0) * RP + i];
-    __syncthreads();
-    // warps take interleaved groups of UNR rows of the chunk
-    for (int i0 = warp * UNR; i0 < rn; i0 += NW * UNR) {
-      float4 bv[UNR];
+  // warps take interleaved groups of UNR rows; each warp stages the Phat
+  // rows of its own group (a warp barrier only), so no warp waits for another
+  for (int i0 = warp * UNR; i0 < nrows; i0 += NW * UNR) {
+    float4 bv[UNR];
 #pragma unroll
-      for (int u = 0; u < UNR; ++u)
-        bv[u] = (act && i0 + u < rn) ? __ldcs(reinterpret_cast<const float4*>(Bw + (int64_t)(row0 + r0 + i0 + u) * L.ld))
-                                     : zero4();
+    for (int u = 0; u < UNR; ++u)
+      bv[u] = (act && i0 + u < nrows) ? __ldcs(reinterpret_cast<const float4*>(Bw + (int64_t)(row0 + i0 + u) * L.ld))
+                                      : zero4();
+    const int ne = min(UNR, nrows - i0) * RP;
+    __syncwarp();  // the previous group's Phat rows are no longer read
+    for (int e = lane; e < ne; e += 32) s_mine[e] = __ldg(Ph + (int64_t)i0 * RP + e);
+    __syncwarp();
 #pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        if (i0 + u < rn) {
+    for (int u = 0; u < UNR; ++u) {
+      if (i0 + u < nrows) {
 #pragma unroll
-          for (int k = 0; k < RP; ++k) {
-            const float p = s_ph[(i0 + u) * RP + k];
-            acc[0][k] = fmaf(bv[u].x, p, acc[0][k]);
-            acc[1][k] = fmaf(bv[u].y, p, acc[1][k]);
-            acc[2][k] = fmaf(bv[u].z, p, acc[2][k]);
-            acc[3][k] = fmaf(bv[u].w, p, acc[3][k]);
-          }
+        for (int k = 0; k < RP; ++k) {
+          const float p = s_mine[u * RP + k];
+          acc[0][k] = fmaf(bv[u].x, p, acc[0][k]);
+          acc[1][k] = fmaf(bv[u].y, p, acc[1][k]);
+          acc[2][k] = fmaf(bv[u].z, p, acc[2][k]);
+          acc[3][k] = fmaf(bv[u].w, p, acc[3][k]);
         }
       }
     }
