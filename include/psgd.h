@@ -196,6 +196,16 @@ int psgd_get_stats(const psgd_ctx* ctx, psgd_stats* out);
  */
 int psgd_get_phase_times(psgd_ctx* ctx, float* ms);
 
+/*
+ * Turn the per-phase events on (on != 0) or off for the following steps,
+ * whatever options.timing said at creation.  The phase kernels are launched
+ * as programmatic dependents of the kernel before them, so each one's CTAs
+ * are resident when its predecessor ends; an event recorded between two
+ * phases orders them strictly again, so timed steps show each phase alone
+ * and untimed steps run with the launches overlapped.
+ */
+int psgd_set_timing(psgd_ctx* ctx, int on);
+
 /* Placement of layer l in a packed buffer: element offset, n, m, row stride. */
 int psgd_layer_info(const psgd_ctx* ctx, int layer, int64_t* offset, int64_t* n, int64_t* m,
                     int64_t* ld);

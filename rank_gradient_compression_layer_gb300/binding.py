@@ -24,7 +24,7 @@ EXPORTS = (
     "psgd_create", "psgd_create_ex", "psgd_destroy", "psgd_set_stream", "psgd_step", "psgd_step_host",
     "psgd_sync", "psgd_get_PQ", "psgd_get_Qw", "psgd_get_error", "psgd_set_state", "psgd_get_stats",
     "psgd_layer_info", "psgd_plan_layout", "psgd_count_sent", "psgd_last_error", "psgd_version",
-    "psgd_get_phase_times", "psgd_step_noalloc", "psgd_step_momentum",
+    "psgd_get_phase_times", "psgd_step_noalloc", "psgd_step_momentum", "psgd_set_timing",
 )
 
 PHASES = ("project", "orthonormalise", "back_project", "decompress")
@@ -95,6 +95,7 @@ def lib() -> ctypes.CDLL:
         "psgd_last_error": ([], ctypes.c_char_p),
         "psgd_version": ([], ctypes.c_char_p),
         "psgd_get_phase_times": ([_P, ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
+        "psgd_set_timing": ([_P, ctypes.c_int], ctypes.c_int),
         "psgd_step_noalloc": ([ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_P),
                                _P, _P, _P, _P, _P, ctypes.c_int, _P], ctypes.c_int),
     }
@@ -283,6 +284,10 @@ class PowerSGD:
         out["tiles"] = dict(zip(PHASES, list(s.tiles)))
         out["tile_rows"] = list(s.tile_rows)
         return out
+
+    def set_timing(self, on: bool) -> None:
+        """Per-phase events on or off for the following steps."""
+        _check(lib().psgd_set_timing(self._h, 1 if on else 0))
 
     def phase_times(self) -> dict:
         """Device milliseconds of each phase of the last step (context created with timing=True)."""

@@ -551,6 +551,18 @@ int psgd_sync(psgd_ctx* c) {
   return sync_and_check(c);
 }
 
+int psgd_set_timing(psgd_ctx* c, int on) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  if (on && c->ev.empty()) {
+    c->ev.assign((size_t)kTimedSteps * (kPhases + 1), nullptr);
+    for (auto& e : c->ev) CUDA_TRY(cudaEventCreate(&e));
+  }
+  c->timing = on != 0;
+  c->timed_since = 0;
+  return PSGD_OK;
+}
+
 int psgd_get_phase_times(psgd_ctx* c, float* ms) {
   int rc = ctx_ok(c);
   if (rc) return rc;

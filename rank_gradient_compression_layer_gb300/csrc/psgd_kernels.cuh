@@ -121,6 +121,16 @@ __device__ __forceinline__ void tri_index(int e, int rp, int& i, int& j) {
   j = i + e;
 }
 
+// Programmatic dependent launch (the phase kernels are launched as dependents
+// of the kernel before them in the stream): wait until that kernel has
+// completed and its writes are visible -- a no-op for a normal launch -- then
+// let the next kernel's CTAs be scheduled while this grid runs, so they are
+// resident and waiting when it ends.  Every phase kernel calls this first.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // Whole CTA: make the CTA's global writes visible, count one arrival on *cnt
 // and return true (in every thread) when this was arrival number `total`.
 // The last arriver resets the counter for the next launch and may then read
@@ -390,6 +400,7 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
   __shared__ float s_prow[R1 * RP];
   __shared__ double s_gram[RP * RP];
   __shared__ int s_flag;
+  pdl_enter();
   const Tile t = a.tiles[blockIdx.x];
   const LayerDev L = a.layers[t.layer];  // by value: stores to B cannot alias it
   const P1Tile T = p1_tile<RP>(a, t, L);
@@ -434,6 +445,7 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
 template <int RP>
 __global__ void __launch_bounds__(kPHThreads) ph_kernel(const StepArgs a) {
   __shared__ double s_r[RP * RP + RP];
+  pdl_enter();
   const Tile t = a.tiles[blockIdx.x];
   const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
   for (int e = threadIdx.x; e < RP * RP + RP; e += blockDim.x) s_r[e] = a.rinv[L.rinv_off + e];
@@ -514,6 +526,7 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
   __shared__ float s_ph[NW][UNR * RP];            // each warp's Phat rows of its current group
   extern __shared__ __align__(16) float s_red[];  // NW x 32 x 4 x RP
   __shared__ int s_flag;
+  pdl_enter();
   const Tile t = a.tiles[blockIdx.x];
   const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
   const int rt = t.a, seg = t.b, w = t.c;
@@ -606,6 +619,7 @@ template <int RP>
 __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
   constexpr int RU = Cfg<RP>::RU;
   __shared__ float s_ph[RU * RP];
+  pdl_enter();
   const Tile t = a.tiles[blockIdx.x];
   if (t.c == 1) {  // vector layer: U = mean_w G_w
     const VecDev V = a.vecs[t.layer];
@@ -712,6 +726,7 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
   __shared__ float s_prow[TR * RP];
   __shared__ double s_gram[RP * RP];
   __shared__ int s_flag;
+  pdl_enter();
   const Tile t = a.tiles[blockIdx.x];
   const LayerDev L = a.layers[t.layer];  // by value
   const P1Tile T = p1_tile<RP>(a, t, L);
@@ -828,6 +843,7 @@ template <int RP>
 __global__ void __launch_bounds__(kSeg * 4) ut_kernel(const StepArgs a) {
   constexpr int RU = Cfg<RP>::RU;
   __shared__ __align__(16) float s_ph[RU * RP];
+  pdl_enter();
   const Tile t = a.tiles[blockIdx.x];
   if (t.c == 1) {  // vector layer: U = mean_w G_w
     const VecDev V = a.vecs[t.layer];

@@ -16,35 +16,47 @@ constexpr size_t kP3Dyn = (size_t)(kP3Threads / 32) * 32 * 4 * kRP * sizeof(floa
 constexpr size_t kP1TDyn = (size_t)(2 * kRP * kSeg * 4 + 32 * kRP) * sizeof(float);
 #endif
 
+// A phase kernel launched as a programmatic dependent of the kernel before it
+// in the stream (the kernels wait for it in pdl_enter before touching data).
+cudaError_t launch_dependent(void (*kernel)(StepArgs), int tiles, int threads, size_t smem, cudaStream_t s,
+                             const StepArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 cudaError_t launch(int phase, const StepArgs& a, int tiles, cudaStream_t s) {
   if (tiles <= 0) return cudaSuccess;
   switch (phase) {
     case kProject: {
 #if PSGD_RP >= 8
-      p1t_kernel<kRP><<<tiles, kTThreads, kP1TDyn, s>>>(a);
+      return launch_dependent(p1t_kernel<kRP>, tiles, kTThreads, kP1TDyn, s, a);
 #else
       const int warps = a.W < Cfg<kRP>::P1_WARPS ? a.W : Cfg<kRP>::P1_WARPS;
-      p1_kernel<kRP><<<tiles, 32 * warps, 0, s>>>(a);
+      return launch_dependent(p1_kernel<kRP>, tiles, 32 * warps, 0, s, a);
 #endif
-      break;
     }
     case kOrthonormalise:
-      ph_kernel<kRP><<<tiles, kPHThreads, 0, s>>>(a);
-      break;
+      return launch_dependent(ph_kernel<kRP>, tiles, kPHThreads, 0, s, a);
     case kBackProject:
-      p3_kernel<kRP><<<tiles, kP3Threads, kP3Dyn, s>>>(a);
-      break;
+      return launch_dependent(p3_kernel<kRP>, tiles, kP3Threads, kP3Dyn, s, a);
     case kDecompress:
 #if PSGD_RP >= 8
-      ut_kernel<kRP><<<tiles, kSeg * 4, 0, s>>>(a);
+      return launch_dependent(ut_kernel<kRP>, tiles, kSeg * 4, 0, s, a);
 #else
-      u_kernel<kRP><<<tiles, kUThreads, 0, s>>>(a);
+      return launch_dependent(u_kernel<kRP>, tiles, kUThreads, 0, s, a);
 #endif
-      break;
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_error(float* E, const float* B, const float* Phat, const float* Qw, int n, int m, int ld,

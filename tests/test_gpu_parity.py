@@ -253,6 +253,15 @@ def test_phase_timing():
         assert all(v >= 0.0 for v in t.values()) and t["project"] > 0.0
         s = run.ctx.stats()
         assert s["launches_per_step"] in (3, 4) and s["tiles"]["project"] > 0
+        # timing off: steps still run, phase times are refused; on again: averaged anew
+        from rank_gradient_compression_layer_gb300 import PsgdError
+        run.ctx.set_timing(False)
+        run.step(workloads.gradients(cfg, 1, sig))
+        with pytest.raises(PsgdError):
+            run.ctx.phase_times()
+        run.ctx.set_timing(True)
+        run.step(workloads.gradients(cfg, 2, sig))
+        assert run.ctx.phase_times()["project"] > 0.0
     finally:
         run.close()
 
