@@ -154,13 +154,14 @@ int psgd_step_momentum(psgd_ctx* ctx, const float* const* grad_ptrs, float* para
                        float lr, float beta, float* out_update);
 
 /*
- * The same step fed from HOST memory: copies each worker's packed buffer
- * grad_host[w] (pinned host memory for an asynchronous copy) into device
- * staging buffers owned by the context (allocated on first use), runs
- * psgd_step, then copies the compressed message of every matrix layer
- * (Phat then Qbar, each row-major, layers in order: sum (n+m) r floats) into
- * msg_host and, when update_host is not NULL, the packed update into it.
- * Waits for the copies before returning.
+ * The same step fed from HOST memory.  A worker's packed buffer grad_host[w]
+ * in pinned (page-locked, mapped) host memory is read in place by the
+ * kernels over the CPU-GPU link; any other host buffer is first copied into a
+ * device staging buffer owned by the context (allocated on first use).  Then
+ * psgd_step runs, and the compressed message of every matrix layer (Phat
+ * then Qbar, each row-major, layers in order: sum (n+m) r floats; P alone in
+ * the unbiased variant) is copied into msg_host and, when update_host is not
+ * NULL, the packed update into it.  Waits for the copies before returning.
  */
 int psgd_step_host(psgd_ctx* ctx, const float* const* grad_host, float* msg_host, float* update_host);
 

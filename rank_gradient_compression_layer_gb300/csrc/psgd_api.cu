@@ -591,15 +591,26 @@ int psgd_step_host(psgd_ctx* c, const float* const* grad_host, float* msg_host, 
   if (rc) return rc;
   if (!grad_host || !msg_host) return fail(PSGD_ERR_INVALID, "grad_host and msg_host must not be NULL");
   const int W = c->W;
-  if (!c->stage_G) {
-    rc = dalloc(&c->stage_G, (int64_t)W * c->total, "stage_G");
-    if (!rc) rc = dalloc(&c->stage_U, c->total, "stage_U");
+  if (!c->stage_U) {
+    rc = dalloc(&c->stage_U, c->total, "stage_U");
     if (!rc) rc = dalloc(&c->stage_msg, c->msg_floats, "stage_msg");
     if (rc) return rc;
   }
+  // A pinned, mapped host buffer is read in place by the kernels over the
+  // CPU-GPU link (its device alias); any other buffer is copied to staging.
   std::vector<const float*> dptr(W);
   for (int w = 0; w < W; ++w) {
     if (!grad_host[w]) return fail(PSGD_ERR_INVALID, "grad_host[%d] is NULL", w);
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, grad_host[w]) != cudaSuccess) {
+      cudaGetLastError();
+      at.type = cudaMemoryTypeUnregistered;
+    }
+    if (at.type == cudaMemoryTypeHost && at.devicePointer && aligned16(at.devicePointer)) {
+      dptr[w] = static_cast<const float*>(at.devicePointer);
+      continue;
+    }
+    if (!c->stage_G && (rc = dalloc(&c->stage_G, (int64_t)W * c->total, "stage_G"))) return rc;
     dptr[w] = c->stage_G + (int64_t)w * c->total;
     CUDA_TRY(cudaMemcpyAsync(const_cast<float*>(dptr[w]), grad_host[w], (size_t)c->total * sizeof(float),
                              cudaMemcpyHostToDevice, c->stream));

@@ -24,10 +24,10 @@ def _built():
     build()
 
 
-@pytest.mark.parametrize("rank,with_update", [(2, True), (4, False)])
+@pytest.mark.parametrize("rank,with_update", [(2, True), (4, False), (8, True), (16, False)])
 def test_momentum_update_matches_oracle(rank, with_update):
     import torch
-    layers = [(64, 27), (128, 576), (9, 0), (257, 650), (10, 512), (33, 0)]
+    layers = [(64, 27), (128, 576), (9, 0), (257, 650), (20, 512), (33, 0)]
     cfg = workloads.scaled(workloads.c2_resnet18(), layers, rank=rank, workers=3)
     lr, beta = 0.5, 0.9
     run = GpuRun(cfg)
