@@ -285,3 +285,33 @@ def test_invalid_arguments_are_rejected():
     with pytest.raises(PsgdError):
         PowerSGD([(16, 8)], 9, 2)  # rank > min(n, m)
 
+
+
+@pytest.mark.parametrize("rank,workers", [(2, 9), (4, 64), (16, 9)])
+def test_many_workers(rank, workers):
+    # more workers than warps in a project CTA (warps loop over workers), up
+    # to the limit of 64 pointers in the step arguments
+    # (the rank-sweep signal: 32 decaying singular values, so even r = 16
+    # keeps a spectral gap between ranks r and r + 1)
+    layers = [(40, 27), (7, 0), (96, 130), (33, 64)]
+    cfg = workloads.scaled(workloads.c5_rank_sweep(rank), layers, rank=rank, workers=workers, seed=31)
+    _run_config(cfg, 3)
+
+
+def test_vector_layers_only():
+    # no matrix at all: only the decompress kernel's vector tiles run
+    layers = [(5, 0), (1, 0), (8195, 0)]
+    cfg = workloads.scaled(workloads.c1_single_matrix(), layers, rank=1, workers=3, seed=2)
+    run = GpuRun(cfg)
+    try:
+        sig = {}
+        for t in range(2):
+            grads = workloads.gradients(cfg, t, sig)
+            run.step(grads)
+            for li in range(len(layers)):
+                want = sum(np.asarray(grads[w][li], dtype=np.float64) for w in range(3)) / 3
+                assert rel_fro(run.update(li), want) < 1e-6
+        s = run.ctx.stats()
+        assert s["floats_sent_per_step"] == sum(n for n, _ in layers) and s["tiles"]["project"] == 0
+    finally:
+        run.close()
