@@ -41,16 +41,27 @@ UNIT = "GB/s"
 # ncu capture (see profiles/), valid only for the kernel sources whose hash is
 # recorded with it.
 NCU_TRAFFIC = {  # {config: (sources_sha256_prefix, bytes_per_launch)}
+    # ResNet-18 set, r = 2, W = 4: mean of two project launches, 361.6 MB read +
+    # 123.9 MB written (profiles/bench_all_configs.md)
+    "c2": ("2901bf61869cd906", 485531136),
+}
     # ResNet-18 set, r = 2, W = 4: mean of two project launches, 365.7 MB read +
     # 125.8 MB written (profiles/bench_all_configs.md)
     "c2": ("77489d7555fb16b0", 491524992),
 }
 
 
+# the sources that define the phase kernels of a step and their launch
+# (the allocation-free entry point and other compressors are not among them)
+STEP_SOURCES = ("psgd_api.cu", "psgd_dispatch.h", "psgd_internal.h", "psgd_kernels.cuh", "psgd_plan.h",
+                "psgd_step_impl.cuh", "psgd_step_r1.cu", "psgd_step_r2.cu", "psgd_step_r4.cu", "psgd_step_r8.cu",
+                "psgd_step_r16.cu", "psgd_step_r32.cu")
+
+
 def kernel_sources_hash() -> str:
     csrc = os.path.join(ROOT, "rank_gradient_compression_layer_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
+    for f in STEP_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
