@@ -277,6 +277,105 @@ def unbiased_data_sent(layers: Sequence[Tuple[int, int]], rank: int) -> int:
     return sum(n * rank if m else n for n, m in layers)
 
 
+# --------------------------------------------------------------------------
+# rTop-k sparsification (the rTop-k review page, "rTop-k: A Statistical
+# Estimation Approach to Distributed SGD", section 제안 방법 / proposed method,
+# bullet 3: a random subset of the top-k magnitude gradient entries)
+# --------------------------------------------------------------------------
+#
+# Readings taken where the page is silent:
+#   * the top set has r = ceil(d / top_div) entries of a layer's d, the sent
+#     subset k = ceil(r / sample_div) of them, chosen uniformly at random;
+#   * it runs on M_w = G_w + E_w with error feedback, E_w <- M_w - S_w (the
+#     page calls it a compression operator with the convergence guarantees
+#     of error-fed compressors);
+#   * "largest magnitude" orders by |M| (float32) and then by the smaller
+#     index; the random subset takes the k smallest of (upper 32 bits of a
+#     splitmix64 draw keyed by (seed, step, worker, layer, index), index);
+#   * U = (sum_w S_w) / W, summed in worker order in float32; 1-D tensors
+#     are averaged, as in PowerSGD.
+# M, E, S and U are float32 here, as on the GPU, so the selections (integer
+# decisions) and the results agree exactly.
+
+def rtopk_counts(d: int, top_div: int, sample_div: int) -> Tuple[int, int]:
+    """(r, k) for a layer of d entries."""
+    r = -(-d // top_div)
+    return r, -(-r // sample_div)
+
+
+def rtopk_draw_key(seed: int, step: int, worker: int, layer: int) -> int:
+    """Stream key of one (step, worker, layer): splitmix64 mixes of the step seed."""
+    return splitmix64_mix((step_seed(seed, step) + (worker * 65536 + layer + 1) * GOLDEN_GAMMA) & MASK64)
+
+
+def rtopk_select(M: np.ndarray, r: int, k: int, key: int) -> np.ndarray:
+    """Flat indices of the k entries sent out of the r largest |M| (float32 M)."""
+    a = np.abs(np.asarray(M, dtype=np.float32).ravel())
+    d = a.size
+    idx = np.arange(d, dtype=np.int64)
+    order = np.lexsort((idx, -a.astype(np.float64)))  # |M| descending, then index ascending
+    top = order[:r]
+    with np.errstate(over="ignore"):
+        z = np.uint64(key) + (top.astype(np.uint64) + np.uint64(1)) * np.uint64(GOLDEN_GAMMA)
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+        z = z ^ (z >> np.uint64(31))
+    hi = (z >> np.uint64(32)).astype(np.int64)
+    pick = np.lexsort((top, hi))[:k]  # the k smallest (draw, index)
+    return np.sort(top[pick])
+
+
+class RTopKState:
+    """Error buffers of W workers under rTop-k, over a layer set."""
+
+    def __init__(self, layers: Sequence[Tuple[int, int]], workers: int, seed: int, top_div: int, sample_div: int):
+        self.layers = [tuple(l) for l in layers]
+        self.W, self.seed, self.top_div, self.sample_div = workers, seed, top_div, sample_div
+        self.E = [None if m == 0 else [np.zeros((n, m), dtype=np.float32) for _ in range(workers)]
+                  for n, m in self.layers]
+        self.steps = 0
+
+    def step(self, grads: Sequence[Sequence[np.ndarray]]):
+        """One step: returns (U per layer, sent index lists [layer][worker])."""
+        W = self.W
+        U, sent = [], []
+        for li, (n, m) in enumerate(self.layers):
+            if m == 0:
+                acc = np.zeros(n, dtype=np.float64)
+                for w in range(W):
+                    acc += np.asarray(grads[w][li], dtype=np.float64)
+                U.append(acc / W)
+                sent.append(None)
+                continue
+            r, k = rtopk_counts(n * m, self.top_div, self.sample_div)
+            u = np.zeros(n * m, dtype=np.float32)
+            per = []
+            for w in range(W):
+                M = (np.asarray(grads[w][li], dtype=np.float32) + self.E[li][w]).astype(np.float32)
+                sel = rtopk_select(M, r, k, rtopk_draw_key(self.seed, self.steps, w, li))
+                flat = M.ravel()
+                u[sel] = (u[sel] + flat[sel]).astype(np.float32)
+                E = flat.copy()
+                E[sel] = 0.0
+                self.E[li][w] = E.reshape(n, m)
+                per.append(sel)
+            U.append((u * np.float32(1.0 / W)).astype(np.float32).reshape(n, m))
+            sent.append(per)
+        self.steps += 1
+        return U, sent
+
+
+def rtopk_data_sent(layers: Sequence[Tuple[int, int]], top_div: int, sample_div: int) -> int:
+    """Words one worker sends per step: k values + k indices per matrix, vectors whole."""
+    tot = 0
+    for n, m in layers:
+        if m == 0:
+            tot += n
+        else:
+            tot += 2 * rtopk_counts(n * m, top_div, sample_div)[1]
+    return tot
+
+
 class OracleState:
     """Per-layer error buffers E_w and warm-start Q of a W-worker PowerSGD run."""
 

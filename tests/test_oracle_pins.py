@@ -374,6 +374,96 @@ def test_planted_unbiased_mistakes_are_caught(kind):
         check_unbiased(mutant)
 
 
+def check_rtopk(select):
+    rng = np.random.default_rng(21)
+    # distinct magnitudes: the top set is numpy's partition of |M|
+    M = rng.standard_normal((20, 15)).astype(np.float32)
+    d = M.size
+    r, k = O.rtopk_counts(d, 7, 1)
+    sel = select(M, r, k, 12345)
+    want = np.sort(np.argpartition(-np.abs(M.ravel()), r - 1)[:r])
+    np.testing.assert_array_equal(sel, want)
+    # with sampling: k distinct indices out of that top set
+    r, k = O.rtopk_counts(d, 7, 3)
+    sel = select(M, r, k, 99)
+    assert len(sel) == k and len(set(sel.tolist())) == k and set(sel.tolist()) <= set(want.tolist())
+    # every entry kept (r = k = d): all indices
+    np.testing.assert_array_equal(select(M, d, d, 5), np.arange(d))
+    # ties (all zero): the top set is the lowest indices
+    Z = np.zeros((6, 5), dtype=np.float32)
+    assert set(select(Z, 8, 8, 1).tolist()) == set(range(8))
+    assert set(select(Z, 8, 3, 1).tolist()) <= set(range(8))
+    # uniform subset: over many draws each top-set entry is sent k / r of the time
+    r, k = 12, 4
+    counts = np.zeros(d)
+    draws = 3000
+    for t in range(draws):
+        counts[select(M, r, k, O.rtopk_draw_key(7, t, 0, 0))] += 1
+    top = np.argpartition(-np.abs(M.ravel()), r - 1)[:r]
+    p = k / r
+    se = math.sqrt(draws * p * (1 - p))
+    assert np.all(np.abs(counts[top] - draws * p) < 5 * se) and counts.sum() == draws * k
+
+
+def test_rtopk_select():
+    check_rtopk(O.rtopk_select)
+
+
+def test_rtopk_step_conservation_and_full_case():
+    rng = np.random.default_rng(4)
+    layers = [(12, 9), (5, 0), (7, 13)]
+    W = 3
+    grads = lambda: [[rng.standard_normal(s if s[1] else (s[0],)).astype(np.float32) for s in layers] for _ in range(W)]
+    # r = k = d: nothing left behind, U is the float32 mean
+    st = O.RTopKState(layers, W, seed=3, top_div=1, sample_div=1)
+    g = grads()
+    U, sent = st.step(g)
+    for li, (n, m) in enumerate(layers):
+        if m:
+            tot = np.zeros(n * m, dtype=np.float32)
+            for w in range(W):
+                tot = (tot + g[w][li].ravel()).astype(np.float32)
+                assert np.all(st.E[li][w] == 0)
+            np.testing.assert_array_equal(U[li].ravel(), (tot * np.float32(1.0 / W)).astype(np.float32))
+    # sampling with error feedback: M = S + E exactly, k entries sent per worker
+    st = O.RTopKState(layers, W, seed=3, top_div=4, sample_div=2)
+    for t in range(3):
+        Eold = [None if e is None else [x.copy() for x in e] for e in st.E]
+        g = grads()
+        U, sent = st.step(g)
+        for li, (n, m) in enumerate(layers):
+            if not m:
+                continue
+            r, k = O.rtopk_counts(n * m, 4, 2)
+            u = np.zeros(n * m, dtype=np.float32)
+            for w in range(W):
+                M = (g[w][li] + Eold[li][w]).ravel().astype(np.float32)
+                S = np.zeros_like(M)
+                S[sent[li][w]] = M[sent[li][w]]
+                assert len(sent[li][w]) == k
+                np.testing.assert_array_equal(S + st.E[li][w].ravel(), M)
+                u = (u + S).astype(np.float32)
+            np.testing.assert_array_equal(U[li].ravel(), (u * np.float32(1.0 / W)).astype(np.float32))
+    assert O.rtopk_data_sent(layers, 4, 2) == 2 * O.rtopk_counts(108, 4, 2)[1] + 2 * O.rtopk_counts(91, 4, 2)[1] + 5
+
+
+@pytest.mark.parametrize("kind", ["smallest", "ties_high_index", "no_subset_draw"])
+def test_planted_rtopk_mistakes_are_caught(kind):
+    def mutant(M, r, k, key):
+        a = np.abs(np.asarray(M, dtype=np.float32).ravel())
+        idx = np.arange(a.size)
+        if kind == "smallest":
+            order = np.lexsort((idx, a.astype(np.float64)))
+        elif kind == "ties_high_index":
+            order = np.lexsort((-idx, -a.astype(np.float64)))
+        else:
+            order = np.lexsort((idx, -a.astype(np.float64)))
+            return np.sort(order[:k])  # the k largest, not a random k of the top r
+        return np.sort(order[:r][:k])
+    with pytest.raises(AssertionError):
+        check_rtopk(mutant)
+
+
 # ------------------------------------------------- planted mistakes -----
 
 def _mutant_compress(kind):
