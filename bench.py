@@ -45,10 +45,6 @@ NCU_TRAFFIC = {  # {config: (sources_sha256_prefix, bytes_per_launch)}
     # 123.9 MB written (profiles/bench_all_configs.md)
     "c2": ("2901bf61869cd906", 485531136),
 }
-    # ResNet-18 set, r = 2, W = 4: mean of two project launches, 365.7 MB read +
-    # 125.8 MB written (profiles/bench_all_configs.md)
-    "c2": ("77489d7555fb16b0", 491524992),
-}
 
 
 # the sources that define the phase kernels of a step and their launch
