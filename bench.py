@@ -294,7 +294,8 @@ def run_ours(args, ws, rank, local):
     cfg = config_of(args.config)
     stream = torch.cuda.Stream(device=device)
     ctx = PowerSGD(cfg.layers, cfg.rank, cfg.workers, seed=cfg.seed, stream=stream, timing=True,
-                   unbiased=args.unbiased)
+                   unbiased=args.unbiased, compressor="rtopk" if args.rtopk else "powersgd",
+                   top_div=args.rtopk_top_div, sample_div=args.rtopk_sample_div)
     sets = 3
     grads = fill_gradients(ctx, cfg, sets, device)
     upd = ctx.empty_buffer()
@@ -351,7 +352,7 @@ def run_ours(args, ws, rank, local):
     step_achieved = ab["total"] / (ms_per_step * 1e-3) / 1e9
     h = kernel_sources_hash()
     traffic = None
-    if not args.unbiased and not args.momentum and args.config in NCU_TRAFFIC and NCU_TRAFFIC[args.config][0] == h:
+    if not (args.unbiased or args.momentum or args.rtopk) and args.config in NCU_TRAFFIC and NCU_TRAFFIC[args.config][0] == h:
         traffic = NCU_TRAFFIC[args.config][1]
 
     # end to end through the C ABI with host buffers (pinned), copies inside
@@ -366,13 +367,16 @@ def run_ours(args, ws, rank, local):
                    "l2": "inputs larger than L2: 3 rotating gradient sets of "
                          f"{comp / 1e6:.1f} MB + error buffers {comp / 1e6:.1f} MB per step",
                    "seed": cfg.seed, "out_update": not args.momentum,
-                   "fused_momentum_update": bool(args.momentum), "variant": "unbiased" if args.unbiased else "powersgd",
+                   "fused_momentum_update": bool(args.momentum),
+                   "variant": "unbiased" if args.unbiased else (
+                       f"rtopk top 1/{args.rtopk_top_div}, sent 1/{args.rtopk_sample_div}" if args.rtopk else "powersgd"),
                    "tile_rows": st["tile_rows"]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                      "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
                      else "fallback 6.8 TB/s",
-                     "kernel": (f"psgd::p1_kernel<{st['kernel_rank']}> (project: P = G Q)" if args.unbiased else
+                     "kernel": ("rTop-k step (all its kernels; phase 'project' spans the step)" if args.rtopk else
+                                f"psgd::p1_kernel<{st['kernel_rank']}> (project: P = G Q)" if args.unbiased else
                                 f"psgd::p1_kernel<{st['kernel_rank']}> (project: error add, E write, P = M Q)"),
                      "algorithmic_bytes_per_launch": project_bytes, "launch_ms": round(project_ms, 5),
                      "launch_ms_source": "CUDA events around the project kernel on the context's stream, "
@@ -443,6 +447,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unbiased", action="store_true",
                     help="time the unbiased rank-r variant (fresh shared Q per step, no error feedback)")
+    ap.add_argument("--rtopk", action="store_true", help="time rTop-k sparsification instead of PowerSGD")
+    ap.add_argument("--rtopk-top-div", type=int, default=100, help="rTop-k top set: 1 / this of each layer")
+    ap.add_argument("--rtopk-sample-div", type=int, default=4, help="rTop-k: 1 / this of the top set is sent")
     ap.add_argument("--momentum", action="store_true",
                     help="time psgd_step_momentum (step + fused momentum-SGD update) instead of psgd_step")
     args = ap.parse_args()

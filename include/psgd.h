@@ -83,6 +83,7 @@ typedef struct {
   int32_t launches_per_step;            /* kernels one psgd_step enqueues (with an update) */
   int32_t tile_rows[3];                 /* rows per tile: project, back-project (least), decompress */
   int32_t reserved;
+  int64_t message_floats;               /* floats psgd_step_host writes to msg_host */
 } psgd_stats;
 
 /* Optional knobs of psgd_create_ex (zero-initialise, then set what you need). */
@@ -90,8 +91,12 @@ typedef struct {
   int32_t timing;       /* 1: time every phase of every step with CUDA events (psgd_get_phase_times) */
   int32_t project_rows; /* rows per project tile (0: chosen so the grid holds several waves of CTAs) */
   int32_t unbiased;     /* 1: the unbiased rank-r variant (see below) instead of PowerSGD */
-  int32_t reserved;
+  int32_t compressor;   /* PSGD_POWERSGD (0) or PSGD_RTOPK (1): rTop-k sparsification (see below) */
+  int32_t rtopk_top_div;    /* rTop-k: the top set of a layer of d entries has ceil(d / top_div) */
+  int32_t rtopk_sample_div; /* rTop-k: k = ceil(r / sample_div) of them are sent */
 } psgd_options;
+
+enum { PSGD_POWERSGD = 0, PSGD_RTOPK = 1 };
 
 /*
  * The unbiased rank-r variant (options.unbiased = 1).  The PowerSGD review
@@ -106,6 +111,28 @@ typedef struct {
  * with no error feedback, no warm start and no orthonormalisation.  In this
  * variant psgd_get_PQ returns P and the step's Q, psgd_get_error returns
  * zeros, and psgd_get_Qw and psgd_set_state answer PSGD_ERR_INVALID.
+ */
+
+/*
+ * rTop-k sparsification (options.compressor = PSGD_RTOPK), the second
+ * compressor behind this ABI (rTop-k review page, "rTop-k: A Statistical
+ * Estimation Approach to Distributed SGD", proposed method, bullet 3: a
+ * random subset of the top magnitude entries).  Per worker w and matrix
+ * layer (d = n m entries, flat row-major index i), with error feedback:
+ *     M_w = G_w + E_w                                  (float32)
+ *     T   = the r = ceil(d / top_div) entries with the largest (|M_w|, -i)
+ *     K   = the k = ceil(r / sample_div) members of T with the smallest
+ *           (upper 32 bits of splitmix64(key + (i + 1) * 0x9E3779B97F4A7C15), i),
+ *           key = splitmix64_mix(s + (w * 65536 + layer + 1) * 0x9E3779B97F4A7C15),
+ *           s = the step seed of the unbiased variant
+ *     E_w <- M_w with K zeroed; worker w sends K's indices and values
+ *     U   = (sum_w S_w) / W, summed in worker order in float32
+ * 1-D tensors are averaged.  Layers must have fewer than 2^31 entries;
+ * top_div, sample_div >= 1.  psgd_get_error gives E_w, psgd_get_sparse the
+ * message; psgd_get_PQ, psgd_get_Qw, psgd_set_state, psgd_step_momentum and
+ * the unbiased option answer PSGD_ERR_INVALID.  psgd_step_host's message is,
+ * per matrix layer and per worker in order, the k indices (int32 bits in
+ * float slots) then the k values.
  */
 
 /*
@@ -175,6 +202,12 @@ int psgd_sync(psgd_ctx* ctx);
  * (Qbar, also the warm start of the next step).
  */
 int psgd_get_PQ(psgd_ctx* ctx, int layer, float* P, float* Q);
+/*
+ * rTop-k: the message of worker w for matrix layer l in the last step --
+ * *count (= k) flat indices (ascending, row-major over n x m) into idx and
+ * their values into val (host or device memory, either may be NULL).
+ */
+int psgd_get_sparse(psgd_ctx* ctx, int layer, int worker, int32_t* idx, float* val, int64_t* count);
 /* Q_w = M_w^T Phat of worker w in the last step: m x r row-major. */
 int psgd_get_Qw(psgd_ctx* ctx, int layer, int worker, float* Q);
 /* Error buffer E_w of layer l: dense n x m row-major (host or device memory). */

@@ -24,8 +24,11 @@ EXPORTS = (
     "psgd_create", "psgd_create_ex", "psgd_destroy", "psgd_set_stream", "psgd_step", "psgd_step_host",
     "psgd_sync", "psgd_get_PQ", "psgd_get_Qw", "psgd_get_error", "psgd_set_state", "psgd_get_stats",
     "psgd_layer_info", "psgd_plan_layout", "psgd_count_sent", "psgd_last_error", "psgd_version",
-    "psgd_get_phase_times", "psgd_step_noalloc", "psgd_step_momentum", "psgd_set_timing",
+    "psgd_get_phase_times", "psgd_step_noalloc", "psgd_step_momentum", "psgd_set_timing", "psgd_get_sparse",
 )
+
+PSGD_POWERSGD = 0
+PSGD_RTOPK = 1
 
 PHASES = ("project", "orthonormalise", "back_project", "decompress")
 
@@ -51,12 +54,14 @@ class Stats(ctypes.Structure):
         ("launches_per_step", ctypes.c_int32),
         ("tile_rows", ctypes.c_int32 * 3),
         ("reserved", ctypes.c_int32),
+        ("message_floats", ctypes.c_int64),
     ]
 
 
 class Options(ctypes.Structure):
     _fields_ = [("timing", ctypes.c_int32), ("project_rows", ctypes.c_int32), ("unbiased", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("compressor", ctypes.c_int32), ("rtopk_top_div", ctypes.c_int32),
+                ("rtopk_sample_div", ctypes.c_int32)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -96,6 +101,7 @@ def lib() -> ctypes.CDLL:
         "psgd_version": ([], ctypes.c_char_p),
         "psgd_get_phase_times": ([_P, ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
         "psgd_set_timing": ([_P, ctypes.c_int], ctypes.c_int),
+        "psgd_get_sparse": ([_P, ctypes.c_int, ctypes.c_int, _P, _P, _I64P], ctypes.c_int),
         "psgd_step_noalloc": ([ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_P),
                                _P, _P, _P, _P, _P, ctypes.c_int, _P], ctypes.c_int),
     }
@@ -161,7 +167,8 @@ class PowerSGD:
     """
 
     def __init__(self, shapes: Sequence[Tuple[int, int]], rank: int, workers: int, seed: int = 0,
-                 stream=None, timing: bool = False, project_rows: int = 0, unbiased: bool = False):
+                 stream=None, timing: bool = False, project_rows: int = 0, unbiased: bool = False,
+                 compressor: str = "powersgd", top_div: int = 100, sample_div: int = 4):
         import torch
 
         if not torch.cuda.is_available():
@@ -171,7 +178,10 @@ class PowerSGD:
         self.device = torch.device("cuda", torch.cuda.current_device())
         self._stream = stream
         n, m = _shapes(self.shapes)
-        opt = Options(int(bool(timing)), int(project_rows), int(bool(unbiased)))
+        if compressor not in ("powersgd", "rtopk"):
+            raise ValueError(f"unknown compressor {compressor!r}")
+        opt = Options(int(bool(timing)), int(project_rows), int(bool(unbiased)),
+                      PSGD_RTOPK if compressor == "rtopk" else PSGD_POWERSGD, int(top_div), int(sample_div))
         h = _P()
         _check(lib().psgd_create_ex(ctypes.byref(h), len(self.shapes), n, m, self.rank, self.workers,
                                     ctypes.c_uint64(self.seed), _stream_ptr(stream), ctypes.byref(opt)))
@@ -254,6 +264,16 @@ class PowerSGD:
         _check(lib().psgd_get_PQ(self._h, layer, _ptr(P), _ptr(Q)))
         return P, Q
 
+    def get_sparse(self, layer: int, worker: int):
+        """rTop-k: (indices int32, values float32) of worker's message for a matrix layer."""
+        import torch
+        cnt = ctypes.c_int64()
+        _check(lib().psgd_get_sparse(self._h, layer, worker, None, None, ctypes.byref(cnt)))
+        idx = torch.empty(cnt.value, dtype=torch.int32, device=self.device)
+        val = torch.empty(cnt.value, dtype=torch.float32, device=self.device)
+        _check(lib().psgd_get_sparse(self._h, layer, worker, _ptr(idx), _ptr(val), None))
+        return idx, val
+
     def get_Qw(self, layer: int, worker: int):
         import torch
         n, m = self._shape(layer)
@@ -297,7 +317,8 @@ class PowerSGD:
 
     @property
     def message_floats(self) -> int:
-        return sum((n + m) * self.rank for n, m in self.shapes if m)
+        """Floats step_host writes to its message buffer (the library's count)."""
+        return int(self.stats()["message_floats"])
 
 
 # ------------------------------------------------------ no-allocation step --

@@ -21,6 +21,7 @@
 #include "psgd_dispatch.h"
 #include "psgd_kernels.cuh"
 #include "psgd_plan.h"
+#include "psgd_rtopk.h"
 
 using namespace psgd;
 
@@ -158,6 +159,8 @@ struct psgd_ctx {
   int tile_rows[3] = {0, 0, 0};  // project rows, least back-project rows, decompress rows
   int has_prev = 0;
   bool unbiased = false;  // psgd_options.unbiased: fresh shared Q per step, no error feedback
+  RTopK* rk = nullptr;    // psgd_options.compressor == PSGD_RTOPK: the rTop-k plan
+  int top_div = 0, sample_div = 0;
   bool broken = false;
   // stats
   int64_t steps = 0, sent_step = 0, unc_step = 0, mat_el = 0, vec_el = 0;
@@ -171,6 +174,8 @@ void free_all(psgd_ctx* c) {
                   c->e_scratch, c->stage_G, c->stage_U, c->stage_msg};
   for (void* p : ptrs)
     if (p) cudaFree(p);
+  rtopk_destroy(c->rk);
+  c->rk = nullptr;
   for (cudaEvent_t e : c->ev)
     if (e) cudaEventDestroy(e);
   c->ev.clear();
@@ -303,6 +308,19 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   c->ks = kernels_for(c->rp);
   c->timing = opt && opt->timing;
   c->unbiased = opt && opt->unbiased;
+  const bool rtopk = opt && opt->compressor == PSGD_RTOPK;
+  if (opt && opt->compressor != PSGD_POWERSGD && !rtopk) {
+    delete c;
+    return fail(PSGD_ERR_INVALID, "unknown compressor %d", opt->compressor);
+  }
+  if (rtopk && (c->unbiased || opt->rtopk_top_div < 1 || opt->rtopk_sample_div < 1)) {
+    delete c;
+    return fail(PSGD_ERR_INVALID, "rTop-k needs top_div, sample_div >= 1 and no unbiased option");
+  }
+  if (rtopk) {
+    c->top_div = opt->rtopk_top_div;
+    c->sample_div = opt->rtopk_sample_div;
+  }
   if (cudaGetDevice(&c->device) != cudaSuccess) {
     cudaGetLastError();
     delete c;
@@ -359,10 +377,12 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     if (L.S > 1) c->ppart_total += (int64_t)L.nrb * L.S * c->ks->r1 * rp;
     L.cnt_off = (int32_t)c->n_counters;
     c->n_counters += ncnt;
-    // the message: Phat and Qbar; the unbiased variant sends P alone
-    const int64_t sent = c->unbiased ? n[l] * rank : (n[l] + m[l]) * rank;
+    // the message: Phat and Qbar; the unbiased variant sends P alone;
+    // rTop-k: k indices and k values per worker
+    int64_t sent = c->unbiased ? n[l] * rank : (n[l] + m[l]) * rank;
+    if (rtopk) sent = 2 * ceil_div(ceil_div(n[l] * m[l], c->top_div), c->sample_div);
     c->pack.push_back({L.p_off, L.q_off, c->msg_floats, L.n, c->unbiased ? 0 : L.m});
-    c->msg_floats += sent;
+    c->msg_floats += rtopk ? sent * num_workers : sent;
     c->mat_of[l] = (int)c->hl.size();
     c->hl.push_back(L);
     c->mat_el += n[l] * m[l];
@@ -425,6 +445,10 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
       CUDA_TRY(cudaGetLastError());
     }
     CUDA_TRY(cudaStreamSynchronize(s));
+    if (rtopk) {
+      int rc2 = rtopk_create(&c->rk, c->hl, c->hv, c->d_layers, c->d_vecs, c->W, c->seed, c->top_div, c->sample_div);
+      if (rc2) return rc2;
+    }
     return PSGD_OK;
   };
   rc = setup();
@@ -500,6 +524,19 @@ int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, flo
     ev = &c->ev[(size_t)(c->timed_since % kTimedSteps) * (kPhases + 1)];
     c->timed_since += 1;
     CUDA_TRY(cudaEventRecord(ev[0], c->stream));
+  }
+  if (c->rk) {
+    if (X) return fail(PSGD_ERR_INVALID, "rTop-k has no fused momentum update");
+    rc = rtopk_step(c->rk, grad_ptrs, c->B, c->total, out_update, c->steps, c->stream);
+    if (rc) {
+      c->broken = true;
+      return rc;
+    }
+    if (ev)
+      for (int ph = 0; ph < kPhases; ++ph) CUDA_TRY(cudaEventRecord(ev[ph + 1], c->stream));
+    c->has_prev = 1;
+    c->steps += 1;
+    return PSGD_OK;
   }
   if (c->unbiased && !c->hl.empty()) {
     // this step's Q: N(0,1) draws from the step's seed, shared by all workers
@@ -617,7 +654,19 @@ int psgd_step_host(psgd_ctx* c, const float* const* grad_host, float* msg_host, 
   }
   rc = psgd_step(c, dptr.data(), update_host ? c->stage_U : nullptr);
   if (rc) return rc;
-  if (!c->pack.empty()) {
+  if (c->rk) {  // per matrix layer and worker: k indices, then k values
+    int64_t at = 0;
+    for (int mi = 0; mi < (int)c->hl.size(); ++mi)
+      for (int w = 0; w < W; ++w) {
+        const int64_t k = rtopk_k(c->rk, mi);
+        const int32_t* di;
+        const float* dv;
+        rtopk_message(c->rk, mi, w, &di, &dv);
+        CUDA_TRY(cudaMemcpyAsync(msg_host + at, di, (size_t)k * sizeof(int32_t), cudaMemcpyDeviceToHost, c->stream));
+        CUDA_TRY(cudaMemcpyAsync(msg_host + at + k, dv, (size_t)k * sizeof(float), cudaMemcpyDeviceToHost, c->stream));
+        at += 2 * k;
+      }
+  } else if (!c->pack.empty()) {
     dim3 grid(32, (unsigned)c->pack.size());
     pack_msg_kernel<<<grid, 256, 0, c->stream>>>(c->stage_msg, c->unbiased ? c->P : c->Phat, c->Qbar, c->d_pack,
                                                  c->rank, c->rp);
@@ -634,11 +683,30 @@ int psgd_step_host(psgd_ctx* c, const float* const* grad_host, float* msg_host, 
 int psgd_get_PQ(psgd_ctx* c, int layer, float* P, float* Q) {
   int rc = ctx_ok(c);
   if (rc) return rc;
+  if (c->rk) return fail(PSGD_ERR_INVALID, "rTop-k keeps no factors");
   const LayerDev* L;
   if ((rc = matrix_layer(c, layer, &L))) return rc;
   const size_t rb = (size_t)c->rank * sizeof(float), pb = (size_t)c->rp * sizeof(float);
   if (P) CUDA_TRY(cudaMemcpy2DAsync(P, rb, (c->unbiased ? c->P : c->Phat) + L->p_off, pb, rb, L->n, cudaMemcpyDefault, c->stream));
   if (Q) CUDA_TRY(cudaMemcpy2DAsync(Q, rb, c->Qbar + L->q_off, pb, rb, L->m, cudaMemcpyDefault, c->stream));
+  return sync_and_check(c);
+}
+
+int psgd_get_sparse(psgd_ctx* c, int layer, int worker, int32_t* idx, float* val, int64_t* count) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  if (!c->rk) return fail(PSGD_ERR_INVALID, "not an rTop-k context");
+  const LayerDev* L;
+  if ((rc = matrix_layer(c, layer, &L))) return rc;
+  if (worker < 0 || worker >= c->W) return fail(PSGD_ERR_INVALID, "worker %d out of range", worker);
+  const int mi = c->mat_of[layer];
+  const int64_t k = rtopk_k(c->rk, mi);
+  const int32_t* di;
+  const float* dv;
+  rtopk_message(c->rk, mi, worker, &di, &dv);
+  if (count) *count = k;
+  if (idx) CUDA_TRY(cudaMemcpyAsync(idx, di, (size_t)k * sizeof(int32_t), cudaMemcpyDefault, c->stream));
+  if (val) CUDA_TRY(cudaMemcpyAsync(val, dv, (size_t)k * sizeof(float), cudaMemcpyDefault, c->stream));
   return sync_and_check(c);
 }
 
@@ -649,7 +717,7 @@ int psgd_get_Qw(psgd_ctx* c, int layer, int worker, float* Q) {
   if ((rc = matrix_layer(c, layer, &L))) return rc;
   if (worker < 0 || worker >= c->W) return fail(PSGD_ERR_INVALID, "worker %d out of range", worker);
   if (!Q) return fail(PSGD_ERR_INVALID, "Q must not be NULL");
-  if (c->unbiased) return fail(PSGD_ERR_INVALID, "the unbiased variant forms no Q_w");
+  if (c->unbiased || c->rk) return fail(PSGD_ERR_INVALID, "this compressor forms no Q_w");
   const size_t rb = (size_t)c->rank * sizeof(float), pb = (size_t)c->rp * sizeof(float);
   CUDA_TRY(cudaMemcpy2DAsync(Q, rb, c->Qw + (int64_t)worker * c->q_total + L->q_off, pb, rb, L->m,
                              cudaMemcpyDefault, c->stream));
@@ -697,7 +765,7 @@ int psgd_set_state(psgd_ctx* c, int layer, const float* Q, const float* const* E
   const LayerDev* L;
   if ((rc = matrix_layer(c, layer, &L))) return rc;
   if (!Q) return fail(PSGD_ERR_INVALID, "Q must not be NULL");
-  if (c->unbiased) return fail(PSGD_ERR_INVALID, "the unbiased variant keeps no state");
+  if (c->unbiased || c->rk) return fail(PSGD_ERR_INVALID, "this compressor's state cannot be set");
   if (E)
     for (int w = 0; w < c->W; ++w)
       if (!E[w]) return fail(PSGD_ERR_INVALID, "E[%d] is NULL", w);
@@ -733,6 +801,8 @@ int psgd_get_stats(const psgd_ctx* c, psgd_stats* out) {
   for (int i = 0; i < 3; ++i) out->tile_rows[i] = c->tile_rows[i];
   out->launches_per_step = kPhases;  // the unbiased variant: Q draw, project, decompress
   if (c->unbiased) out->launches_per_step = 3;
+  if (c->rk) out->launches_per_step = rtopk_launches(c->rk);
+  out->message_floats = c->msg_floats;
   return PSGD_OK;
 }
 
