@@ -15,11 +15,24 @@
 // Both selections are radix selects over composite 64-bit keys that are
 // unique per entry -- (|M| bits, ~i) and (h(i), i) -- so the k-th key is one
 // value and "key >= / <= threshold" selects exactly r / k entries.  Six
-// 11-bit digit passes per select; each pass histograms the digit of the
-// entries still matching the prefix found so far, and the last CTA of a
-// problem to finish its chunk picks the digit and narrows the prefix.  A
-// count / scan / apply sequence then writes every worker's message in index
-// order and U, so the whole step is deterministic.
+// 11-bit digits per select; each pass histograms the digit of the entries
+// still matching the prefix found so far, and the last CTA of a problem to
+// finish picks the digit and narrows the prefix (a select whose chosen bin
+// holds exactly the entries still needed is finished early).
+//
+// Only two passes read the whole layer: pass 0 forms M and histograms the
+// top digit of |M|; pass 1 lists the entries whose top digit is above the
+// chosen one -- members of T for sure -- and, with their values, those
+// equal to it, the candidates.  Both are persistent kernels: each CTA takes
+// a contiguous run of tiles and arrives once per problem it touches, with
+// the number of tiles it did.  A tail kernel (one CTA per problem, so its
+// passes need no grid-wide hand-off) finishes the magnitude select over the
+// candidates, completes the list of T with its draws, runs the draw select
+// over it, sets the sent entries K in a bitmap (one bit per packed
+// position) and turns their per-span counts into message offsets.  The
+// apply kernel then writes the messages, E and U from the bitmaps and
+// clears them for the next step.  The step costs two reads of B plus work
+// in proportion to the candidates and T.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -33,9 +46,12 @@ namespace psgd {
 namespace {
 
 constexpr int kRkThreads = 256;
-constexpr int kRkPer = 8;                        // consecutive entries per thread
-constexpr int kRkChunk = kRkThreads * kRkPer;    // entries per tile
-constexpr int kRkBins = 2048;                    // 11-bit digits
+constexpr int kRkGroups = 8;                           // float4 groups per thread (full passes)
+constexpr int kRkChunk = kRkThreads * kRkGroups * 4;   // packed positions per full-pass tile
+constexpr int kRkApplyWords = kRkThreads;              // bitmap words per apply tile (1 per thread)
+constexpr int kRkSpan = kRkApplyWords * 32;            // packed positions per apply tile / count chunk
+constexpr int kRkTail = 1024;                          // threads of the per-problem tail CTA
+constexpr int kRkBins = 2048;                          // 11-bit digits
 constexpr int kRkPasses = 6;
 __constant__ int c_shift[kRkPasses] = {53, 42, 31, 20, 9, 0};
 __constant__ int c_width[kRkPasses] = {11, 11, 11, 11, 11, 9};
@@ -44,22 +60,42 @@ constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
 struct RkProb {   // one (worker, matrix layer) problem
   int32_t mi, w;  // matrix layer position, worker
   int64_t d, r, k;
-  int64_t nchunks, chunk0;  // chunks of the layer; first chunk counter of this problem
-  int64_t msg_off;          // first message entry of this problem
+  int64_t len;     // packed positions n x ld
+  int64_t nchunks; // full-pass tiles (kRkChunk positions each)
+  int64_t nwords;  // bitmap words, ceil(len / 32) (storage rounded up to 4; the rest stays 0)
+  int64_t nspans;  // apply tiles / count chunks (kRkSpan positions each)
+  int64_t chunk0;  // first chunk count of this problem
+  int64_t msg_off; // first message entry of this problem
+  int64_t list_off, bm_off;  // candidate list and list of T (capacity d each); K's bitmap
 };
 
-struct RkState {
-  uint64_t prefix;  // key bits found so far (bits above the current digit)
+struct RkSel {      // one radix select
+  uint64_t prefix;  // key bits found so far (the threshold once done)
   int64_t need;     // entries still to take from those matching the prefix
-  uint64_t vm;      // magnitude threshold: T = {Km >= vm}
-  uint64_t vr;      // draw threshold: K = {i in T : Kr <= vr}
-  uint64_t dkey;    // draw stream key of this step
-  int32_t done;     // the current select needs no further digits
+  int32_t done;     // the threshold is known
   int32_t pad;
 };
 
+struct RkState {
+  RkSel sel[2];    // 0: the top set by magnitude (T = {Km >= threshold});
+                   // 1: the draw among T (K = {Kr <= threshold})
+  uint64_t dkey;   // draw stream key of this step
+  unsigned long long counts;  // pass 1's list lengths: candidates (low 32 bits), sure members of T (high)
+  uint32_t nT;     // members of T (the tail's list)
+  uint32_t pad;
+};
+
+struct RkDraw {  // a member of T in the tail's list: flat index, draw h(i)
+  uint32_t i, h;
+};
+
+struct RkCand {  // a candidate: flat index and M
+  uint32_t i;
+  float m;
+};
+
 struct RkTile {
-  int32_t p;      // problem (hist passes) or matrix layer (count / apply)
+  int32_t p;      // problem, or matrix layer (apply)
   int32_t chunk;
 };
 
@@ -74,6 +110,10 @@ struct RkArgs {
   uint32_t* hist;     // problems x kRkBins
   unsigned* arrive;   // problems
   const RkTile* tiles;
+  int32_t ntiles;     // tiles of the persistent passes
+  uint32_t* bm;       // bitmaps of K (zero between steps)
+  RkCand* cand;       // candidate lists
+  RkDraw* tlist;      // lists of T
   int64_t* ccount;    // per problem chunk counts, then exclusive offsets
   int32_t* sidx;
   float* sval;
@@ -88,29 +128,43 @@ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
   return z ^ (z >> 31);
 }
 
-__device__ __forceinline__ uint64_t key_mag(float m, int64_t i) {
+__device__ __forceinline__ uint64_t key_mag(float m, uint32_t i) {
   const uint32_t pat = __float_as_uint(m) & 0x7FFFFFFFu;
-  return ((uint64_t)pat << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i);
+  return ((uint64_t)pat << 32) | (uint64_t)(0xFFFFFFFFu - i);
 }
 
-__device__ __forceinline__ uint64_t key_draw(uint64_t dkey, int64_t i) {
-  const uint64_t h = mix64(dkey + (uint64_t)(i + 1) * kGamma) >> 32;
-  return (h << 32) | (uint64_t)(uint32_t)i;
+// h(i): the upper 32 bits of the draw stream at entry i (the draw key is (h(i), i)).
+__device__ __forceinline__ uint32_t draw_hi(uint64_t dkey, uint32_t i) {
+  return (uint32_t)(mix64(dkey + (uint64_t)(i + 1) * kGamma) >> 32);
 }
 
-// Packed-buffer position of flat entry i of layer L.
-__device__ __forceinline__ int64_t pos_of(const LayerDev& L, int64_t i) {
-  const int64_t row = i / L.m;
-  return L.off + row * L.ld + (i - row * L.m);
+__device__ __forceinline__ uint64_t mask_above(int q) {
+  const int top = c_shift[q] + c_width[q];
+  return top >= 64 ? 0ull : (~0ull << top);
 }
 
-// Last CTA of a problem's pass: pick the digit at `shift` of the need-th key
-// (largest first for the top set, smallest first for the draw) and narrow
-// the prefix.  h: the pass's histogram in shared memory.
-__device__ void rk_find(RkState& st, const uint32_t* h, int shift, int width, bool largest, uint64_t* s_sum) {
+// Flat index of packed position p (relative to the layer; p < 2^31).
+__device__ __forceinline__ uint32_t flat_of(const LayerDev& L, uint32_t p) {
+  if (L.ld == L.m) return p;
+  const uint32_t row = p / (uint32_t)L.ld;
+  return p - row * (uint32_t)(L.ld - L.m);
+}
+
+// Packed position of flat index i.
+__device__ __forceinline__ uint32_t packed_of(const LayerDev& L, uint32_t i) {
+  if (L.ld == L.m) return i;
+  const uint32_t row = i / (uint32_t)L.m;
+  return i + row * (uint32_t)(L.ld - L.m);
+}
+
+// Pick the digit at `shift` of the need-th key (largest first for the top
+// set, smallest first for the draw) from the pass histogram h and narrow the
+// select.  All NT threads of the CTA call it.
+template <int NT>
+__device__ void rk_find(RkSel& st, const uint32_t* h, int shift, int width, bool largest, uint64_t* s_sum) {
   const int t = threadIdx.x;
   const int nb = 1 << width;
-  const int per = kRkBins / kRkThreads;  // 8 bins per thread
+  constexpr int per = kRkBins / NT;
   // thread t owns walk positions [t per, t per + per); walk position j is
   // bin nb - 1 - j (largest first) or bin j (smallest first)
   uint64_t mine = 0;
@@ -119,18 +173,19 @@ __device__ void rk_find(RkState& st, const uint32_t* h, int shift, int width, bo
   s_sum[t] = mine;
   __syncthreads();
   // inclusive scan over threads (Hillis-Steele)
-  for (int o = 1; o < kRkThreads; o <<= 1) {
+  for (int o = 1; o < NT; o <<= 1) {
     const uint64_t v = (t >= o) ? s_sum[t - o] : 0;
     __syncthreads();
     s_sum[t] += v;
     __syncthreads();
   }
-  const uint64_t incl = s_sum[t], excl = incl - mine, all = s_sum[kRkThreads - 1];
-  const uint64_t mask_above = (shift + width >= 64) ? 0ull : (~0ull << (shift + width));
+  const uint64_t incl = s_sum[t], excl = incl - mine, all = s_sum[NT - 1];
+  const uint64_t above = (shift + width >= 64) ? 0ull : (~0ull << (shift + width));
+  const uint64_t below = (1ull << shift) - 1ull;  // bits under this digit
   if (t == 0 && (uint64_t)st.need > all) {
     // every entry matching the prefix is taken: the threshold is the lowest
     // (largest first) or highest (smallest first) key with that prefix
-    st.prefix = largest ? (st.prefix & mask_above) : ((st.prefix & mask_above) | ~mask_above);
+    st.prefix = largest ? (st.prefix & above) : ((st.prefix & above) | ~above);
     st.done = 1;
   }
   __syncthreads();
@@ -140,8 +195,13 @@ __device__ void rk_find(RkState& st, const uint32_t* h, int shift, int width, bo
     for (int j = t * per; j < t * per + per && j < nb; ++j) {
       const int b = largest ? nb - 1 - j : j;
       if (c + h[b] >= (uint64_t)st.need) {
-        st.prefix = (st.prefix & mask_above) | ((uint64_t)b << shift);
-        st.need -= (int64_t)c;
+        const int64_t left = st.need - (int64_t)c;
+        st.prefix = (st.prefix & above) | ((uint64_t)b << shift);
+        st.need = left;
+        if ((uint64_t)left == h[b]) {  // the whole bin is taken: the bin's end is the threshold
+          if (!largest) st.prefix |= below;
+          st.done = 1;
+        }
         break;
       }
       c += h[b];
@@ -149,168 +209,427 @@ __device__ void rk_find(RkState& st, const uint32_t* h, int shift, int width, bo
   }
 }
 
-// One digit pass of one select over all problems.  draw = false: the top
-// set by magnitude (pass 0 also forms M = G + E into B); draw = true: the
-// sent subset among the top set.
-__global__ void __launch_bounds__(kRkThreads) rk_hist_kernel(RkArgs a, int q, int draw) {
-  __shared__ uint32_t h[kRkBins];
-  __shared__ uint64_t s_sum[kRkThreads];
-  __shared__ int s_flag;
-  const RkTile t = a.tiles[blockIdx.x];
-  const RkProb P = a.probs[t.p];
-  const LayerDev L = a.layers[P.mi];
-  RkState* stp = a.state + t.p;
-  const int shift = c_shift[q], width = c_width[q];
-  const uint64_t mask_above = (shift + width >= 64) ? 0ull : (~0ull << (shift + width));
-  const uint64_t prefix = stp->prefix, vm = stp->vm, dkey = stp->dkey;
-  const bool skip = stp->done != 0;
-  for (int b = threadIdx.x; b < kRkBins; b += blockDim.x) h[b] = 0u;
+template <int NT>
+__device__ __forceinline__ void rk_zero_hist(uint32_t* h) {
+  for (int b = threadIdx.x; b < kRkBins; b += NT) h[b] = 0u;
   __syncthreads();
-  if (!skip) {
-    const int64_t i0 = (int64_t)t.chunk * kRkChunk + (int64_t)threadIdx.x * kRkPer;
-    float* Bw = a.B + (int64_t)P.w * a.total;
-    const float* Gw = a.G[P.w];
-    for (int j = 0; j < kRkPer; ++j) {
-      const int64_t i = i0 + j;
-      if (i >= P.d) break;
-      const int64_t pos = pos_of(L, i);
-      float m;
-      if (!draw && q == 0) {
-        m = __ldcs(Gw + pos) + Bw[pos];
-        Bw[pos] = m;
-      } else {
-        m = Bw[pos];
-      }
-      uint64_t K = key_mag(m, i);
-      if (draw) {
-        if (K < vm) continue;  // not in the top set
-        K = key_draw(dkey, i);
-      }
-      if ((K & mask_above) == (prefix & mask_above)) atomicAdd(&h[(K >> shift) & (uint64_t)((1 << width) - 1)], 1u);
-    }
+}
+
+// End of one persistent pass's run over problem p (`done` of its `total`
+// tiles): merge the CTA's histogram and, in the CTA that completes the
+// problem, pick the magnitude digit q and reset the global histogram.
+// q == 0 starts the problem's select (need = r) and its candidate count.
+__device__ void rk_close_run(const RkArgs& a, int p, int q, unsigned done, unsigned total, uint32_t* h,
+                             uint64_t* s_sum, int* s_flag) {
+  __shared__ RkSel s_sel;
+  uint32_t* gh = a.hist + (int64_t)p * kRkBins;
+  __syncthreads();
+  for (int b = threadIdx.x; b < kRkBins; b += kRkThreads)
+    if (h[b]) atomicAdd(gh + b, h[b]);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned old = atom_add_acq_rel(a.arrive + p, done);
+    const bool last = (old + done == total);
+    if (last) a.arrive[p] = 0u;
+    *s_flag = last ? 1 : 0;
   }
   __syncthreads();
-  uint32_t* gh = a.hist + (int64_t)t.p * kRkBins;
-  if (!skip)
-    for (int b = threadIdx.x; b < kRkBins; b += blockDim.x)
-      if (h[b]) atomicAdd(gh + b, h[b]);
-  if (!cta_arrive_last(a.arrive + t.p, (unsigned)P.nchunks, &s_flag)) return;
-  // last CTA of the problem: the digit, then a clean histogram for the next pass
-  for (int b = threadIdx.x; b < kRkBins; b += blockDim.x) {
+  if (!*s_flag) return;
+  for (int b = threadIdx.x; b < kRkBins; b += kRkThreads) {
     h[b] = __ldcg(gh + b);
     gh[b] = 0u;
   }
+  if (threadIdx.x == 0) s_sel = q == 0 ? RkSel{0ull, a.probs[p].r, 0, 0} : a.state[p].sel[0];
   __syncthreads();
-  __shared__ RkState s_st;
-  if (threadIdx.x == 0) s_st = *stp;
-  __syncthreads();
-  if (!s_st.done) rk_find(s_st, h, shift, width, !draw, s_sum);
+  rk_find<kRkThreads>(s_sel, h, c_shift[q], c_width[q], true, s_sum);
   __syncthreads();
   if (threadIdx.x == 0) {
-    if (q == kRkPasses - 1) {
-      if (!draw) {  // the top set is fixed: start the draw select
-        s_st.vm = s_st.prefix;
-        s_st.prefix = 0;
-        s_st.need = P.k;
-        s_st.done = 0;
-      } else {
-        s_st.vr = s_st.prefix;
+    a.state[p].sel[0] = s_sel;
+    if (q == 0) a.state[p].counts = 0ull;
+  }
+}
+
+// Valid lanes of float4 group g of layer L (the padding of a row is not an entry).
+__device__ __forceinline__ unsigned group_valid(const LayerDev& L, uint32_t g) {
+  if (L.ld == L.m) return 0xFu;
+  const uint32_t row = g / (uint32_t)L.F;
+  const int col = 4 * (int)(g - row * (uint32_t)L.F);
+  const int n = min(4, L.m - col);
+  return (1u << n) - 1u;
+}
+
+__device__ __forceinline__ float comp(const float4& v, int c) {
+  return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+}
+
+// This CTA's contiguous run of the persistent passes' tiles.
+__device__ __forceinline__ void rk_run(const RkArgs& a, int* t0, int* t1) {
+  *t0 = (int)((int64_t)blockIdx.x * a.ntiles / gridDim.x);
+  *t1 = (int)((int64_t)(blockIdx.x + 1) * a.ntiles / gridDim.x);
+}
+
+// Pass 0 (persistent, tiles in order): M = G + E into B, the top digit of
+// |M|, and (worker 0's problems) U zeroed.
+__global__ void __launch_bounds__(kRkThreads, 4) rk_pass0_kernel(RkArgs a) {
+  __shared__ uint32_t h[kRkBins];
+  __shared__ uint64_t s_sum[kRkThreads];
+  __shared__ int s_flag;
+  int t, t1;
+  rk_run(a, &t, &t1);
+  while (t < t1) {
+    const RkTile first = a.tiles[t];
+    const RkProb P = a.probs[first.p];
+    const LayerDev L = a.layers[P.mi];
+    const int te = (int)min((int64_t)t1, t + (P.nchunks - first.chunk));
+    rk_zero_hist<kRkThreads>(h);
+    const uint32_t ng = (uint32_t)(P.len / 4);
+    const float4* G4 = reinterpret_cast<const float4*>(a.G[P.w] + L.off);
+    float4* B4 = reinterpret_cast<float4*>(a.B + (int64_t)P.w * a.total + L.off);
+    float4* U4 = (a.U && P.w == 0) ? reinterpret_cast<float4*>(a.U + L.off) : nullptr;
+    constexpr int kHalf = kRkGroups / 2;
+#pragma unroll 1
+    for (int c = first.chunk; c < first.chunk + (te - t); ++c) {
+      const uint32_t base = (uint32_t)c * (kRkThreads * kRkGroups) + threadIdx.x;
+#pragma unroll 1
+      for (int jb = 0; jb < kRkGroups; jb += kHalf) {
+        float4 gv[kHalf], bv[kHalf];
+#pragma unroll
+        for (int u = 0; u < kHalf; ++u) {
+          const uint32_t g = base + (uint32_t)(jb + u) * kRkThreads;
+          if (g < ng) {
+            gv[u] = __ldcs(G4 + g);
+            bv[u] = B4[g];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kHalf; ++u) {
+          const uint32_t g = base + (uint32_t)(jb + u) * kRkThreads;
+          if (g >= ng) continue;
+          const unsigned ok = group_valid(L, g);
+          float4 mv = bv[u];
+          if (ok & 1u) mv.x = gv[u].x + bv[u].x;
+          if (ok & 2u) mv.y = gv[u].y + bv[u].y;
+          if (ok & 4u) mv.z = gv[u].z + bv[u].z;
+          if (ok & 8u) mv.w = gv[u].w + bv[u].w;
+          B4[g] = mv;
+          if (U4) U4[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (ok >> k & 1u) atomicAdd(&h[(__float_as_uint(comp(mv, k)) & 0x7FFFFFFFu) >> 21], 1u);
+        }
       }
     }
-    *stp = s_st;
+    rk_close_run(a, first.p, 0, (unsigned)(te - t), (unsigned)P.nchunks, h, s_sum, &s_flag);
+    t = te;
   }
 }
 
-// Sent entries of layer mi per chunk and worker (for the index-ordered
-// message offsets).  Thread = 8 consecutive entries.
-__global__ void __launch_bounds__(kRkThreads) rk_count_kernel(RkArgs a) {
-  __shared__ int s_part[kRkThreads / 32];
-  const RkTile t = a.tiles[blockIdx.x];
-  const int mi = t.p;
-  const LayerDev L = a.layers[mi];
-  const int64_t i0 = (int64_t)t.chunk * kRkChunk + (int64_t)threadIdx.x * kRkPer;
-  for (int w = 0; w < a.W; ++w) {
-    const int p = w * a.nmat + mi;
+// Pass 1 (persistent, each CTA's run backwards: pass 0 wrote its end last,
+// so it is still in L2): the list of the entries above the chosen top digit
+// (members of T for sure) and the list of candidates (top digit equal to it).
+__global__ void __launch_bounds__(kRkThreads, 4) rk_pass1_kernel(RkArgs a) {
+  const int lane = threadIdx.x & 31;
+  int t0, t;
+  rk_run(a, &t0, &t);
+  while (t > t0) {
+    const RkTile last = a.tiles[t - 1];
+    const int p = last.p;
     const RkProb P = a.probs[p];
-    const RkState st = a.state[p];
-    const float* Bw = a.B + (int64_t)w * a.total;
-    int c = 0;
-    for (int j = 0; j < kRkPer; ++j) {
-      const int64_t i = i0 + j;
-      if (i >= P.d) break;
-      const float m = Bw[pos_of(L, i)];
-      if (key_mag(m, i) >= st.vm && key_draw(st.dkey, i) <= st.vr) ++c;
+    const LayerDev L = a.layers[P.mi];
+    RkState* stp = a.state + p;
+    const RkSel sel = stp->sel[0];
+    const int tb = max(t0, t - 1 - last.chunk);
+    const uint32_t ng = (uint32_t)(P.len / 4);
+    const float4* B4 = reinterpret_cast<const float4*>(a.B + (int64_t)P.w * a.total + L.off);
+    RkCand* cl = a.cand + P.list_off;
+    RkDraw* sl = a.tlist + P.list_off;
+    // |M| bit patterns: [lo, hi) holds the chosen top digit, >= hi is above it
+    // (a finished select: everything from lo up is in T, no candidates)
+    const uint32_t lo = (uint32_t)(sel.prefix >> 53) << 21;
+    const uint32_t hi = sel.done ? lo : lo + (1u << 21);
+    constexpr int kHalf = kRkGroups / 2;
+#pragma unroll 1
+    for (int c = last.chunk; c > last.chunk - (t - tb); --c) {
+      const uint32_t base = (uint32_t)c * (kRkThreads * kRkGroups) + threadIdx.x;
+#pragma unroll 1
+      for (int jb = 0; jb < kRkGroups; jb += kHalf) {
+        float4 bv[kHalf];
+#pragma unroll
+        for (int u = 0; u < kHalf; ++u) {
+          const uint32_t g = base + (uint32_t)(jb + u) * kRkThreads;
+          if (g < ng) bv[u] = B4[g];
+        }
+        unsigned smask = 0, cmask = 0;  // sure / candidate lanes, 4 bits per group
+#pragma unroll
+        for (int u = 0; u < kHalf; ++u) {
+          const uint32_t g = base + (uint32_t)(jb + u) * kRkThreads;
+          const unsigned ok = g < ng ? group_valid(L, g) : 0u;
+          unsigned sure = 0, cnd = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t pat = __float_as_uint(comp(bv[u], k)) & 0x7FFFFFFFu;
+            sure |= (pat >= hi ? 1u : 0u) << k;
+            cnd |= (pat - lo < hi - lo ? 1u : 0u) << k;
+          }
+          smask |= (sure & ok) << (4 * u);
+          cmask |= (cnd & ok) << (4 * u);
+        }
+        // one reservation per warp in both lists (a 64-bit counter pair)
+        if (__any_sync(kFull, (smask | cmask) != 0)) {
+          const uint32_t mine = ((uint32_t)__popc(smask) << 16) | (uint32_t)__popc(cmask);
+          uint32_t incl = mine;  // <= 512 of each per warp: the halves never carry
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += x;
+          }
+          unsigned long long b0 = 0;
+          if (lane == 31) b0 = atomicAdd(&stp->counts, ((unsigned long long)(incl >> 16) << 32) | (incl & 0xFFFFu));
+          b0 = __shfl_sync(kFull, b0, 31);
+          const uint32_t ex = incl - mine;
+          uint32_t ss = (uint32_t)(b0 >> 32) + (ex >> 16);
+          uint32_t cs = (uint32_t)b0 + (ex & 0xFFFFu);
+#pragma unroll
+          for (int u = 0; u < kHalf; ++u) {
+            const unsigned sm = (smask >> (4 * u)) & 0xFu, cm = (cmask >> (4 * u)) & 0xFu;
+            if (!(sm | cm)) continue;
+            const uint32_t g = base + (uint32_t)(jb + u) * kRkThreads;
+            uint32_t i0;
+            if (L.ld == L.m) {
+              i0 = 4 * g;
+            } else {
+              const uint32_t row = g / (uint32_t)L.F;
+              i0 = row * (uint32_t)L.m + 4 * (g - row * (uint32_t)L.F);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              if (sm >> k & 1u) sl[ss++] = RkDraw{i0 + k, 0u};
+              if (cm >> k & 1u) cl[cs++] = RkCand{i0 + k, comp(bv[u], k)};
+            }
+          }
+        }
+      }
     }
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
-    if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = c;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int s = 0;
-      for (int v = 0; v < kRkThreads / 32; ++v) s += s_part[v];
-      a.ccount[P.chunk0 + t.chunk] = s;
-    }
-    __syncthreads();
+    t = tb;
   }
 }
 
-// Exclusive offsets of each problem's chunk counts (one CTA per problem).
-__global__ void __launch_bounds__(kRkThreads) rk_scan_kernel(RkArgs a) {
-  __shared__ int64_t s_sum[kRkThreads];
-  const RkProb P = a.probs[blockIdx.x];
-  int64_t* c = a.ccount + P.chunk0;
-  const int64_t per = (P.nchunks + kRkThreads - 1) / kRkThreads;
-  const int64_t b0 = threadIdx.x * per, b1 = min(P.nchunks, b0 + per);
-  int64_t mine = 0;
-  for (int64_t b = b0; b < b1; ++b) mine += c[b];
-  s_sum[threadIdx.x] = mine;
+// The rest of one problem's selection, one CTA (kRkTail threads) per
+// problem: magnitude digits 1.. over the candidates, the list of T
+// completed (the sure members' draws, then the candidates that make T), the
+// draw select over it, the sent entries set in K's bitmap and counted per
+// span, and the spans' exclusive offsets.  Every loop keeps kRkBatch loads
+// in flight per thread: one CTA has to cover a whole problem.
+constexpr int kRkBatch = 8;
+
+__global__ void __launch_bounds__(kRkTail, 1) rk_tail_kernel(RkArgs a) {
+  __shared__ uint32_t h[kRkBins];
+  __shared__ uint64_t s_sum[kRkTail];
+  __shared__ RkSel s_sel;
+  __shared__ uint32_t s_cnt;
+  const int p = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const RkProb P = a.probs[p];
+  const LayerDev L = a.layers[P.mi];
+  RkState* stp = a.state + p;
+  const unsigned long long cnts = stp->counts;
+  const uint32_t nc = (uint32_t)cnts, ns = (uint32_t)(cnts >> 32);
+  const RkCand* cl = a.cand + P.list_off;
+  RkDraw* tl = a.tlist + P.list_off;
+  uint32_t* bm = a.bm + P.bm_off;
+  if (tid == 0) s_sel = stp->sel[0];
   __syncthreads();
-  for (int o = 1; o < kRkThreads; o <<= 1) {
-    const int64_t v = (threadIdx.x >= (unsigned)o) ? s_sum[threadIdx.x - o] : 0;
+  // magnitude digits 1.. over the candidates
+  for (int q = 1; q < kRkPasses && !s_sel.done; ++q) {
+    rk_zero_hist<kRkTail>(h);
+    const int shift = c_shift[q];
+    const uint64_t above = mask_above(q), want = s_sel.prefix & above;
+    const uint32_t dmask = (1u << c_width[q]) - 1u;
+    for (uint32_t e0 = tid; e0 < nc; e0 += kRkTail * kRkBatch) {
+      RkCand cv[kRkBatch];
+#pragma unroll
+      for (int u = 0; u < kRkBatch; ++u)
+        if (e0 + u * kRkTail < nc) cv[u] = cl[e0 + u * kRkTail];
+#pragma unroll
+      for (int u = 0; u < kRkBatch; ++u)
+        if (e0 + u * kRkTail < nc) {
+          const uint64_t K = key_mag(cv[u].m, cv[u].i);
+          if ((K & above) == want) atomicAdd(&h[(uint32_t)(K >> shift) & dmask], 1u);
+        }
+    }
     __syncthreads();
-    s_sum[threadIdx.x] += v;
+    rk_find<kRkTail>(s_sel, h, shift, c_width[q], true, s_sum);
     __syncthreads();
   }
-  int64_t run = s_sum[threadIdx.x] - mine;
+  const uint64_t vm = s_sel.prefix;
+  const uint64_t step_key = mix64(a.seed + (uint64_t)(a.step + 1) * kGamma);
+  const uint64_t dkey = mix64(step_key + (uint64_t)(P.w * 65536 + L.index + 1) * kGamma);
+  __syncthreads();  // every thread has read vm
+  if (tid == 0) {
+    stp->sel[0] = s_sel;
+    s_sel = RkSel{0ull, P.k, 0, 0};
+    s_cnt = ns;
+  }
+  for (int b = tid; b < kRkBins; b += kRkTail) h[b] = 0u;
+  __syncthreads();
+  // the list of T with its draws, the top draw digit on the way: first the
+  // sure members (in place) ...
+  for (uint32_t e0 = tid; e0 < ns; e0 += kRkTail * kRkBatch) {
+    uint32_t iv[kRkBatch];
+#pragma unroll
+    for (int u = 0; u < kRkBatch; ++u)
+      if (e0 + u * kRkTail < ns) iv[u] = tl[e0 + u * kRkTail].i;
+#pragma unroll
+    for (int u = 0; u < kRkBatch; ++u)
+      if (e0 + u * kRkTail < ns) {
+        const uint32_t hv = draw_hi(dkey, iv[u]);
+        tl[e0 + u * kRkTail].h = hv;
+        atomicAdd(&h[hv >> 21], 1u);
+      }
+  }
+  // ... then the candidates that make T, appended (warp-uniform batches, one
+  // reservation per warp and batch)
+  for (uint32_t eb = (uint32_t)(tid >> 5) * 32 * kRkBatch; eb < nc; eb += kRkTail * kRkBatch) {
+    RkCand cv[kRkBatch];
+    unsigned take = 0;
+#pragma unroll
+    for (int u = 0; u < kRkBatch; ++u) {
+      const uint32_t e = eb + u * 32 + lane;
+      if (e < nc) cv[u] = cl[e];
+    }
+#pragma unroll
+    for (int u = 0; u < kRkBatch; ++u) {
+      const uint32_t e = eb + u * 32 + lane;
+      if (e < nc && key_mag(cv[u].m, cv[u].i) >= vm) take |= 1u << u;
+    }
+    const int n = __popc(take);
+    int incl = n;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += x;
+    }
+    uint32_t slot = 0;
+    if (lane == 31 && incl) slot = atomicAdd(&s_cnt, (uint32_t)incl);
+    slot = __shfl_sync(kFull, slot, 31) + (uint32_t)(incl - n);
+#pragma unroll
+    for (int u = 0; u < kRkBatch; ++u)
+      if (take >> u & 1u) {
+        const uint32_t hv = draw_hi(dkey, cv[u].i);
+        tl[slot++] = RkDraw{cv[u].i, hv};
+        atomicAdd(&h[hv >> 21], 1u);
+      }
+  }
+  __syncthreads();
+  const uint32_t nT = s_cnt;
+  rk_find<kRkTail>(s_sel, h, c_shift[0], c_width[0], false, s_sum);
+  __syncthreads();
+  for (int q = 1; q < kRkPasses && !s_sel.done; ++q) {
+    rk_zero_hist<kRkTail>(h);
+    const int shift = c_shift[q];
+    const uint64_t above = mask_above(q), want = s_sel.prefix & above;
+    const uint32_t dmask = (1u << c_width[q]) - 1u;
+    for (uint32_t e0 = tid; e0 < nT; e0 += kRkTail * kRkBatch) {
+      RkDraw dv[kRkBatch];
+#pragma unroll
+      for (int u = 0; u < kRkBatch; ++u)
+        if (e0 + u * kRkTail < nT) dv[u] = tl[e0 + u * kRkTail];
+#pragma unroll
+      for (int u = 0; u < kRkBatch; ++u)
+        if (e0 + u * kRkTail < nT) {
+          const uint64_t K = ((uint64_t)dv[u].h << 32) | dv[u].i;
+          if ((K & above) == want) atomicAdd(&h[(uint32_t)(K >> shift) & dmask], 1u);
+        }
+    }
+    __syncthreads();
+    rk_find<kRkTail>(s_sel, h, shift, c_width[q], false, s_sum);
+    __syncthreads();
+  }
+  const uint64_t vr = s_sel.prefix;
+  // K: the sent entries set in the bitmap (zero since the last apply) and
+  // counted per span (in the free histogram when there are at most kRkBins
+  // spans)
+  int64_t* cc = a.ccount + P.chunk0;
+  const bool local = P.nspans <= kRkBins;
+  for (int c = tid; c < kRkBins; c += kRkTail) h[c] = 0u;
+  if (!local)
+    for (int64_t c = tid; c < P.nspans; c += kRkTail) cc[c] = 0;
+  __syncthreads();
+  for (uint32_t e0 = tid; e0 < nT; e0 += kRkTail * kRkBatch) {
+    RkDraw dv[kRkBatch];
+#pragma unroll
+    for (int u = 0; u < kRkBatch; ++u)
+      if (e0 + u * kRkTail < nT) dv[u] = tl[e0 + u * kRkTail];
+#pragma unroll
+    for (int u = 0; u < kRkBatch; ++u)
+      if (e0 + u * kRkTail < nT && (((uint64_t)dv[u].h << 32) | dv[u].i) <= vr) {
+        const uint32_t pp = packed_of(L, dv[u].i);
+        atomicOr(bm + (pp >> 5), 1u << (pp & 31));
+        if (local)
+          atomicAdd(&h[pp / kRkSpan], 1u);
+        else
+          atomicAdd(reinterpret_cast<unsigned long long*>(cc + pp / kRkSpan), 1ull);
+      }
+  }
+  __syncthreads();
+  // exclusive offsets of the span counts
+  const int64_t per = (P.nspans + kRkTail - 1) / kRkTail;
+  const int64_t b0 = tid * per, b1 = min(P.nspans, b0 + per);
+  int64_t mine = 0;
+  for (int64_t b = b0; b < b1; ++b) mine += local ? (int64_t)h[b] : __ldcg(cc + b);
+  s_sum[tid] = (uint64_t)mine;
+  __syncthreads();
+  for (int o = 1; o < kRkTail; o <<= 1) {
+    const uint64_t v = (tid >= o) ? s_sum[tid - o] : 0;
+    __syncthreads();
+    s_sum[tid] += v;
+    __syncthreads();
+  }
+  int64_t run = (int64_t)s_sum[tid] - mine;
   for (int64_t b = b0; b < b1; ++b) {
-    const int64_t x = c[b];
-    c[b] = run;
+    const int64_t x = local ? (int64_t)h[b] : __ldcg(cc + b);
+    cc[b] = run;
     run += x;
   }
+  if (tid == 0) {
+    stp->sel[1] = s_sel;
+    stp->dkey = dkey;
+    stp->nT = nT;
+  }
 }
 
-// Messages, error and update of layer mi over one chunk, all workers in
-// order: the sent entries go to the worker's message at their index-ordered
-// position, are zeroed in B (E = M - S), and summed into U.
+// Messages, error and update of layer mi over one span, all workers in
+// order: thread = one bitmap word (the scattered reads and writes of the
+// sent entries are latency-bound, so one word per thread keeps the most of
+// them in flight); the sent entries go to the worker's message at their
+// index-ordered position, are zeroed in B (E = M - S) and summed into U
+// (zeroed by pass 0), which is then scaled by 1 / W; the bitmap words are
+// cleared.  The workers' records and span offsets are read once into shared
+// memory, and the next worker's word is fetched while one is written.
 __global__ void __launch_bounds__(kRkThreads) rk_apply_kernel(RkArgs a) {
   __shared__ int s_warp[kRkThreads / 32];
+  __shared__ int64_t s_at[kMaxWorkers], s_end[kMaxWorkers], s_bm[kMaxWorkers];
   const RkTile t = a.tiles[blockIdx.x];
   const int mi = t.p;
   const LayerDev L = a.layers[mi];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t i0 = (int64_t)t.chunk * kRkChunk + (int64_t)threadIdx.x * kRkPer;
-  float u[kRkPer];
-#pragma unroll
-  for (int j = 0; j < kRkPer; ++j) u[j] = 0.f;
-  for (int w = 0; w < a.W; ++w) {
-    const int p = w * a.nmat + mi;
-    const RkProb P = a.probs[p];
-    const RkState st = a.state[p];
-    float* Bw = a.B + (int64_t)w * a.total;
-    bool sel[kRkPer];
-    float mv[kRkPer];
-    int c = 0;
-#pragma unroll
-    for (int j = 0; j < kRkPer; ++j) {
-      const int64_t i = i0 + j;
-      sel[j] = false;
-      mv[j] = 0.f;
-      if (i < P.d) {
-        mv[j] = Bw[pos_of(L, i)];
-        sel[j] = key_mag(mv[j], i) >= st.vm && key_draw(st.dkey, i) <= st.vr;
-        c += sel[j] ? 1 : 0;
-      }
-    }
-    // exclusive rank of this thread's first sent entry within the chunk
+  if (threadIdx.x < a.W) {
+    const RkProb P = a.probs[threadIdx.x * a.nmat + mi];
+    s_at[threadIdx.x] = P.msg_off + a.ccount[P.chunk0 + t.chunk];
+    s_end[threadIdx.x] = P.msg_off + P.k;  // exactly k entries are selected; never write past them
+    s_bm[threadIdx.x] = P.bm_off;
+  }
+  __syncthreads();
+  const uint32_t w = (uint32_t)t.chunk * kRkApplyWords + threadIdx.x;
+  const uint32_t nw = (uint32_t)(((int64_t)L.n * L.ld + 31) / 32);  // same for every worker
+  const bool in = w < nw;
+  float* Ul = a.U ? a.U + L.off : nullptr;
+  uint32_t uni = 0;
+  uint32_t nxt = in ? __ldcg(a.bm + s_bm[0] + w) : 0u;
+  for (int wk = 0; wk < a.W; ++wk) {
+    const uint32_t K = nxt;
+    if (wk + 1 < a.W && in) nxt = __ldcg(a.bm + s_bm[wk + 1] + w);
+    const int c = __popc(K);
+    // exclusive rank of this word's first sent entry within the span
     int incl = c;
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(kFull, incl, o);
@@ -321,60 +640,41 @@ __global__ void __launch_bounds__(kRkThreads) rk_apply_kernel(RkArgs a) {
     int base = 0;
     for (int v = 0; v < warp; ++v) base += s_warp[v];
     __syncthreads();
-    int64_t at = P.msg_off + a.ccount[P.chunk0 + t.chunk] + base + incl - c;
-    const int64_t end = P.msg_off + P.k;  // exactly k entries are selected; never write past them
-#pragma unroll
-    for (int j = 0; j < kRkPer; ++j) {
-      if (sel[j]) {
-        const int64_t i = i0 + j;
-        if (at < end) {
-          a.sidx[at] = (int32_t)i;
-          a.sval[at] = mv[j];
-        }
-        ++at;
-        u[j] += mv[j];
-        Bw[pos_of(L, i)] = 0.f;
+    if (!c) continue;
+    a.bm[s_bm[wk] + w] = 0u;  // K's bitmap is zero again for the next step
+    int64_t at = s_at[wk] + base + incl - c;
+    const int64_t end = s_end[wk];
+    float* Bw = a.B + (int64_t)wk * a.total + L.off;
+    for (uint32_t bits = K; bits; bits &= bits - 1) {
+      const uint32_t pp = w * 32 + (uint32_t)(__ffs(bits) - 1);
+      const float v = Bw[pp];
+      if (at < end) {
+        a.sidx[at] = (int32_t)flat_of(L, pp);
+        a.sval[at] = v;
       }
+      ++at;
+      Bw[pp] = 0.f;
+      if (Ul) Ul[pp] += v;
     }
+    uni |= K;
   }
-  if (a.U) {
+  if (Ul && uni) {
     const float inv = 1.0f / (float)a.W;
-#pragma unroll
-    for (int j = 0; j < kRkPer; ++j) {
-      const int64_t i = i0 + j;
-      if (i < (int64_t)L.n * L.m) a.U[pos_of(L, i)] = u[j] * inv;
+    for (uint32_t bits = uni; bits; bits &= bits - 1) {
+      const uint32_t pp = w * 32 + (uint32_t)(__ffs(bits) - 1);
+      Ul[pp] *= inv;
     }
   }
 }
 
-// Vector layers: U = the worker mean (one thread per entry).
-__global__ void rk_vec_kernel(const VecDev* vecs, int nvec, RkArgs a) {
-  for (int vi = 0; vi < nvec; ++vi) {
-    const VecDev V = vecs[vi];
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < V.n; i += (int64_t)gridDim.x * blockDim.x) {
-      float s = 0.f;
-      for (int w = 0; w < a.W; ++w) s += a.G[w][V.off + i];
-      a.U[V.off + i] = s / (float)a.W;
-    }
+// Vector layers: U = the worker mean; grid.y = vector layer.
+__global__ void rk_vec_kernel(const VecDev* vecs, RkArgs a) {
+  const VecDev V = vecs[blockIdx.y];
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < V.n; i += (int64_t)gridDim.x * blockDim.x) {
+    float s = 0.f;
+    for (int w = 0; w < a.W; ++w) s += a.G[w][V.off + i];
+    a.U[V.off + i] = s / (float)a.W;
   }
-}
-
-// Per-step draw keys and select state of every problem.
-__global__ void rk_begin_kernel(RkArgs a, int nprob) {
-  const int p = blockIdx.x * blockDim.x + threadIdx.x;
-  if (p >= nprob) return;
-  const RkProb P = a.probs[p];
-  const LayerDev L = a.layers[P.mi];
-  const uint64_t s = mix64(a.seed + (uint64_t)(a.step + 1) * kGamma);
-  RkState st;
-  st.prefix = 0;
-  st.need = P.r;
-  st.vm = 0;
-  st.vr = 0;
-  st.dkey = mix64(s + (uint64_t)(P.w * 65536 + L.index + 1) * kGamma);
-  st.done = 0;
-  st.pad = 0;
-  a.state[p] = st;
 }
 
 }  // namespace
@@ -384,7 +684,8 @@ struct RTopK {
   uint64_t seed = 0;
   std::vector<RkProb> hp;
   std::vector<int64_t> kk;  // k per matrix layer
-  std::vector<RkTile> htiles, ltiles;
+  std::vector<RkTile> ftiles, ltiles;
+  int pgrid = 0;  // CTAs of the persistent passes
   const LayerDev* d_layers = nullptr;
   const VecDev* d_vecs = nullptr;
   int nvec = 0;
@@ -392,12 +693,15 @@ struct RTopK {
   RkState* d_state = nullptr;
   uint32_t* d_hist = nullptr;
   unsigned* d_arrive = nullptr;
-  RkTile* d_htiles = nullptr;
-  RkTile* d_ltiles = nullptr;
+  RkTile* d_ftiles = nullptr;  // (problem, chunk): passes 0 and 1
+  RkTile* d_ltiles = nullptr;  // (matrix layer, span): apply
+  uint32_t* d_bm = nullptr;
+  RkCand* d_cand = nullptr;
+  RkDraw* d_tlist = nullptr;
   int64_t* d_ccount = nullptr;
   int32_t* d_sidx = nullptr;
   float* d_sval = nullptr;
-  int64_t nchunk_total = 0, msg_total = 0;
+  int64_t nchunk_total = 0, msg_total = 0, cand_total = 0, bm_total = 0;
 };
 
 namespace {
@@ -413,12 +717,18 @@ int rk_alloc(T** p, int64_t count, const char* what) {
   return PSGD_OK;
 }
 
+template <class T>
+int rk_upload(T* d, const std::vector<T>& h) {
+  if (!h.empty()) CUDA_TRY(cudaMemcpy(d, h.data(), h.size() * sizeof(T), cudaMemcpyHostToDevice));
+  return PSGD_OK;
+}
+
 }  // namespace
 
 void rtopk_destroy(RTopK* rk) {
   if (!rk) return;
-  void* ptrs[] = {rk->d_probs, rk->d_state, rk->d_hist, rk->d_arrive, rk->d_htiles, rk->d_ltiles,
-                  rk->d_ccount, rk->d_sidx, rk->d_sval};
+  void* ptrs[] = {rk->d_probs, rk->d_state, rk->d_hist,   rk->d_arrive, rk->d_ftiles, rk->d_ltiles,
+                  rk->d_bm,    rk->d_cand,  rk->d_tlist,  rk->d_ccount, rk->d_sidx, rk->d_sval};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete rk;
@@ -429,6 +739,9 @@ int rtopk_create(RTopK** out, const std::vector<LayerDev>& hl, const std::vector
                  int sample_div) {
   *out = nullptr;
   if (top_div < 1 || sample_div < 1) return fail(PSGD_ERR_INVALID, "rTop-k divisors must be >= 1");
+  for (const LayerDev& L : hl)
+    if ((int64_t)L.n * L.ld >= ((int64_t)1 << 31))
+      return fail(PSGD_ERR_INVALID, "rTop-k needs layers of fewer than 2^31 packed entries");
   RTopK* rk = new RTopK();
   rk->W = W;
   rk->nmat = (int)hl.size();
@@ -439,39 +752,44 @@ int rtopk_create(RTopK** out, const std::vector<LayerDev>& hl, const std::vector
   rk->nvec = (int)hv.size();
   for (int mi = 0; mi < rk->nmat; ++mi) {
     const int64_t d = (int64_t)hl[mi].n * hl[mi].m;
-    if (d >= ((int64_t)1 << 31)) {
-      delete rk;
-      return fail(PSGD_ERR_INVALID, "rTop-k needs layers of fewer than 2^31 entries");
-    }
-    const int64_t r = ceil_div(d, top_div);
-    rk->kk.push_back(ceil_div(r, sample_div));
+    rk->kk.push_back(ceil_div(ceil_div(d, top_div), sample_div));
   }
   for (int w = 0; w < W; ++w)
     for (int mi = 0; mi < rk->nmat; ++mi) {
-      const int64_t d = (int64_t)hl[mi].n * hl[mi].m;
+      const int32_t p = w * rk->nmat + mi;
       RkProb P;
       P.mi = mi;
       P.w = w;
-      P.d = d;
-      P.r = ceil_div(d, top_div);
+      P.d = (int64_t)hl[mi].n * hl[mi].m;
+      P.r = ceil_div(P.d, top_div);
       P.k = rk->kk[mi];
-      P.nchunks = ceil_div(d, kRkChunk);
+      P.len = (int64_t)hl[mi].n * hl[mi].ld;
+      P.nchunks = ceil_div(P.len, kRkChunk);
+      P.nwords = ceil_div(P.len, 32);
+      P.nspans = ceil_div(P.len, kRkSpan);
       P.chunk0 = rk->nchunk_total;
-      rk->nchunk_total += P.nchunks;
+      rk->nchunk_total += P.nspans;
       P.msg_off = rk->msg_total;
       rk->msg_total += P.k;
+      P.list_off = rk->cand_total;
+      rk->cand_total += P.d;
+      P.bm_off = rk->bm_total;
+      rk->bm_total += (P.nwords + 3) & ~(int64_t)3;  // 16-byte aligned, whole uint4 per apply thread
       rk->hp.push_back(P);
-      for (int64_t c = 0; c < P.nchunks; ++c) rk->htiles.push_back({(int32_t)(w * rk->nmat + mi), (int32_t)c});
+      for (int64_t c = 0; c < P.nchunks; ++c) rk->ftiles.push_back({p, (int32_t)c});
     }
   for (int mi = 0; mi < rk->nmat; ++mi)
-    for (int64_t c = 0; c < rk->hp[mi].nchunks; ++c) rk->ltiles.push_back({mi, (int32_t)c});
+    for (int64_t c = 0; c < rk->hp[mi].nspans; ++c) rk->ltiles.push_back({mi, (int32_t)c});
   int rc = PSGD_OK;
   if (!rc) rc = rk_alloc(&rk->d_probs, rk->nprob, "rtopk problems");
   if (!rc) rc = rk_alloc(&rk->d_state, rk->nprob, "rtopk state");
   if (!rc) rc = rk_alloc(&rk->d_hist, (int64_t)rk->nprob * kRkBins, "rtopk histograms");
   if (!rc) rc = rk_alloc(&rk->d_arrive, rk->nprob, "rtopk counters");
-  if (!rc) rc = rk_alloc(&rk->d_htiles, (int64_t)rk->htiles.size(), "rtopk tiles");
+  if (!rc) rc = rk_alloc(&rk->d_ftiles, (int64_t)rk->ftiles.size(), "rtopk tiles");
   if (!rc) rc = rk_alloc(&rk->d_ltiles, (int64_t)rk->ltiles.size(), "rtopk tiles");
+  if (!rc) rc = rk_alloc(&rk->d_bm, rk->bm_total, "rtopk bitmaps");
+  if (!rc) rc = rk_alloc(&rk->d_cand, rk->cand_total, "rtopk candidate lists");
+  if (!rc) rc = rk_alloc(&rk->d_tlist, rk->cand_total, "rtopk top-set lists");
   if (!rc) rc = rk_alloc(&rk->d_ccount, rk->nchunk_total, "rtopk chunk counts");
   if (!rc) rc = rk_alloc(&rk->d_sidx, rk->msg_total, "rtopk message indices");
   if (!rc) rc = rk_alloc(&rk->d_sval, rk->msg_total, "rtopk message values");
@@ -480,16 +798,22 @@ int rtopk_create(RTopK** out, const std::vector<LayerDev>& hl, const std::vector
     return rc;
   }
   auto setup = [&]() -> int {
-    if (!rk->hp.empty())
-      CUDA_TRY(cudaMemcpy(rk->d_probs, rk->hp.data(), rk->hp.size() * sizeof(RkProb), cudaMemcpyHostToDevice));
-    if (!rk->htiles.empty())
-      CUDA_TRY(cudaMemcpy(rk->d_htiles, rk->htiles.data(), rk->htiles.size() * sizeof(RkTile), cudaMemcpyHostToDevice));
-    if (!rk->ltiles.empty())
-      CUDA_TRY(cudaMemcpy(rk->d_ltiles, rk->ltiles.data(), rk->ltiles.size() * sizeof(RkTile), cudaMemcpyHostToDevice));
+    int e = rk_upload(rk->d_probs, rk->hp);
+    if (!e) e = rk_upload(rk->d_ftiles, rk->ftiles);
+    if (!e) e = rk_upload(rk->d_ltiles, rk->ltiles);
+    if (e) return e;
+    CUDA_TRY(cudaMemset(rk->d_bm, 0, (size_t)std::max<int64_t>(rk->bm_total, 1) * sizeof(uint32_t)));
     CUDA_TRY(cudaMemset(rk->d_hist, 0, (size_t)std::max(rk->nprob, 1) * kRkBins * sizeof(uint32_t)));
     CUDA_TRY(cudaMemset(rk->d_arrive, 0, (size_t)std::max(rk->nprob, 1) * sizeof(unsigned)));
     CUDA_TRY(cudaMemset(rk->d_sidx, 0, (size_t)std::max<int64_t>(rk->msg_total, 1) * sizeof(int32_t)));
     CUDA_TRY(cudaMemset(rk->d_sval, 0, (size_t)std::max<int64_t>(rk->msg_total, 1) * sizeof(float)));
+    // persistent passes: one wave of resident CTAs
+    int dev = 0, sms = 0, o0 = 0, o1 = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o0, rk_pass0_kernel, kRkThreads, 0));
+    CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o1, rk_pass1_kernel, kRkThreads, 0));
+    rk->pgrid = (int)std::min<int64_t>((int64_t)rk->ftiles.size(), (int64_t)sms * std::max(1, std::min(o0, o1)));
     return PSGD_OK;
   };
   if ((rc = setup())) {
@@ -512,6 +836,9 @@ int rtopk_step(RTopK* rk, const float* const* G, float* B, int64_t total, float*
   a.state = rk->d_state;
   a.hist = rk->d_hist;
   a.arrive = rk->d_arrive;
+  a.bm = rk->d_bm;
+  a.cand = rk->d_cand;
+  a.tlist = rk->d_tlist;
   a.ccount = rk->d_ccount;
   a.sidx = rk->d_sidx;
   a.sval = rk->d_sval;
@@ -519,26 +846,22 @@ int rtopk_step(RTopK* rk, const float* const* G, float* B, int64_t total, float*
   a.nmat = rk->nmat;
   a.seed = rk->seed;
   a.step = step;
-  if (U) CUDA_TRY(cudaMemsetAsync(U, 0, (size_t)total * sizeof(float), s));
   if (rk->nprob > 0) {
-    rk_begin_kernel<<<(rk->nprob + 127) / 128, 128, 0, s>>>(a, rk->nprob);
+    a.tiles = rk->d_ftiles;
+    a.ntiles = (int32_t)rk->ftiles.size();
+    rk_pass0_kernel<<<(unsigned)rk->pgrid, kRkThreads, 0, s>>>(a);
     CUDA_TRY(cudaGetLastError());
-    a.tiles = rk->d_htiles;
-    for (int draw = 0; draw < 2; ++draw)
-      for (int q = 0; q < kRkPasses; ++q) {
-        rk_hist_kernel<<<(unsigned)rk->htiles.size(), kRkThreads, 0, s>>>(a, q, draw);
-        CUDA_TRY(cudaGetLastError());
-      }
+    rk_pass1_kernel<<<(unsigned)rk->pgrid, kRkThreads, 0, s>>>(a);
+    CUDA_TRY(cudaGetLastError());
+    rk_tail_kernel<<<(unsigned)rk->nprob, kRkTail, 0, s>>>(a);
+    CUDA_TRY(cudaGetLastError());
     a.tiles = rk->d_ltiles;
-    rk_count_kernel<<<(unsigned)rk->ltiles.size(), kRkThreads, 0, s>>>(a);
-    CUDA_TRY(cudaGetLastError());
-    rk_scan_kernel<<<(unsigned)rk->nprob, kRkThreads, 0, s>>>(a);
-    CUDA_TRY(cudaGetLastError());
+    a.ntiles = (int32_t)rk->ltiles.size();
     rk_apply_kernel<<<(unsigned)rk->ltiles.size(), kRkThreads, 0, s>>>(a);
     CUDA_TRY(cudaGetLastError());
   }
   if (U && rk->nvec > 0) {
-    rk_vec_kernel<<<64, 256, 0, s>>>(rk->d_vecs, rk->nvec, a);
+    rk_vec_kernel<<<dim3(16, (unsigned)rk->nvec), 256, 0, s>>>(rk->d_vecs, a);
     CUDA_TRY(cudaGetLastError());
   }
   return PSGD_OK;
@@ -552,6 +875,9 @@ void rtopk_message(const RTopK* rk, int mi, int w, const int32_t** idx, const fl
   *val = rk->d_sval + P.msg_off;
 }
 
-int rtopk_launches(const RTopK* rk) { return rk->nprob > 0 ? 1 + 2 * kRkPasses + 3 + (rk->nvec > 0 ? 1 : 0) : 1; }
+int rtopk_launches(const RTopK* rk) {
+  // passes 0 and 1, tail, apply (+ vectors)
+  return (rk->nprob > 0 ? 4 : 0) + (rk->nvec > 0 ? 1 : 0);
+}
 
 }  // namespace psgd
