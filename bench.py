@@ -90,6 +90,24 @@ def algorithmic_bytes(cfg: workloads.Workload, with_update: bool, momentum: bool
     return {"core": core, "update": upd, "vectors": vec, "total": core + upd + vec}
 
 
+def rtopk_bytes(cfg: workloads.Workload, top_div: int, sample_div: int) -> dict:
+    """Minimum HBM bytes of one rTop-k step.
+
+    Per matrix: every worker's gradient read and its error buffer read and
+    written (3 n m floats per worker), U written (n m), and each worker's
+    message (k indices and k values).  Pass 0 moves all of it but the
+    messages; the per-vector terms are as for PowerSGD.
+    """
+    W = cfg.workers
+    pass0 = sum((3 * W + 1) * n * m * 4 for n, m in cfg.matrices)
+    msgs = 0
+    for n, m in cfg.matrices:
+        r = -(-(n * m) // top_div)
+        msgs += W * 2 * (-(-r // sample_div)) * 4
+    vec = sum(4 * (W + 1) * n for n, _ in cfg.vectors)
+    return {"pass0": pass0, "messages": msgs, "vectors": vec, "total": pass0 + msgs + vec}
+
+
 def unbiased_bytes(cfg: workloads.Workload) -> dict:
     """Minimum HBM bytes of one step of the unbiased variant: every worker's
     gradient read once, P (n r) written, U (n m) written; vectors as above."""
@@ -310,7 +328,12 @@ def run_ours(args, ws, rank, local):
     else:
         def one_step(g):
             ctx.step(g, upd)
-    ab = unbiased_bytes(cfg) if args.unbiased else algorithmic_bytes(cfg, with_update=True, momentum=args.momentum)
+    if args.rtopk:
+        ab = rtopk_bytes(cfg, args.rtopk_top_div, args.rtopk_sample_div)
+    elif args.unbiased:
+        ab = unbiased_bytes(cfg)
+    else:
+        ab = algorithmic_bytes(cfg, with_update=True, momentum=args.momentum)
     comp = compressed_bytes(cfg)
     st = ctx.stats()
 
@@ -346,8 +369,14 @@ def run_ours(args, ws, rank, local):
     phases = ctx.phase_times()  # device ms per phase, averaged over those steps
     ms_per_step, value = replica_throughput(comp, args.steps, ev0.elapsed_time(ev1), ws, device)
     peaks = measured_peaks()
-    project_ms = phases["project"]
-    project_bytes = ab["core"]  # read G, read E, write E of every worker (+ the factors); unbiased: read G
+    if args.rtopk:
+        # rTop-k's four phase slots are its kernels; pass 0 moves nearly all the bytes
+        phases = dict(zip(("pass0", "pass1", "tail", "apply"), phases.values()))
+        project_ms = phases["pass0"]
+        project_bytes = ab["pass0"]  # read G, read E, write M of every worker, U zeroed
+    else:
+        project_ms = phases["project"]
+        project_bytes = ab["core"]  # read G, read E, write E of every worker (+ the factors); unbiased: read G
     achieved = project_bytes / (project_ms * 1e-3) / 1e9
     step_achieved = ab["total"] / (ms_per_step * 1e-3) / 1e9
     h = kernel_sources_hash()
@@ -375,11 +404,12 @@ def run_ours(args, ws, rank, local):
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                      "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
                      else "fallback 6.8 TB/s",
-                     "kernel": ("rTop-k step (all its kernels; phase 'project' spans the step)" if args.rtopk else
+                     "kernel": ("psgd::rk_pass0_kernel (M = G + E written over E, top digit of |M|, U zeroed)"
+                                if args.rtopk else
                                 f"psgd::p1_kernel<{st['kernel_rank']}> (project: P = G Q)" if args.unbiased else
                                 f"psgd::p1_kernel<{st['kernel_rank']}> (project: error add, E write, P = M Q)"),
                      "algorithmic_bytes_per_launch": project_bytes, "launch_ms": round(project_ms, 5),
-                     "launch_ms_source": "CUDA events around the project kernel on the context's stream, "
+                     "launch_ms_source": "CUDA events around the kernel on the context's stream, "
                                          "averaged over a second pass of the timed steps with per-phase events",
                      "kernel_sources": h},
         "step_roofline": {"achieved": round(step_achieved, 1), "frac": round(step_achieved / peaks["hbm_gbs"], 4),

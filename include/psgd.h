@@ -225,8 +225,11 @@ int psgd_get_stats(const psgd_ctx* ctx, psgd_stats* out);
 /*
  * Device time of each phase, in milliseconds, averaged over the steps since
  * the previous call (the last 256 at most): project, orthonormalise,
- * back-project, decompress (ms[4]).  Needs options.timing = 1; waits for the
- * stream.  Each timed step records five CUDA events on the stream.
+ * back-project, decompress (ms[4]); under rTop-k the four slots are its
+ * kernels: the pass forming M, the pass listing the top-set candidates, the
+ * per-problem selection tail, and the message / error / update writes.
+ * Needs options.timing = 1; waits for the stream.  Each timed step records
+ * five CUDA events on the stream.
  */
 int psgd_get_phase_times(psgd_ctx* ctx, float* ms);
 

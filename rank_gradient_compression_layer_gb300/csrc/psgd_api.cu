@@ -527,13 +527,12 @@ int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, flo
   }
   if (c->rk) {
     if (X) return fail(PSGD_ERR_INVALID, "rTop-k has no fused momentum update");
-    rc = rtopk_step(c->rk, grad_ptrs, c->B, c->total, out_update, c->steps, c->stream);
+    // phase slots: pass 0, pass 1, tail, apply (+ vectors)
+    rc = rtopk_step(c->rk, grad_ptrs, c->B, c->total, out_update, c->steps, c->stream, ev ? ev + 1 : nullptr);
     if (rc) {
       c->broken = true;
       return rc;
     }
-    if (ev)
-      for (int ph = 0; ph < kPhases; ++ph) CUDA_TRY(cudaEventRecord(ev[ph + 1], c->stream));
     c->has_prev = 1;
     c->steps += 1;
     return PSGD_OK;

@@ -15,7 +15,7 @@
 // Both selections are radix selects over composite 64-bit keys that are
 // unique per entry -- (|M| bits, ~i) and (h(i), i) -- so the k-th key is one
 // value and "key >= / <= threshold" selects exactly r / k entries.  Six
-// 11-bit digits per select; each pass histograms the digit of the entries
+// digits per select; each pass histograms the digit of the entries
 // still matching the prefix found so far, and the last CTA of a problem to
 // finish picks the digit and narrows the prefix (a select whose chosen bin
 // holds exactly the entries still needed is finished early).
@@ -51,10 +51,26 @@ constexpr int kRkChunk = kRkThreads * kRkGroups * 4;   // packed positions per f
 constexpr int kRkApplyWords = kRkThreads;              // bitmap words per apply tile (1 per thread)
 constexpr int kRkSpan = kRkApplyWords * 32;            // packed positions per apply tile / count chunk
 constexpr int kRkTail = 1024;                          // threads of the per-problem tail CTA
-constexpr int kRkBins = 2048;                          // 11-bit digits
+constexpr int kRkBins = 2048;                          // digits of at most 11 bits
 constexpr int kRkPasses = 6;
-__constant__ int c_shift[kRkPasses] = {53, 42, 31, 20, 9, 0};
-__constant__ int c_width[kRkPasses] = {11, 11, 11, 11, 11, 9};
+// Digit layouts.  Magnitude keys: the first digit is bits 63..53 (bit 63 is
+// |M|'s sign, clear), i.e. |M|'s exponent and top 2 mantissa bits; the
+// second, bits 52..43, is the one pass 0 resolves too when it can (below).
+// Draw keys: six digits over all 64 bits.
+__constant__ int c_mshift[kRkPasses] = {53, 43, 32, 21, 10, 0};
+__constant__ int c_mwidth[kRkPasses] = {11, 10, 11, 11, 11, 10};
+__constant__ int c_dshift[kRkPasses] = {53, 42, 31, 20, 9, 0};
+__constant__ int c_dwidth[kRkPasses] = {11, 11, 11, 11, 11, 9};
+// Under error feedback many entries pile up just below the threshold, so
+// the threshold's first-digit bin holds several percent of a layer, all
+// candidates.  The bin moves little from step to step: pass 0 also counts
+// the second digit of the entries whose first digit is within one of the
+// previous step's (kRkWin bins of kRkFine sub-bins), and when this step's
+// first digit lands there, both digits are known before pass 1.
+constexpr int kRkWin = 3;
+constexpr int kRkFine = 1024;           // second magnitude digit: 10 bits
+constexpr int kRkTopBins = kRkBins + kRkWin * kRkFine;  // pass 0's counters per problem
+constexpr uint32_t kRkNoTop = 0xFFFFFFFFu;
 constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
 
 struct RkProb {   // one (worker, matrix layer) problem
@@ -82,6 +98,8 @@ struct RkState {
   uint64_t dkey;   // draw stream key of this step
   unsigned long long counts;  // pass 1's list lengths: candidates (low 32 bits), sure members of T (high)
   uint32_t nT;     // members of T (the tail's list)
+  uint32_t depth;  // magnitude digits pass 0 resolved (1 or 2)
+  uint32_t prev_top;  // the first magnitude digit of the previous step (kRkNoTop: none); kept across steps
   uint32_t pad;
 };
 
@@ -107,7 +125,7 @@ struct RkArgs {
   const LayerDev* layers;
   const RkProb* probs;
   RkState* state;
-  uint32_t* hist;     // problems x kRkBins
+  uint32_t* hist;     // problems x kRkTopBins: pass 0's first-digit and windowed second-digit counts
   unsigned* arrive;   // problems
   const RkTile* tiles;
   int32_t ntiles;     // tiles of the persistent passes
@@ -138,9 +156,8 @@ __device__ __forceinline__ uint32_t draw_hi(uint64_t dkey, uint32_t i) {
   return (uint32_t)(mix64(dkey + (uint64_t)(i + 1) * kGamma) >> 32);
 }
 
-__device__ __forceinline__ uint64_t mask_above(int q) {
-  const int top = c_shift[q] + c_width[q];
-  return top >= 64 ? 0ull : (~0ull << top);
+__device__ __forceinline__ uint64_t mask_above(int shift, int width) {
+  return shift + width >= 64 ? 0ull : (~0ull << (shift + width));
 }
 
 // Flat index of packed position p (relative to the layer; p < 2^31).
@@ -157,74 +174,107 @@ __device__ __forceinline__ uint32_t packed_of(const LayerDev& L, uint32_t i) {
   return i + row * (uint32_t)(L.ld - L.m);
 }
 
+// Exclusive prefix sum over the NT threads of the CTA (warp shuffles, then
+// one warp over the warp totals: two barriers).  s_w: NT / 32 words of
+// shared scratch; *all receives the total.  All threads call it.
+template <int NT>
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_w, uint32_t* all) {
+  constexpr int NW = NT / 32;
+  static_assert(NW <= 32, "one warp scans the warp totals");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) s_w[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t x = lane < NW ? s_w[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane < NW) s_w[lane] = x;
+  }
+  __syncthreads();
+  *all = s_w[NW - 1];
+  const uint32_t r = incl - v + (warp ? s_w[warp - 1] : 0u);
+  __syncthreads();  // s_w may be reused at once
+  return r;
+}
+
 // Pick the digit at `shift` of the need-th key (largest first for the top
 // set, smallest first for the draw) from the pass histogram h and narrow the
-// select.  All NT threads of the CTA call it.
+// select.  All NT threads of the CTA call it.  Counts fit 32 bits (a problem
+// has fewer than 2^31 entries).
 template <int NT>
-__device__ void rk_find(RkSel& st, const uint32_t* h, int shift, int width, bool largest, uint64_t* s_sum) {
+__device__ void rk_find(RkSel& st, const uint32_t* h, int shift, int width, bool largest, uint32_t* s_w) {
+  auto bin = [&](int b) -> uint32_t { return h[b]; };
   const int t = threadIdx.x;
   const int nb = 1 << width;
-  constexpr int per = kRkBins / NT;
+  const int per = (nb + NT - 1) / NT;
   // thread t owns walk positions [t per, t per + per); walk position j is
   // bin nb - 1 - j (largest first) or bin j (smallest first)
-  uint64_t mine = 0;
-  for (int j = t * per; j < t * per + per; ++j)
-    if (j < nb) mine += h[largest ? nb - 1 - j : j];
-  s_sum[t] = mine;
-  __syncthreads();
-  // inclusive scan over threads (Hillis-Steele)
-  for (int o = 1; o < NT; o <<= 1) {
-    const uint64_t v = (t >= o) ? s_sum[t - o] : 0;
-    __syncthreads();
-    s_sum[t] += v;
-    __syncthreads();
-  }
-  const uint64_t incl = s_sum[t], excl = incl - mine, all = s_sum[NT - 1];
+  uint32_t mine = 0;
+  for (int j = t * per; j < t * per + per && j < nb; ++j) mine += bin(largest ? nb - 1 - j : j);
+  // read before the scan's barriers: the thread that finds the digit
+  // rewrites st right after them
+  const uint64_t need = (uint64_t)st.need;
+  uint32_t all;
+  const uint32_t excl = block_excl_scan<NT>(mine, s_w, &all), incl = excl + mine;
   const uint64_t above = (shift + width >= 64) ? 0ull : (~0ull << (shift + width));
   const uint64_t below = (1ull << shift) - 1ull;  // bits under this digit
-  if (t == 0 && (uint64_t)st.need > all) {
+  if (need > all) {
     // every entry matching the prefix is taken: the threshold is the lowest
     // (largest first) or highest (smallest first) key with that prefix
-    st.prefix = largest ? (st.prefix & above) : ((st.prefix & above) | ~above);
-    st.done = 1;
+    if (t == 0) {
+      st.prefix = largest ? (st.prefix & above) : ((st.prefix & above) | ~above);
+      st.done = 1;
+    }
+    return;
   }
-  __syncthreads();
-  if (st.done) return;
-  if (excl < (uint64_t)st.need && (uint64_t)st.need <= incl) {
-    uint64_t c = excl;
+  if (excl < need && need <= incl) {
+    uint32_t c = excl;
     for (int j = t * per; j < t * per + per && j < nb; ++j) {
       const int b = largest ? nb - 1 - j : j;
-      if (c + h[b] >= (uint64_t)st.need) {
-        const int64_t left = st.need - (int64_t)c;
+      const uint32_t hb = bin(b);
+      if (c + hb >= need) {
+        const int64_t left = (int64_t)(need - c);
         st.prefix = (st.prefix & above) | ((uint64_t)b << shift);
         st.need = left;
-        if ((uint64_t)left == h[b]) {  // the whole bin is taken: the bin's end is the threshold
+        if ((uint64_t)left == hb) {  // the whole bin is taken: the bin's end is the threshold
           if (!largest) st.prefix |= below;
           st.done = 1;
         }
         break;
       }
-      c += h[b];
+      c += hb;
     }
   }
 }
 
-template <int NT>
+template <int NT, int NB = kRkBins>
 __device__ __forceinline__ void rk_zero_hist(uint32_t* h) {
-  for (int b = threadIdx.x; b < kRkBins; b += NT) h[b] = 0u;
+  for (int b = threadIdx.x; b < NB; b += NT) h[b] = 0u;
   __syncthreads();
 }
 
-// End of one persistent pass's run over problem p (`done` of its `total`
-// tiles): merge the CTA's histogram and, in the CTA that completes the
-// problem, pick the magnitude digit q and reset the global histogram.
-// q == 0 starts the problem's select (need = r) and its candidate count.
-__device__ void rk_close_run(const RkArgs& a, int p, int q, unsigned done, unsigned total, uint32_t* h,
-                             uint64_t* s_sum, int* s_flag) {
+// End of pass 0's run over problem p (`done` of its `total` tiles): merge
+// the CTA's counts and, in the CTA that completes the problem, start its
+// top-set select (need = r) with the first magnitude digit and, when it
+// lies in the window counted at the second digit, that digit too; then
+// reset the global counts and the list counters and keep the first digit
+// for the next step's window.  h: kRkTopBins counters (first digit, then
+// the window's second digit).
+__device__ __noinline__ void rk_close_run(const RkArgs& a, int p, uint32_t win0, unsigned done, unsigned total,
+                                          uint32_t* h, uint32_t* s_sum, int* s_flag) {
   __shared__ RkSel s_sel;
-  uint32_t* gh = a.hist + (int64_t)p * kRkBins;
+  uint32_t* gh = a.hist + (int64_t)p * kRkTopBins;
   __syncthreads();
-  for (int b = threadIdx.x; b < kRkBins; b += kRkThreads)
+  for (int b = threadIdx.x; b < kRkTopBins; b += kRkThreads)
     if (h[b]) atomicAdd(gh + b, h[b]);
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -233,20 +283,37 @@ __device__ void rk_close_run(const RkArgs& a, int p, int q, unsigned done, unsig
     const bool last = (old + done == total);
     if (last) a.arrive[p] = 0u;
     *s_flag = last ? 1 : 0;
+    if (last) s_sel = RkSel{0ull, a.probs[p].r, 0, 0};
   }
   __syncthreads();
   if (!*s_flag) return;
-  for (int b = threadIdx.x; b < kRkBins; b += kRkThreads) {
-    h[b] = __ldcg(gh + b);
-    gh[b] = 0u;
+  static_assert(kRkTopBins % kRkThreads == 0, "whole rows of counters per thread");
+  {
+    uint32_t v[kRkTopBins / kRkThreads];  // all loads in flight at once
+#pragma unroll
+    for (int k = 0; k < kRkTopBins / kRkThreads; ++k) v[k] = __ldcg(gh + threadIdx.x + k * kRkThreads);
+#pragma unroll
+    for (int k = 0; k < kRkTopBins / kRkThreads; ++k) {
+      h[threadIdx.x + k * kRkThreads] = v[k];
+      gh[threadIdx.x + k * kRkThreads] = 0u;
+    }
   }
-  if (threadIdx.x == 0) s_sel = q == 0 ? RkSel{0ull, a.probs[p].r, 0, 0} : a.state[p].sel[0];
   __syncthreads();
-  rk_find<kRkThreads>(s_sel, h, c_shift[q], c_width[q], true, s_sum);
+  rk_find<kRkThreads>(s_sel, h, c_mshift[0], c_mwidth[0], true, s_sum);
   __syncthreads();
+  const uint32_t top = (uint32_t)(s_sel.prefix >> c_mshift[0]);
+  const uint32_t slot = top - win0;  // the window's sub-histogram of this first digit, if counted
+  uint32_t depth = 1;
+  if (!s_sel.done && win0 != kRkNoTop && slot < (uint32_t)kRkWin) {
+    rk_find<kRkThreads>(s_sel, h + kRkBins + slot * kRkFine, c_mshift[1], c_mwidth[1], true, s_sum);
+    __syncthreads();
+    depth = 2;
+  }
   if (threadIdx.x == 0) {
     a.state[p].sel[0] = s_sel;
-    if (q == 0) a.state[p].counts = 0ull;
+    a.state[p].counts = 0ull;
+    a.state[p].depth = depth;
+    a.state[p].prev_top = top;
   }
 }
 
@@ -272,8 +339,8 @@ __device__ __forceinline__ void rk_run(const RkArgs& a, int* t0, int* t1) {
 // Pass 0 (persistent, tiles in order): M = G + E into B, the top digit of
 // |M|, and (worker 0's problems) U zeroed.
 __global__ void __launch_bounds__(kRkThreads, 4) rk_pass0_kernel(RkArgs a) {
-  __shared__ uint32_t h[kRkBins];
-  __shared__ uint64_t s_sum[kRkThreads];
+  __shared__ uint32_t h[kRkTopBins];  // first digit, then the window's second digit
+  __shared__ uint32_t s_sum[kRkThreads / 32];
   __shared__ int s_flag;
   int t, t1;
   rk_run(a, &t, &t1);
@@ -282,7 +349,10 @@ __global__ void __launch_bounds__(kRkThreads, 4) rk_pass0_kernel(RkArgs a) {
     const RkProb P = a.probs[first.p];
     const LayerDev L = a.layers[P.mi];
     const int te = (int)min((int64_t)t1, t + (P.nchunks - first.chunk));
-    rk_zero_hist<kRkThreads>(h);
+    rk_zero_hist<kRkThreads, kRkTopBins>(h);
+    // the window: first digits prev_top - 1 .. prev_top + 1 (none before the first step)
+    const uint32_t prev = a.state[first.p].prev_top;
+    const uint32_t win0 = prev == kRkNoTop ? kRkNoTop : prev - 1u;
     const uint32_t ng = (uint32_t)(P.len / 4);
     const float4* G4 = reinterpret_cast<const float4*>(a.G[P.w] + L.off);
     float4* B4 = reinterpret_cast<float4*>(a.B + (int64_t)P.w * a.total + L.off);
@@ -316,11 +386,16 @@ __global__ void __launch_bounds__(kRkThreads, 4) rk_pass0_kernel(RkArgs a) {
           if (U4) U4[g] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            if (ok >> k & 1u) atomicAdd(&h[(__float_as_uint(comp(mv, k)) & 0x7FFFFFFFu) >> 21], 1u);
+            if (ok >> k & 1u) {
+              const uint32_t pat = __float_as_uint(comp(mv, k)) & 0x7FFFFFFFu;
+              atomicAdd(&h[pat >> 21], 1u);
+              const uint32_t slot = (pat >> 21) - win0;  // wraps (large) outside the window
+              if (slot < (uint32_t)kRkWin) atomicAdd(&h[kRkBins + slot * kRkFine + ((pat >> 11) & (kRkFine - 1))], 1u);
+            }
         }
       }
     }
-    rk_close_run(a, first.p, 0, (unsigned)(te - t), (unsigned)P.nchunks, h, s_sum, &s_flag);
+    rk_close_run(a, first.p, win0, (unsigned)(te - t), (unsigned)P.nchunks, h, s_sum, &s_flag);
     t = te;
   }
 }
@@ -344,71 +419,84 @@ __global__ void __launch_bounds__(kRkThreads, 4) rk_pass1_kernel(RkArgs a) {
     const float4* B4 = reinterpret_cast<const float4*>(a.B + (int64_t)P.w * a.total + L.off);
     RkCand* cl = a.cand + P.list_off;
     RkDraw* sl = a.tlist + P.list_off;
-    // |M| bit patterns: [lo, hi) holds the chosen top digit, >= hi is above it
-    // (a finished select: everything from lo up is in T, no candidates)
-    const uint32_t lo = (uint32_t)(sel.prefix >> 53) << 21;
-    const uint32_t hi = sel.done ? lo : lo + (1u << 21);
+    // |M| bit patterns: [lo, hi) holds the digits pass 0 resolved, >= hi is above
+    // them (a finished select: everything from lo up is in T, no candidates)
+    const uint32_t lo = (uint32_t)(sel.prefix >> 32);
+    const uint32_t hi = sel.done ? lo : lo + (1u << (c_mshift[stp->depth - 1] - 32));
+    // the run's half tiles, last chunk first; the next half's loads are in
+    // flight while this half's list reservation (an atomic each warp waits
+    // on) comes back
     constexpr int kHalf = kRkGroups / 2;
+    const int nh = 2 * (t - tb);
+    auto group_of = [&](int hh, int u) -> uint32_t {
+      const uint32_t c = (uint32_t)(last.chunk - (hh >> 1));
+      return c * (kRkThreads * kRkGroups) + threadIdx.x + (uint32_t)((hh & 1) * kHalf + u) * kRkThreads;
+    };
+    float4 cur[kHalf], nxt[kHalf];
+#pragma unroll
+    for (int u = 0; u < kHalf; ++u) {
+      const uint32_t g = group_of(0, u);
+      if (g < ng) cur[u] = B4[g];
+    }
 #pragma unroll 1
-    for (int c = last.chunk; c > last.chunk - (t - tb); --c) {
-      const uint32_t base = (uint32_t)c * (kRkThreads * kRkGroups) + threadIdx.x;
-#pragma unroll 1
-      for (int jb = 0; jb < kRkGroups; jb += kHalf) {
-        float4 bv[kHalf];
+    for (int hh = 0; hh < nh; ++hh) {
+      if (hh + 1 < nh) {
 #pragma unroll
         for (int u = 0; u < kHalf; ++u) {
-          const uint32_t g = base + (uint32_t)(jb + u) * kRkThreads;
-          if (g < ng) bv[u] = B4[g];
+          const uint32_t g = group_of(hh + 1, u);
+          if (g < ng) nxt[u] = B4[g];
         }
-        unsigned smask = 0, cmask = 0;  // sure / candidate lanes, 4 bits per group
+      }
+      unsigned smask = 0, cmask = 0;  // sure / candidate lanes, 4 bits per group
+#pragma unroll
+      for (int u = 0; u < kHalf; ++u) {
+        const uint32_t g = group_of(hh, u);
+        const unsigned ok = g < ng ? group_valid(L, g) : 0u;
+        unsigned sure = 0, cnd = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t pat = __float_as_uint(comp(cur[u], k)) & 0x7FFFFFFFu;
+          sure |= (pat >= hi ? 1u : 0u) << k;
+          cnd |= (pat - lo < hi - lo ? 1u : 0u) << k;
+        }
+        smask |= (sure & ok) << (4 * u);
+        cmask |= (cnd & ok) << (4 * u);
+      }
+      // one reservation per warp in both lists (a 64-bit counter pair)
+      if (__any_sync(kFull, (smask | cmask) != 0)) {
+        const uint32_t mine = ((uint32_t)__popc(smask) << 16) | (uint32_t)__popc(cmask);
+        uint32_t incl = mine;  // <= 512 of each per warp: the halves never carry
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t x = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += x;
+        }
+        unsigned long long b0 = 0;
+        if (lane == 31) b0 = atomicAdd(&stp->counts, ((unsigned long long)(incl >> 16) << 32) | (incl & 0xFFFFu));
+        b0 = __shfl_sync(kFull, b0, 31);
+        const uint32_t ex = incl - mine;
+        uint32_t ss = (uint32_t)(b0 >> 32) + (ex >> 16);
+        uint32_t cs = (uint32_t)b0 + (ex & 0xFFFFu);
 #pragma unroll
         for (int u = 0; u < kHalf; ++u) {
-          const uint32_t g = base + (uint32_t)(jb + u) * kRkThreads;
-          const unsigned ok = g < ng ? group_valid(L, g) : 0u;
-          unsigned sure = 0, cnd = 0;
+          const unsigned sm = (smask >> (4 * u)) & 0xFu, cm = (cmask >> (4 * u)) & 0xFu;
+          if (!(sm | cm)) continue;
+          const uint32_t g = group_of(hh, u);
+          uint32_t i0;
+          if (L.ld == L.m) {
+            i0 = 4 * g;
+          } else {
+            const uint32_t row = g / (uint32_t)L.F;
+            i0 = row * (uint32_t)L.m + 4 * (g - row * (uint32_t)L.F);
+          }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t pat = __float_as_uint(comp(bv[u], k)) & 0x7FFFFFFFu;
-            sure |= (pat >= hi ? 1u : 0u) << k;
-            cnd |= (pat - lo < hi - lo ? 1u : 0u) << k;
-          }
-          smask |= (sure & ok) << (4 * u);
-          cmask |= (cnd & ok) << (4 * u);
-        }
-        // one reservation per warp in both lists (a 64-bit counter pair)
-        if (__any_sync(kFull, (smask | cmask) != 0)) {
-          const uint32_t mine = ((uint32_t)__popc(smask) << 16) | (uint32_t)__popc(cmask);
-          uint32_t incl = mine;  // <= 512 of each per warp: the halves never carry
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t x = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += x;
-          }
-          unsigned long long b0 = 0;
-          if (lane == 31) b0 = atomicAdd(&stp->counts, ((unsigned long long)(incl >> 16) << 32) | (incl & 0xFFFFu));
-          b0 = __shfl_sync(kFull, b0, 31);
-          const uint32_t ex = incl - mine;
-          uint32_t ss = (uint32_t)(b0 >> 32) + (ex >> 16);
-          uint32_t cs = (uint32_t)b0 + (ex & 0xFFFFu);
-#pragma unroll
-          for (int u = 0; u < kHalf; ++u) {
-            const unsigned sm = (smask >> (4 * u)) & 0xFu, cm = (cmask >> (4 * u)) & 0xFu;
-            if (!(sm | cm)) continue;
-            const uint32_t g = base + (uint32_t)(jb + u) * kRkThreads;
-            uint32_t i0;
-            if (L.ld == L.m) {
-              i0 = 4 * g;
-            } else {
-              const uint32_t row = g / (uint32_t)L.F;
-              i0 = row * (uint32_t)L.m + 4 * (g - row * (uint32_t)L.F);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              if (sm >> k & 1u) sl[ss++] = RkDraw{i0 + k, 0u};
-              if (cm >> k & 1u) cl[cs++] = RkCand{i0 + k, comp(bv[u], k)};
-            }
+            if (sm >> k & 1u) sl[ss++] = RkDraw{i0 + k, 0u};
+            if (cm >> k & 1u) cl[cs++] = RkCand{i0 + k, comp(cur[u], k)};
           }
         }
       }
+#pragma unroll
+      for (int u = 0; u < kHalf; ++u) cur[u] = nxt[u];
     }
     t = tb;
   }
@@ -424,7 +512,7 @@ constexpr int kRkBatch = 8;
 
 __global__ void __launch_bounds__(kRkTail, 1) rk_tail_kernel(RkArgs a) {
   __shared__ uint32_t h[kRkBins];
-  __shared__ uint64_t s_sum[kRkTail];
+  __shared__ uint32_t s_sum[kRkTail / 32];
   __shared__ RkSel s_sel;
   __shared__ uint32_t s_cnt;
   const int p = blockIdx.x;
@@ -439,12 +527,12 @@ __global__ void __launch_bounds__(kRkTail, 1) rk_tail_kernel(RkArgs a) {
   uint32_t* bm = a.bm + P.bm_off;
   if (tid == 0) s_sel = stp->sel[0];
   __syncthreads();
-  // magnitude digits 1.. over the candidates
-  for (int q = 1; q < kRkPasses && !s_sel.done; ++q) {
+  // the magnitude digits pass 0 left, over the candidates
+  for (int q = (int)stp->depth; q < kRkPasses && !s_sel.done; ++q) {
     rk_zero_hist<kRkTail>(h);
-    const int shift = c_shift[q];
-    const uint64_t above = mask_above(q), want = s_sel.prefix & above;
-    const uint32_t dmask = (1u << c_width[q]) - 1u;
+    const int shift = c_mshift[q], width = c_mwidth[q];
+    const uint64_t above = mask_above(shift, width), want = s_sel.prefix & above;
+    const uint32_t dmask = (1u << width) - 1u;
     for (uint32_t e0 = tid; e0 < nc; e0 += kRkTail * kRkBatch) {
       RkCand cv[kRkBatch];
 #pragma unroll
@@ -458,7 +546,7 @@ __global__ void __launch_bounds__(kRkTail, 1) rk_tail_kernel(RkArgs a) {
         }
     }
     __syncthreads();
-    rk_find<kRkTail>(s_sel, h, shift, c_width[q], true, s_sum);
+    rk_find<kRkTail>(s_sel, h, shift, width, true, s_sum);
     __syncthreads();
   }
   const uint64_t vm = s_sel.prefix;
@@ -521,13 +609,13 @@ __global__ void __launch_bounds__(kRkTail, 1) rk_tail_kernel(RkArgs a) {
   }
   __syncthreads();
   const uint32_t nT = s_cnt;
-  rk_find<kRkTail>(s_sel, h, c_shift[0], c_width[0], false, s_sum);
+  rk_find<kRkTail>(s_sel, h, c_dshift[0], c_dwidth[0], false, s_sum);
   __syncthreads();
   for (int q = 1; q < kRkPasses && !s_sel.done; ++q) {
     rk_zero_hist<kRkTail>(h);
-    const int shift = c_shift[q];
-    const uint64_t above = mask_above(q), want = s_sel.prefix & above;
-    const uint32_t dmask = (1u << c_width[q]) - 1u;
+    const int shift = c_dshift[q], width = c_dwidth[q];
+    const uint64_t above = mask_above(shift, width), want = s_sel.prefix & above;
+    const uint32_t dmask = (1u << width) - 1u;
     for (uint32_t e0 = tid; e0 < nT; e0 += kRkTail * kRkBatch) {
       RkDraw dv[kRkBatch];
 #pragma unroll
@@ -541,7 +629,7 @@ __global__ void __launch_bounds__(kRkTail, 1) rk_tail_kernel(RkArgs a) {
         }
     }
     __syncthreads();
-    rk_find<kRkTail>(s_sel, h, shift, c_width[q], false, s_sum);
+    rk_find<kRkTail>(s_sel, h, shift, width, false, s_sum);
     __syncthreads();
   }
   const uint64_t vr = s_sel.prefix;
@@ -574,17 +662,10 @@ __global__ void __launch_bounds__(kRkTail, 1) rk_tail_kernel(RkArgs a) {
   // exclusive offsets of the span counts
   const int64_t per = (P.nspans + kRkTail - 1) / kRkTail;
   const int64_t b0 = tid * per, b1 = min(P.nspans, b0 + per);
-  int64_t mine = 0;
-  for (int64_t b = b0; b < b1; ++b) mine += local ? (int64_t)h[b] : __ldcg(cc + b);
-  s_sum[tid] = (uint64_t)mine;
-  __syncthreads();
-  for (int o = 1; o < kRkTail; o <<= 1) {
-    const uint64_t v = (tid >= o) ? s_sum[tid - o] : 0;
-    __syncthreads();
-    s_sum[tid] += v;
-    __syncthreads();
-  }
-  int64_t run = (int64_t)s_sum[tid] - mine;
+  uint32_t mine = 0;
+  for (int64_t b = b0; b < b1; ++b) mine += local ? h[b] : (uint32_t)__ldcg(cc + b);
+  uint32_t tot;
+  int64_t run = block_excl_scan<kRkTail>(mine, s_sum, &tot);
   for (int64_t b = b0; b < b1; ++b) {
     const int64_t x = local ? (int64_t)h[b] : __ldcg(cc + b);
     cc[b] = run;
@@ -783,7 +864,7 @@ int rtopk_create(RTopK** out, const std::vector<LayerDev>& hl, const std::vector
   int rc = PSGD_OK;
   if (!rc) rc = rk_alloc(&rk->d_probs, rk->nprob, "rtopk problems");
   if (!rc) rc = rk_alloc(&rk->d_state, rk->nprob, "rtopk state");
-  if (!rc) rc = rk_alloc(&rk->d_hist, (int64_t)rk->nprob * kRkBins, "rtopk histograms");
+  if (!rc) rc = rk_alloc(&rk->d_hist, (int64_t)rk->nprob * kRkTopBins, "rtopk histograms");
   if (!rc) rc = rk_alloc(&rk->d_arrive, rk->nprob, "rtopk counters");
   if (!rc) rc = rk_alloc(&rk->d_ftiles, (int64_t)rk->ftiles.size(), "rtopk tiles");
   if (!rc) rc = rk_alloc(&rk->d_ltiles, (int64_t)rk->ltiles.size(), "rtopk tiles");
@@ -803,7 +884,8 @@ int rtopk_create(RTopK** out, const std::vector<LayerDev>& hl, const std::vector
     if (!e) e = rk_upload(rk->d_ltiles, rk->ltiles);
     if (e) return e;
     CUDA_TRY(cudaMemset(rk->d_bm, 0, (size_t)std::max<int64_t>(rk->bm_total, 1) * sizeof(uint32_t)));
-    CUDA_TRY(cudaMemset(rk->d_hist, 0, (size_t)std::max(rk->nprob, 1) * kRkBins * sizeof(uint32_t)));
+    CUDA_TRY(cudaMemset(rk->d_hist, 0, (size_t)std::max(rk->nprob, 1) * kRkTopBins * sizeof(uint32_t)));
+    CUDA_TRY(cudaMemset(rk->d_state, 0xFF, (size_t)std::max(rk->nprob, 1) * sizeof(RkState)));  // prev_top: none
     CUDA_TRY(cudaMemset(rk->d_arrive, 0, (size_t)std::max(rk->nprob, 1) * sizeof(unsigned)));
     CUDA_TRY(cudaMemset(rk->d_sidx, 0, (size_t)std::max<int64_t>(rk->msg_total, 1) * sizeof(int32_t)));
     CUDA_TRY(cudaMemset(rk->d_sval, 0, (size_t)std::max<int64_t>(rk->msg_total, 1) * sizeof(float)));
@@ -824,7 +906,8 @@ int rtopk_create(RTopK** out, const std::vector<LayerDev>& hl, const std::vector
   return PSGD_OK;
 }
 
-int rtopk_step(RTopK* rk, const float* const* G, float* B, int64_t total, float* U, int64_t step, cudaStream_t s) {
+int rtopk_step(RTopK* rk, const float* const* G, float* B, int64_t total, float* U, int64_t step, cudaStream_t s,
+               const cudaEvent_t* ev) {
   RkArgs a;
   std::memset(&a, 0, sizeof(a));
   for (int w = 0; w < rk->W; ++w) a.G[w] = G[w];
@@ -846,25 +929,36 @@ int rtopk_step(RTopK* rk, const float* const* G, float* B, int64_t total, float*
   a.nmat = rk->nmat;
   a.seed = rk->seed;
   a.step = step;
+  auto mark = [&](int k) -> int {
+    if (ev) CUDA_TRY(cudaEventRecord(ev[k], s));
+    return PSGD_OK;
+  };
+  int rc;
   if (rk->nprob > 0) {
     a.tiles = rk->d_ftiles;
     a.ntiles = (int32_t)rk->ftiles.size();
     rk_pass0_kernel<<<(unsigned)rk->pgrid, kRkThreads, 0, s>>>(a);
     CUDA_TRY(cudaGetLastError());
+    if ((rc = mark(0))) return rc;
     rk_pass1_kernel<<<(unsigned)rk->pgrid, kRkThreads, 0, s>>>(a);
     CUDA_TRY(cudaGetLastError());
+    if ((rc = mark(1))) return rc;
     rk_tail_kernel<<<(unsigned)rk->nprob, kRkTail, 0, s>>>(a);
     CUDA_TRY(cudaGetLastError());
+    if ((rc = mark(2))) return rc;
     a.tiles = rk->d_ltiles;
     a.ntiles = (int32_t)rk->ltiles.size();
     rk_apply_kernel<<<(unsigned)rk->ltiles.size(), kRkThreads, 0, s>>>(a);
     CUDA_TRY(cudaGetLastError());
+  } else {
+    for (int k = 0; k < 3; ++k)
+      if ((rc = mark(k))) return rc;
   }
   if (U && rk->nvec > 0) {
     rk_vec_kernel<<<dim3(16, (unsigned)rk->nvec), 256, 0, s>>>(rk->d_vecs, a);
     CUDA_TRY(cudaGetLastError());
   }
-  return PSGD_OK;
+  return mark(3);
 }
 
 int64_t rtopk_k(const RTopK* rk, int mi) { return rk->kk[mi]; }

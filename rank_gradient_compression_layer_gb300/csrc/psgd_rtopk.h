@@ -27,8 +27,10 @@ void rtopk_destroy(RTopK* rk);
 // sampled subset of every problem, B_w <- M_w - S_w, the sparse messages,
 // and U (matrix layers: (sum_w S_w) / W; vector layers: the worker mean)
 // when U is not NULL.  step: the index of this step (for the draws).
+// ev: NULL, or four events recorded after pass 0, pass 1, the tail and the
+// apply (+ vector) kernels.
 int rtopk_step(RTopK* rk, const float* const* G, float* B, int64_t total, float* U, int64_t step,
-               cudaStream_t s);
+               cudaStream_t s, const cudaEvent_t* ev);
 
 // k of matrix layer mi (its position among the matrix layers).
 int64_t rtopk_k(const RTopK* rk, int mi);

@@ -116,3 +116,26 @@ def test_rtopk_rejects_factor_calls():
         ctx.close()
     with pytest.raises(PsgdError):
         PowerSGD([(16, 8)], 2, 2, compressor="rtopk", top_div=0)
+
+
+def test_rtopk_many_steps_predicted_digit():
+    # from the second step on, pass 0 may resolve the second magnitude digit
+    # from the previous step's first digit; error feedback keeps the
+    # threshold near it, so most of these steps take that path
+    layers = [(96, 300), (7, 0), (64, 129), (33, 64)]
+    cfg = workloads.scaled(workloads.c2_resnet18(), layers, rank=2, workers=2, seed=31)
+    _run(cfg, 20, 3, 10)
+
+
+def test_rtopk_scale_jumps_between_steps():
+    # the gradient scale changes by 2^8 between steps: the previous step's
+    # first digit predicts nothing, and pass 0 falls back to one digit
+    layers = [(64, 200), (9, 0)]
+    cfg = workloads.scaled(workloads.c2_resnet18(), layers, rank=2, workers=2, seed=5)
+    scale = [1.0, 256.0, 1.0 / 256.0, 256.0, 1.0]
+
+    def grads_of(t):
+        g = workloads.gradients(cfg, t)
+        return [[(x * np.float32(scale[t])).astype(np.float32) for x in gw] for gw in g]
+
+    _run(cfg, 10, 2, len(scale), grads_of=grads_of)
