@@ -20,19 +20,20 @@
 // finish picks the digit and narrows the prefix (a select whose chosen bin
 // holds exactly the entries still needed is finished early).
 //
-// Only two passes read the whole layer: pass 0 forms M and histograms the
-// top digit of |M|; pass 1 lists the entries whose top digit is above the
-// chosen one -- members of T for sure -- and, with their values, those
-// equal to it, the candidates.  Both are persistent kernels: each CTA takes
-// a contiguous run of tiles and arrives once per problem it touches, with
-// the number of tiles it did.  A tail kernel (one CTA per problem, so its
-// passes need no grid-wide hand-off) finishes the magnitude select over the
-// candidates, completes the list of T with its draws, runs the draw select
-// over it, sets the sent entries K in a bitmap (one bit per packed
-// position) and turns their per-span counts into message offsets.  The
-// apply kernel then writes the messages, E and U from the bitmaps and
-// clears them for the next step.  The step costs two reads of B plus work
-// in proportion to the candidates and T.
+// Only pass 0 reads the whole layer: it forms M, counts the top digit of
+// |M| (and the second one, near the previous step's top digit) and records
+// the largest |M| of every 32 entries.  It is persistent: each CTA takes a
+// contiguous run of tiles and arrives once per problem it touches, with the
+// number of tiles it did.  Pass 1 reads only the groups of 32 whose largest
+// |M| reaches the digits pass 0 chose, and lists the entries above them --
+// members of T for sure -- and, with their values, those equal to them, the
+// candidates.  A tail kernel (one CTA per problem, so its passes need no
+// grid-wide hand-off) finishes the magnitude select over the candidates,
+// completes the list of T with its draws, runs the draw select over it,
+// sets the sent entries K in a bitmap (one bit per packed position) and
+// turns their per-span counts into message offsets.  The apply kernel then
+// writes the messages, E and U from the bitmaps and clears them for the
+// next step.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -128,8 +129,9 @@ struct RkArgs {
   uint32_t* hist;     // problems x kRkTopBins: pass 0's first-digit and windowed second-digit counts
   unsigned* arrive;   // problems
   const RkTile* tiles;
-  int32_t ntiles;     // tiles of the persistent passes
+  int32_t ntiles;     // tiles of the kernel
   uint32_t* bm;       // bitmaps of K (zero between steps)
+  uint32_t* wmax;     // per bitmap word: the largest |M| bit pattern among its entries (pass 0)
   RkCand* cand;       // candidate lists
   RkDraw* tlist;      // lists of T
   int64_t* ccount;    // per problem chunk counts, then exclusive offsets
@@ -287,6 +289,7 @@ __device__ __noinline__ void rk_close_run(const RkArgs& a, int p, uint32_t win0,
   }
   __syncthreads();
   if (!*s_flag) return;
+  static_assert((kRkChunk / 32) == 32 * (kRkThreads / 32), "pass 1: a warp per 32 words of a tile");
   static_assert(kRkTopBins % kRkThreads == 0, "whole rows of counters per thread");
   {
     uint32_t v[kRkTopBins / kRkThreads];  // all loads in flight at once
@@ -330,14 +333,15 @@ __device__ __forceinline__ float comp(const float4& v, int c) {
   return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
 }
 
-// This CTA's contiguous run of the persistent passes' tiles.
+// This CTA's contiguous run of pass 0's tiles.
 __device__ __forceinline__ void rk_run(const RkArgs& a, int* t0, int* t1) {
   *t0 = (int)((int64_t)blockIdx.x * a.ntiles / gridDim.x);
   *t1 = (int)((int64_t)(blockIdx.x + 1) * a.ntiles / gridDim.x);
 }
 
 // Pass 0 (persistent, tiles in order): M = G + E into B, the top digit of
-// |M|, and (worker 0's problems) U zeroed.
+// |M| (and the second, near the previous step's top digit), the largest |M|
+// of every bitmap word, and (worker 0's problems) U zeroed.
 __global__ void __launch_bounds__(kRkThreads, 4) rk_pass0_kernel(RkArgs a) {
   __shared__ uint32_t h[kRkTopBins];  // first digit, then the window's second digit
   __shared__ uint32_t s_sum[kRkThreads / 32];
@@ -357,6 +361,7 @@ __global__ void __launch_bounds__(kRkThreads, 4) rk_pass0_kernel(RkArgs a) {
     const float4* G4 = reinterpret_cast<const float4*>(a.G[P.w] + L.off);
     float4* B4 = reinterpret_cast<float4*>(a.B + (int64_t)P.w * a.total + L.off);
     float4* U4 = (a.U && P.w == 0) ? reinterpret_cast<float4*>(a.U + L.off) : nullptr;
+    uint32_t* wmax = a.wmax + P.bm_off;
     constexpr int kHalf = kRkGroups / 2;
 #pragma unroll 1
     for (int c = first.chunk; c < first.chunk + (te - t); ++c) {
@@ -375,23 +380,31 @@ __global__ void __launch_bounds__(kRkThreads, 4) rk_pass0_kernel(RkArgs a) {
 #pragma unroll
         for (int u = 0; u < kHalf; ++u) {
           const uint32_t g = base + (uint32_t)(jb + u) * kRkThreads;
-          if (g >= ng) continue;
-          const unsigned ok = group_valid(L, g);
-          float4 mv = bv[u];
-          if (ok & 1u) mv.x = gv[u].x + bv[u].x;
-          if (ok & 2u) mv.y = gv[u].y + bv[u].y;
-          if (ok & 4u) mv.z = gv[u].z + bv[u].z;
-          if (ok & 8u) mv.w = gv[u].w + bv[u].w;
-          B4[g] = mv;
-          if (U4) U4[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+          uint32_t mx = 0;  // the group's largest |M| bit pattern
+          if (g < ng) {
+            const unsigned ok = group_valid(L, g);
+            float4 mv = bv[u];
+            if (ok & 1u) mv.x = gv[u].x + bv[u].x;
+            if (ok & 2u) mv.y = gv[u].y + bv[u].y;
+            if (ok & 4u) mv.z = gv[u].z + bv[u].z;
+            if (ok & 8u) mv.w = gv[u].w + bv[u].w;
+            B4[g] = mv;
+            if (U4) U4[g] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (ok >> k & 1u) {
-              const uint32_t pat = __float_as_uint(comp(mv, k)) & 0x7FFFFFFFu;
-              atomicAdd(&h[pat >> 21], 1u);
-              const uint32_t slot = (pat >> 21) - win0;  // wraps (large) outside the window
-              if (slot < (uint32_t)kRkWin) atomicAdd(&h[kRkBins + slot * kRkFine + ((pat >> 11) & (kRkFine - 1))], 1u);
-            }
+            for (int k = 0; k < 4; ++k)
+              if (ok >> k & 1u) {
+                const uint32_t pat = __float_as_uint(comp(mv, k)) & 0x7FFFFFFFu;
+                mx = max(mx, pat);
+                atomicAdd(&h[pat >> 21], 1u);
+                const uint32_t slot = (pat >> 21) - win0;  // wraps (large) outside the window
+                if (slot < (uint32_t)kRkWin) atomicAdd(&h[kRkBins + slot * kRkFine + ((pat >> 11) & (kRkFine - 1))], 1u);
+              }
+          }
+          // the word's maximum over its 8 lanes (consecutive groups), for pass 1
+          mx = max(mx, __shfl_xor_sync(kFull, mx, 1));
+          mx = max(mx, __shfl_xor_sync(kFull, mx, 2));
+          mx = max(mx, __shfl_xor_sync(kFull, mx, 4));
+          if ((threadIdx.x & 7) == 0 && g < ng) wmax[g >> 3] = mx;
         }
       }
     }
@@ -400,105 +413,131 @@ __global__ void __launch_bounds__(kRkThreads, 4) rk_pass0_kernel(RkArgs a) {
   }
 }
 
-// Pass 1 (persistent, each CTA's run backwards: pass 0 wrote its end last,
-// so it is still in L2): the list of the entries above the chosen top digit
-// (members of T for sure) and the list of candidates (top digit equal to it).
-__global__ void __launch_bounds__(kRkThreads, 4) rk_pass1_kernel(RkArgs a) {
-  const int lane = threadIdx.x & 31;
-  int t0, t;
-  rk_run(a, &t0, &t);
-  while (t > t0) {
-    const RkTile last = a.tiles[t - 1];
-    const int p = last.p;
-    const RkProb P = a.probs[p];
-    const LayerDev L = a.layers[P.mi];
-    RkState* stp = a.state + p;
-    const RkSel sel = stp->sel[0];
-    const int tb = max(t0, t - 1 - last.chunk);
-    const uint32_t ng = (uint32_t)(P.len / 4);
-    const float4* B4 = reinterpret_cast<const float4*>(a.B + (int64_t)P.w * a.total + L.off);
-    RkCand* cl = a.cand + P.list_off;
-    RkDraw* sl = a.tlist + P.list_off;
-    // |M| bit patterns: [lo, hi) holds the digits pass 0 resolved, >= hi is above
-    // them (a finished select: everything from lo up is in T, no candidates)
-    const uint32_t lo = (uint32_t)(sel.prefix >> 32);
-    const uint32_t hi = sel.done ? lo : lo + (1u << (c_mshift[stp->depth - 1] - 32));
-    // the run's half tiles, last chunk first; the next half's loads are in
-    // flight while this half's list reservation (an atomic each warp waits
-    // on) comes back
-    constexpr int kHalf = kRkGroups / 2;
-    const int nh = 2 * (t - tb);
-    auto group_of = [&](int hh, int u) -> uint32_t {
-      const uint32_t c = (uint32_t)(last.chunk - (hh >> 1));
-      return c * (kRkThreads * kRkGroups) + threadIdx.x + (uint32_t)((hh & 1) * kHalf + u) * kRkThreads;
-    };
-    float4 cur[kHalf], nxt[kHalf];
+// Pass 1: the list of the entries above the digits pass 0 resolved
+// (members of T for sure) and the list of candidates (equal to them).  Only
+// the bitmap words whose largest |M| reaches the candidates' range are
+// read: with one percent of a layer in T, about a quarter of B.  One CTA per
+// kRkP1Words words of a problem (last first: pass 0 wrote the end of B
+// last, so it is still in L2); each warp owns 128 of them, finds the marked
+// ones from the word maxima, and reads them 16 at a time (8 lanes per word,
+// a float4 each), the next 16 in flight while it lists the current ones.
+// The pass is latency bound: its CTAs are not persistent, so many keep
+// loads in flight.
+constexpr int kRkP1Words = 1024;
+constexpr int kRkP1Sub = kRkP1Words / (kRkThreads / 32) / 32;  // 32-word blocks per warp (4)
+
+__global__ void __launch_bounds__(kRkThreads) rk_pass1_kernel(RkArgs a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const RkTile tile = a.tiles[a.ntiles - 1 - blockIdx.x];
+  const int p = tile.p;
+  const RkProb P = a.probs[p];
+  const LayerDev L = a.layers[P.mi];
+  RkState* stp = a.state + p;
+  const RkSel sel = stp->sel[0];
+  const uint32_t ng = (uint32_t)(P.len / 4), nw = (uint32_t)P.nwords;
+  const float4* B4 = reinterpret_cast<const float4*>(a.B + (int64_t)P.w * a.total + L.off);
+  RkCand* cl = a.cand + P.list_off;
+  RkDraw* sl = a.tlist + P.list_off;
+  // |M| bit patterns: [lo, hi) holds the digits pass 0 resolved, >= hi is above
+  // them (a finished select: everything from lo up is in T, no candidates)
+  const uint32_t lo = (uint32_t)(sel.prefix >> 32);
+  const uint32_t hi = sel.done ? lo : lo + (1u << (c_mshift[stp->depth - 1] - 32));
+  const uint32_t w0 = (uint32_t)tile.chunk * kRkP1Words + (uint32_t)warp * (32 * kRkP1Sub);  // this warp's words
+  unsigned m[kRkP1Sub];
+  int nall = 0;
+  {
+    uint32_t mx[kRkP1Sub];
 #pragma unroll
-    for (int u = 0; u < kHalf; ++u) {
-      const uint32_t g = group_of(0, u);
-      if (g < ng) cur[u] = B4[g];
+    for (int b = 0; b < kRkP1Sub; ++b) {
+      const uint32_t w = w0 + b * 32 + lane;
+      mx[b] = w < nw ? __ldcg(a.wmax + P.bm_off + w) : 0u;
     }
+#pragma unroll
+    for (int b = 0; b < kRkP1Sub; ++b) {
+      const uint32_t w = w0 + b * 32 + lane;
+      m[b] = __ballot_sync(kFull, w < nw && mx[b] >= lo);
+      nall += __popc(m[b]);
+    }
+  }
+  // word (relative to w0) of the n-th marked word, or -1
+  auto nth = [&](int n) -> int {
+#pragma unroll
+    for (int b = 0; b < kRkP1Sub; ++b) {
+      const int c = __popc(m[b]);
+      if (n < c) return b * 32 + (int)__fns(m[b], 0, n + 1);
+      n -= c;
+    }
+    return -1;
+  };
+  constexpr int kWords = 4;  // per lane group and batch: 4 groups of 8 lanes -> 16 words
+  float4 cur[kWords], nxt[kWords];
+  uint32_t gc[kWords], gn[kWords];
+  auto fetch = [&](int batch, float4* v, uint32_t* gw) {
+#pragma unroll
+    for (int u = 0; u < kWords; ++u) {
+      const int j = batch * 16 + (lane >> 3) + 4 * u;
+      const int r = j < nall ? nth(j) : -1;
+      gw[u] = r >= 0 ? (w0 + (uint32_t)r) * 8 + (lane & 7) : 0xFFFFFFFFu;
+      if (gw[u] < ng) v[u] = B4[gw[u]];
+    }
+  };
+  const int nb = (nall + 15) / 16;
+  if (nb > 0) fetch(0, cur, gc);
 #pragma unroll 1
-    for (int hh = 0; hh < nh; ++hh) {
-      if (hh + 1 < nh) {
+  for (int bt = 0; bt < nb; ++bt) {
+    if (bt + 1 < nb) fetch(bt + 1, nxt, gn);
+    unsigned smask = 0, cmask = 0;  // sure / candidate lanes, 4 bits per group
 #pragma unroll
-        for (int u = 0; u < kHalf; ++u) {
-          const uint32_t g = group_of(hh + 1, u);
-          if (g < ng) nxt[u] = B4[g];
-        }
+    for (int u = 0; u < kWords; ++u) {
+      const unsigned ok = gc[u] < ng ? group_valid(L, gc[u]) : 0u;
+      unsigned sure = 0, cnd = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t pat = __float_as_uint(comp(cur[u], k)) & 0x7FFFFFFFu;
+        sure |= (pat >= hi ? 1u : 0u) << k;
+        cnd |= (pat - lo < hi - lo ? 1u : 0u) << k;
       }
-      unsigned smask = 0, cmask = 0;  // sure / candidate lanes, 4 bits per group
+      smask |= (sure & ok) << (4 * u);
+      cmask |= (cnd & ok) << (4 * u);
+    }
+    // one reservation per warp in both lists (a 64-bit counter pair)
+    if (__any_sync(kFull, (smask | cmask) != 0)) {
+      const uint32_t mine = ((uint32_t)__popc(smask) << 16) | (uint32_t)__popc(cmask);
+      uint32_t incl = mine;  // <= 512 of each per warp: the halves never carry
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += x;
+      }
+      unsigned long long b0 = 0;
+      if (lane == 31) b0 = atomicAdd(&stp->counts, ((unsigned long long)(incl >> 16) << 32) | (incl & 0xFFFFu));
+      b0 = __shfl_sync(kFull, b0, 31);
+      const uint32_t ex = incl - mine;
+      uint32_t ss = (uint32_t)(b0 >> 32) + (ex >> 16);
+      uint32_t cs = (uint32_t)b0 + (ex & 0xFFFFu);
 #pragma unroll
-      for (int u = 0; u < kHalf; ++u) {
-        const uint32_t g = group_of(hh, u);
-        const unsigned ok = g < ng ? group_valid(L, g) : 0u;
-        unsigned sure = 0, cnd = 0;
+      for (int u = 0; u < kWords; ++u) {
+        const unsigned sm = (smask >> (4 * u)) & 0xFu, cm = (cmask >> (4 * u)) & 0xFu;
+        if (!(sm | cm)) continue;
+        const uint32_t g = gc[u];
+        uint32_t i0;
+        if (L.ld == L.m) {
+          i0 = 4 * g;
+        } else {
+          const uint32_t row = g / (uint32_t)L.F;
+          i0 = row * (uint32_t)L.m + 4 * (g - row * (uint32_t)L.F);
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint32_t pat = __float_as_uint(comp(cur[u], k)) & 0x7FFFFFFFu;
-          sure |= (pat >= hi ? 1u : 0u) << k;
-          cnd |= (pat - lo < hi - lo ? 1u : 0u) << k;
-        }
-        smask |= (sure & ok) << (4 * u);
-        cmask |= (cnd & ok) << (4 * u);
-      }
-      // one reservation per warp in both lists (a 64-bit counter pair)
-      if (__any_sync(kFull, (smask | cmask) != 0)) {
-        const uint32_t mine = ((uint32_t)__popc(smask) << 16) | (uint32_t)__popc(cmask);
-        uint32_t incl = mine;  // <= 512 of each per warp: the halves never carry
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t x = __shfl_up_sync(kFull, incl, o);
-          if (lane >= o) incl += x;
-        }
-        unsigned long long b0 = 0;
-        if (lane == 31) b0 = atomicAdd(&stp->counts, ((unsigned long long)(incl >> 16) << 32) | (incl & 0xFFFFu));
-        b0 = __shfl_sync(kFull, b0, 31);
-        const uint32_t ex = incl - mine;
-        uint32_t ss = (uint32_t)(b0 >> 32) + (ex >> 16);
-        uint32_t cs = (uint32_t)b0 + (ex & 0xFFFFu);
-#pragma unroll
-        for (int u = 0; u < kHalf; ++u) {
-          const unsigned sm = (smask >> (4 * u)) & 0xFu, cm = (cmask >> (4 * u)) & 0xFu;
-          if (!(sm | cm)) continue;
-          const uint32_t g = group_of(hh, u);
-          uint32_t i0;
-          if (L.ld == L.m) {
-            i0 = 4 * g;
-          } else {
-            const uint32_t row = g / (uint32_t)L.F;
-            i0 = row * (uint32_t)L.m + 4 * (g - row * (uint32_t)L.F);
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            if (sm >> k & 1u) sl[ss++] = RkDraw{i0 + k, 0u};
-            if (cm >> k & 1u) cl[cs++] = RkCand{i0 + k, comp(cur[u], k)};
-          }
+          if (sm >> k & 1u) sl[ss++] = RkDraw{i0 + k, 0u};
+          if (cm >> k & 1u) cl[cs++] = RkCand{i0 + k, comp(cur[u], k)};
         }
       }
-#pragma unroll
-      for (int u = 0; u < kHalf; ++u) cur[u] = nxt[u];
     }
-    t = tb;
+#pragma unroll
+    for (int u = 0; u < kWords; ++u) {
+      cur[u] = nxt[u];
+      gc[u] = gn[u];
+    }
   }
 }
 
@@ -765,8 +804,8 @@ struct RTopK {
   uint64_t seed = 0;
   std::vector<RkProb> hp;
   std::vector<int64_t> kk;  // k per matrix layer
-  std::vector<RkTile> ftiles, ltiles;
-  int pgrid = 0;  // CTAs of the persistent passes
+  std::vector<RkTile> ftiles, ptiles, ltiles;
+  int pgrid = 0;  // CTAs of the persistent pass 0
   const LayerDev* d_layers = nullptr;
   const VecDev* d_vecs = nullptr;
   int nvec = 0;
@@ -774,9 +813,11 @@ struct RTopK {
   RkState* d_state = nullptr;
   uint32_t* d_hist = nullptr;
   unsigned* d_arrive = nullptr;
-  RkTile* d_ftiles = nullptr;  // (problem, chunk): passes 0 and 1
+  RkTile* d_ftiles = nullptr;  // (problem, chunk): pass 0
+  RkTile* d_ptiles = nullptr;  // (problem, block of kRkP1Words words): pass 1
   RkTile* d_ltiles = nullptr;  // (matrix layer, span): apply
   uint32_t* d_bm = nullptr;
+  uint32_t* d_wmax = nullptr;
   RkCand* d_cand = nullptr;
   RkDraw* d_tlist = nullptr;
   int64_t* d_ccount = nullptr;
@@ -808,8 +849,8 @@ int rk_upload(T* d, const std::vector<T>& h) {
 
 void rtopk_destroy(RTopK* rk) {
   if (!rk) return;
-  void* ptrs[] = {rk->d_probs, rk->d_state, rk->d_hist,   rk->d_arrive, rk->d_ftiles, rk->d_ltiles,
-                  rk->d_bm,    rk->d_cand,  rk->d_tlist,  rk->d_ccount, rk->d_sidx, rk->d_sval};
+  void* ptrs[] = {rk->d_probs, rk->d_state, rk->d_hist,  rk->d_arrive, rk->d_ftiles, rk->d_ptiles, rk->d_ltiles,
+                  rk->d_bm,    rk->d_wmax,  rk->d_cand,  rk->d_tlist,  rk->d_ccount, rk->d_sidx,   rk->d_sval};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete rk;
@@ -858,6 +899,7 @@ int rtopk_create(RTopK** out, const std::vector<LayerDev>& hl, const std::vector
       rk->bm_total += (P.nwords + 3) & ~(int64_t)3;  // 16-byte aligned, whole uint4 per apply thread
       rk->hp.push_back(P);
       for (int64_t c = 0; c < P.nchunks; ++c) rk->ftiles.push_back({p, (int32_t)c});
+      for (int64_t c = 0; c < ceil_div(P.nwords, kRkP1Words); ++c) rk->ptiles.push_back({p, (int32_t)c});
     }
   for (int mi = 0; mi < rk->nmat; ++mi)
     for (int64_t c = 0; c < rk->hp[mi].nspans; ++c) rk->ltiles.push_back({mi, (int32_t)c});
@@ -868,7 +910,9 @@ int rtopk_create(RTopK** out, const std::vector<LayerDev>& hl, const std::vector
   if (!rc) rc = rk_alloc(&rk->d_arrive, rk->nprob, "rtopk counters");
   if (!rc) rc = rk_alloc(&rk->d_ftiles, (int64_t)rk->ftiles.size(), "rtopk tiles");
   if (!rc) rc = rk_alloc(&rk->d_ltiles, (int64_t)rk->ltiles.size(), "rtopk tiles");
+  if (!rc) rc = rk_alloc(&rk->d_ptiles, (int64_t)rk->ptiles.size(), "rtopk tiles");
   if (!rc) rc = rk_alloc(&rk->d_bm, rk->bm_total, "rtopk bitmaps");
+  if (!rc) rc = rk_alloc(&rk->d_wmax, rk->bm_total, "rtopk word maxima");
   if (!rc) rc = rk_alloc(&rk->d_cand, rk->cand_total, "rtopk candidate lists");
   if (!rc) rc = rk_alloc(&rk->d_tlist, rk->cand_total, "rtopk top-set lists");
   if (!rc) rc = rk_alloc(&rk->d_ccount, rk->nchunk_total, "rtopk chunk counts");
@@ -882,6 +926,7 @@ int rtopk_create(RTopK** out, const std::vector<LayerDev>& hl, const std::vector
     int e = rk_upload(rk->d_probs, rk->hp);
     if (!e) e = rk_upload(rk->d_ftiles, rk->ftiles);
     if (!e) e = rk_upload(rk->d_ltiles, rk->ltiles);
+    if (!e) e = rk_upload(rk->d_ptiles, rk->ptiles);
     if (e) return e;
     CUDA_TRY(cudaMemset(rk->d_bm, 0, (size_t)std::max<int64_t>(rk->bm_total, 1) * sizeof(uint32_t)));
     CUDA_TRY(cudaMemset(rk->d_hist, 0, (size_t)std::max(rk->nprob, 1) * kRkTopBins * sizeof(uint32_t)));
@@ -889,13 +934,12 @@ int rtopk_create(RTopK** out, const std::vector<LayerDev>& hl, const std::vector
     CUDA_TRY(cudaMemset(rk->d_arrive, 0, (size_t)std::max(rk->nprob, 1) * sizeof(unsigned)));
     CUDA_TRY(cudaMemset(rk->d_sidx, 0, (size_t)std::max<int64_t>(rk->msg_total, 1) * sizeof(int32_t)));
     CUDA_TRY(cudaMemset(rk->d_sval, 0, (size_t)std::max<int64_t>(rk->msg_total, 1) * sizeof(float)));
-    // persistent passes: one wave of resident CTAs
-    int dev = 0, sms = 0, o0 = 0, o1 = 0;
+    // pass 0 is persistent: one wave of resident CTAs
+    int dev = 0, sms = 0, o0 = 0;
     CUDA_TRY(cudaGetDevice(&dev));
     CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o0, rk_pass0_kernel, kRkThreads, 0));
-    CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o1, rk_pass1_kernel, kRkThreads, 0));
-    rk->pgrid = (int)std::min<int64_t>((int64_t)rk->ftiles.size(), (int64_t)sms * std::max(1, std::min(o0, o1)));
+    rk->pgrid = (int)std::min<int64_t>((int64_t)rk->ftiles.size(), (int64_t)sms * std::max(1, o0));
     return PSGD_OK;
   };
   if ((rc = setup())) {
@@ -920,6 +964,7 @@ int rtopk_step(RTopK* rk, const float* const* G, float* B, int64_t total, float*
   a.hist = rk->d_hist;
   a.arrive = rk->d_arrive;
   a.bm = rk->d_bm;
+  a.wmax = rk->d_wmax;
   a.cand = rk->d_cand;
   a.tlist = rk->d_tlist;
   a.ccount = rk->d_ccount;
@@ -940,7 +985,9 @@ int rtopk_step(RTopK* rk, const float* const* G, float* B, int64_t total, float*
     rk_pass0_kernel<<<(unsigned)rk->pgrid, kRkThreads, 0, s>>>(a);
     CUDA_TRY(cudaGetLastError());
     if ((rc = mark(0))) return rc;
-    rk_pass1_kernel<<<(unsigned)rk->pgrid, kRkThreads, 0, s>>>(a);
+    a.tiles = rk->d_ptiles;
+    a.ntiles = (int32_t)rk->ptiles.size();
+    rk_pass1_kernel<<<(unsigned)rk->ptiles.size(), kRkThreads, 0, s>>>(a);
     CUDA_TRY(cudaGetLastError());
     if ((rc = mark(1))) return rc;
     rk_tail_kernel<<<(unsigned)rk->nprob, kRkTail, 0, s>>>(a);
