@@ -40,10 +40,13 @@ UNIT = "GB/s"
 # DRAM bytes (read + write) of one project-kernel launch per workload, from an
 # ncu capture (see profiles/), valid only for the kernel sources whose hash is
 # recorded with it.
-NCU_TRAFFIC = {  # {config: (sources_sha256_prefix, bytes_per_launch)}
-    # ResNet-18 set, r = 2, W = 4: mean of two project launches, 361.6 MB read +
-    # 123.9 MB written (profiles/bench_all_configs.md)
-    "c2": ("2901bf61869cd906", 485531136),
+NCU_TRAFFIC = {  # {(config, variant): (sources_sha256_prefix, bytes_per_launch)}
+    # ResNet-18 set, r = 2, W = 4: mean of two project launches, 361.7 MB read +
+    # 124.0 MB written (profiles/bench_all_configs.md)
+    ("c2", "powersgd"): ("71e7f26690d1f911", 485674624),
+    # ResNet-18 set, rTop-k, W = 4: mean of nine pass-0 launches, 362.9 MB read +
+    # 176.1 MB written (profiles/rk_kernels_resnet18_w4.md)
+    ("c2", "rtopk"): ("71e7f26690d1f911", 539040398),
 }
 
 
@@ -51,7 +54,7 @@ NCU_TRAFFIC = {  # {config: (sources_sha256_prefix, bytes_per_launch)}
 # (the allocation-free entry point and other compressors are not among them)
 STEP_SOURCES = ("psgd_api.cu", "psgd_dispatch.h", "psgd_internal.h", "psgd_kernels.cuh", "psgd_plan.h",
                 "psgd_step_impl.cuh", "psgd_step_r1.cu", "psgd_step_r2.cu", "psgd_step_r4.cu", "psgd_step_r8.cu",
-                "psgd_step_r16.cu", "psgd_step_r32.cu")
+                "psgd_step_r16.cu", "psgd_step_r32.cu", "psgd_rtopk.cu", "psgd_rtopk.h")
 
 
 def kernel_sources_hash() -> str:
@@ -381,8 +384,9 @@ def run_ours(args, ws, rank, local):
     step_achieved = ab["total"] / (ms_per_step * 1e-3) / 1e9
     h = kernel_sources_hash()
     traffic = None
-    if not (args.unbiased or args.momentum or args.rtopk) and args.config in NCU_TRAFFIC and NCU_TRAFFIC[args.config][0] == h:
-        traffic = NCU_TRAFFIC[args.config][1]
+    variant = "rtopk" if args.rtopk else ("powersgd" if not (args.unbiased or args.momentum) else None)
+    if (args.config, variant) in NCU_TRAFFIC and NCU_TRAFFIC[(args.config, variant)][0] == h:
+        traffic = NCU_TRAFFIC[(args.config, variant)][1]
 
     # end to end through the C ABI with host buffers (pinned), copies inside
     e2e = run_e2e(ctx, cfg, args, ws, device)
@@ -446,7 +450,8 @@ def run_e2e(ctx, cfg, args, ws, device):
     return {"value": round(comp * ws / dt / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": cfg.workers * ctx.total * 4, "d2h_bytes_per_step": ctx.message_floats * 4,
             "ms_per_step": round(dt * 1e3, 4), "steps": steps,
-            "api": "psgd_step_host (pinned host gradients in, compressed message Phat/Qbar out)"}
+            "api": ("psgd_step_host (pinned host gradients in, sparse messages out)" if args.rtopk else
+                    "psgd_step_host (pinned host gradients in, compressed message Phat/Qbar out)")}
 
 
 def run_reference(args, ws, rank):
