@@ -427,6 +427,7 @@ constexpr int kRkP1Words = 1024;
 constexpr int kRkP1Sub = kRkP1Words / (kRkThreads / 32) / 32;  // 32-word blocks per warp (4)
 
 __global__ void __launch_bounds__(kRkThreads) rk_pass1_kernel(RkArgs a) {
+  __shared__ uint8_t s_words[kRkThreads / 32][32 * kRkP1Sub];  // each warp's marked words, in order
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const RkTile tile = a.tiles[a.ntiles - 1 - blockIdx.x];
   const int p = tile.p;
@@ -443,7 +444,6 @@ __global__ void __launch_bounds__(kRkThreads) rk_pass1_kernel(RkArgs a) {
   const uint32_t lo = (uint32_t)(sel.prefix >> 32);
   const uint32_t hi = sel.done ? lo : lo + (1u << (c_mshift[stp->depth - 1] - 32));
   const uint32_t w0 = (uint32_t)tile.chunk * kRkP1Words + (uint32_t)warp * (32 * kRkP1Sub);  // this warp's words
-  unsigned m[kRkP1Sub];
   int nall = 0;
   {
     uint32_t mx[kRkP1Sub];
@@ -452,23 +452,17 @@ __global__ void __launch_bounds__(kRkThreads) rk_pass1_kernel(RkArgs a) {
       const uint32_t w = w0 + b * 32 + lane;
       mx[b] = w < nw ? __ldcg(a.wmax + P.bm_off + w) : 0u;
     }
+    // the marked words listed in order: a marked lane writes its word at its rank
 #pragma unroll
     for (int b = 0; b < kRkP1Sub; ++b) {
       const uint32_t w = w0 + b * 32 + lane;
-      m[b] = __ballot_sync(kFull, w < nw && mx[b] >= lo);
-      nall += __popc(m[b]);
+      const bool mark = w < nw && mx[b] >= lo;
+      const unsigned m = __ballot_sync(kFull, mark);
+      if (mark) s_words[warp][nall + __popc(m & ((1u << lane) - 1u))] = (uint8_t)(b * 32 + lane);
+      nall += __popc(m);
     }
+    __syncwarp();
   }
-  // word (relative to w0) of the n-th marked word, or -1
-  auto nth = [&](int n) -> int {
-#pragma unroll
-    for (int b = 0; b < kRkP1Sub; ++b) {
-      const int c = __popc(m[b]);
-      if (n < c) return b * 32 + (int)__fns(m[b], 0, n + 1);
-      n -= c;
-    }
-    return -1;
-  };
   constexpr int kWords = 4;  // per lane group and batch: 4 groups of 8 lanes -> 16 words
   float4 cur[kWords], nxt[kWords];
   uint32_t gc[kWords], gn[kWords];
@@ -476,7 +470,7 @@ __global__ void __launch_bounds__(kRkThreads) rk_pass1_kernel(RkArgs a) {
 #pragma unroll
     for (int u = 0; u < kWords; ++u) {
       const int j = batch * 16 + (lane >> 3) + 4 * u;
-      const int r = j < nall ? nth(j) : -1;
+      const int r = j < nall ? (int)s_words[warp][j] : -1;
       gw[u] = r >= 0 ? (w0 + (uint32_t)r) * 8 + (lane & 7) : 0xFFFFFFFFu;
       if (gw[u] < ng) v[u] = B4[gw[u]];
     }
@@ -717,6 +711,8 @@ __global__ void __launch_bounds__(kRkTail, 1) rk_tail_kernel(RkArgs a) {
   }
 }
 
+constexpr int kRkApplyFastW = 8;  // workers the apply kernel handles with all words in registers
+
 // Messages, error and update of layer mi over one span, all workers in
 // order: thread = one bitmap word (the scattered reads and writes of the
 // sent entries are latency-bound, so one word per thread keeps the most of
@@ -743,6 +739,55 @@ __global__ void __launch_bounds__(kRkThreads) rk_apply_kernel(RkArgs a) {
   const uint32_t nw = (uint32_t)(((int64_t)L.n * L.ld + 31) / 32);  // same for every worker
   const bool in = w < nw;
   float* Ul = a.U ? a.U + L.off : nullptr;
+  if (a.W <= kRkApplyFastW) {
+    // all workers' words at once, their ranks by block scans with no scattered
+    // access in between (two workers per scan, 16 bits each: a CTA has at most
+    // 8192 sent entries per worker), then every sent entry of the word with all
+    // workers' loads in flight together; U is stored once, summed in worker order
+    uint32_t K[kRkApplyFastW];
+    int64_t at0[kRkApplyFastW];
+#pragma unroll
+    for (int wk = 0; wk < kRkApplyFastW; ++wk) K[wk] = (wk < a.W && in) ? __ldcg(a.bm + s_bm[wk] + w) : 0u;
+#pragma unroll
+    for (int wk = 0; wk < kRkApplyFastW; wk += 2) {
+      if (wk >= a.W) break;
+      uint32_t tot;
+      const uint32_t ex = block_excl_scan<kRkThreads>((uint32_t)__popc(K[wk]) | ((uint32_t)__popc(K[wk + 1]) << 16),
+                                                      reinterpret_cast<uint32_t*>(s_warp), &tot);
+      at0[wk] = s_at[wk] + (ex & 0xFFFFu);
+      at0[wk + 1] = wk + 1 < a.W ? s_at[wk + 1] + (ex >> 16) : 0;
+    }
+    uint32_t uni = 0;
+#pragma unroll
+    for (int wk = 0; wk < kRkApplyFastW; ++wk) uni |= K[wk];
+    const float inv = 1.0f / (float)a.W;
+    for (uint32_t bits = uni; bits; bits &= bits - 1) {
+      const int b = __ffs(bits) - 1;
+      const uint32_t pp = w * 32 + (uint32_t)b;
+      const uint32_t below = (1u << b) - 1u;
+      float v[kRkApplyFastW];
+#pragma unroll
+      for (int wk = 0; wk < kRkApplyFastW; ++wk)
+        v[wk] = (K[wk] >> b & 1u) ? a.B[(int64_t)wk * a.total + L.off + pp] : 0.f;
+      float u = 0.f;
+#pragma unroll
+      for (int wk = 0; wk < kRkApplyFastW; ++wk)
+        if (K[wk] >> b & 1u) {
+          const int64_t at = at0[wk] + __popc(K[wk] & below);
+          if (at < s_end[wk]) {
+            a.sidx[at] = (int32_t)flat_of(L, pp);
+            a.sval[at] = v[wk];
+          }
+          a.B[(int64_t)wk * a.total + L.off + pp] = 0.f;
+          u += v[wk];
+        }
+      if (Ul) Ul[pp] = u * inv;
+    }
+#pragma unroll
+    for (int wk = 0; wk < kRkApplyFastW; ++wk)
+      if (K[wk]) a.bm[s_bm[wk] + w] = 0u;  // K's bitmap is zero again for the next step
+    return;
+  }
   uint32_t uni = 0;
   uint32_t nxt = in ? __ldcg(a.bm + s_bm[0] + w) : 0u;
   for (int wk = 0; wk < a.W; ++wk) {

@@ -139,3 +139,10 @@ def test_rtopk_scale_jumps_between_steps():
         return [[(x * np.float32(scale[t])).astype(np.float32) for x in gw] for gw in g]
 
     _run(cfg, 10, 2, len(scale), grads_of=grads_of)
+
+
+def test_rtopk_many_workers():
+    # more workers than the apply kernel keeps in registers (its general path)
+    layers = [(40, 96), (6, 0), (17, 33)]
+    cfg = workloads.scaled(workloads.c2_resnet18(), layers, rank=2, workers=9, seed=17)
+    _run(cfg, 8, 2, 3)
