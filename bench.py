@@ -131,7 +131,7 @@ def measured_peaks() -> dict:
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "sm_max_mhz": float(d.get("sm_max_mhz", 2070.0)), "source": "measured"}
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
@@ -416,6 +416,7 @@ def run_ours(args, ws, rank, local):
                      "launch_ms_source": "CUDA events around the kernel on the context's stream, "
                                          "averaged over a second pass of the timed steps with per-phase events",
                      "kernel_sources": h},
+        "project_fp32": project_fp32(cfg, args, project_ms, peaks, device),
         "step_roofline": {"achieved": round(step_achieved, 1), "frac": round(step_achieved / peaks["hbm_gbs"], 4),
                           "algorithmic_bytes_per_step": ab["total"],
                           "phase_ms": {k: round(v, 5) for k, v in phases.items()}},
@@ -427,6 +428,30 @@ def run_ours(args, ws, rank, local):
         out["cpu_baseline"] = time_oracle(cfg, steps=3, warmup=1, budget_s=args.cpu_budget)
     ctx.close()
     return out
+
+
+FP32_LANES_PER_SM = 128  # FP32 FMA lanes per Blackwell SM (nominal)
+
+
+def project_fp32(cfg, args, project_ms: float, peaks: dict, device):
+    """The project kernel's FP32 FMA rate against the CUDA cores' peak.
+
+    Per element and worker the kernel does 2 r FMAs (the error rebuild
+    against the previous factors and the projection onto Q); the peak is
+    SMs x FP32 lanes x 2 flop x the maximum SM clock.  Not the roofline's
+    bound at any rank (HBM is), but it shows how far from arithmetic
+    limits the r >= 8 kernels run.
+    """
+    if args.rtopk or args.unbiased:
+        return None
+    import torch
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    flop = 2 * 2 * cfg.rank * cfg.workers * sum(n * m for n, m in cfg.matrices)
+    achieved = flop / (project_ms * 1e-3) / 1e12
+    peak = sms * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    return {"fma_per_element_worker": 2 * cfg.rank, "achieved_tflops": round(achieved, 2),
+            "peak_tflops": round(peak, 1), "frac": round(achieved / peak, 4),
+            "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x max SM clock"}
 
 
 def run_e2e(ctx, cfg, args, ws, device):

@@ -15,10 +15,10 @@
 // Both selections are radix selects over composite 64-bit keys that are
 // unique per entry -- (|M| bits, ~i) and (h(i), i) -- so the k-th key is one
 // value and "key >= / <= threshold" selects exactly r / k entries.  Six
-// digits per select; each pass histograms the digit of the entries
-// still matching the prefix found so far, and the last CTA of a problem to
-// finish picks the digit and narrows the prefix (a select whose chosen bin
-// holds exactly the entries still needed is finished early).
+// digits per select; each round counts the digit of the entries still
+// matching the prefix found so far and picks the bin that holds the key
+// still needed (a select whose chosen bin holds exactly the entries still
+// needed is finished early).
 //
 // Only pass 0 reads the whole layer: it forms M, counts the top digit of
 // |M| (and the second one, near the previous step's top digit) and records
@@ -81,7 +81,7 @@ struct RkProb {   // one (worker, matrix layer) problem
   int64_t nchunks; // full-pass tiles (kRkChunk positions each)
   int64_t nwords;  // bitmap words, ceil(len / 32) (storage rounded up to 4; the rest stays 0)
   int64_t nspans;  // apply tiles / count chunks (kRkSpan positions each)
-  int64_t chunk0;  // first chunk count of this problem
+  int64_t chunk0;  // first span count of this problem
   int64_t msg_off; // first message entry of this problem
   int64_t list_off, bm_off;  // candidate list and list of T (capacity d each); K's bitmap
 };
@@ -134,7 +134,7 @@ struct RkArgs {
   uint32_t* wmax;     // per bitmap word: the largest |M| bit pattern among its entries (pass 0)
   RkCand* cand;       // candidate lists
   RkDraw* tlist;      // lists of T
-  int64_t* ccount;    // per problem chunk counts, then exclusive offsets
+  int64_t* ccount;    // per problem span counts of K, then their exclusive offsets
   int32_t* sidx;
   float* sval;
   int32_t W, nmat;
