@@ -43,24 +43,25 @@ UNIT = "GB/s"
 NCU_TRAFFIC = {  # {(config, variant): (sources_sha256_prefix, bytes_per_launch)}
     # ResNet-18 set, r = 2, W = 4: mean of two project launches, 361.7 MB read +
     # 124.0 MB written (profiles/bench_all_configs.md)
-    ("c2", "powersgd"): ("71e7f26690d1f911", 485674624),
+    ("c2", "powersgd"): ("74c58c701339d449", 485674624),
     # ResNet-18 set, rTop-k, W = 4: mean of nine pass-0 launches, 362.9 MB read +
-    # 176.1 MB written (profiles/rk_kernels_resnet18_w4.md)
-    ("c2", "rtopk"): ("71e7f26690d1f911", 539040398),
+    # 176.2 MB written (profiles/rk_kernels_resnet18_w4.md)
+    ("c2", "rtopk"): ("dbfcb98f0bc220fb", 539120924),
 }
 
 
 # the sources that define the phase kernels of a step and their launch
-# (the allocation-free entry point and other compressors are not among them)
+# (the allocation-free entry point is not among them; rTop-k adds its own files)
 STEP_SOURCES = ("psgd_api.cu", "psgd_dispatch.h", "psgd_internal.h", "psgd_kernels.cuh", "psgd_plan.h",
                 "psgd_step_impl.cuh", "psgd_step_r1.cu", "psgd_step_r2.cu", "psgd_step_r4.cu", "psgd_step_r8.cu",
-                "psgd_step_r16.cu", "psgd_step_r32.cu", "psgd_rtopk.cu", "psgd_rtopk.h")
+                "psgd_step_r16.cu", "psgd_step_r32.cu")
+RTOPK_SOURCES = ("psgd_rtopk.cu", "psgd_rtopk.h")  # and STEP_SOURCES (the API and shared headers)
 
 
-def kernel_sources_hash() -> str:
+def kernel_sources_hash(rtopk: bool = False) -> str:
     csrc = os.path.join(ROOT, "rank_gradient_compression_layer_gb300", "csrc")
     h = hashlib.sha256()
-    for f in STEP_SOURCES:
+    for f in STEP_SOURCES + (RTOPK_SOURCES if rtopk else ()):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -69,6 +70,9 @@ def kernel_sources_hash() -> str:
 def config_of(name: str) -> workloads.Workload:
     if name.startswith("c5r"):
         return workloads.c5_rank_sweep(int(name[3:]))
+    if name.startswith("c5s"):  # the rank sweep shrunk to 4096 x 4096, W = 4: a case small enough for ncu
+        r = int(name[3:])
+        return workloads.scaled(workloads.c5_rank_sweep(r), [(4096, 4096)], name=f"square4096_r{r}_w4", workers=4)
     if name.startswith("c2x"):  # the ResNet-18 set repeated k times (a larger model of the same shapes)
         base = workloads.c2_resnet18()
         return workloads.scaled(base, list(base.layers) * int(name[3:]), name=f"resnet18x{name[3:]}_r2_w4")
@@ -382,7 +386,7 @@ def run_ours(args, ws, rank, local):
         project_bytes = ab["core"]  # read G, read E, write E of every worker (+ the factors); unbiased: read G
     achieved = project_bytes / (project_ms * 1e-3) / 1e9
     step_achieved = ab["total"] / (ms_per_step * 1e-3) / 1e9
-    h = kernel_sources_hash()
+    h = kernel_sources_hash(rtopk=args.rtopk)
     traffic = None
     variant = "rtopk" if args.rtopk else ("powersgd" if not (args.unbiased or args.momentum) else None)
     if (args.config, variant) in NCU_TRAFFIC and NCU_TRAFFIC[(args.config, variant)][0] == h:
