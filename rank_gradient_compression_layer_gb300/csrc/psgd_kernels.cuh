@@ -52,6 +52,7 @@ struct Cfg {
   static constexpr int RU = 128;
 };
 
+constexpr int kP1TRow = kSeg * 4 + 4;  // tiled project: shared row stride of the staged Q rows (floats)
 constexpr int kP3Threads = 256;
 constexpr int kUThreads = 256;
 constexpr int kPHThreads = 128;
@@ -519,12 +520,23 @@ __device__ void qf_segment_worker(const StepArgs& a, const LayerDev& L, int seg,
   }
 }
 
+// Back-project: rank slices per row group (warps that read the same rows),
+// and its dynamic shared memory (the cross-warp reduction), in bytes.
+constexpr int p3_slices(int rp) { return rp >= 32 ? 2 : 1; }
+constexpr size_t p3_dyn_bytes(int rp) { return (size_t)(kP3Threads / 32 / p3_slices(rp)) * 32 * 4 * rp * sizeof(float); }
+
 template <int RP>
 __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
   constexpr int UNR = Cfg<RP>::UNR3;
   constexpr int NW = kP3Threads / 32;
-  __shared__ float s_ph[NW][UNR * RP];            // each warp's Phat rows of its current group
-  extern __shared__ __align__(16) float s_red[];  // NW x 32 x 4 x RP
+  // r = 32: the ranks are split over warp pairs that read the same rows (the
+  // second read hits in cache), so a warp holds 4 x RP / 2 accumulators and
+  // two CTAs fit on an SM instead of one
+  constexpr int HS = p3_slices(RP);  // rank slices
+  constexpr int RH = RP / HS;        // ranks per warp
+  constexpr int NG = NW / HS;        // row groups in flight
+  __shared__ float s_ph[NW][UNR * RH];            // each warp's Phat values of its current group
+  extern __shared__ __align__(16) float s_red[];  // NG x 32 x 4 x RP
   __shared__ int s_flag;
   pdl_enter();
   const Tile t = a.tiles[blockIdx.x];
@@ -533,34 +545,36 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
   const int row0 = rt * L.r3;
   const int nrows = min(L.r3, L.n - row0);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int hs = warp % HS, grp = warp / HS;
   const int c = seg * kSeg + lane;
   const bool act = c < L.F;
   const float* Bw = a.B + (int64_t)w * a.total + L.off + 4 * c;
-  const float* Ph = a.Phat + L.p_off + (int64_t)row0 * RP;
+  const float* Ph = a.Phat + L.p_off + (int64_t)row0 * RP + hs * RH;
   float* s_mine = s_ph[warp];
-  float acc[4][RP];
+  float acc[4][RH];
 #pragma unroll
   for (int j = 0; j < 4; ++j)
 #pragma unroll
-    for (int k = 0; k < RP; ++k) acc[j][k] = 0.f;
-  // warps take interleaved groups of UNR rows; each warp stages the Phat
-  // rows of its own group (a warp barrier only), so no warp waits for another
-  for (int i0 = warp * UNR; i0 < nrows; i0 += NW * UNR) {
+    for (int k = 0; k < RH; ++k) acc[j][k] = 0.f;
+  // row groups of UNR rows interleaved over the NG groups; each warp stages
+  // its own slice of the group's Phat rows (a warp barrier only)
+  for (int i0 = grp * UNR; i0 < nrows; i0 += NG * UNR) {
     float4 bv[UNR];
 #pragma unroll
-    for (int u = 0; u < UNR; ++u)
-      bv[u] = (act && i0 + u < nrows) ? __ldcs(reinterpret_cast<const float4*>(Bw + (int64_t)(row0 + i0 + u) * L.ld))
-                                      : zero4();
-    const int ne = min(UNR, nrows - i0) * RP;
+    for (int u = 0; u < UNR; ++u) {
+      const float4* src = reinterpret_cast<const float4*>(Bw + (int64_t)(row0 + i0 + u) * L.ld);
+      bv[u] = (act && i0 + u < nrows) ? (HS > 1 ? __ldg(src) : __ldcs(src)) : zero4();
+    }
+    const int ne = min(UNR, nrows - i0) * RH;
     __syncwarp();  // the previous group's Phat rows are no longer read
-    for (int e = lane; e < ne; e += 32) s_mine[e] = __ldg(Ph + (int64_t)i0 * RP + e);
+    for (int e = lane; e < ne; e += 32) s_mine[e] = __ldg(Ph + (int64_t)(i0 + e / RH) * RP + e % RH);
     __syncwarp();
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       if (i0 + u < nrows) {
 #pragma unroll
-        for (int k = 0; k < RP; ++k) {
-          const float p = s_mine[u * RP + k];
+        for (int k = 0; k < RH; ++k) {
+          const float p = s_mine[u * RH + k];
           acc[0][k] = fmaf(bv[u].x, p, acc[0][k]);
           acc[1][k] = fmaf(bv[u].y, p, acc[1][k]);
           acc[2][k] = fmaf(bv[u].z, p, acc[2][k]);
@@ -569,12 +583,12 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
       }
     }
   }
-  // fixed-order reduction over the warps
-  float* mine = s_red + (warp * 32 + lane) * 4 * RP;
+  // fixed-order reduction over the row groups
+  float* mine = s_red + (grp * 32 + lane) * 4 * RP + hs * RH;
 #pragma unroll
   for (int j = 0; j < 4; ++j)
 #pragma unroll
-    for (int k = 0; k < RP; ++k) mine[j * RP + k] = acc[j][k];
+    for (int k = 0; k < RH; ++k) mine[j * RP + k] = acc[j][k];
   __syncthreads();
   {
     float* part = a.qpart + L.qpart_off + ((int64_t)rt * a.W + w) * L.ld * RP;
@@ -583,7 +597,7 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
       const int ln = idx / (4 * RP), jk = idx % (4 * RP);
       float s = 0.f;
 #pragma unroll
-      for (int v = 0; v < NW; ++v) s += s_red[(v * 32 + ln) * 4 * RP + jk];
+      for (int v = 0; v < NG; ++v) s += s_red[(v * 32 + ln) * 4 * RP + jk];
       part[(int64_t)(seg * kSeg + ln) * 4 * RP + jk] = s;
     }
   }
@@ -701,7 +715,7 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
 // r-wide dot products so that each value loaded from shared memory feeds
 // several fused multiply-adds.  (The back-project kernel serves every rank.)
 
-constexpr int kTThreads = 256;  // threads of a tiled project or decompress CTA
+constexpr int kTThreads = 256;  // threads of a tiled project CTA: 32 rows x 8 column groups
 
 // Project, r >= 8.  A CTA owns up to 32 rows x one segment (128 columns) and
 // loops over the workers.  Thread (row i = tid / 8, column group cg = tid % 8)
@@ -718,11 +732,12 @@ template <int RP>
 __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
   constexpr int TR = 32;
   constexpr int SC = kSeg * 4;  // columns of a segment
-  static_assert(Cfg<RP>::R1 == TR, "the tiled project kernel covers 32 rows");
+  constexpr int SCP = kP1TRow;  // their row stride in shared memory (padded: the staging stores hit 4-way, not 32-way)
+  static_assert(Cfg<RP>::R1 == TR && TR * 8 == kTThreads, "the tiled project kernel covers 32 rows, 8 threads each");
   extern __shared__ __align__(16) float s_t[];
-  float* s_qT = s_t;              // Q rows of the segment, transposed: [RP][SC]
-  float* s_qwT = s_qT + RP * SC;  // Q_w' rows of the current worker, transposed: [RP][SC]
-  float* s_pp = s_qwT + RP * SC;  // previous Phat rows of the tile: [TR][RP]
+  float* s_qT = s_t;               // Q rows of the segment, transposed: [RP][SCP]
+  float* s_qwT = s_qT + RP * SCP;  // Q_w' rows of the current worker, transposed: [RP][SCP]
+  float* s_pp = s_qwT + RP * SCP;  // previous Phat rows of the tile: [TR][RP]
   __shared__ float s_prow[TR * RP];
   __shared__ double s_gram[RP * RP];
   __shared__ int s_flag;
@@ -735,10 +750,11 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
   const int c40 = T.seg * kSeg + cg;  // float4 column of v = 0; v-th is c40 + 8 v
   const int64_t q0 = L.q_off + (int64_t)T.seg * SC * RP;
   const int segcols = min(SC, L.ld - T.seg * SC);
-  // staging: column fastest, so consecutive threads store to consecutive words
+  // staging: rank fastest, so consecutive threads load consecutive words
+  // (the rows are m x RP in memory) and store down a padded column
   for (int e = threadIdx.x; e < RP * SC; e += blockDim.x) {
-    const int k = e / SC, c = e - k * SC;
-    s_qT[e] = c < segcols ? __ldg(a.Qbar + q0 + (int64_t)c * RP + k) : 0.f;
+    const int c = e / RP, k = e - c * RP;
+    s_qT[k * SCP + c] = c < segcols ? __ldg(a.Qbar + q0 + e) : 0.f;
   }
   for (int e = threadIdx.x; e < TR * RP; e += blockDim.x)
     s_pp[e] = (T.prev && e < T.rcnt * RP) ? __ldg(a.Phat + L.p_off + (int64_t)T.row0 * RP + e) : 0.f;
@@ -746,15 +762,7 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
 #pragma unroll
   for (int k = 0; k < RP; ++k) pacc[k] = 0.f;
   for (int w = 0; w < a.W; ++w) {
-    __syncthreads();  // the previous worker's Q_w' rows are no longer read
-    if (T.prev) {
-      const float* qw = a.Qw + (int64_t)w * a.q_total + q0;
-      for (int e = threadIdx.x; e < RP * SC; e += blockDim.x) {
-        const int k = e / SC, c = e - k * SC;
-        s_qwT[e] = c < segcols ? __ldg(qw + (int64_t)c * RP + k) : 0.f;
-      }
-    }
-    __syncthreads();
+    // this worker's G and B first: their loads are in flight during the staging
     const float* Gw = a.G[w] + L.off + (int64_t)(T.row0 + i) * L.ld;
     float* Bw = a.B + (int64_t)w * a.total + L.off + (int64_t)(T.row0 + i) * L.ld;
     float g[16], m[16];
@@ -769,11 +777,20 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
       g[4 * v] = gv.x; g[4 * v + 1] = gv.y; g[4 * v + 2] = gv.z; g[4 * v + 3] = gv.w;
       m[4 * v] = bv.x; m[4 * v + 1] = bv.y; m[4 * v + 2] = bv.z; m[4 * v + 3] = bv.w;
     }
+    __syncthreads();  // the previous worker's Q_w' rows are no longer read
+    if (T.prev) {
+      const float* qw = a.Qw + (int64_t)w * a.q_total + q0;
+      for (int e = threadIdx.x; e < RP * SC; e += blockDim.x) {
+        const int c = e / RP, k = e - c * RP;
+        s_qwT[k * SCP + c] = c < segcols ? __ldg(qw + e) : 0.f;
+      }
+    }
+    __syncthreads();
     if (T.prev) {
 #pragma unroll 4
       for (int k = 0; k < RP; ++k) {
         const float p = s_pp[i * RP + k];
-        const float4* qk = reinterpret_cast<const float4*>(s_qwT + k * SC) + cg;
+        const float4* qk = reinterpret_cast<const float4*>(s_qwT + k * SCP) + cg;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const float4 q = qk[8 * v];
@@ -798,7 +815,7 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
     // P partial: for each rank, the thread's 16 columns in order; workers in order
 #pragma unroll 4
     for (int k = 0; k < RP; ++k) {
-      const float4* qk = reinterpret_cast<const float4*>(s_qT + k * SC) + cg;
+      const float4* qk = reinterpret_cast<const float4*>(s_qT + k * SCP) + cg;
       float acc = pacc[k];
 #pragma unroll
       for (int v = 0; v < 4; ++v) {

@@ -9,11 +9,11 @@ namespace psgd {
 namespace {
 
 constexpr int kRP = PSGD_RP;
-constexpr size_t kP3Dyn = (size_t)(kP3Threads / 32) * 32 * 4 * kRP * sizeof(float);
+constexpr size_t kP3Dyn = p3_dyn_bytes(kRP);
 
 #if PSGD_RP >= 8
 // r >= 8: the register-tiled kernels
-constexpr size_t kP1TDyn = (size_t)(2 * kRP * kSeg * 4 + 32 * kRP) * sizeof(float);
+constexpr size_t kP1TDyn = (size_t)(2 * kRP * kP1TRow + Cfg<kRP>::R1 * kRP) * sizeof(float);
 #endif
 
 // A phase kernel launched as a programmatic dependent of the kernel before it
