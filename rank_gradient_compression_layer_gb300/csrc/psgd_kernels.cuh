@@ -761,6 +761,21 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
   float pacc[RP];
 #pragma unroll
   for (int k = 0; k < RP; ++k) pacc[k] = 0.f;
+  // each worker's Q_w' values are loaded one worker ahead (NQ per thread) and
+  // stored into shared memory after the barrier, so their latency hides
+  // behind the previous worker's arithmetic
+  constexpr int NQ = RP * SC / kTThreads;
+  static_assert(NQ * kTThreads == RP * SC, "whole staging rows per thread");
+  float qv[NQ];
+  auto fetch_qw = [&](int wk) {
+    const float* qw = a.Qw + (int64_t)wk * a.q_total + q0;
+#pragma unroll
+    for (int u = 0; u < NQ; ++u) {
+      const int e = threadIdx.x + u * kTThreads;
+      qv[u] = (e / RP) < segcols ? __ldg(qw + e) : 0.f;
+    }
+  };
+  if (T.prev) fetch_qw(0);
   for (int w = 0; w < a.W; ++w) {
     // this worker's G and B first: their loads are in flight during the staging
     const float* Gw = a.G[w] + L.off + (int64_t)(T.row0 + i) * L.ld;
@@ -779,13 +794,15 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
     }
     __syncthreads();  // the previous worker's Q_w' rows are no longer read
     if (T.prev) {
-      const float* qw = a.Qw + (int64_t)w * a.q_total + q0;
-      for (int e = threadIdx.x; e < RP * SC; e += blockDim.x) {
+#pragma unroll
+      for (int u = 0; u < NQ; ++u) {
+        const int e = threadIdx.x + u * kTThreads;
         const int c = e / RP, k = e - c * RP;
-        s_qwT[k * SCP + c] = c < segcols ? __ldg(qw + e) : 0.f;
+        s_qwT[k * SCP + c] = qv[u];
       }
     }
     __syncthreads();
+    if (T.prev && w + 1 < a.W) fetch_qw(w + 1);
     if (T.prev) {
 #pragma unroll 4
       for (int k = 0; k < RP; ++k) {
