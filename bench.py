@@ -41,12 +41,12 @@ UNIT = "GB/s"
 # ncu capture (see profiles/), valid only for the kernel sources whose hash is
 # recorded with it.
 NCU_TRAFFIC = {  # {(config, variant): (sources_sha256_prefix, bytes_per_launch)}
-    # ResNet-18 set, r = 2, W = 4: mean of two project launches, 361.7 MB read +
-    # 124.0 MB written (profiles/bench_all_configs.md)
-    ("c2", "powersgd"): ("74c58c701339d449", 485674624),
+    # ResNet-18 set, r = 2, W = 4: mean of two project launches, 361.6 MB read +
+    # 123.9 MB written (profiles/bench_all_configs.md)
+    ("c2", "powersgd"): ("6bc20720424a822c", 485492224),
     # ResNet-18 set, rTop-k, W = 4: mean of nine pass-0 launches, 362.9 MB read +
     # 176.2 MB written (profiles/rk_kernels_resnet18_w4.md)
-    ("c2", "rtopk"): ("dbfcb98f0bc220fb", 539120924),
+    ("c2", "rtopk"): ("2a5febb22a906ffc", 539186801),
 }
 
 
