@@ -43,10 +43,10 @@ UNIT = "GB/s"
 NCU_TRAFFIC = {  # {(config, variant): (sources_sha256_prefix, bytes_per_launch)}
     # ResNet-18 set, r = 2, W = 4: mean of two project launches, 361.6 MB read +
     # 123.9 MB written (profiles/bench_all_configs.md)
-    ("c2", "powersgd"): ("6bc20720424a822c", 485492224),
-    # ResNet-18 set, rTop-k, W = 4: mean of nine pass-0 launches, 362.9 MB read +
-    # 176.2 MB written (profiles/rk_kernels_resnet18_w4.md)
-    ("c2", "rtopk"): ("2a5febb22a906ffc", 539186801),
+    ("c2", "powersgd"): ("22bf5ecd9443ee00", 485510400),
+    # ResNet-18 set, rTop-k, W = 4: mean of nine pass-0 launches, 363.0 MB read +
+    # 176.1 MB written (profiles/rk_kernels_resnet18_w4.md)
+    ("c2", "rtopk"): ("e3b8fd30010fd18f", 539048106),
 }
 
 

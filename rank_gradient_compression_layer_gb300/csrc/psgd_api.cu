@@ -653,18 +653,11 @@ int psgd_step_host(psgd_ctx* c, const float* const* grad_host, float* msg_host, 
   }
   rc = psgd_step(c, dptr.data(), update_host ? c->stage_U : nullptr);
   if (rc) return rc;
-  if (c->rk) {  // per matrix layer and worker: k indices, then k values
-    int64_t at = 0;
-    for (int mi = 0; mi < (int)c->hl.size(); ++mi)
-      for (int w = 0; w < W; ++w) {
-        const int64_t k = rtopk_k(c->rk, mi);
-        const int32_t* di;
-        const float* dv;
-        rtopk_message(c->rk, mi, w, &di, &dv);
-        CUDA_TRY(cudaMemcpyAsync(msg_host + at, di, (size_t)k * sizeof(int32_t), cudaMemcpyDeviceToHost, c->stream));
-        CUDA_TRY(cudaMemcpyAsync(msg_host + at + k, dv, (size_t)k * sizeof(float), cudaMemcpyDeviceToHost, c->stream));
-        at += 2 * k;
-      }
+  if (c->rk) {  // per matrix layer and worker: k indices, then k values; gathered, then one copy
+    if ((rc = rtopk_pack(c->rk, c->stage_msg, c->stream))) return rc;
+    if (c->msg_floats)
+      CUDA_TRY(cudaMemcpyAsync(msg_host, c->stage_msg, (size_t)c->msg_floats * sizeof(float),
+                               cudaMemcpyDeviceToHost, c->stream));
   } else if (!c->pack.empty()) {
     dim3 grid(32, (unsigned)c->pack.size());
     pack_msg_kernel<<<grid, 256, 0, c->stream>>>(c->stage_msg, c->unbiased ? c->P : c->Phat, c->Qbar, c->d_pack,

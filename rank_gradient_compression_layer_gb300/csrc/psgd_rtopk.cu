@@ -84,6 +84,7 @@ struct RkProb {   // one (worker, matrix layer) problem
   int64_t chunk0;  // first span count of this problem
   int64_t msg_off; // first message entry of this problem
   int64_t list_off, bm_off;  // candidate list and list of T (capacity d each); K's bitmap
+  int64_t host_off;          // its message in psgd_step_host's order (layer-major)
 };
 
 struct RkSel {      // one radix select
@@ -832,6 +833,17 @@ __global__ void __launch_bounds__(kRkThreads) rk_apply_kernel(RkArgs a) {
   }
 }
 
+// Every problem's message into one buffer, layer-major: k indices (int32
+// bits), then k values; grid.y = problem.
+__global__ void rk_pack_kernel(const RkProb* probs, const int32_t* sidx, const float* sval, float* dst) {
+  const RkProb P = probs[blockIdx.y];
+  float* d = dst + P.host_off;
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < P.k; e += (int64_t)gridDim.x * blockDim.x) {
+    d[e] = __int_as_float(sidx[P.msg_off + e]);
+    d[P.k + e] = sval[P.msg_off + e];
+  }
+}
+
 // Vector layers: U = the worker mean; grid.y = vector layer.
 __global__ void rk_vec_kernel(const VecDev* vecs, RkArgs a) {
   const VecDev V = vecs[blockIdx.y];
@@ -948,6 +960,15 @@ int rtopk_create(RTopK** out, const std::vector<LayerDev>& hl, const std::vector
     }
   for (int mi = 0; mi < rk->nmat; ++mi)
     for (int64_t c = 0; c < rk->hp[mi].nspans; ++c) rk->ltiles.push_back({mi, (int32_t)c});
+  {
+    int64_t at = 0;  // psgd_step_host's message: layer-major, then worker
+    for (int mi = 0; mi < rk->nmat; ++mi)
+      for (int w = 0; w < W; ++w) {
+        RkProb& P = rk->hp[(size_t)w * rk->nmat + mi];
+        P.host_off = at;
+        at += 2 * P.k;
+      }
+  }
   int rc = PSGD_OK;
   if (!rc) rc = rk_alloc(&rk->d_probs, rk->nprob, "rtopk problems");
   if (!rc) rc = rk_alloc(&rk->d_state, rk->nprob, "rtopk state");
@@ -1059,6 +1080,13 @@ void rtopk_message(const RTopK* rk, int mi, int w, const int32_t** idx, const fl
   const RkProb& P = rk->hp[(size_t)w * rk->nmat + mi];
   *idx = rk->d_sidx + P.msg_off;
   *val = rk->d_sval + P.msg_off;
+}
+
+int rtopk_pack(const RTopK* rk, float* dst, cudaStream_t s) {
+  if (rk->nprob == 0) return PSGD_OK;
+  rk_pack_kernel<<<dim3(8, (unsigned)rk->nprob), 256, 0, s>>>(rk->d_probs, rk->d_sidx, rk->d_sval, dst);
+  CUDA_TRY(cudaGetLastError());
+  return PSGD_OK;
 }
 
 int rtopk_launches(const RTopK* rk) {

@@ -39,5 +39,9 @@ int64_t rtopk_k(const RTopK* rk, int mi);
 void rtopk_message(const RTopK* rk, int mi, int w, const int32_t** idx, const float** val);
 // Kernel launches one step enqueues.
 int rtopk_launches(const RTopK* rk);
+// Gathers every message of the last step into dst (device, rtopk_message_floats
+// floats) in psgd_step_host's order: per matrix layer, per worker, its k
+// indices (int32 bits) then its k values.  One kernel on stream s.
+int rtopk_pack(const RTopK* rk, float* dst, cudaStream_t s);
 
 }  // namespace psgd
