@@ -41,12 +41,12 @@ UNIT = "GB/s"
 # ncu capture (see profiles/), valid only for the kernel sources whose hash is
 # recorded with it.
 NCU_TRAFFIC = {  # {(config, variant): (sources_sha256_prefix, bytes_per_launch)}
-    # ResNet-18 set, r = 2, W = 4: mean of two project launches, 361.6 MB read +
-    # 123.9 MB written (profiles/bench_all_configs.md)
-    ("c2", "powersgd"): ("22bf5ecd9443ee00", 485510400),
-    # ResNet-18 set, rTop-k, W = 4: mean of nine pass-0 launches, 363.0 MB read +
-    # 176.1 MB written (profiles/rk_kernels_resnet18_w4.md)
-    ("c2", "rtopk"): ("e3b8fd30010fd18f", 539048106),
+    # ResNet-18 set, r = 2, W = 4: mean of two project launches, 361.7 MB read +
+    # 123.7 MB written (profiles/bench_all_configs.md)
+    ("c2", "powersgd"): ("5a5f0d8e73cc8271", 485403264),
+    # ResNet-18 set, rTop-k, W = 4: mean of three pass-0 launches, 363.0 MB read +
+    # 177.2 MB written (profiles/rk_kernels_resnet18_w4.md)
+    ("c2", "rtopk"): ("7ca7c00426395cdf", 540190976),
 }
 
 

@@ -728,6 +728,25 @@ constexpr int kTThreads = 256;  // threads of a tiled project CTA: 32 rows x 8 c
 // in registers; the 8 column groups of a row are summed with a butterfly
 // over their 8 lanes at the end.  Q and Q_w' are staged transposed
 // ([k][column]) so a thread reads its 4 float4 columns at fixed k.
+// The tiled project kernel's G and B float4 of worker w: row i of the tile,
+// float4 columns c40 + 8 v (zeros past the row or the layer; no B in the
+// unbiased variant).
+__device__ __forceinline__ void p1t_load_gb(const StepArgs& a, const LayerDev& L, const P1Tile& T, int w, int i,
+                                            int c40, bool row_ok, float4 (&gv)[4], float4 (&bv)[4]) {
+  const float4* G4 = reinterpret_cast<const float4*>(a.G[w] + L.off + (int64_t)(T.row0 + i) * L.ld);
+  const float4* B4 = reinterpret_cast<const float4*>(a.B + (int64_t)w * a.total + L.off + (int64_t)(T.row0 + i) * L.ld);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const int c4 = c40 + 8 * v;
+    gv[v] = zero4();
+    bv[v] = zero4();
+    if (row_ok && c4 < L.F) {
+      gv[v] = __ldcs(G4 + c4);
+      if (!T.ub) bv[v] = __ldcs(B4 + c4);
+    }
+  }
+}
+
 template <int RP>
 __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
   constexpr int TR = 32;
@@ -776,21 +795,29 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
     }
   };
   if (T.prev) fetch_qw(0);
+  // below r = 32 the registers allow G and B to be loaded one worker ahead
+  constexpr bool kAhead = RP <= 16;
+  float4 gn[4], bn[4];
+  if (kAhead) p1t_load_gb(a, L, T, 0, i, c40, row_ok, gn, bn);
   for (int w = 0; w < a.W; ++w) {
     // this worker's G and B first: their loads are in flight during the staging
-    const float* Gw = a.G[w] + L.off + (int64_t)(T.row0 + i) * L.ld;
     float* Bw = a.B + (int64_t)w * a.total + L.off + (int64_t)(T.row0 + i) * L.ld;
+    float4 gc[4], bc[4];
+    if (kAhead) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        gc[v] = gn[v];
+        bc[v] = bn[v];
+      }
+      if (w + 1 < a.W) p1t_load_gb(a, L, T, w + 1, i, c40, row_ok, gn, bn);
+    } else {
+      p1t_load_gb(a, L, T, w, i, c40, row_ok, gc, bc);
+    }
     float g[16], m[16];
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
-      const int c4 = c40 + 8 * v;
-      float4 gv = zero4(), bv = zero4();
-      if (row_ok && c4 < L.F) {
-        gv = __ldcs(reinterpret_cast<const float4*>(Gw) + c4);
-        if (!T.ub) bv = __ldcs(reinterpret_cast<const float4*>(Bw) + c4);
-      }
-      g[4 * v] = gv.x; g[4 * v + 1] = gv.y; g[4 * v + 2] = gv.z; g[4 * v + 3] = gv.w;
-      m[4 * v] = bv.x; m[4 * v + 1] = bv.y; m[4 * v + 2] = bv.z; m[4 * v + 3] = bv.w;
+      g[4 * v] = gc[v].x; g[4 * v + 1] = gc[v].y; g[4 * v + 2] = gc[v].z; g[4 * v + 3] = gc[v].w;
+      m[4 * v] = bc[v].x; m[4 * v + 1] = bc[v].y; m[4 * v + 2] = bc[v].z; m[4 * v + 3] = bc[v].w;
     }
     __syncthreads();  // the previous worker's Q_w' rows are no longer read
     if (T.prev) {
