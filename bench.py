@@ -46,7 +46,7 @@ NCU_TRAFFIC = {  # {(config, variant): (sources_sha256_prefix, bytes_per_launch)
     ("c2", "powersgd"): ("5a5f0d8e73cc8271", 485403264),
     # ResNet-18 set, rTop-k, W = 4: mean of three pass-0 launches, 363.0 MB read +
     # 177.2 MB written (profiles/rk_kernels_resnet18_w4.md)
-    ("c2", "rtopk"): ("7ca7c00426395cdf", 540190976),
+    ("c2", "rtopk"): ("f06f8d79ceb1a692", 540190976),
 }
 
 

@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(kRkThreads, 4) rk_pass0_kernel(RkArgs a) {
 // Pass 1: the list of the entries above the digits pass 0 resolved
 // (members of T for sure) and the list of candidates (equal to them).  Only
 // the bitmap words whose largest |M| reaches the candidates' range are
-// read: with one percent of a layer in T, about a quarter of B.  One CTA per
+// read: with one percent of a layer in T, about a third of B.  One CTA per
 // kRkP1Words words of a problem (last first: pass 0 wrote the end of B
 // last, so it is still in L2); each warp owns 128 of them, finds the marked
 // ones from the word maxima, and reads them 16 at a time (8 lanes per word,
@@ -721,7 +721,10 @@ constexpr int kRkApplyFastW = 8;  // workers the apply kernel handles with all w
 // index-ordered position, are zeroed in B (E = M - S) and summed into U
 // (zeroed by pass 0), which is then scaled by 1 / W; the bitmap words are
 // cleared.  The workers' records and span offsets are read once into shared
-// memory, and the next worker's word is fetched while one is written.
+// memory.  Up to kRkApplyFastW workers, all their words are loaded at once
+// and each sent entry is handled with every worker's load in flight; with
+// more, the workers go one by one, the next one's word fetched while one is
+// written.
 __global__ void __launch_bounds__(kRkThreads) rk_apply_kernel(RkArgs a) {
   __shared__ int s_warp[kRkThreads / 32];
   __shared__ int64_t s_at[kMaxWorkers], s_end[kMaxWorkers], s_bm[kMaxWorkers];
