@@ -12,6 +12,16 @@ replica of the workload (weak scaling; the method has no data exchange
 between the simulated workers of one GPU and the GPUs).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config c2]
+                  [--momentum | --unbiased | --rtopk [--rtopk-top-div D] [--rtopk-sample-div S]]
+
+Configs: c1 (256 x 128), c2 (the ResNet-18 set, default), c3 (LSTM-650),
+c4 (the 1.2 B-parameter transformer set), c5r<r> (one 8192 x 8192 layer, W = 8,
+rank r), c5s<r> (the same signal on 4096 x 4096, W = 4: a case small enough
+for a full ncu capture), c2x<k> (the ResNet-18 set repeated k times).
+--momentum fuses the momentum-SGD update into the decompress phase;
+--unbiased times the unbiased rank-r variant; --rtopk times rTop-k
+sparsification (its four kernels fill the phase slots, and pass 0 is the
+roofline kernel).
 """
 from __future__ import annotations
 
