@@ -22,9 +22,9 @@ approaches the best rank-r approximation without an SVD.
 
 Where the page leaves a step open, the plainest reading is taken (each one
 is listed where it is used):
-  * orthonormalisation = Gram-Schmidt (modified, column by column), the thin-QR
-    factor with a positive diagonal of R; a column whose remainder is exactly
-    zero stays zero;
+  * orthonormalisation = Gram-Schmidt (modified, column by column, each
+    column orthogonalised twice), the thin-QR factor with a positive diagonal
+    of R; a column whose remainder is exactly zero stays zero;
   * P is the SUM of the workers' M_w Q; Q is the MEAN of the workers' M_w^T P,
     so the decompressed P Q^T approximates the mean gradient;
   * the error is worker-local: E_w <- M_w - Phat Q_w^T with the worker's own
@@ -113,19 +113,29 @@ def q_init(seed: int, layer: int, m: int, r: int) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 def gram_schmidt(P: np.ndarray) -> np.ndarray:
-    """Modified Gram-Schmidt on the columns of P (float64).
+    """Gram-Schmidt on the columns of P (float64), each column orthogonalised twice.
 
     Column k has the projections on the already finished columns 0..k-1
-    removed one at a time, then is scaled to unit length.  The result is the
-    thin-QR factor of P whose R has a positive diagonal.  A column whose
-    remainder has norm exactly 0 is left as the zero vector.
+    removed one at a time (modified Gram-Schmidt), and then once more, and
+    is scaled to unit length.  The result is the thin-QR factor of P whose R
+    has a positive diagonal.  A column whose remainder has norm exactly 0 is
+    left as the zero vector.
+
+    The second pass changes nothing in exact arithmetic.  In floating point a
+    single pass leaves column k off orthogonal by about eps times the ratio
+    of its norm to its remainder's, which reaches 1e-2 when the warm-started
+    Q's last column carries almost nothing outside the other columns' span
+    (a rank-deficient P); the error feedback then compounds it step after
+    step.  One more pass brings the columns back to orthogonal to working
+    precision ("twice is enough": Giraud, Langou and Rozloznik, 2005).
     """
     Ph = np.array(P, dtype=np.float64, copy=True)
     n, r = Ph.shape
     for k in range(r):
         v = Ph[:, k]
-        for j in range(k):
-            v -= (Ph[:, j] @ v) * Ph[:, j]
+        for _ in range(2):
+            for j in range(k):
+                v -= (Ph[:, j] @ v) * Ph[:, j]
         nrm = math.sqrt(float(v @ v))
         if nrm > 0.0:
             v /= nrm

@@ -60,6 +60,14 @@ def check_gram_schmidt(gs):
     base = _rng(10).standard_normal((200, 1))
     P = base + 1e-6 * _rng(11).standard_normal((200, 4))
     np.testing.assert_allclose(gs(P), _qr_posdiag(P), atol=1e-7)
+    # a last column within 1e-13 of the span of the others (what a warm start
+    # gives when M has rank < r): the basis is still orthonormal to working
+    # precision, and the leading columns are QR's
+    a, b, c = (_rng(s).standard_normal((500, 1)) for s in (13, 14, 15))
+    P = np.hstack([a, b, a - 2.0 * b + 1e-13 * c])
+    Ph = gs(P)
+    np.testing.assert_allclose(Ph.T @ Ph, np.eye(3), atol=1e-12)
+    np.testing.assert_allclose(Ph[:, :2], _qr_posdiag(P[:, :2]), atol=1e-13)
     # zero columns stay zero; the all-zero matrix maps to zero
     P = _rng(12).standard_normal((30, 3))
     P[:, 1] = 0.0
@@ -489,15 +497,17 @@ def _mutant_compress(kind):
 
 
 def _mutant_gs(kind):
+    # "single_pass": plain modified Gram-Schmidt, one pass per column
     def gs(P):
         Ph = np.array(P, dtype=np.float64)
         for k in range(Ph.shape[1]):
             v = Ph[:, k]
-            for j in range(k):
-                if kind == "skip_last_projection" and j == k - 1:
-                    continue
-                coef = Ph[:, j] @ v
-                v -= (coef if kind != "projection_sign" else -coef) * Ph[:, j]
+            for _ in range(1 if kind == "single_pass" else 2):
+                for j in range(k):
+                    if kind == "skip_last_projection" and j == k - 1:
+                        continue
+                    coef = Ph[:, j] @ v
+                    v -= (coef if kind != "projection_sign" else -coef) * Ph[:, j]
             Ph[:, k] = v / np.linalg.norm(v)
         return Ph
     return gs
@@ -526,7 +536,7 @@ def test_planted_mistakes_are_caught(kind):
     assert caught >= 1, kind
 
 
-@pytest.mark.parametrize("kind", ["skip_last_projection", "projection_sign"])
+@pytest.mark.parametrize("kind", ["skip_last_projection", "projection_sign", "single_pass"])
 def test_planted_gram_schmidt_mistakes_are_caught(kind):
     with pytest.raises(AssertionError):
         check_gram_schmidt(_mutant_gs(kind))
