@@ -47,22 +47,19 @@ import workloads  # noqa: E402
 METRIC = "gradient GB/s compressed per PowerSGD step (1 GB300) and % of HBM roofline"
 UNIT = "GB/s"
 
-# DRAM bytes (read + write) of one project-kernel launch per workload, from an
-# ncu capture (see profiles/), valid only for the kernel sources whose hash is
-# recorded with it.
+# DRAM bytes (read + write) of one launch of the roofline kernel per workload,
+# from a one-kernel ncu capture, valid only for the kernel sources whose hash
+# is recorded with it.
 NCU_TRAFFIC = {  # {(config, variant): (sources_sha256_prefix, bytes_per_launch)}
-    # ResNet-18 set, r = 2, W = 4: mean of two project launches, 361.7 MB read +
-    # 123.7 MB written (profiles/bench_all_configs.md)
-    ("c2", "powersgd"): ("5a5f0d8e73cc8271", 485403264),
-    # ResNet-18 set, rTop-k, W = 4: mean of three pass-0 launches, 363.0 MB read +
-    # 177.2 MB written (profiles/rk_kernels_resnet18_w4.md)
+    # ResNet-18 set, rTop-k, W = 4: ncu capture of three pass-0 launches, DRAM
+    # 363.0 MB read + 177.2 MB written per launch
     ("c2", "rtopk"): ("f06f8d79ceb1a692", 540190976),
 }
 
 
 # the sources that define the phase kernels of a step and their launch
 # (the allocation-free entry point is not among them; rTop-k adds its own files)
-STEP_SOURCES = ("psgd_api.cu", "psgd_dispatch.h", "psgd_internal.h", "psgd_kernels.cuh", "psgd_plan.h",
+STEP_SOURCES = ("psgd_api.cu", "psgd_dispatch.h", "psgd_fused.cuh", "psgd_internal.h", "psgd_kernels.cuh", "psgd_plan.h",
                 "psgd_step_impl.cuh", "psgd_step_r1.cu", "psgd_step_r2.cu", "psgd_step_r4.cu", "psgd_step_r8.cu",
                 "psgd_step_r16.cu", "psgd_step_r32.cu")
 RTOPK_SOURCES = ("psgd_rtopk.cu", "psgd_rtopk.h")  # and STEP_SOURCES (the API and shared headers)
@@ -330,7 +327,8 @@ def run_ours(args, ws, rank, local):
     stream = torch.cuda.Stream(device=device)
     ctx = PowerSGD(cfg.layers, cfg.rank, cfg.workers, seed=cfg.seed, stream=stream, timing=True,
                    unbiased=args.unbiased, compressor="rtopk" if args.rtopk else "powersgd",
-                   top_div=args.rtopk_top_div, sample_div=args.rtopk_sample_div)
+                   top_div=args.rtopk_top_div, sample_div=args.rtopk_sample_div,
+                   fused=args.fused, queue_lag_kb=args.queue_lag_kb, project_rows=args.project_rows)
     sets = 3
     grads = fill_gradients(ctx, cfg, sets, device)
     upd = ctx.empty_buffer()
@@ -363,19 +361,33 @@ def run_ours(args, ws, rank, local):
     barrier(ws)
     torch.cuda.synchronize()
 
+    # the timed region: repeats of exactly `steps` steps, each bracketed by a
+    # barrier and a device synchronisation, until at least --min-time seconds
+    # have passed (so the clock sampler sees the GPU under load); the value
+    # is the median repeat, each repeat taking the slowest rank
     sampler = ClockSampler(local)
     sampler.start()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    barrier(ws)
-    torch.cuda.synchronize()
-    ev0.record(stream)
-    for i in range(args.steps):
-        one_step(grads[i % sets])
-    ev1.record(stream)
-    ctx.sync()
-    torch.cuda.synchronize()
-    barrier(ws)
+
+    def timed_repeat() -> float:
+        barrier(ws)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            one_step(grads[i % sets])
+        ev1.record(stream)
+        ctx.sync()
+        torch.cuda.synchronize()
+        barrier(ws)
+        return max_over_ranks(ev0.elapsed_time(ev1), ws, device)
+
+    rep_ms = [timed_repeat()]
+    # every rank runs the same number of repeats (from the slowest first one)
+    repeats = max(3, int(math.ceil(args.min_time * 1e3 / max(rep_ms[0], 1e-3))))
+    repeats = int(max_over_ranks(float(min(repeats, 10000)), ws, device))
+    for _ in range(repeats - 1):
+        rep_ms.append(timed_repeat())
     clocks = sampler.stop()
     # the same number of steps again with an event between phases: each phase
     # alone, for the per-phase times and the roofline kernel's duration
@@ -384,13 +396,23 @@ def run_ours(args, ws, rank, local):
         one_step(grads[i % sets])
     ctx.sync()
     phases = ctx.phase_times()  # device ms per phase, averaged over those steps
-    ms_per_step, value = replica_throughput(comp, args.steps, ev0.elapsed_time(ev1), ws, device)
+    med_ms = statistics.median(rep_ms)
+    ms_per_step, value = replica_throughput(comp, args.steps, med_ms, 1, device)
+    value *= ws  # each repeat is already the max over ranks; ws replicas
+    repeat_stats = {"repeats": len(rep_ms), "median_ms_per_step": round(med_ms / args.steps, 5),
+                    "min_ms_per_step": round(min(rep_ms) / args.steps, 5),
+                    "max_ms_per_step": round(max(rep_ms) / args.steps, 5),
+                    "timed_s": round(sum(rep_ms) / 1e3, 3)}
     peaks = measured_peaks()
     if args.rtopk:
         # rTop-k's four phase slots are its kernels; pass 0 moves nearly all the bytes
         phases = dict(zip(("pass0", "pass1", "tail", "apply"), phases.values()))
         project_ms = phases["pass0"]
         project_bytes = ab["pass0"]  # read G, read E, write M of every worker, U zeroed
+    elif "step" in phases:
+        # the fused step: one launch moves every byte of the step
+        project_ms = phases["step"]
+        project_bytes = ab["total"]
     else:
         project_ms = phases["project"]
         project_bytes = ab["core"]  # read G, read E, write E of every worker (+ the factors); unbiased: read G
@@ -398,7 +420,8 @@ def run_ours(args, ws, rank, local):
     step_achieved = ab["total"] / (ms_per_step * 1e-3) / 1e9
     h = kernel_sources_hash(rtopk=args.rtopk)
     traffic = None
-    variant = "rtopk" if args.rtopk else ("powersgd" if not (args.unbiased or args.momentum) else None)
+    variant = "rtopk" if args.rtopk else (
+        ("powersgd_fused" if st["fused_step"] else "powersgd") if not (args.unbiased or args.momentum) else None)
     if (args.config, variant) in NCU_TRAFFIC and NCU_TRAFFIC[(args.config, variant)][0] == h:
         traffic = NCU_TRAFFIC[(args.config, variant)][1]
 
@@ -424,13 +447,16 @@ def run_ours(args, ws, rank, local):
                      else "fallback 6.8 TB/s",
                      "kernel": ("psgd::rk_pass0_kernel (M = G + E written over E, top digit of |M|, U zeroed)"
                                 if args.rtopk else
+                                f"psgd::fused_step_kernel<{st['kernel_rank']}> (the whole step: error add, E write, "
+                                "P = M Q, Gram-Schmidt, Q_w = M_w^T Phat, Qbar, U)" if st["fused_step"] else
                                 f"psgd::p1_kernel<{st['kernel_rank']}> (project: P = G Q)" if args.unbiased else
                                 f"psgd::p1_kernel<{st['kernel_rank']}> (project: error add, E write, P = M Q)"),
                      "algorithmic_bytes_per_launch": project_bytes, "launch_ms": round(project_ms, 5),
                      "launch_ms_source": "CUDA events around the kernel on the context's stream, "
                                          "averaged over a second pass of the timed steps with per-phase events",
                      "kernel_sources": h},
-        "project_fp32": project_fp32(cfg, args, project_ms, peaks, device),
+        "project_fp32": None if st["fused_step"] else project_fp32(cfg, args, project_ms, peaks, device),
+        "timing": repeat_stats,
         "step_roofline": {"achieved": round(step_achieved, 1), "frac": round(step_achieved / peaks["hbm_gbs"], 4),
                           "algorithmic_bytes_per_step": ab["total"],
                           "phase_ms": {k: round(v, 5) for k, v in phases.items()}},
@@ -518,6 +544,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="c2")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for the CPU leg")
+    ap.add_argument("--min-time", type=float, default=0.5,
+                    help="repeat the timed --steps loop until this many seconds have passed (at least 3 repeats)")
+    ap.add_argument("--fused", action="store_true",
+                    help="time the fused step (one launch per step over a queue of every phase's tiles, r <= 4)")
+    ap.add_argument("--queue-lag-kb", type=int, default=0, help="fused step: queue lag between a layer's phases")
+    ap.add_argument("--project-rows", type=int, default=0, help="rows per project tile (0: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unbiased", action="store_true",
                     help="time the unbiased rank-r variant (fresh shared Q per step, no error feedback)")

@@ -39,11 +39,24 @@
  *
  * Errors: every call returns a psgd_status; nothing throws across the ABI.
  * psgd_last_error() gives a message for the calling thread.  psgd_step is
- * asynchronous on the context's stream (four kernel launches, no host
- * synchronisation); a CUDA error raised while it runs is reported by the next
- * synchronising call (psgd_sync or any psgd_get_*), after which the context
- * only answers PSGD_ERR_STATE until destroyed.  No kernel of this library
- * waits on another kernel or on another CTA, so a step cannot hang.
+ * asynchronous on the context's stream (no host synchronisation); a CUDA
+ * error raised while it runs is reported by the next synchronising call
+ * (psgd_sync or any psgd_get_*), after which the context only answers
+ * PSGD_ERR_STATE until destroyed.
+ *
+ * Launches: a PowerSGD step is one kernel per phase (project, orthonormalise,
+ * back-project, decompress; at r >= 8 a fifth forms the second Cholesky-QR
+ * pass's Phat rows), each a grid of independent tiles over all layers
+ * launched as a programmatic dependent of the one before; none waits on
+ * another CTA.  At r >= 16 the project phase's products run on the tensor
+ * cores (tcgen05, error-compensated TF32); a wait on them that runs out is
+ * reported as PSGD_ERR_TIMEOUT.  With options.fused (padded rank 1, 2 or 4, one process) a step
+ * is instead ONE launch whose CTAs take the tiles of all four phases from one
+ * queue in dependency order; a tile whose inputs another CTA is still
+ * producing waits for a flag.  Every such wait is bounded (options.wait_ms,
+ * 2 s by default): one that runs out abandons the step, and the next
+ * synchronising call answers PSGD_ERR_TIMEOUT (the context is then unusable,
+ * the CUDA context is not harmed).
  *
  * Thread safety: a context must not be used from two host threads at once.
  * Two contexts are independent and may run concurrently on different streams.
@@ -65,7 +78,8 @@ typedef enum {
   PSGD_ERR_INVALID = -1,  /* bad argument (null / misaligned pointer, bad size, rank) */
   PSGD_ERR_OOM = -2,      /* device or pinned-host allocation failed */
   PSGD_ERR_CUDA = -3,     /* a CUDA runtime call failed (message in psgd_last_error) */
-  PSGD_ERR_STATE = -5     /* the context hit an earlier CUDA error and is unusable */
+  PSGD_ERR_TIMEOUT = -4,  /* a fused step waited past options.wait_ms and was abandoned */
+  PSGD_ERR_STATE = -5     /* the context hit an earlier error and is unusable */
 } psgd_status;
 
 /* Cumulative counters of a context (exact integers). */
@@ -82,7 +96,7 @@ typedef struct {
   int32_t kernel_rank;                  /* rank the kernels were compiled for (r rounded up to 1,2,4,8,16,32) */
   int32_t launches_per_step;            /* kernels one psgd_step enqueues (with an update) */
   int32_t tile_rows[3];                 /* rows per tile: project, back-project (least), decompress */
-  int32_t reserved;
+  int32_t fused_step;                   /* 1: each step is one fused launch (see the header comment) */
   int64_t message_floats;               /* floats psgd_step_host writes to msg_host */
 } psgd_stats;
 
@@ -94,6 +108,15 @@ typedef struct {
   int32_t compressor;   /* PSGD_POWERSGD (0) or PSGD_RTOPK (1): rTop-k sparsification (see below) */
   int32_t rtopk_top_div;    /* rTop-k: the top set of a layer of d entries has ceil(d / top_div) */
   int32_t rtopk_sample_div; /* rTop-k: k = ceil(r / sample_div) of them are sent */
+  int32_t fused;        /* 1: each step is ONE launch over a queue of every phase's tiles (PowerSGD at
+                           r <= 4 in one process; see "Launches" above); 0: one kernel per phase */
+  int32_t wait_ms;      /* fused step: longest wait of a tile for its inputs (0: 2000 ms) */
+  int32_t queue_lag_kb; /* fused step: bytes of other tiles between a layer's phases in the
+                           queue, in KiB (0: about what the resident CTAs hold in flight) */
+  int32_t test_stall;   /* tests of the timeout path only: k > 0 never raises the first flag
+                           of matrix layer k - 1, so its later tiles wait until wait_ms */
+  int32_t total_workers; /* workers over all processes when this context's num_workers are one
+                            process's share (the split step below); 0: num_workers */
 } psgd_options;
 
 enum { PSGD_POWERSGD = 0, PSGD_RTOPK = 1 };
@@ -192,6 +215,47 @@ int psgd_step_momentum(psgd_ctx* ctx, const float* const* grad_ptrs, float* para
  */
 int psgd_step_host(psgd_ctx* ctx, const float* const* grad_host, float* msg_host, float* update_host);
 
+/*
+ * The split step: one PowerSGD step whose workers are spread over several
+ * processes (one per GPU, the page's deployment: main findings, bullets 1
+ * and 6 -- P and Q summed by all-reduce, NCCL or GLOO).  Each process's
+ * context holds its own num_workers workers and knows the total
+ * (options.total_workers); the caller runs the two all-reduces (sum) between
+ * the three calls, on buffers it owns (device memory, float32):
+ *
+ *   psgd_step_begin(ctx, grads, p_out)  error add, P = sum over this
+ *       process's workers of M_w Q  ->  p_out (p_floats: every matrix
+ *       layer's n x r block, row-major, layers in order)
+ *   -- all-reduce(sum) p_out over the processes into p_sum --
+ *   psgd_step_mid(ctx, p_sum, q_out)   Gram-Schmidt of the summed P
+ *       (Cholesky-QR2), Q_w = M_w^T Phat for this process's workers, and
+ *       (1 / total_workers) sum over them of Q_w  ->  q_out (q_floats: every
+ *       matrix layer's m x r block, then every vector layer's n floats of
+ *       (1 / total_workers) sum of this process's gradients)
+ *   -- all-reduce(sum) q_out into q_sum: Qbar and the vector means --
+ *   psgd_step_end(ctx, q_sum, out_update)  Qbar <- q_sum (the next warm
+ *       start), U = Phat Qbar^T and the vector means into out_update (may
+ *       be NULL)
+ *
+ * p_floats and q_floats come from psgd_exchange_sizes; they are what one
+ * process sends per step ((n + m) r per matrix, vectors whole, as
+ * psgd_count_sent).  The all-reduced P is bitwise the same on every process,
+ * so every process forms the same Phat.  grads must stay valid until
+ * psgd_step_end; p_sum may be p_out and q_sum may be q_out (in-place
+ * all-reduce).  Asynchronous on the context's stream; the caller orders its
+ * collectives after the enqueued work (same stream, or an event).  The
+ * calls must come in the order begin, mid, end (else PSGD_ERR_INVALID, and
+ * nothing is enqueued).  psgd_step answers PSGD_ERR_INVALID on a context
+ * whose total_workers exceeds num_workers.  PowerSGD only (not the unbiased
+ * variant or rTop-k); a context with total_workers == num_workers may use
+ * either form, and the split step with the identity as all-reduce gives
+ * psgd_step's results.
+ */
+int psgd_exchange_sizes(const psgd_ctx* ctx, int64_t* p_floats, int64_t* q_floats);
+int psgd_step_begin(psgd_ctx* ctx, const float* const* grad_ptrs, float* p_out);
+int psgd_step_mid(psgd_ctx* ctx, const float* p_sum, float* q_out);
+int psgd_step_end(psgd_ctx* ctx, const float* q_sum, float* out_update);
+
 /* Wait for the context's stream and report a device-side error, if any. */
 int psgd_sync(psgd_ctx* ctx);
 
@@ -216,7 +280,11 @@ int psgd_get_error(psgd_ctx* ctx, int layer, int worker, float* E);
  * Overwrite the state of layer l: Q (m x r row-major, the next step's warm
  * start) and, when E is not NULL, E[w] (dense n x m row-major) for every worker;
  * E == NULL sets the errors to zero.  Host or device memory.  With
- * psgd_get_PQ/psgd_get_error this checkpoints and restores a run bit-exactly.
+ * psgd_get_PQ/psgd_get_error this checkpoints and restores a run bit-exactly
+ * at r <= 8.  At r >= 16 the project phase rebuilds E on the tensor cores
+ * (TF32 products with error compensation, ~2^-21 relative) while
+ * psgd_get_error uses float32 multiply-adds, so a restored run agrees with an
+ * uninterrupted one to that rounding, not bit for bit.
  */
 int psgd_set_state(psgd_ctx* ctx, int layer, const float* Q, const float* const* E);
 
@@ -225,7 +293,8 @@ int psgd_get_stats(const psgd_ctx* ctx, psgd_stats* out);
 /*
  * Device time of each phase, in milliseconds, averaged over the steps since
  * the previous call (the last 256 at most): project, orthonormalise,
- * back-project, decompress (ms[4]); under rTop-k the four slots are its
+ * back-project, decompress (ms[4]); for a fused step (stats.fused_step) ms[0]
+ * is the whole launch and the other slots are 0; under rTop-k the four slots are its
  * kernels: the pass forming M, the pass listing the top-set candidates, the
  * per-problem selection tail, and the message / error / update writes.
  * Needs options.timing = 1; waits for the stream.  Each timed step records
@@ -298,7 +367,10 @@ int psgd_layer_info(const psgd_ctx* ctx, int layer, int64_t* offset, int64_t* n,
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) and sets the kernels' shared-memory limits; make that
- * first call before any stream capture.  Later calls only enqueue work.
+ * first call before any stream capture.  Later calls only enqueue work.  The
+ * address and the limits are kept for the life of the process: after a
+ * cudaDeviceReset on a device that has seen a call, this entry point must not
+ * be called again on it (the kept address would belong to the old context).
  *
  * Concurrency: every call on a device uses the same scratch array.  Two calls
  * whose work overlaps on the device (different streams, or host threads,
@@ -321,6 +393,22 @@ int psgd_plan_layout(int num_layers, const int64_t* n, const int64_t* m, int64_t
                      int64_t* ld, int64_t* total);
 int psgd_count_sent(int num_layers, const int64_t* n, const int64_t* m, int rank,
                     int64_t* compressed, int64_t* uncompressed);
+
+/*
+ * The fused step's queue for a layer set (host only, no GPU): the items a
+ * context with these layers would run, in order, 4 int32 each -- (phase << 24
+ * | matrix index, a, b, c) with phase 0 project (a = row block, b = segment),
+ * 1 orthonormalise (a = row chunk), 2 back-project (a = row tile, b =
+ * segment, c = worker), 3 decompress (a = row block, b = segment; c = 1 marks
+ * a vector layer's chunk a, its index counting vector layers only).  The
+ * matrix index counts matrix layers only.  project_rows: rows per project
+ * tile (0: the kernels' maximum); lag_bytes: as options.queue_lag_kb, in
+ * bytes.  With items == NULL only *count is set.  For checking the queue's
+ * order: every tile comes after the tiles whose results it reads.
+ */
+int psgd_plan_queue(int num_layers, const int64_t* n, const int64_t* m, int rank, int num_workers,
+                    int project_rows, int64_t lag_bytes, int with_update, int32_t* items,
+                    int64_t* count);
 
 const char* psgd_last_error(void);
 const char* psgd_version(void);

@@ -17,6 +17,7 @@ PSGD_OK = 0
 PSGD_ERR_INVALID = -1
 PSGD_ERR_OOM = -2
 PSGD_ERR_CUDA = -3
+PSGD_ERR_TIMEOUT = -4
 PSGD_ERR_STATE = -5
 
 # every symbol include/psgd.h declares
@@ -25,6 +26,7 @@ EXPORTS = (
     "psgd_sync", "psgd_get_PQ", "psgd_get_Qw", "psgd_get_error", "psgd_set_state", "psgd_get_stats",
     "psgd_layer_info", "psgd_plan_layout", "psgd_count_sent", "psgd_last_error", "psgd_version",
     "psgd_get_phase_times", "psgd_step_noalloc", "psgd_step_momentum", "psgd_set_timing", "psgd_get_sparse",
+    "psgd_plan_queue", "psgd_exchange_sizes", "psgd_step_begin", "psgd_step_mid", "psgd_step_end",
 )
 
 PSGD_POWERSGD = 0
@@ -53,7 +55,7 @@ class Stats(ctypes.Structure):
         ("kernel_rank", ctypes.c_int32),
         ("launches_per_step", ctypes.c_int32),
         ("tile_rows", ctypes.c_int32 * 3),
-        ("reserved", ctypes.c_int32),
+        ("fused_step", ctypes.c_int32),
         ("message_floats", ctypes.c_int64),
     ]
 
@@ -61,7 +63,9 @@ class Stats(ctypes.Structure):
 class Options(ctypes.Structure):
     _fields_ = [("timing", ctypes.c_int32), ("project_rows", ctypes.c_int32), ("unbiased", ctypes.c_int32),
                 ("compressor", ctypes.c_int32), ("rtopk_top_div", ctypes.c_int32),
-                ("rtopk_sample_div", ctypes.c_int32)]
+                ("rtopk_sample_div", ctypes.c_int32), ("fused", ctypes.c_int32), ("wait_ms", ctypes.c_int32),
+                ("queue_lag_kb", ctypes.c_int32), ("test_stall", ctypes.c_int32),
+                ("total_workers", ctypes.c_int32)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -97,6 +101,12 @@ def lib() -> ctypes.CDLL:
         "psgd_layer_info": ([_P, ctypes.c_int, _I64P, _I64P, _I64P, _I64P], ctypes.c_int),
         "psgd_plan_layout": ([ctypes.c_int, _I64P, _I64P, _I64P, _I64P, _I64P], ctypes.c_int),
         "psgd_count_sent": ([ctypes.c_int, _I64P, _I64P, ctypes.c_int, _I64P, _I64P], ctypes.c_int),
+        "psgd_exchange_sizes": ([_P, _I64P, _I64P], ctypes.c_int),
+        "psgd_step_begin": ([_P, ctypes.POINTER(_P), _P], ctypes.c_int),
+        "psgd_step_mid": ([_P, _P, _P], ctypes.c_int),
+        "psgd_step_end": ([_P, _P, _P], ctypes.c_int),
+        "psgd_plan_queue": ([ctypes.c_int, _I64P, _I64P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                             ctypes.c_int, ctypes.POINTER(ctypes.c_int32), _I64P], ctypes.c_int),
         "psgd_last_error": ([], ctypes.c_char_p),
         "psgd_version": ([], ctypes.c_char_p),
         "psgd_get_phase_times": ([_P, ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
@@ -145,6 +155,25 @@ def psgd_count_sent(shapes: Sequence[Tuple[int, int]], rank: int) -> Tuple[int, 
     return c.value, u.value
 
 
+def psgd_plan_queue(shapes: Sequence[Tuple[int, int]], rank: int, workers: int, project_rows: int = 0,
+                    lag_bytes: int = 0, with_update: bool = True) -> List[Tuple[int, int, int, int, int]]:
+    """The fused step's queue for a layer set, needs no GPU: a list of
+    (phase, matrix or vector index, a, b, c) in queue order (see
+    psgd_plan_queue in include/psgd.h)."""
+    n, m = _shapes(shapes)
+    cnt = ctypes.c_int64()
+    _check(lib().psgd_plan_queue(len(shapes), n, m, rank, workers, project_rows, lag_bytes, int(with_update), None,
+                                 ctypes.byref(cnt)))
+    buf = (ctypes.c_int32 * (4 * cnt.value))()
+    _check(lib().psgd_plan_queue(len(shapes), n, m, rank, workers, project_rows, lag_bytes, int(with_update), buf,
+                                 ctypes.byref(cnt)))
+    out = []
+    for i in range(cnt.value):
+        lay, a, b, c = buf[4 * i:4 * i + 4]
+        out.append((lay >> 24, lay & 0xFFFFFF, a, b, c))
+    return out
+
+
 def _stream_ptr(stream) -> Optional[int]:
     if stream is None:
         import torch
@@ -168,7 +197,9 @@ class PowerSGD:
 
     def __init__(self, shapes: Sequence[Tuple[int, int]], rank: int, workers: int, seed: int = 0,
                  stream=None, timing: bool = False, project_rows: int = 0, unbiased: bool = False,
-                 compressor: str = "powersgd", top_div: int = 100, sample_div: int = 4):
+                 compressor: str = "powersgd", top_div: int = 100, sample_div: int = 4,
+                 fused: bool = False, wait_ms: int = 0, queue_lag_kb: int = 0, test_stall: int = 0,
+                 total_workers: int = 0):
         import torch
 
         if not torch.cuda.is_available():
@@ -181,7 +212,9 @@ class PowerSGD:
         if compressor not in ("powersgd", "rtopk"):
             raise ValueError(f"unknown compressor {compressor!r}")
         opt = Options(int(bool(timing)), int(project_rows), int(bool(unbiased)),
-                      PSGD_RTOPK if compressor == "rtopk" else PSGD_POWERSGD, int(top_div), int(sample_div))
+                      PSGD_RTOPK if compressor == "rtopk" else PSGD_POWERSGD, int(top_div), int(sample_div),
+                      int(bool(fused)), int(wait_ms), int(queue_lag_kb), int(test_stall),
+                      int(total_workers))
         h = _P()
         _check(lib().psgd_create_ex(ctypes.byref(h), len(self.shapes), n, m, self.rank, self.workers,
                                     ctypes.c_uint64(self.seed), _stream_ptr(stream), ctypes.byref(opt)))
@@ -248,6 +281,48 @@ class PowerSGD:
         ptrs = (_P * self.workers)(*[_ptr(g) for g in grads_host])
         _check(lib().psgd_step_host(self._h, ptrs, _ptr(msg_host), _ptr(update_host)))
 
+    # -- the split step (workers spread over processes)
+    def exchange_sizes(self) -> Tuple[int, int]:
+        """Floats of the two exchange buffers of a split step (P, then Q + vectors)."""
+        p, q = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().psgd_exchange_sizes(self._h, ctypes.byref(p), ctypes.byref(q)))
+        return p.value, q.value
+
+    def step_begin(self, grads: Sequence, p_out) -> None:
+        if len(grads) != self.workers:
+            raise ValueError(f"expected {self.workers} gradient buffers, got {len(grads)}")
+        self._split_grads = list(grads)  # kept alive until step_end
+        ptrs = (_P * self.workers)(*[_ptr(g) for g in grads])
+        _check(lib().psgd_step_begin(self._h, ptrs, _ptr(p_out)))
+
+    def step_mid(self, p_sum, q_out) -> None:
+        _check(lib().psgd_step_mid(self._h, _ptr(p_sum), _ptr(q_out)))
+
+    def step_end(self, q_sum, out_update=None) -> None:
+        _check(lib().psgd_step_end(self._h, _ptr(q_sum), _ptr(out_update)))
+        self._split_grads = None
+
+    def step_split(self, grads: Sequence, out_update=None, all_reduce=None) -> None:
+        """One step whose workers span processes: all_reduce(t) must sum the
+        float32 device tensor t in place over the processes (for example
+        torch.distributed.all_reduce); None means one process.  Runs on the
+        context's stream, which must be the one the collectives follow (the
+        current stream when the context was made with stream=None)."""
+        import torch
+        if getattr(self, "_xbufs", None) is None:
+            p, q = self.exchange_sizes()
+            self._xbufs = (torch.empty(max(p, 1), dtype=torch.float32, device=self.device),
+                           torch.empty(max(q, 1), dtype=torch.float32, device=self.device))
+        xp, xq = self._xbufs
+        p, q = self.exchange_sizes()
+        self.step_begin(grads, xp)
+        if all_reduce is not None and p:
+            all_reduce(xp[:p])
+        self.step_mid(xp, xq)
+        if all_reduce is not None and q:
+            all_reduce(xq[:q])
+        self.step_end(xq, out_update)
+
     def sync(self) -> None:
         _check(lib().psgd_sync(self._h))
 
@@ -310,10 +385,18 @@ class PowerSGD:
         _check(lib().psgd_set_timing(self._h, 1 if on else 0))
 
     def phase_times(self) -> dict:
-        """Device milliseconds of each phase of the last step (context created with timing=True)."""
+        """Device milliseconds of each phase, averaged over the steps since the
+        last call (timing on); a fused step gives {"step": ms of the launch}."""
         ms = (ctypes.c_float * 4)()
         _check(lib().psgd_get_phase_times(self._h, ms))
+        if self.fused:
+            return {"step": ms[0]}
         return dict(zip(PHASES, list(ms)))
+
+    @property
+    def fused(self) -> bool:
+        """True when each step is one fused launch."""
+        return bool(self.stats()["fused_step"])
 
     @property
     def message_floats(self) -> int:

@@ -122,6 +122,42 @@ __global__ void pack_msg_kernel(float* dst, const float* Phat, const float* Qbar
   }
 }
 
+// One layer's block in an exchange buffer of the split step: the dense
+// rows x r block at dense_off <-> rows x RP at pad_off of P or Qbar (vec = 0),
+// or a vector layer's n floats <-> the packed gradient offset pad_off (vec = 1).
+struct XEntry {
+  int64_t pad_off, dense_off;
+  int32_t rows, vec;
+};
+
+// Split step exchange.  to_dense: matrix blocks from `padded` into `dense`;
+// vector blocks get qbar_scale * the sum of this process's gradients (their
+// share of the all-reduced mean).  !to_dense: matrix blocks from `dense` into
+// `padded`; vector blocks into the update a.U (when not NULL).  One
+// blockIdx.y per entry.
+__global__ void xchg_kernel(const StepArgs a, float* dense, float* padded, const XEntry* ent, int r, int rp,
+                            int to_dense) {
+  const XEntry e = ent[blockIdx.y];
+  const int64_t cnt = e.vec ? (int64_t)e.rows : (int64_t)e.rows * r;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < cnt; i += (int64_t)gridDim.x * blockDim.x) {
+    if (e.vec) {
+      if (to_dense) {
+        float sum = 0.f;
+        for (int w = 0; w < a.W; ++w) sum += a.G[w][e.pad_off + i];
+        dense[e.dense_off + i] = sum * a.qbar_scale;
+      } else if (a.U) {
+        a.U[e.pad_off + i] = dense[e.dense_off + i];
+      }
+      continue;
+    }
+    float* pp = padded + e.pad_off + (i / r) * rp + (i % r);
+    if (to_dense)
+      dense[e.dense_off + i] = *pp;
+    else
+      *pp = dense[e.dense_off + i];
+  }
+}
+
 }  // namespace
 
 struct psgd_ctx {
@@ -162,6 +198,29 @@ struct psgd_ctx {
   RTopK* rk = nullptr;    // psgd_options.compressor == PSGD_RTOPK: the rTop-k plan
   int top_div = 0, sample_div = 0;
   bool broken = false;
+  // the fused step (padded rank <= 4, PowerSGD): queues without [0] and with
+  // [1] the decompress tiles, flags, ticket / status words, CTAs per launch
+  bool fused = false;
+  std::vector<Tile> queue[2];
+  Tile* d_queue[2] = {nullptr, nullptr};
+  unsigned* flags = nullptr;
+  unsigned* sync_words = nullptr;
+  int64_t n_flags = 0;
+  int fused_ctas = 0;
+  int64_t wait_ns = 2000000000LL;
+  int stall_layer = -1;
+  // the split step (psgd_step_begin / mid / end): workers over all
+  // processes, where the step stands (0 idle, 1 after begin, 2 after mid),
+  // the gradients of begin, the Gram tiles, the decompress tiles of the
+  // matrix layers, and the exchange layouts of P and of Q (+ vector sums)
+  int total_workers = 0;
+  int split_phase = 0;
+  std::vector<const float*> split_grads;
+  std::vector<Tile> gram_tiles, mat_u_tiles;
+  std::vector<XEntry> xp, xq;
+  Tile *d_gram_tiles = nullptr, *d_mat_u_tiles = nullptr;
+  XEntry *d_xp = nullptr, *d_xq = nullptr;
+  int64_t xp_floats = 0, xq_floats = 0;
   // stats
   int64_t steps = 0, sent_step = 0, unc_step = 0, mat_el = 0, vec_el = 0;
 };
@@ -171,7 +230,8 @@ namespace {
 void free_all(psgd_ctx* c) {
   void* ptrs[] = {c->B, c->P, c->Phat, c->Qbar, c->Qw, c->qpart, c->ppart, c->gram, c->rinv, c->counters,
                   c->d_layers, c->d_vecs, c->d_tiles[0], c->d_tiles[1], c->d_tiles[2], c->d_tiles[3], c->d_pack,
-                  c->e_scratch, c->stage_G, c->stage_U, c->stage_msg};
+                  c->e_scratch, c->stage_G, c->stage_U, c->stage_msg, c->d_queue[0], c->d_queue[1], c->flags,
+                  c->sync_words, c->d_gram_tiles, c->d_mat_u_tiles, c->d_xp, c->d_xq};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   rtopk_destroy(c->rk);
@@ -202,7 +262,7 @@ void build_tiles(psgd_ctx* c) {
     const LayerDev& L = c->hl[li];
     for (int rb = 0; rb < L.nrb; ++rb)
       for (int s = 0; s < L.S; ++s) c->tiles[kProject].push_back({li, rb, s, 0});
-    for (int t = 0; t < (int)ceil_div(L.n, kPHThreads); ++t) c->tiles[kOrthonormalise].push_back({li, t, 0, 0});
+    for (int t = 0; t < L.nph; ++t) c->tiles[kOrthonormalise].push_back({li, t, 0, 0});
     for (int rb = 0; rb < (int)ceil_div(L.n, L.ru); ++rb)
       for (int s = 0; s < L.S; ++s) c->tiles[kDecompress].push_back({li, rb, s, 0});
   }
@@ -238,7 +298,44 @@ int sync_and_check(psgd_ctx* c) {
     c->broken = true;
     return cuda_fail(e, "step");
   }
+  if (c->steps > 0) {
+    unsigned status = 0;
+    e = cudaMemcpy(&status, c->sync_words + 2, sizeof(status), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+      c->broken = true;
+      return cuda_fail(e, "step status");
+    }
+    if (status == 2) {
+      c->broken = true;
+      return fail(PSGD_ERR_TIMEOUT, "a step was abandoned: a wait for the tensor cores ran out");
+    }
+    if (status != 0) {
+      c->broken = true;
+      return fail(PSGD_ERR_TIMEOUT, "a fused step was abandoned: a tile waited longer than %lld ms for its inputs",
+                  (long long)(c->wait_ns / 1000000));
+    }
+  }
   return PSGD_OK;
+}
+
+// Tiles per layer phase and the fused queues of a context (all matrix
+// layers and vector chunks, with and without the decompress tiles).
+void build_queues(psgd_ctx* c, int64_t lag) {
+  std::vector<Tile> vec_tiles;
+  for (const Tile& t : c->tiles[kDecompress])
+    if (t.c == 1) vec_tiles.push_back(t);
+  c->queue[0] = build_queue(c->hl, vec_tiles, c->W, lag, false);
+  c->queue[1] = build_queue(c->hl, vec_tiles, c->W, lag, true);
+}
+
+// The default lag between a layer's phases in the fused queue: twice what
+// the resident CTAs of the fused step have in flight, one average project
+// tile each.
+int64_t default_lag(const psgd_ctx* c, int ctas) {
+  int64_t bytes = 0;
+  for (const Tile& t : c->tiles[kProject]) bytes += tile_bytes(c->hl[t.layer], kProject, t, c->W);
+  const int64_t nt = std::max<int64_t>(1, (int64_t)c->tiles[kProject].size());
+  return 2 * (int64_t)ctas * (bytes / nt);
 }
 
 }  // namespace
@@ -279,6 +376,50 @@ int psgd_count_sent(int num_layers, const int64_t* n, const int64_t* m, int rank
   return PSGD_OK;
 }
 
+int psgd_plan_queue(int num_layers, const int64_t* n, const int64_t* m, int rank, int num_workers,
+                    int project_rows, int64_t lag_bytes, int with_update, int32_t* items, int64_t* count) {
+  int rc = check_layers(num_layers, n, m);
+  if (rc) return rc;
+  if (rank < 1 || rank > 32) return fail(PSGD_ERR_INVALID, "rank must be in [1, 32] (got %d)", rank);
+  if (num_workers < 1 || num_workers > kMaxWorkers)
+    return fail(PSGD_ERR_INVALID, "num_workers must be in [1, %d] (got %d)", kMaxWorkers, num_workers);
+  if (!count) return fail(PSGD_ERR_INVALID, "count must not be NULL");
+  const int rp = padded_rank(rank);
+  const KernelSet* ks = kernels_for(rp);
+  if (project_rows < 0 || project_rows > ks->r1) return fail(PSGD_ERR_INVALID, "project_rows out of range");
+  TileRows tr;
+  tr.r1 = project_rows > 0 ? project_rows : ks->r1;
+  tr.ru = ks->ru;
+  std::vector<int64_t> off(num_layers), ld(num_layers);
+  int64_t total = 0;
+  layout(num_layers, n, m, off.data(), ld.data(), &total);
+  std::vector<LayerDev> hl;
+  std::vector<Tile> vec_tiles;
+  int nv = 0;
+  for (int l = 0; l < num_layers; ++l) {
+    if (m[l] == 0) {
+      for (int t = 0; t < (int)ceil_div(n[l], kVChunk); ++t) vec_tiles.push_back({nv, t, 0, 1});
+      ++nv;
+      continue;
+    }
+    LayerDev L;
+    std::memset(&L, 0, sizeof(L));
+    plan_matrix(L, n[l], m[l], ld[l], rp, num_workers, tr);
+    L.index = l;
+    hl.push_back(L);
+  }
+  const std::vector<Tile> q = build_queue(hl, vec_tiles, num_workers, std::max<int64_t>(0, lag_bytes), with_update != 0);
+  *count = (int64_t)q.size();
+  if (items)
+    for (size_t i = 0; i < q.size(); ++i) {
+      items[4 * i] = q[i].layer;
+      items[4 * i + 1] = q[i].a;
+      items[4 * i + 2] = q[i].b;
+      items[4 * i + 3] = q[i].c;
+    }
+  return PSGD_OK;
+}
+
 int psgd_create(psgd_ctx** out, int num_layers, const int64_t* n, const int64_t* m, int rank, int num_workers,
                 uint64_t seed, void* cuda_stream) {
   return psgd_create_ex(out, num_layers, n, m, rank, num_workers, seed, cuda_stream, nullptr);
@@ -308,6 +449,7 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   c->ks = kernels_for(c->rp);
   c->timing = opt && opt->timing;
   c->unbiased = opt && opt->unbiased;
+  c->total_workers = (opt && opt->total_workers > 0) ? opt->total_workers : num_workers;
   const bool rtopk = opt && opt->compressor == PSGD_RTOPK;
   if (opt && opt->compressor != PSGD_POWERSGD && !rtopk) {
     delete c;
@@ -320,6 +462,10 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   if (rtopk) {
     c->top_div = opt->rtopk_top_div;
     c->sample_div = opt->rtopk_sample_div;
+  }
+  if (c->total_workers < num_workers || (c->total_workers != num_workers && (rtopk || c->unbiased))) {
+    delete c;
+    return fail(PSGD_ERR_INVALID, "total_workers must be >= num_workers, and is for PowerSGD only");
   }
   if (cudaGetDevice(&c->device) != cudaSuccess) {
     cudaGetLastError();
@@ -336,10 +482,30 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   const int rp = c->rp;
   const int NG = rp * (rp + 1) / 2;
   TileRows tr;
+  // the kernels' shared-memory limits first: the occupancy the tile planner
+  // reads depends on them (above 48 KB of dynamic shared memory a kernel
+  // reports no resident CTAs until its limit is raised)
+  {
+    cudaError_t e = c->ks->prepare();
+    if (e != cudaSuccess) {
+      delete c;
+      return cuda_fail(e, "kernel attributes");
+    }
+  }
   if ((rc = choose_tile_rows(c->n, c->m, rp, c->W, *c->ks, c->device, &tr))) {
     delete c;
     return rc;
   }
+  // the fused step takes its tiles from a queue, with no phase tail to fill:
+  // the largest project tiles halve the number of tiles it runs
+  if (c->ks->launch_fused && !c->unbiased && !rtopk && opt && opt->fused && c->total_workers == c->W)
+    tr.r1 = c->ks->r1;
+  const bool mma = c->ks->mma_rows > 0 && !c->unbiased && !rtopk;
+  if (mma && opt && opt->project_rows > 0) {
+    delete c;
+    return fail(PSGD_ERR_INVALID, "project_rows is fixed at %d rows for the tensor-core project tiles", c->ks->mma_rows);
+  }
+  if (mma) tr.r1 = c->ks->mma_rows;
   if (opt && opt->project_rows > 0) {
     if (opt->project_rows > c->ks->r1 || opt->project_rows % c->ks->rsb != 0) {
       delete c;
@@ -368,15 +534,17 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     L.q_off = c->q_total;
     c->q_total += c->ld[l] * rp;
     L.gram_off = c->gram_total;
-    c->gram_total += (int64_t)(L.nrb + L.g1) * NG;
+    c->gram_total += (int64_t)(L.nrb + L.g1 + L.nph) * NG;
     L.rinv_off = c->rinv_total;
-    c->rinv_total += (int64_t)rp * rp + rp;
+    c->rinv_total += rinv_len(rp);
     L.qpart_off = c->qpart_total;
     c->qpart_total += (int64_t)L.t3r * c->W * c->ld[l] * rp;
     L.ppart_off = c->ppart_total;
-    if (L.S > 1) c->ppart_total += (int64_t)L.nrb * L.S * c->ks->r1 * rp;
+    if (L.S > 1) c->ppart_total += (int64_t)L.nrb * L.S * L.r1 * rp;
     L.cnt_off = (int32_t)c->n_counters;
     c->n_counters += ncnt;
+    L.f_off = (int32_t)c->n_flags;
+    c->n_flags += kFlagQbar + L.S;
     // the message: Phat and Qbar; the unbiased variant sends P alone;
     // rTop-k: k indices and k values per worker
     int64_t sent = c->unbiased ? n[l] * rank : (n[l] + m[l]) * rank;
@@ -390,6 +558,43 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     c->unc_step += n[l] * m[l];
   }
   build_tiles(c);
+  // the fused step: PowerSGD at padded rank <= 4 with at least one matrix
+  c->fused = c->ks->launch_fused && !c->unbiased && !rtopk && opt && opt->fused && !c->hl.empty() &&
+             c->total_workers == c->W;
+  // the split step's tiles and exchange layouts
+  for (const Tile& t : c->tiles[kProject])
+    if (t.b == 0) c->gram_tiles.push_back(t);
+  for (const Tile& t : c->tiles[kDecompress])
+    if (t.c == 0) c->mat_u_tiles.push_back(t);
+  for (int l = 0; l < num_layers; ++l) {
+    if (m[l] == 0) continue;
+    const LayerDev& L = c->hl[c->mat_of[l]];
+    c->xp.push_back({L.p_off, c->xp_floats, L.n, 0});
+    c->xp_floats += (int64_t)L.n * rank;
+    c->xq.push_back({L.q_off, c->xq_floats, L.m, 0});
+    c->xq_floats += (int64_t)L.m * rank;
+  }
+  for (int l = 0; l < num_layers; ++l)
+    if (m[l] == 0) {
+      c->xq.push_back({c->off[l], c->xq_floats, (int32_t)n[l], 1});
+      c->xq_floats += n[l];
+    }
+  if (opt && opt->wait_ms > 0) c->wait_ns = (int64_t)opt->wait_ms * 1000000;
+  if (opt && opt->test_stall > 0 && !c->hl.empty())
+    c->stall_layer = c->hl[std::min<int>(opt->test_stall - 1, (int)c->hl.size() - 1)].index;
+  if (c->fused) {
+    int per_sm = 0, sms = 0;
+    cudaError_t e = c->ks->occupancy_fused(&per_sm);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (e != cudaSuccess) {
+      delete c;
+      return cuda_fail(e, "fused step occupancy");
+    }
+    const int resident = std::max(1, per_sm * sms);
+    const int64_t lag = (opt && opt->queue_lag_kb > 0) ? (int64_t)opt->queue_lag_kb * 1024 : default_lag(c, resident);
+    build_queues(c, lag);
+    c->fused_ctas = resident;
+  }
 
   const int W = c->W;
   rc = PSGD_OK;
@@ -409,6 +614,16 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   ALLOC(d_vecs, (int64_t)c->hv.size());
   for (int ph = 0; ph < kPhases; ++ph) ALLOC(d_tiles[ph], (int64_t)c->tiles[ph].size());
   ALLOC(d_pack, (int64_t)c->pack.size());
+  ALLOC(d_gram_tiles, (int64_t)c->gram_tiles.size());
+  ALLOC(d_mat_u_tiles, (int64_t)c->mat_u_tiles.size());
+  ALLOC(d_xp, (int64_t)c->xp.size());
+  ALLOC(d_xq, (int64_t)c->xq.size());
+  ALLOC(sync_words, 4);
+  if (c->fused) {
+    ALLOC(d_queue[0], (int64_t)c->queue[0].size());
+    ALLOC(d_queue[1], (int64_t)c->queue[1].size());
+    ALLOC(flags, c->n_flags);
+  }
 #undef ALLOC
   if (rc) {
     free_all(c);
@@ -417,7 +632,6 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   }
   auto setup = [&]() -> int {
     cudaStream_t s = c->stream;
-    CUDA_TRY(c->ks->prepare());
     if (c->timing) {
       c->ev.assign((size_t)kTimedSteps * (kPhases + 1), nullptr);
       for (auto& e : c->ev) CUDA_TRY(cudaEventCreate(&e));
@@ -439,6 +653,23 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     if (!c->pack.empty())
       CUDA_TRY(cudaMemcpyAsync(c->d_pack, c->pack.data(), c->pack.size() * sizeof(PackEntry),
                                cudaMemcpyHostToDevice, s));
+    auto up = [&](void* dst, const void* src, size_t bytes) -> int {
+      if (bytes) CUDA_TRY(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s));
+      return PSGD_OK;
+    };
+    int rcu = up(c->d_gram_tiles, c->gram_tiles.data(), c->gram_tiles.size() * sizeof(Tile));
+    if (!rcu) rcu = up(c->d_mat_u_tiles, c->mat_u_tiles.data(), c->mat_u_tiles.size() * sizeof(Tile));
+    if (!rcu) rcu = up(c->d_xp, c->xp.data(), c->xp.size() * sizeof(XEntry));
+    if (!rcu) rcu = up(c->d_xq, c->xq.data(), c->xq.size() * sizeof(XEntry));
+    if (rcu) return rcu;
+    if (c->fused) {
+      for (int q = 0; q < 2; ++q)
+        if (!c->queue[q].empty())
+          CUDA_TRY(cudaMemcpyAsync(c->d_queue[q], c->queue[q].data(), c->queue[q].size() * sizeof(Tile),
+                                   cudaMemcpyHostToDevice, s));
+      CUDA_TRY(cudaMemsetAsync(c->flags, 0, (size_t)c->n_flags * sizeof(unsigned), s));
+    }
+    CUDA_TRY(cudaMemsetAsync(c->sync_words, 0, 4 * sizeof(unsigned), s));
     if (!c->hl.empty()) {
       dim3 grid(64, (unsigned)c->hl.size());
       q_init_kernel<<<grid, 256, 0, s>>>(c->Qbar, c->d_layers, c->rank, c->rp, c->seed);
@@ -481,12 +712,10 @@ namespace {
 
 // One step; when X is not NULL the decompress phase also applies the
 // momentum-SGD update to X and Mom.
-int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, float* X, float* Mom, float lr,
-              float beta) {
-  int rc = ctx_ok(c);
-  if (rc) return rc;
+// The kernel arguments of a step of context c (checked gradient pointers,
+// the context's buffers); the caller sets the optional update fields.
+int make_args(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, StepArgs& a) {
   if (!grad_ptrs) return fail(PSGD_ERR_INVALID, "grad_ptrs must not be NULL");
-  StepArgs a;
   std::memset(&a, 0, sizeof(a));
   for (int w = 0; w < c->W; ++w) {
     if (!grad_ptrs[w]) return fail(PSGD_ERR_INVALID, "grad_ptrs[%d] is NULL", w);
@@ -511,12 +740,26 @@ int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, flo
   a.vecs = c->d_vecs;
   a.W = c->W;
   a.has_prev = c->has_prev;
+  a.unbiased = c->unbiased ? 1 : 0;
+  a.u_scale = 1.0f / ((float)c->W * (float)c->rank);
+  a.stall_layer = -1;
+  a.qbar_scale = 1.0f / (float)c->total_workers;
+  a.sync = c->sync_words;
+  return PSGD_OK;
+}
+
+int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, float* X, float* Mom, float lr,
+              float beta) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  if (c->total_workers != c->W)
+    return fail(PSGD_ERR_INVALID, "the workers of this context span processes: use psgd_step_begin/mid/end");
+  StepArgs a;
+  if ((rc = make_args(c, grad_ptrs, out_update, a))) return rc;
   a.X = X;
   a.Mom = Mom;
   a.lr = lr;
   a.beta = beta;
-  a.unbiased = c->unbiased ? 1 : 0;
-  a.u_scale = 1.0f / ((float)c->W * (float)c->rank);
   // the decompress phase only writes U and the optional update
   const int phases = (out_update || X) ? kPhases : kPhases - 1;
   cudaEvent_t* ev = nullptr;
@@ -546,6 +789,26 @@ int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, flo
       c->broken = true;
       return cuda_fail(e, "Q draw launch");
     }
+  }
+  if (c->fused) {
+    const int q = (out_update || X) ? 1 : 0;
+    a.tiles = c->d_queue[q];
+    a.n_items = (int32_t)c->queue[q].size();
+    a.flags = c->flags;
+    a.sync = c->sync_words;
+    a.epoch = (uint32_t)(c->steps + 1);
+    a.wait_ns = c->wait_ns;
+    a.stall_layer = c->stall_layer;
+    cudaError_t e = c->ks->launch_fused(a, std::min<int>(c->fused_ctas, a.n_items), c->stream);
+    if (e != cudaSuccess) {
+      c->broken = true;
+      return cuda_fail(e, "fused step launch");
+    }
+    if (ev)
+      for (int ph = 0; ph < kPhases; ++ph) CUDA_TRY(cudaEventRecord(ev[ph + 1], c->stream));
+    c->has_prev = 1;
+    c->steps += 1;
+    return PSGD_OK;
   }
   for (int ph = 0; ph < kPhases; ++ph) {
     const bool skip = c->unbiased && (ph == kOrthonormalise || ph == kBackProject);
@@ -579,6 +842,101 @@ int psgd_step_momentum(psgd_ctx* c, const float* const* grad_ptrs, float* params
     return fail(PSGD_ERR_INVALID, "params and momentum must be 16-byte aligned");
   if (!std::isfinite(lr) || !std::isfinite(beta)) return fail(PSGD_ERR_INVALID, "lr and beta must be finite");
   return step_impl(c, grad_ptrs, out_update, params, momentum, lr, beta);
+}
+
+int psgd_exchange_sizes(const psgd_ctx* c, int64_t* p_floats, int64_t* q_floats) {
+  if (!c) return fail(PSGD_ERR_INVALID, "context is NULL");
+  if (p_floats) *p_floats = c->xp_floats;
+  if (q_floats) *q_floats = c->xq_floats;
+  return PSGD_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+int split_ok(psgd_ctx* c, int phase, const char* what) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  if (c->rk || c->unbiased) return fail(PSGD_ERR_INVALID, "%s: the split step is for PowerSGD contexts", what);
+  if (c->split_phase != phase)
+    return fail(PSGD_ERR_INVALID, "%s called out of order (begin, mid, end)", what);
+  return PSGD_OK;
+}
+
+int xchg(psgd_ctx* c, const StepArgs& a, float* dense, float* padded, const std::vector<XEntry>& ent,
+         const XEntry* d_ent, int to_dense) {
+  if (ent.empty()) return PSGD_OK;
+  dim3 grid(16, (unsigned)ent.size());
+  xchg_kernel<<<grid, 256, 0, c->stream>>>(a, dense, padded, d_ent, c->rank, c->rp, to_dense);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    c->broken = true;
+    return cuda_fail(e, "exchange kernel");
+  }
+  return PSGD_OK;
+}
+
+int launch_phase(psgd_ctx* c, int phase, StepArgs& a, const Tile* tiles, int n) {
+  a.tiles = tiles;
+  cudaError_t e = (phase < 0) ? c->ks->launch_gram(a, n, c->stream) : c->ks->launch(phase, a, n, c->stream);
+  if (e != cudaSuccess) {
+    c->broken = true;
+    return cuda_fail(e, "phase kernel launch");
+  }
+  return PSGD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int psgd_step_begin(psgd_ctx* c, const float* const* grad_ptrs, float* p_out) {
+  int rc = split_ok(c, 0, "psgd_step_begin");
+  if (rc) return rc;
+  if (!p_out && c->xp_floats) return fail(PSGD_ERR_INVALID, "p_out must not be NULL");
+  StepArgs a;
+  if ((rc = make_args(c, grad_ptrs, nullptr, a))) return rc;
+  a.split = 1;
+  if ((rc = launch_phase(c, kProject, a, c->d_tiles[kProject], (int)c->tiles[kProject].size()))) return rc;
+  if ((rc = xchg(c, a, p_out, c->P, c->xp, c->d_xp, 1))) return rc;
+  c->split_grads.assign(grad_ptrs, grad_ptrs + c->W);
+  c->split_phase = 1;
+  return PSGD_OK;
+}
+
+int psgd_step_mid(psgd_ctx* c, const float* p_sum, float* q_out) {
+  int rc = split_ok(c, 1, "psgd_step_mid");
+  if (rc) return rc;
+  if ((!p_sum && c->xp_floats) || (!q_out && c->xq_floats))
+    return fail(PSGD_ERR_INVALID, "p_sum and q_out must not be NULL");
+  StepArgs a;
+  if ((rc = make_args(c, c->split_grads.data(), nullptr, a))) return rc;
+  if ((rc = xchg(c, a, const_cast<float*>(p_sum), c->P, c->xp, c->d_xp, 0))) return rc;
+  if ((rc = launch_phase(c, -1, a, c->d_gram_tiles, (int)c->gram_tiles.size()))) return rc;
+  if ((rc = launch_phase(c, kOrthonormalise, a, c->d_tiles[kOrthonormalise], (int)c->tiles[kOrthonormalise].size())))
+    return rc;
+  if ((rc = launch_phase(c, kBackProject, a, c->d_tiles[kBackProject], (int)c->tiles[kBackProject].size())))
+    return rc;
+  if ((rc = xchg(c, a, q_out, c->Qbar, c->xq, c->d_xq, 1))) return rc;
+  c->split_phase = 2;
+  return PSGD_OK;
+}
+
+int psgd_step_end(psgd_ctx* c, const float* q_sum, float* out_update) {
+  int rc = split_ok(c, 2, "psgd_step_end");
+  if (rc) return rc;
+  if (!q_sum && c->xq_floats) return fail(PSGD_ERR_INVALID, "q_sum must not be NULL");
+  StepArgs a;
+  if ((rc = make_args(c, c->split_grads.data(), out_update, a))) return rc;
+  if ((rc = xchg(c, a, const_cast<float*>(q_sum), c->Qbar, c->xq, c->d_xq, 0))) return rc;
+  if (out_update &&
+      (rc = launch_phase(c, kDecompress, a, c->d_mat_u_tiles, (int)c->mat_u_tiles.size())))
+    return rc;
+  c->split_phase = 0;
+  c->has_prev = 1;
+  c->steps += 1;
+  return PSGD_OK;
 }
 
 int psgd_sync(psgd_ctx* c) {
@@ -791,8 +1149,11 @@ int psgd_get_stats(const psgd_ctx* c, psgd_stats* out) {
   for (int ph = 0; ph < kPhases; ++ph) out->tiles[ph] = (int64_t)c->tiles[ph].size();
   out->kernel_rank = c->rp;
   for (int i = 0; i < 3; ++i) out->tile_rows[i] = c->tile_rows[i];
-  out->launches_per_step = kPhases;  // the unbiased variant: Q draw, project, decompress
+  out->launches_per_step = kPhases + (c->rp >= 8 ? 1 : 0);  // r >= 8: the second pass's Phat rows
+  // the unbiased variant: Q draw, project, decompress
   if (c->unbiased) out->launches_per_step = 3;
+  if (c->fused) out->launches_per_step = 1;
+  out->fused_step = c->fused ? 1 : 0;
   if (c->rk) out->launches_per_step = rtopk_launches(c->rk);
   out->message_floats = c->msg_floats;
   return PSGD_OK;

@@ -25,6 +25,15 @@ struct KernelSet {
   // tile geometry: most project rows per tile, most decompress rows per tile,
   // rows per project pass
   int r1, ru, rsb;
+  // the fused step (padded ranks <= 4; null above): one launch of `ctas` CTAs
+  // over a.n_items queue items, and its resident CTAs per SM
+  cudaError_t (*launch_fused)(const StepArgs& a, int ctas, cudaStream_t s);
+  cudaError_t (*occupancy_fused)(int* ctas_per_sm);
+  // split step: the Gram factor of an all-reduced P over `tiles` row blocks
+  cudaError_t (*launch_gram)(const StepArgs& a, int tiles, cudaStream_t s);
+  // the project phase runs on the tensor cores (padded ranks 16, 32; not the
+  // unbiased variant): its tiles have mma_rows rows
+  int mma_rows;
 };
 
 extern const KernelSet kKernelsR1, kKernelsR2, kKernelsR4, kKernelsR8, kKernelsR16, kKernelsR32;

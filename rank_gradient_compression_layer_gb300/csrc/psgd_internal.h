@@ -10,6 +10,15 @@ namespace psgd {
 constexpr int kMaxWorkers = 64;   // W limit (pointer table passed by value)
 constexpr int kSeg = 32;          // float4 columns per segment (one warp width)
 constexpr int kGramGroup = 32;    // project row blocks whose Gram partials one group sums
+// Rows of one orthonormalise tile (one thread per row): fewer at large r, so
+// that the tiles' float64 work (about r^2 per row) spreads over more SMs.
+constexpr int ph_rows(int rp) { return rp >= 32 ? 32 : (rp == 16 ? 64 : 128); }
+
+// Doubles per layer of the factor record: R of the first Cholesky-QR pass
+// (RP x RP, row-major) and 1 / diag R (RP); X = R2^-1 of the second pass
+// (RP x RP, upper triangular); a flag that is 1 when the first pass alone is
+// orthogonal enough (then Phat = P1 and X is not formed).
+constexpr int64_t rinv_len(int rp) { return 2 * (int64_t)rp * rp + rp + 1; }
 
 // One tile of a phase kernel (one CTA).  Meaning of the fields per phase:
 //   project:        layer, row block, segment
@@ -39,8 +48,8 @@ struct LayerDev {
   int64_t p_off;      // P and Phat: n x RP (16-byte aligned)
   int64_t q_off;      // Qbar: ld x RP; Q_w of worker w at w*q_total + q_off
   int64_t ppart_off;  // floats: nrb x S x R1 x RP partial P rows (S > 1)
-  int64_t gram_off;   // doubles: (nrb + g1) x NG partial Grams
-  int64_t rinv_off;   // doubles: RP x RP (R), RP (1 / diag R)
+  int64_t gram_off;   // doubles: (nrb + g1 + nph) x NG partial Grams (P, then P1)
+  int64_t rinv_off;   // doubles: rinv_len(RP), the factor record
   int64_t qpart_off;  // floats: t3r x W x ld x RP partial Q_w
   int32_t cnt_off;    // first counter of the layer; the others sit at cnt_off + c_*
   int32_t c_gram;     // Gram groups done (1)
@@ -48,7 +57,23 @@ struct LayerDev {
   int32_t c_qs;       // workers done per segment (S)
   int32_t c_p3;       // row tiles done per (segment, worker) (S x W)
   int32_t c_rb;       // segments done per row block (nrb, when S > 1)
+  int32_t nph;        // orthonormalise tiles (rph rows each)
+  int32_t c_ph;       // orthonormalise tiles done (1)
+  int32_t f_off;      // fused step: first of the layer's 2 + S flags (R ready, X ready, Qbar per segment)
+  int32_t rph;        // rows per orthonormalise tile (ph_rows)
 };
+
+// The fused step runs every phase's tiles from one queue; an item is a Tile
+// whose layer field carries the phase in its top byte.
+enum ItemKind : int32_t { kItemProject = 0, kItemOrtho = 1, kItemBack = 2, kItemDecomp = 3 };
+constexpr int32_t kLayerBits = 24;
+constexpr int32_t item_layer(int32_t kind, int32_t layer) { return (kind << kLayerBits) | layer; }
+
+// Flags of one matrix layer, relative to its f_off: each holds the number
+// (epoch) of the last step that raised it.
+constexpr int kFlagR = 0;     // R of the first Cholesky-QR pass stored
+constexpr int kFlagX = 1;     // X = R2^-1 stored: the back-project may start
+constexpr int kFlagQbar = 2;  // + segment: that segment's Qbar stored
 
 struct VecDev {
   int64_t off;
@@ -87,6 +112,22 @@ struct StepArgs {
   // (no Gram tail, no back-project), U = u_scale P Q^T with Q the step's draw
   int32_t unbiased;
   float u_scale;
+  // fused step: the queue in `tiles` (n_items items, in dependency order),
+  // the flags, and sync[0] = next ticket, sync[1] = CTAs finished,
+  // sync[2] = status (0: ok, else the step was abandoned after a wait ran
+  // past wait_ns); epoch = the value this step raises flags to
+  unsigned* flags;
+  unsigned* sync;
+  int32_t n_items;
+  uint32_t epoch;
+  int64_t wait_ns;
+  int32_t stall_layer;  // test hook: the R flag of this layer index is never raised (-1: none)
+  // split step (workers spread over processes): the project phase stops
+  // after writing this process's P (the sum over its workers; the Gram
+  // factor follows once P has been all-reduced), and Qbar is
+  // qbar_scale * sum over this process's workers of Q_w (1 / W in one process)
+  int32_t split;
+  float qbar_scale;
 };
 
 }  // namespace psgd

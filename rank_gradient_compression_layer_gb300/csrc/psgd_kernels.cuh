@@ -9,12 +9,19 @@
 //                   block writes its P rows and their Gram partial P^T P
 //                   (float64); the CTA that completes a layer sums the Gram
 //                   (fixed order), factors A = R^T R (Cholesky, float64) and
-//                   stores R: Phat = P R^-1 is the Gram-Schmidt basis of P.
-//   orthonormalise  Phat rows: forward substitution Phat R = P (float64); for
-//                   r <= 8 done by the back-project tiles themselves.
+//                   stores R: P R^-1 is the Gram-Schmidt basis of P.
+//   orthonormalise  Cholesky-QR2: rows P1 = P R^-1 by forward substitution
+//                   (float64, rounded to float32, stored over P); the CTA
+//                   that completes the layer factors the Gram matrix of P1
+//                   the same way and stores X = R2^-1, so Phat = P1 X.  The
+//                   second pass restores the orthogonality that one pass
+//                   loses when P is ill-conditioned (a warm-started Q whose
+//                   last columns carry little of M).
 //   back-project    partial Q_w = M_w^T Phat over a row tile of one segment
-//                   and one worker; the CTA that completes (segment, worker)
-//                   sums the partials (fixed order) into Q_w, and the one that
+//                   and one worker, with the Phat rows formed from P1 and X
+//                   as they are staged (one tile per row tile stores them);
+//                   the CTA that completes (segment, worker) sums the
+//                   partials (fixed order) into Q_w, and the one that
 //                   completes the segment forms Qbar = mean_w Q_w.
 //   decompress      U rows = Phat Qbar^T; vector layers U = mean_w G_w.
 //
@@ -55,8 +62,9 @@ struct Cfg {
 constexpr int kP1TRow = kSeg * 4 + 4;  // tiled project: shared row stride of the staged Q rows (floats)
 constexpr int kP3Threads = 256;
 constexpr int kUThreads = 256;
-constexpr int kPHThreads = 128;
+
 constexpr int kVChunk = 8192;  // vector elements per decompress tile
+constexpr int kGramThreads = 128;  // split step: threads of a Gram tile
 constexpr unsigned kFull = 0xffffffffu;
 
 // ----------------------------------------------------------------------------
@@ -154,6 +162,15 @@ __device__ __forceinline__ bool cta_arrive_last(unsigned* cnt, unsigned total, i
   return last;
 }
 
+// Fused step: publish that what this CTA (or warp) wrote before is complete
+// by raising *f to the step's epoch.  The caller has ordered the writes
+// before this thread (barrier or __syncwarp); the fence makes them visible
+// at GPU scope before the release store.
+__device__ __forceinline__ void flag_raise(unsigned* f, unsigned epoch) {
+  __threadfence();
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(epoch) : "memory");
+}
+
 // ----------------------------------------------------------------------------
 // Gram-Schmidt coefficients from the Gram matrix (float64, warp-parallel)
 // ----------------------------------------------------------------------------
@@ -199,11 +216,39 @@ __device__ void warp_cholesky(const double* A, double* out) {
   }
 }
 
+// Upper-triangular inverse X = R^-1 of the factor warp_cholesky left in
+// fr (R row-major, then 1 / diag R), written to X (row-major).  Lane k < RP
+// forms row k: X_kk = 1 / R_kk, X_kj = -(sum_{k <= l < j} X_kl R_lj) / R_jj.
+// A column whose pivot was marked degenerate (1 / R_jj = 0) comes out zero.
+template <int RP>
+__device__ void warp_tri_inverse(const double* fr, double* X) {
+  const int k = threadIdx.x & 31;
+  if (k >= RP) return;
+  double x[RP];
+#pragma unroll
+  for (int j = 0; j < RP; ++j) x[j] = 0.0;
+#pragma unroll
+  for (int j = 0; j < RP; ++j) {
+    if (j == k) {
+      x[j] = fr[RP * RP + j];
+    } else if (j > k) {
+      double s = 0.0;
+#pragma unroll
+      for (int l = 0; l < j; ++l)
+        if (l >= k) s = fma(x[l], fr[l * RP + j], s);
+      x[j] = -s * fr[RP * RP + j];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < RP; ++j) X[k * RP + j] = x[j];
+}
+
 // CTA that completed row block rb of layer L (P rows in s_prow): Gram partial
 // of the rows, then the fixed-order group and layer sums, then the factor.
+// pub (fused step only): the layer's R flag, raised once R is stored.
 template <int RP>
 __device__ void gram_tail(const StepArgs& a, const LayerDev& L, int rb, const float* s_prow, int nrows,
-                          double* s_gram, int* s_flag) {
+                          double* s_gram, int* s_flag, unsigned* pub) {
   constexpr int NG = Cfg<RP>::NG;
   unsigned* cnt = a.counters + L.cnt_off;
   double* gp = a.gram + L.gram_off;
@@ -232,7 +277,32 @@ __device__ void gram_tail(const StepArgs& a, const LayerDev& L, int rb, const fl
     s_gram[j * RP + i] = s;
   }
   __syncthreads();
-  if (threadIdx.x < 32) warp_cholesky<RP>(s_gram, a.rinv + L.rinv_off);
+  if (threadIdx.x < 32) {
+    double* fr = a.rinv + L.rinv_off;
+    warp_cholesky<RP>(s_gram, fr);
+    __syncwarp();
+    // Is one Cholesky-QR pass orthogonal enough?  Its loss of orthogonality
+    // is about kappa(P)^2 eps; kappa_F = ||R||_F ||R^-1||_F bounds kappa(P).
+    // At kappa_F <= 1e3 it is below 1e-9, far under Phat's float32 rounding,
+    // and the second pass is skipped (flag X = I, Phat = P1).
+    warp_tri_inverse<RP>(fr, s_gram);  // R^-1 (s_gram is free once the factor is taken)
+    __syncwarp();
+    double r2 = 0.0, x2 = 0.0;
+    for (int e = threadIdx.x; e < RP * RP; e += 32) {
+      r2 = fma(fr[e], fr[e], r2);
+      x2 = fma(s_gram[e], s_gram[e], x2);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      r2 += __shfl_xor_sync(kFull, r2, o);
+      x2 += __shfl_xor_sync(kFull, x2, o);
+    }
+    if (threadIdx.x == 0) fr[2 * RP * RP + RP] = (r2 * x2 <= 1e6) ? 1.0 : 0.0;
+    if (pub) {
+      __syncwarp();
+      if (threadIdx.x == 0 && L.index != a.stall_layer) flag_raise(pub, a.epoch);
+    }
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -354,108 +424,132 @@ __device__ __forceinline__ void p1_reduce(const P1Tile& T, float (&acc)[Cfg<RP>:
 // order); then P is written and the Gram tail runs.
 template <int RP>
 __device__ __forceinline__ void p1_rows_done(const StepArgs& a, const LayerDev& L, const P1Tile& T, float* s_prow,
-                                             double* s_gram, int* s_flag) {
+                                             double* s_gram, int* s_flag, unsigned* pub) {
   constexpr int R1 = Cfg<RP>::R1;
   if (L.S > 1) {
-    float* pp = a.ppart + L.ppart_off + ((int64_t)T.rb * L.S + T.seg) * R1 * RP;
+    float* pp = a.ppart + L.ppart_off + ((int64_t)T.rb * L.S + T.seg) * L.r1 * RP;
     for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) pp[idx] = s_prow[idx];
     if (!cta_arrive_last(a.counters + L.cnt_off + L.c_rb + T.rb, (unsigned)L.S, s_flag)) return;
-    const float* pb = a.ppart + L.ppart_off + (int64_t)T.rb * L.S * R1 * RP;
+    const float* pb = a.ppart + L.ppart_off + (int64_t)T.rb * L.S * L.r1 * RP;
     for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) {
       float s = 0.f;
-      for (int qq = 0; qq < L.S; ++qq) s += __ldcg(pb + (int64_t)qq * R1 * RP + idx);
+      for (int qq = 0; qq < L.S; ++qq) s += __ldcg(pb + (int64_t)qq * L.r1 * RP + idx);
       s_prow[idx] = s;
     }
     __syncthreads();
   }
   for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x)
     a.P[L.p_off + (int64_t)T.row0 * RP + idx] = s_prow[idx];
-  if (T.ub) return;  // the unbiased variant sends P as it is
-  gram_tail<RP>(a, L, T.rb, s_prow, T.rcnt, s_gram, s_flag);
+  if (T.ub || a.split) return;  // the unbiased variant sends P as it is; a split step all-reduces it first
+  gram_tail<RP>(a, L, T.rb, s_prow, T.rcnt, s_gram, s_flag, pub);
 }
 
-// The tile's P rows: fixed-order sum over the warps, then p1_rows_done.
+// One project tile.  The CTA's warps are split into row groups of
+// WG = min(W, warps) warps each; warp v takes the passes (RSB rows) p with
+// p % NH == v / WG and the workers v % WG, v % WG + WG, ...  With one warp
+// per worker (WG = warps, NH = 1) every warp takes every pass.  Each pass's
+// RSB rows of G and B are loaded into registers (streaming loads), then
+// used; a warp's lanes load their Q and Q_w' rows straight into registers,
+// so the only barrier of a tile is the final sum over the warps of each
+// row's group, in worker order.  s_red: warps x R1 x RP floats.
 template <int RP>
-__device__ __forceinline__ void p1_finish(const StepArgs& a, const LayerDev& L, const P1Tile& T,
-                                          const float (*s_red)[Cfg<RP>::R1 * RP], float* s_prow, double* s_gram,
-                                          int* s_flag) {
+__device__ __forceinline__ void p1_body(const StepArgs& a, const Tile& t, float* s_red, float* s_prow,
+                                        double* s_gram, int* s_flag, unsigned* pub) {
+  constexpr int RSB = Cfg<RP>::RSB;
+  constexpr int R1 = Cfg<RP>::R1;
+  const LayerDev L = a.layers[t.layer];  // by value: stores to B cannot alias it
+  const P1Tile T = p1_tile<RP>(a, t, L);
+  const int WG = min(a.W, T.nwarps);
+  const int NH = T.nwarps / WG;
+  const int h = T.warp / WG, wv = T.warp % WG;
+  if (h < NH) {
+    const float* Pprev = a.Phat + L.p_off + (int64_t)T.row0 * RP;  // previous Phat rows of the tile
+    // this lane's 4 Q rows, held in registers for the whole tile
+    float qv[4][RP];
+    p1_load_q<RP>(a.Qbar + L.q_off, T, false, qv);
+    bool first = true;
+    for (int w = wv; w < a.W; w += WG) {
+      const float* Gw = a.G[w] + L.off + 4 * T.c;
+      float* Bw = a.B + (int64_t)w * a.total + L.off + 4 * T.c;
+      float qw[4][RP];
+      p1_load_q<RP>(a.Qw + (int64_t)w * a.q_total + L.q_off, T, !T.prev, qw);
+      for (int sb = h * RSB; sb < T.rcnt; sb += NH * RSB) {
+        const int rn = min(RSB, T.rcnt - sb);
+        float4 g[RSB], b[RSB];
+#pragma unroll
+        for (int i = 0; i < RSB; ++i) {
+          if (T.act && i < rn) {
+            const int64_t o = (int64_t)(T.row0 + sb + i) * L.ld;
+            g[i] = __ldcs(reinterpret_cast<const float4*>(Gw + o));
+            b[i] = T.ub ? zero4() : __ldcs(reinterpret_cast<const float4*>(Bw + o));
+          } else {
+            g[i] = zero4();
+            b[i] = zero4();
+          }
+        }
+        float acc[RSB * RP];
+        p1_rows<RP>(L, T, g, b, sb, rn, Pprev, qv, qw, Bw, acc);
+        p1_reduce<RP>(T, acc, sb, rn, s_red + T.warp * R1 * RP, first);
+      }
+      first = false;
+    }
+  }
+  __syncthreads();
+  // P rows: the fixed-order sum over the workers' warps of each row's group
   for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) {
+    const int hh = (idx / RP / RSB) % NH;
     float s = 0.f;
-    for (int v = 0; v < T.nwarps; ++v) s += s_red[v][idx];
+    for (int v = 0; v < WG; ++v) s += s_red[(hh * WG + v) * R1 * RP + idx];
     s_prow[idx] = s;
   }
   __syncthreads();
-  p1_rows_done<RP>(a, L, T, s_prow, s_gram, s_flag);
+  p1_rows_done<RP>(a, L, T, s_prow, s_gram, s_flag, pub);
 }
 
-// Each pass's RSB rows of G and B are loaded into registers (streaming
-// loads), then used.  Every warp starts on its own: its lanes load their
-// Q and Q_w' rows straight into registers, so the only barrier of a tile is
-// the final cross-warp sum.
 template <int RP>
 __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_kernel(const StepArgs a) {
-  constexpr int RSB = Cfg<RP>::RSB;
   constexpr int R1 = Cfg<RP>::R1;
   constexpr int NW = Cfg<RP>::P1_WARPS;
-  __shared__ float s_red[NW][R1 * RP];                // per-warp P partials
+  __shared__ float s_red[NW * R1 * RP];  // per-warp P partials
   __shared__ float s_prow[R1 * RP];
   __shared__ double s_gram[RP * RP];
   __shared__ int s_flag;
   pdl_enter();
-  const Tile t = a.tiles[blockIdx.x];
-  const LayerDev L = a.layers[t.layer];  // by value: stores to B cannot alias it
-  const P1Tile T = p1_tile<RP>(a, t, L);
-  const float* Pprev = a.Phat + L.p_off + (int64_t)T.row0 * RP;  // previous Phat rows of the tile
-  // this lane's 4 Q rows, held in registers for the whole tile
-  float qv[4][RP];
-  p1_load_q<RP>(a.Qbar + L.q_off, T, false, qv);
-
-  bool first = true;
-  for (int w = T.warp; w < a.W; w += T.nwarps) {
-    const float* Gw = a.G[w] + L.off + 4 * T.c;
-    float* Bw = a.B + (int64_t)w * a.total + L.off + 4 * T.c;
-    float qw[4][RP];
-    p1_load_q<RP>(a.Qw + (int64_t)w * a.q_total + L.q_off, T, !T.prev, qw);
-    for (int sb = 0; sb < T.rcnt; sb += RSB) {
-      const int rn = min(RSB, T.rcnt - sb);
-      float4 g[RSB], b[RSB];
-#pragma unroll
-      for (int i = 0; i < RSB; ++i) {
-        if (T.act && i < rn) {
-          const int64_t o = (int64_t)(T.row0 + sb + i) * L.ld;
-          g[i] = __ldcs(reinterpret_cast<const float4*>(Gw + o));
-          b[i] = T.ub ? zero4() : __ldcs(reinterpret_cast<const float4*>(Bw + o));
-        } else {
-          g[i] = zero4();
-          b[i] = zero4();
-        }
-      }
-      float acc[RSB * RP];
-      p1_rows<RP>(L, T, g, b, sb, rn, Pprev, qv, qw, Bw, acc);
-      p1_reduce<RP>(T, acc, sb, rn, s_red[T.warp], first);
-    }
-    first = false;
-  }
-  __syncthreads();
-  p1_finish<RP>(a, L, T, s_red, s_prow, s_gram, &s_flag);
+  p1_body<RP>(a, a.tiles[blockIdx.x], s_red, s_prow, s_gram, &s_flag, nullptr);
 }
 
 // ----------------------------------------------------------------------------
-// orthonormalise: Phat rows by forward substitution Phat R = P (float64)
+// orthonormalise: Cholesky-QR2, P1 = P R^-1, then X = R2^-1 from P1's Gram
 // ----------------------------------------------------------------------------
+
+// One orthonormalise tile: rows chunk * NR .. + NR - 1 of layer L, NR =
+// ph_rows(RP), one thread per row (threads past NR, in a larger CTA, only
+// join the barriers).  P1 = P R^-1 by forward substitution in float64,
+// rounded to float32 and stored over P.  When the first pass was orthogonal
+// enough (the flag gram_tail set), that is the basis: at r >= 8 the tile also
+// stores it as Phat (at r <= 4 the back-project stages Phat from P1), and it
+// only counts itself done.  Otherwise the tile's rounded rows go to shared
+// memory and their Gram matrix (float64, each entry summed over the rows in
+// order) to the tile's partial slot; the CTA that completes the layer sums
+// the partials in order, factors the sum (Cholesky, R2) and stores
+// X = R2^-1, so that Phat = P1 X.  s_r: RP x RP + RP doubles; s_p1: NR x RP
+// floats; s_gram: RP x RP doubles.  pub (fused step only): the layer's X
+// flag, raised once the layer's tiles are done.
 template <int RP>
-__global__ void __launch_bounds__(kPHThreads) ph_kernel(const StepArgs a) {
-  __shared__ double s_r[RP * RP + RP];
-  pdl_enter();
-  const Tile t = a.tiles[blockIdx.x];
-  const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
-  for (int e = threadIdx.x; e < RP * RP + RP; e += blockDim.x) s_r[e] = a.rinv[L.rinv_off + e];
+__device__ __forceinline__ void ph_body(const StepArgs& a, const LayerDev& L, int chunk, double* s_r, float* s_p1,
+                                        double* s_gram, int* s_flag, unsigned* pub) {
+  constexpr int NG = Cfg<RP>::NG;
+  constexpr int NR = ph_rows(RP);
+  double* fr = a.rinv + L.rinv_off;
+  for (int e = threadIdx.x; e < RP * RP + RP; e += blockDim.x) s_r[e] = __ldcg(fr + e);
+  const bool one_pass = __ldcg(fr + 2 * RP * RP + RP) != 0.0;
   __syncthreads();
-  const int row = t.a * kPHThreads + threadIdx.x;
-  if (row >= L.n) return;
+  const int row = chunk * NR + threadIdx.x;
+  const bool valid = threadIdx.x < NR && row < L.n;
+  float* prow = a.P + L.p_off + (int64_t)row * RP;
   double x[RP];
 #pragma unroll
-  for (int k = 0; k < RP; ++k) x[k] = (double)a.P[L.p_off + (int64_t)row * RP + k];
+  for (int k = 0; k < RP; ++k) x[k] = valid ? (double)__ldcg(prow + k) : 0.0;
 #pragma unroll
   for (int k = 0; k < RP; ++k) {
     double s = x[k];
@@ -463,16 +557,123 @@ __global__ void __launch_bounds__(kPHThreads) ph_kernel(const StepArgs a) {
     for (int j = 0; j < k; ++j) s = fma(-x[j], s_r[j * RP + k], s);
     x[k] = s * s_r[RP * RP + k];
   }
+  float xf[RP];
+#pragma unroll
+  for (int k = 0; k < RP; ++k) xf[k] = (float)x[k];
+  if (valid) {
+#pragma unroll
+    for (int k = 0; k < RP; ++k) prow[k] = xf[k];
+    if (RP >= 8 && one_pass)
+#pragma unroll
+      for (int k = 0; k < RP; ++k) a.Phat[L.p_off + (int64_t)row * RP + k] = xf[k];
+  }
+  if (one_pass) {
+    // the layer is done once every tile has stored its rows
+    if (cta_arrive_last(a.counters + L.cnt_off + L.c_ph, (unsigned)L.nph, s_flag) && pub && threadIdx.x == 0)
+      flag_raise(pub, a.epoch);
+    return;
+  }
+  if (threadIdx.x < NR)
+#pragma unroll
+    for (int k = 0; k < RP; ++k) s_p1[threadIdx.x * RP + k] = valid ? xf[k] : 0.f;
+  __syncthreads();
+  double* gp = a.gram + L.gram_off + (int64_t)(L.nrb + L.g1) * NG;  // the P1 partials of the layer
+  for (int e = threadIdx.x; e < NG; e += blockDim.x) {
+    int i, j;
+    tri_index(e, RP, i, j);
+    double s = 0.0;
+    for (int rr = 0; rr < NR; ++rr) s = fma((double)s_p1[rr * RP + i], (double)s_p1[rr * RP + j], s);
+    gp[(int64_t)chunk * NG + e] = s;
+  }
+  if (!cta_arrive_last(a.counters + L.cnt_off + L.c_ph, (unsigned)L.nph, s_flag)) return;
+  for (int e = threadIdx.x; e < NG; e += blockDim.x) {
+    double s = 0.0;
+    for (int c = 0; c < L.nph; ++c) s += __ldcg(gp + (int64_t)c * NG + e);
+    int i, j;
+    tri_index(e, RP, i, j);
+    s_gram[i * RP + j] = s;
+    s_gram[j * RP + i] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    warp_cholesky<RP>(s_gram, s_r);  // R2 and 1 / diag R2 (s_r's R is no longer needed)
+    __syncwarp();
+    warp_tri_inverse<RP>(s_r, fr + RP * RP + RP);
+    if (pub) {
+      __syncwarp();
+      if (threadIdx.x == 0) flag_raise(pub, a.epoch);
+    }
+  }
+}
+
+template <int RP>
+__global__ void __launch_bounds__(ph_rows(RP)) ph_kernel(const StepArgs a) {
+  __shared__ double s_r[RP * RP + RP];
+  __shared__ float s_p1[ph_rows(RP) * RP];
+  __shared__ double s_gram[RP * RP];
+  __shared__ int s_flag;
+  pdl_enter();
+  const Tile t = a.tiles[blockIdx.x];
+  const LayerDev L = a.layers[t.layer];  // by value: stores to P cannot alias it
+  ph_body<RP>(a, L, t.a, s_r, s_p1, s_gram, &s_flag, nullptr);
+}
+
+// r >= 8, second pass: Phat rows = P1 X (float64 products, rounded), once per
+// row, for the layers whose first pass was not orthogonal enough (the other
+// layers' orthonormalise tiles stored Phat already).  The same tiles as the
+// orthonormalise phase.
+template <int RP>
+__global__ void __launch_bounds__(ph_rows(RP)) pf_kernel(const StepArgs a) {
+  __shared__ double s_x[RP * RP];
+  pdl_enter();
+  const Tile t = a.tiles[blockIdx.x];
+  const LayerDev L = a.layers[t.layer];
+  const double* X = a.rinv + L.rinv_off + RP * RP + RP;
+  if (X[RP * RP] != 0.0) return;  // one pass was enough (uniform over the CTA)
+  for (int e = threadIdx.x; e < RP * RP; e += blockDim.x) s_x[e] = X[e];
+  __syncthreads();
+  const int row = t.a * ph_rows(RP) + threadIdx.x;
+  if (row >= L.n) return;
+  const float* p1 = a.P + L.p_off + (int64_t)row * RP;
+  double x[RP];
+#pragma unroll
+  for (int j = 0; j < RP; ++j) x[j] = (double)p1[j];
   float* out = a.Phat + L.p_off + (int64_t)row * RP;
 #pragma unroll
-  for (int k = 0; k < RP; ++k) out[k] = (float)x[k];
+  for (int k = 0; k < RP; ++k) {
+    double v = 0.0;
+#pragma unroll
+    for (int j = 0; j <= k; ++j) v = fma(x[j], s_x[j * RP + k], v);
+    out[k] = (float)v;
+  }
+}
+
+// Split step: the Gram factor of an all-reduced P.  One CTA per project row
+// block (segment 0's tile of the project phase): the block's P rows, then
+// the same Gram tail the project phase runs.
+template <int RP>
+__global__ void __launch_bounds__(kGramThreads) gram_kernel(const StepArgs a) {
+  constexpr int R1 = Cfg<RP>::R1;
+  __shared__ float s_prow[R1 * RP];
+  __shared__ double s_gram[RP * RP];
+  __shared__ int s_flag;
+  pdl_enter();
+  const Tile t = a.tiles[blockIdx.x];
+  const LayerDev L = a.layers[t.layer];
+  const int row0 = t.a * L.r1;
+  const int rcnt = min(L.r1, L.n - row0);
+  for (int idx = threadIdx.x; idx < rcnt * RP; idx += blockDim.x)
+    s_prow[idx] = __ldcg(a.P + L.p_off + (int64_t)row0 * RP + idx);
+  __syncthreads();
+  gram_tail<RP>(a, L, t.a, s_prow, rcnt, s_gram, &s_flag, nullptr);
 }
 
 // ----------------------------------------------------------------------------
 // back-project: partial Q_w = M_w^T Phat over a row tile; segment finalise
 // ----------------------------------------------------------------------------
+// pub (fused step only): the segment's Qbar flag, raised once Qbar is stored.
 template <int RP>
-__device__ void qf_segment_worker(const StepArgs& a, const LayerDev& L, int seg, int w, int* s_flag) {
+__device__ void qf_segment_worker(const StepArgs& a, const LayerDev& L, int seg, int w, int* s_flag, unsigned* pub) {
   const int col0 = seg * kSeg * 4;
   const int col1 = min(L.ld, col0 + kSeg * 4);
   const int n4 = (col1 - col0) * RP / 4;  // float4 of the segment's ld x RP slice
@@ -506,7 +707,7 @@ __device__ void qf_segment_worker(const StepArgs& a, const LayerDev& L, int seg,
     reinterpret_cast<float4*>(qw)[q] = s;
   }
   if (!cta_arrive_last(a.counters + L.cnt_off + L.c_qs + seg, (unsigned)a.W, s_flag)) return;
-  const float invw = 1.0f / (float)a.W;
+  const float invw = a.qbar_scale;
   for (int q = threadIdx.x; q < n4; q += blockDim.x) {
     float4 s = zero4();
     for (int v = 0; v < a.W; ++v) {
@@ -518,6 +719,10 @@ __device__ void qf_segment_worker(const StepArgs& a, const LayerDev& L, int seg,
     }
     reinterpret_cast<float4*>(a.Qbar + L.q_off + e0)[q] = make_float4(s.x * invw, s.y * invw, s.z * invw, s.w * invw);
   }
+  if (pub) {
+    __syncthreads();
+    if (threadIdx.x == 0) flag_raise(pub, a.epoch);
+  }
 }
 
 // Back-project: rank slices per row group (warps that read the same rows),
@@ -525,9 +730,16 @@ __device__ void qf_segment_worker(const StepArgs& a, const LayerDev& L, int seg,
 constexpr int p3_slices(int rp) { return rp >= 32 ? 2 : 1; }
 constexpr size_t p3_dyn_bytes(int rp) { return (size_t)(kP3Threads / 32 / p3_slices(rp)) * 32 * 4 * rp * sizeof(float); }
 
-template <int RP>
-__global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
-  constexpr int UNR = Cfg<RP>::UNR3;
+
+// One back-project tile (kP3Threads threads), UNR rows per warp group.
+// FUSED: the tile runs inside the fused step, where B, P1 and X were written
+// by other CTAs of the same launch, so they are read through L2 only
+// (ld.global.cg; an L1 line of this SM could be stale); pub is then the
+// segment's Qbar flag.  s_ph: warps x UNR x RH floats; s_x: RP x RP doubles;
+// s_red: p3_dyn_bytes(RP) bytes.
+template <int RP, int UNR, bool FUSED>
+__device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, float* s_ph, double* s_x, float* s_red,
+                                        int* s_flag, unsigned* pub) {
   constexpr int NW = kP3Threads / 32;
   // r = 32: the ranks are split over warp pairs that read the same rows (the
   // second read hits in cache), so a warp holds 4 x RP / 2 accumulators and
@@ -535,11 +747,7 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
   constexpr int HS = p3_slices(RP);  // rank slices
   constexpr int RH = RP / HS;        // ranks per warp
   constexpr int NG = NW / HS;        // row groups in flight
-  __shared__ float s_ph[NW][UNR * RH];            // each warp's Phat values of its current group
-  extern __shared__ __align__(16) float s_red[];  // NG x 32 x 4 x RP
-  __shared__ int s_flag;
-  pdl_enter();
-  const Tile t = a.tiles[blockIdx.x];
+  static_assert(p3_dyn_bytes(RP) >= (size_t)NW * UNR * RP * sizeof(float), "s_red holds every warp's P1 rows");
   const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
   const int rt = t.a, seg = t.b, w = t.c;
   const int row0 = rt * L.r3;
@@ -549,25 +757,63 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
   const int c = seg * kSeg + lane;
   const bool act = c < L.F;
   const float* Bw = a.B + (int64_t)w * a.total + L.off + 4 * c;
-  const float* Ph = a.Phat + L.p_off + (int64_t)row0 * RP + hs * RH;
-  float* s_mine = s_ph[warp];
+  // r <= 4 (and the fused step): the Phat rows are formed here from P1 (and
+  // X after a second pass; float64 products of RP terms) as they are staged,
+  // and one tile per row tile stores them.  r >= 8: the orthonormalise phase
+  // stored Phat.
+  constexpr bool kForm = FUSED || RP <= 4;
+  const float* P1 = (kForm ? a.P : a.Phat) + L.p_off + (int64_t)row0 * RP;
+  float* Pout = (kForm && seg == 0 && w == 0) ? a.Phat + L.p_off + (int64_t)row0 * RP : nullptr;
+  const double* X = a.rinv + L.rinv_off + RP * RP + RP;
+  const bool ident = !kForm || (FUSED ? __ldcg(X + RP * RP) : __ldg(X + RP * RP)) != 0.0;
+  if (!ident) {
+    for (int e = threadIdx.x; e < RP * RP; e += blockDim.x) s_x[e] = FUSED ? __ldcg(X + e) : __ldg(X + e);
+    __syncthreads();
+  }
+  float* s_mine = s_ph + warp * UNR * RH;
+  float* s_p1 = s_red + warp * UNR * RP;  // this warp's P1 rows (before the final reduction)
   float acc[4][RH];
 #pragma unroll
   for (int j = 0; j < 4; ++j)
 #pragma unroll
     for (int k = 0; k < RH; ++k) acc[j][k] = 0.f;
   // row groups of UNR rows interleaved over the NG groups; each warp stages
-  // its own slice of the group's Phat rows (a warp barrier only)
+  // its own slice of the group's Phat rows (warp barriers only)
   for (int i0 = grp * UNR; i0 < nrows; i0 += NG * UNR) {
+    const int nr = min(UNR, nrows - i0);
+    __syncwarp();  // the previous group's rows are no longer read
+    if (!ident) {
+      // Phat = P1 X (j ascending): the group's P1 rows (all ranks), then the
+      // product, before the B loads so that their registers are not live
+      for (int e = lane; e < nr * RP; e += 32)
+        s_p1[e] = FUSED ? __ldcg(P1 + (int64_t)i0 * RP + e) : __ldg(P1 + (int64_t)i0 * RP + e);
+      __syncwarp();
+      for (int e = lane; e < nr * RH; e += 32) {
+        const int u = e / RH, k = hs * RH + e % RH;
+        // float64: when P was nearly rank deficient, X has large entries and
+        // the terms cancel (X was formed from these rounded P1 values, so
+        // the exact product is orthonormal)
+        double v = 0.0;
+#pragma unroll 8
+        for (int j = 0; j < RP; ++j) v = fma((double)s_p1[u * RP + j], s_x[j * RP + k], v);
+        s_mine[e] = (float)v;
+        if (Pout) Pout[(int64_t)(i0 + u) * RP + k] = (float)v;
+      }
+    }
     float4 bv[UNR];
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const float4* src = reinterpret_cast<const float4*>(Bw + (int64_t)(row0 + i0 + u) * L.ld);
-      bv[u] = (act && i0 + u < nrows) ? (HS > 1 ? __ldg(src) : __ldcs(src)) : zero4();
+      bv[u] = (act && i0 + u < nrows) ? (FUSED ? __ldcg(src) : (HS > 1 ? __ldg(src) : __ldcs(src))) : zero4();
     }
-    const int ne = min(UNR, nrows - i0) * RH;
-    __syncwarp();  // the previous group's Phat rows are no longer read
-    for (int e = lane; e < ne; e += 32) s_mine[e] = __ldg(Ph + (int64_t)(i0 + e / RH) * RP + e % RH);
+    if (ident) {  // Phat = P1, staged while the B loads are in flight
+      for (int e = lane; e < nr * RH; e += 32) {
+        const int64_t o = (int64_t)(i0 + e / RH) * RP + hs * RH + e % RH;
+        const float v = FUSED ? __ldcg(P1 + o) : __ldg(P1 + o);
+        s_mine[e] = v;
+        if (Pout) Pout[o] = v;
+      }
+    }
     __syncwarp();
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
@@ -583,7 +829,8 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
       }
     }
   }
-  // fixed-order reduction over the row groups
+  // fixed-order reduction over the row groups (s_red held the warps' P1 rows)
+  __syncthreads();
   float* mine = s_red + (grp * 32 + lane) * 4 * RP + hs * RH;
 #pragma unroll
   for (int j = 0; j < 4; ++j)
@@ -601,8 +848,20 @@ __global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
       part[(int64_t)(seg * kSeg + ln) * 4 * RP + jk] = s;
     }
   }
-  if (cta_arrive_last(a.counters + L.cnt_off + L.c_p3 + seg * a.W + w, (unsigned)L.t3r, &s_flag))
-    qf_segment_worker<RP>(a, L, seg, w, &s_flag);
+  if (cta_arrive_last(a.counters + L.cnt_off + L.c_p3 + seg * a.W + w, (unsigned)L.t3r, s_flag))
+    qf_segment_worker<RP>(a, L, seg, w, s_flag, pub);
+}
+
+template <int RP>
+__global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
+  constexpr int UNR = Cfg<RP>::UNR3;
+  constexpr int RH = RP / p3_slices(RP);
+  __shared__ float s_ph[(kP3Threads / 32) * UNR * RH];  // each warp's Phat values of its current group
+  __shared__ double s_x[RP * RP];                       // X = R2^-1 (when it is not the identity)
+  extern __shared__ __align__(16) float s_red[];        // the cross-warp reduction; first each warp's P1 rows
+  __shared__ int s_flag;
+  pdl_enter();
+  p3_body<RP, UNR, false>(a, a.tiles[blockIdx.x], s_ph, s_x, s_red, &s_flag, nullptr);
 }
 
 // ----------------------------------------------------------------------------
@@ -629,12 +888,12 @@ __device__ __forceinline__ void momentum4(float* X, float* Mom, int64_t p, float
   __stcs(reinterpret_cast<float4*>(X + p), x);
   __stcs(reinterpret_cast<float4*>(Mom + p), m);
 }
-template <int RP>
-__global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
+// One decompress tile (kUThreads threads).  FUSED: Phat and Qbar were
+// written by other CTAs of the same launch and are read through L2 only.
+// s_ph: RU x RP floats.
+template <int RP, bool FUSED>
+__device__ __forceinline__ void u_body(const StepArgs& a, const Tile& t, float* s_ph) {
   constexpr int RU = Cfg<RP>::RU;
-  __shared__ float s_ph[RU * RP];
-  pdl_enter();
-  const Tile t = a.tiles[blockIdx.x];
   if (t.c == 1) {  // vector layer: U = mean_w G_w
     const VecDev V = a.vecs[t.layer];
     const int base = t.a * kVChunk;
@@ -656,8 +915,8 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
   const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
   const int row0 = t.a * L.ru, seg = t.b;
   const int rcnt = min(L.ru, L.n - row0);
-  const float* Psrc = a.unbiased ? a.P : a.Phat;
-  for (int i = threadIdx.x; i < rcnt * RP; i += blockDim.x) s_ph[i] = __ldg(Psrc + L.p_off + (int64_t)row0 * RP + i);
+  const float* Psrc = (a.unbiased ? a.P : a.Phat) + L.p_off + (int64_t)row0 * RP;
+  for (int i = threadIdx.x; i < rcnt * RP; i += blockDim.x) s_ph[i] = FUSED ? __ldcg(Psrc + i) : __ldg(Psrc + i);
   __syncthreads();
   const int lane = threadIdx.x & 31, sub = threadIdx.x >> 5;  // 8 rows in flight per pass
   const int c = seg * kSeg + lane;
@@ -670,7 +929,7 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
       const float4* qb = reinterpret_cast<const float4*>(qs);
 #pragma unroll
       for (int i = 0; i < RP; ++i) {
-        const float4 v = __ldg(qb + i);
+        const float4 v = FUSED ? __ldcg(qb + i) : __ldg(qb + i);
         flat[4 * i] = v.x;
         flat[4 * i + 1] = v.y;
         flat[4 * i + 2] = v.z;
@@ -678,7 +937,7 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 4 * RP; ++i) flat[i] = __ldg(qs + i);
+      for (int i = 0; i < 4 * RP; ++i) flat[i] = FUSED ? __ldcg(qs + i) : __ldg(qs + i);
     }
   }
   const int valid = (c == L.F - 1) ? L.tail : 4;
@@ -706,6 +965,13 @@ __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
   }
 }
 
+template <int RP>
+__global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
+  __shared__ float s_ph[Cfg<RP>::RU * RP];
+  pdl_enter();
+  u_body<RP, false>(a, a.tiles[blockIdx.x], s_ph);
+}
+
 // ----------------------------------------------------------------------------
 // r >= 8: register-tiled project and decompress
 // ----------------------------------------------------------------------------
@@ -723,11 +989,13 @@ constexpr int kTThreads = 256;  // threads of a tiled project CTA: 32 rows x 8 c
 // columns; each of the 8 threads of a row reads a different 16 bytes, so the
 // loads of a warp are coalesced and the shared-memory reads conflict-free).
 // Per worker: E = B - Phat' Q_w'^T for its 16 elements (fmaf chains, k
-// ascending, as in the error read-back kernel), M = G + E stored to B, and
-// its share of the P row, sum_c M[i][c] Q[c][k], accumulated over the workers
-// in registers; the 8 column groups of a row are summed with a butterfly
-// over their 8 lanes at the end.  Q and Q_w' are staged transposed
-// ([k][column]) so a thread reads its 4 float4 columns at fixed k.
+// ascending, as in the error read-back kernel), M = G + E stored to B and
+// added to the thread's running sum over the workers.  After the last
+// worker, its share of the P row, sum_c (sum_w M_w)[i][c] Q[c][k]: one r-wide
+// product per tile instead of one per worker (P is linear in M).  The 8
+// column groups of a row are summed with a butterfly over their 8 lanes.
+// Q and Q_w' are staged transposed ([k][column]) so a thread reads its 4
+// float4 columns at fixed k.
 // The tiled project kernel's G and B float4 of worker w: row i of the tile,
 // float4 columns c40 + 8 v (zeros past the row or the layer; no B in the
 // unbiased variant).
@@ -777,9 +1045,7 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
   }
   for (int e = threadIdx.x; e < TR * RP; e += blockDim.x)
     s_pp[e] = (T.prev && e < T.rcnt * RP) ? __ldg(a.Phat + L.p_off + (int64_t)T.row0 * RP + e) : 0.f;
-  float pacc[RP];
-#pragma unroll
-  for (int k = 0; k < RP; ++k) pacc[k] = 0.f;
+  float msum[16];  // sum over the workers of the thread's 16 M values
   // each worker's Q_w' values are loaded one worker ahead (NQ per thread) and
   // stored into shared memory after the barrier, so their latency hides
   // behind the previous worker's arithmetic
@@ -856,21 +1122,26 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
       if (row_ok && c4 < L.F && !T.ub)
         reinterpret_cast<float4*>(Bw)[c4] = make_float4(m[4 * v], m[4 * v + 1], m[4 * v + 2], m[4 * v + 3]);
     }
-    // P partial: for each rank, the thread's 16 columns in order; workers in order
-#pragma unroll 4
-    for (int k = 0; k < RP; ++k) {
-      const float4* qk = reinterpret_cast<const float4*>(s_qT + k * SCP) + cg;
-      float acc = pacc[k];
+    // the workers' M summed in order: P = (sum_w M_w) Q needs one product
+    // per tile, not one per worker
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const float4 q = qk[8 * v];
-        acc = fmaf(m[4 * v], q.x, acc);
-        acc = fmaf(m[4 * v + 1], q.y, acc);
-        acc = fmaf(m[4 * v + 2], q.z, acc);
-        acc = fmaf(m[4 * v + 3], q.w, acc);
-      }
-      pacc[k] = acc;
+    for (int x = 0; x < 16; ++x) msum[x] = (w == 0) ? m[x] : msum[x] + m[x];
+  }
+  // P partial: for each rank, the thread's 16 columns in order
+  float pacc[RP];
+#pragma unroll 4
+  for (int k = 0; k < RP; ++k) {
+    const float4* qk = reinterpret_cast<const float4*>(s_qT + k * SCP) + cg;
+    float acc = 0.f;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const float4 q = qk[8 * v];
+      acc = fmaf(msum[4 * v], q.x, acc);
+      acc = fmaf(msum[4 * v + 1], q.y, acc);
+      acc = fmaf(msum[4 * v + 2], q.z, acc);
+      acc = fmaf(msum[4 * v + 3], q.w, acc);
     }
+    pacc[k] = acc;
   }
   // sum the 8 column groups of each row (lanes 8 (i % 4) + cg): a fixed
   // butterfly that leaves lane cg with ranks [base, base + RP / 8)
@@ -894,7 +1165,7 @@ __global__ void __launch_bounds__(kTThreads, 2) p1t_kernel(const StepArgs a) {
       for (int x = 0; x < RP / 8; ++x) s_prow[i * RP + base + x] = pacc[x];
   }
   __syncthreads();
-  p1_rows_done<RP>(a, L, T, s_prow, s_gram, &s_flag);
+  p1_rows_done<RP>(a, L, T, s_prow, s_gram, &s_flag, nullptr);
 }
 
 // Decompress, r >= 8: thread = one column of the segment (its Q rows, RP

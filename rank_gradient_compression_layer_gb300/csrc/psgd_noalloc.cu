@@ -121,6 +121,7 @@ extern "C" int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers
   const std::vector<int64_t> nv{n}, mv{m};
   TileRows tr;
   if ((rc = choose_tile_rows(nv, mv, rp, W, *ks, dev, &tr))) return rc;
+  if (ks->mma_rows > 0) tr.r1 = ks->mma_rows;  // the tensor-core project tiles
   LayerDev L;
   std::memset(&L, 0, sizeof(L));
   ScratchPlan sp;
@@ -135,7 +136,7 @@ extern "C" int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers
   L.ppart_off = 0;
   L.cnt_off = 0;
   sp.ntiles[kProject] = (int)((int64_t)L.nrb * L.S);
-  sp.ntiles[kOrthonormalise] = (int)ceil_div(n, kPHThreads);
+  sp.ntiles[kOrthonormalise] = L.nph;
   sp.ntiles[kBackProject] = (int)((int64_t)L.t3r * L.S * W);
   sp.ntiles[kDecompress] = (int)(ceil_div(n, L.ru) * L.S);
   const int NG = rp * (rp + 1) / 2;
@@ -149,9 +150,9 @@ extern "C" int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers
   for (int ph = 0; ph < kPhases; ++ph) sp.tiles[ph] = take((size_t)sp.ntiles[ph] * sizeof(Tile));
   sp.counters = take((size_t)sp.ncnt * sizeof(unsigned));
   sp.P = take((size_t)n * rp * sizeof(float));
-  sp.gram = take((size_t)(L.nrb + L.g1) * NG * sizeof(double));
-  sp.rinv = take((size_t)(rp * rp + rp) * sizeof(double));
-  sp.ppart = take(L.S > 1 ? (size_t)L.nrb * L.S * ks->r1 * rp * sizeof(float) : 0);
+  sp.gram = take((size_t)(L.nrb + L.g1 + L.nph) * NG * sizeof(double));
+  sp.rinv = take((size_t)rinv_len(rp) * sizeof(double));
+  sp.ppart = take(L.S > 1 ? (size_t)L.nrb * L.S * L.r1 * rp * sizeof(float) : 0);
   sp.qpart = take((size_t)L.t3r * W * ld * rp * sizeof(float));
   sp.total = pos;
   if (sp.total > kNoAllocScratchBytes)
@@ -186,7 +187,9 @@ extern "C" int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers
   a.layers = dL;
   a.vecs = nullptr;
   a.W = W;
+  a.qbar_scale = 1.0f / (float)W;
   a.has_prev = has_prev ? 1 : 0;
+  a.stall_layer = -1;
   const int phases = out_update ? kPhases : kPhases - 1;
   for (int ph = 0; ph < phases; ++ph) {
     if (sp.ntiles[ph] == 0) continue;

@@ -76,7 +76,10 @@ inline int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp
   L.c_qs = 1 + L.g1;
   L.c_p3 = L.c_qs + L.S;
   L.c_rb = L.c_p3 + L.S * W;
-  return (int64_t)L.c_rb + (L.S > 1 ? L.nrb : 0);
+  L.rph = ph_rows(rp);
+  L.nph = (int32_t)ceil_div(n, L.rph);
+  L.c_ph = L.c_rb + (L.S > 1 ? L.nrb : 0);
+  return (int64_t)L.c_ph + 1;
 }
 
 // Chooses the tile rows of a layer set so that each phase grid is at least
@@ -115,6 +118,106 @@ inline int choose_tile_rows(const std::vector<int64_t>& n, const std::vector<int
   }
   *tr = r;
   return PSGD_OK;
+}
+
+// The tiles of one matrix layer, per phase, in the order the phase kernels
+// take them.  Back-project tiles run from the last row tile and segment to
+// the first, so that they start on the rows the project tiles wrote last.
+inline void layer_tiles(const LayerDev& L, int li, int W, std::vector<Tile> (&out)[kPhases]) {
+  for (auto& v : out) v.clear();
+  for (int rb = 0; rb < L.nrb; ++rb)
+    for (int s = 0; s < L.S; ++s) out[kProject].push_back({li, rb, s, 0});
+  for (int t = 0; t < L.nph; ++t) out[kOrthonormalise].push_back({li, t, 0, 0});
+  for (int rt = L.t3r - 1; rt >= 0; --rt)
+    for (int s = L.S - 1; s >= 0; --s)
+      for (int w = 0; w < W; ++w) out[kBackProject].push_back({li, rt, s, w});
+  for (int rb = 0; rb < (int)ceil_div(L.n, L.ru); ++rb)
+    for (int s = 0; s < L.S; ++s) out[kDecompress].push_back({li, rb, s, 0});
+}
+
+// HBM bytes a tile of a phase moves (for the queue's lags; approximate).
+inline int64_t tile_bytes(const LayerDev& L, int phase, const Tile& t, int W) {
+  const int64_t cols = std::min<int64_t>((int64_t)kSeg * 4, (int64_t)L.ld - (int64_t)t.b * kSeg * 4);
+  switch (phase) {
+    case kProject: return 12 * (int64_t)W * std::min(L.r1, L.n - t.a * L.r1) * cols;
+    case kBackProject: return 4 * (int64_t)std::min(L.r3, L.n - t.a * L.r3) * cols;
+    case kDecompress: return 4 * (int64_t)std::min(L.ru, L.n - t.a * L.ru) * cols;
+    default: return 0;
+  }
+}
+
+// The fused step's queue: every tile of every phase, in an order where each
+// tile's producers come first (project before orthonormalise before
+// back-project before decompress, per layer), so that CTAs taking positions
+// in order can always finish.  Layers go largest first, so that the last
+// dependency chains to drain belong to small layers.  A layer's later phases
+// are placed `lag` bytes of other traffic after its previous phase -- about
+// what the resident CTAs have in flight -- so that their inputs are usually
+// ready when a CTA takes them, while the error state the back-project reads
+// is still in L2.  Vector tiles (worker means) go first; with_update false
+// leaves out the decompress and vector tiles.
+struct QueueStage {
+  int layer, phase;
+  int64_t ready;  // queue bytes after which the stage's tiles may go in
+};
+
+inline std::vector<Tile> build_queue(const std::vector<LayerDev>& hl, const std::vector<Tile>& vec_tiles, int W,
+                                     int64_t lag, bool with_update) {
+  std::vector<Tile> q;
+  auto put = [&](int phase, const Tile& t) {
+    Tile x = t;
+    x.layer = item_layer(phase, t.layer);
+    q.push_back(x);
+  };
+  if (with_update)
+    for (const Tile& t : vec_tiles) put(kItemDecomp, t);
+  std::vector<int> order(hl.size());
+  for (size_t i = 0; i < hl.size(); ++i) order[i] = (int)i;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+    return (int64_t)hl[x].n * hl[x].m > (int64_t)hl[y].n * hl[y].m;
+  });
+  const int last_phase = with_update ? kDecompress : kBackProject;
+  std::vector<Tile> tiles[kPhases];
+  std::vector<QueueStage> pending;
+  int64_t cum = 0;
+  std::vector<Tile> stage_tiles[kPhases];
+  auto emit_stage = [&](const QueueStage& st) {
+    auto& tiles = stage_tiles;
+    layer_tiles(hl[st.layer], st.layer, W, tiles);
+    int phase = st.phase;
+    // orthonormalise and back-project go in together: the orthonormalise
+    // tiles are few and short
+    const int first = phase, last = (phase == kOrthonormalise) ? kBackProject : phase;
+    for (int ph = first; ph <= last; ++ph)
+      for (const Tile& t : tiles[ph]) {
+        put(ph, t);
+        cum += tile_bytes(hl[st.layer], ph, t, W);
+      }
+    if (last < last_phase) pending.push_back({st.layer, last + 1, cum + lag});
+  };
+  auto drain = [&](bool all) {
+    for (;;) {
+      int pick = -1;
+      for (size_t i = 0; i < pending.size(); ++i)
+        if ((all || pending[i].ready <= cum) && (pick < 0 || pending[i].ready < pending[pick].ready)) pick = (int)i;
+      if (pick < 0) return;
+      const QueueStage st = pending[pick];
+      pending.erase(pending.begin() + pick);
+      emit_stage(st);
+    }
+  };
+  for (int li : order) {
+    layer_tiles(hl[li], li, W, tiles);
+    for (const Tile& t : tiles[kProject]) {
+      put(kProject, t);
+      cum += tile_bytes(hl[li], kProject, t, W);
+      drain(false);
+    }
+    pending.push_back({li, kOrthonormalise, cum + lag});
+    drain(false);
+  }
+  drain(true);
+  return q;
 }
 
 }  // namespace psgd

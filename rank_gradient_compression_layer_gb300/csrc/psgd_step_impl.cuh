@@ -1,6 +1,12 @@
 // Instantiation of the phase kernels for one padded rank (PSGD_RP).
 #include "psgd_dispatch.h"
 #include "psgd_kernels.cuh"
+#if PSGD_RP <= 4
+#include "psgd_fused.cuh"
+#endif
+#if PSGD_RP >= 16
+#include "psgd_mma.cuh"
+#endif
 
 #define PSGD_CAT2(a, b) a##b
 #define PSGD_CAT(a, b) PSGD_CAT2(a, b)
@@ -37,6 +43,9 @@ cudaError_t launch(int phase, const StepArgs& a, int tiles, cudaStream_t s) {
   if (tiles <= 0) return cudaSuccess;
   switch (phase) {
     case kProject: {
+#if PSGD_RP >= 16
+      if (!a.unbiased) return launch_dependent(p1m_kernel<kRP>, tiles, kMThreads, MmaCfg<kRP>::SMEM, s, a);
+#endif
 #if PSGD_RP >= 8
       return launch_dependent(p1t_kernel<kRP>, tiles, kTThreads, kP1TDyn, s, a);
 #else
@@ -44,8 +53,14 @@ cudaError_t launch(int phase, const StepArgs& a, int tiles, cudaStream_t s) {
       return launch_dependent(p1_kernel<kRP>, tiles, 32 * warps, 0, s, a);
 #endif
     }
-    case kOrthonormalise:
-      return launch_dependent(ph_kernel<kRP>, tiles, kPHThreads, 0, s, a);
+    case kOrthonormalise: {
+      cudaError_t e = launch_dependent(ph_kernel<kRP>, tiles, ph_rows(kRP), 0, s, a);
+#if PSGD_RP >= 8
+      // the second pass's Phat rows, once per row (r <= 4: in the back-project)
+      if (e == cudaSuccess) e = launch_dependent(pf_kernel<kRP>, tiles, ph_rows(kRP), 0, s, a);
+#endif
+      return e;
+    }
     case kBackProject:
       return launch_dependent(p3_kernel<kRP>, tiles, kP3Threads, kP3Dyn, s, a);
     case kDecompress:
@@ -75,6 +90,10 @@ cudaError_t prepare() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(p1t_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP1TDyn);
 #endif
+#if PSGD_RP >= 16
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(p1m_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MmaCfg<kRP>::SMEM);
+#endif
   return e;
 }
 
@@ -98,13 +117,41 @@ cudaError_t occupancy(int phase, int W, int* ctas) {
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, u_kernel<kRP>, kUThreads, 0);
 #endif
     default:
-      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, ph_kernel<kRP>, kPHThreads, 0);
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, ph_kernel<kRP>, ph_rows(kRP), 0);
   }
 }
+
+cudaError_t launch_gram(const StepArgs& a, int tiles, cudaStream_t s) {
+  if (tiles <= 0) return cudaSuccess;
+  return launch_dependent(gram_kernel<kRP>, tiles, kGramThreads, 0, s, a);
+}
+
+#if PSGD_RP <= 4
+cudaError_t launch_fused(const StepArgs& a, int ctas, cudaStream_t s) {
+  if (ctas <= 0) return cudaSuccess;
+  return launch_dependent(fused_step_kernel<kRP>, ctas, kFThreads, 0, s, a);
+}
+
+cudaError_t occupancy_fused(int* ctas) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, fused_step_kernel<kRP>, kFThreads, 0);
+}
+#endif
 
 }  // namespace
 
 extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {
-    kRP, launch, launch_error, prepare, occupancy, Cfg<kRP>::R1, Cfg<kRP>::RU, Cfg<kRP>::RSB};
+    kRP, launch, launch_error, prepare, occupancy, Cfg<kRP>::R1, Cfg<kRP>::RU, Cfg<kRP>::RSB,
+#if PSGD_RP <= 4
+    launch_fused, occupancy_fused,
+#else
+    nullptr, nullptr,
+#endif
+    launch_gram,
+#if PSGD_RP >= 16
+    kMRows
+#else
+    0
+#endif
+};
 
 }  // namespace psgd

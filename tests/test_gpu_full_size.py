@@ -5,10 +5,11 @@ context over the whole layer set, phase timing on, its own stream).
 The step treats every layer on its own, so the oracle checks sampled layers
 exactly: it is built for those layers only (their initial Q drawn from the
 same (seed, layer) streams) and fed the same gradients, generated on the
-device and copied back.  Tolerances: 1e-4 after the first step, 1e-3 after
-the second (relative Frobenius error on Phat, Qbar, U, every Q_w and E_w).
+device and copied back.  Ten steps with error feedback and warm start; steps
+1, 5 and 10 are compared.  Tolerances: 1e-4 after the first step, 1e-3 after
+later ones (plain relative Frobenius error on Phat, Qbar, U, every Q_w and
+every E_w: every layer here has rank far above r, so no E_w is near zero).
 """
-import numpy as np
 import pytest
 
 import workloads
@@ -35,7 +36,10 @@ def _fill(ctx, cfg, step, bufs, device):
             ctx.layer_view(bufs[w], li).copy_(workloads.device_gradient_matrix(cfg, li, step, w, device))
 
 
-def _check_sampled(cfg, sample, steps):
+CHECK = (0, 4, 9)  # steps 1, 5 and 10
+
+
+def _check_sampled(cfg, sample, steps, check=CHECK):
     import torch
     from rank_gradient_compression_layer_gb300 import PowerSGD
 
@@ -55,6 +59,9 @@ def _check_sampled(cfg, sample, steps):
             ctx.sync()
             grads = [[ctx.layer_view(bufs[w], li).cpu().numpy() for li in sample] for w in range(cfg.workers)]
             ref = st.step(grads)
+            del grads
+            if t not in check:
+                continue
             tol = TOL[min(t, 1)]
             for k, li in enumerate(sample):
                 P, Q = ctx.get_PQ(li)
@@ -63,9 +70,8 @@ def _check_sampled(cfg, sample, steps):
                 assert rel_fro(ctx.layer_view(upd, li).cpu().numpy(), ref.U[k]) <= tol, (t, li, "U")
                 for w in range(cfg.workers):
                     assert rel_fro(ctx.get_Qw(li, w).cpu().numpy(), ref.Q_w[k][w]) <= tol, (t, li, "Qw", w)
-                    floor = 1e-2 * float(np.linalg.norm(grads[w][k]))
                     E = ctx.get_error(li, w).cpu().numpy()
-                    assert rel_fro(E, st.E[k][w], floor) <= tol, (t, li, "E", w)
+                    assert rel_fro(E, st.E[k][w]) <= tol, (t, li, "E", w)
                     del E
         s = ctx.stats()
         assert s["floats_sent_per_step"] == O.data_sent_per_step(cfg.layers, cfg.rank)[0]
@@ -75,12 +81,13 @@ def _check_sampled(cfg, sample, steps):
 
 def test_transformer_1p2b_full_size_sampled_layers():
     cfg = workloads.c4_transformer()
-    n_layers = len(cfg.layers)
-    # first attention and MLP matrices, one from the middle block, the last MLP
-    sample = [0, 5, 6 * (n_layers // 12) + 2, n_layers - 1]
-    _check_sampled(cfg, sample, steps=2)
+    blocks = len(cfg.layers) // 6
+    # one matrix of each shape (d x d attention, d x ff MLP) from the first,
+    # the middle and the last block
+    sample = [b * 6 + k for b in (0, blocks // 2, blocks - 1) for k in (0, 5)]
+    _check_sampled(cfg, sample, steps=10)
 
 
-@pytest.mark.parametrize("rank,steps", [(1, 1), (4, 2), (32, 1)])
-def test_square8192_w8_full_size(rank, steps):
-    _check_sampled(workloads.c5_rank_sweep(rank), [0], steps=steps)
+@pytest.mark.parametrize("rank", [1, 2, 4, 8, 16, 32])
+def test_square8192_w8_full_size(rank):
+    _check_sampled(workloads.c5_rank_sweep(rank), [0], steps=10)

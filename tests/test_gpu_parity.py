@@ -3,6 +3,8 @@
 Tolerances (relative Frobenius error on Phat, Qbar, U, every Q_w and every
 E_w): 1e-4 after the first step, 1e-3 after later steps.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -161,8 +163,27 @@ def _outputs(run):
     return out
 
 
-def test_bit_reproducible_across_contexts_and_timing():
-    cfg = workloads.scaled(workloads.c2_resnet18(), workloads.resnet18_cifar_layers()[:12] + [(64, 0)])
+def test_first_context_of_a_process_plans_like_the_rest():
+    # the tile planner reads the kernels' occupancy, which depends on their
+    # shared-memory limits: a fresh process's first context must see them set
+    import subprocess
+    import sys
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "from rank_gradient_compression_layer_gb300 import PowerSGD\n"
+        "layers = [(256, 1152), (512, 4608), (64, 0)]\n"
+        "rows = [PowerSGD(layers, r, 4).stats()['tile_rows'] for r in (16, 16, 32, 32)]\n"
+        "assert rows[0] == rows[1] and rows[2] == rows[3], rows\n"
+        "print('ok')\n" % (os.path.dirname(os.path.dirname(os.path.abspath(__file__))),))
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0 and "ok" in out.stdout, out.stderr[-2000:]
+
+
+@pytest.mark.parametrize("rank", [2, 16])
+def test_bit_reproducible_across_contexts_and_timing(rank):
+    # r = 16: the back-project needs more than 48 KB of dynamic shared memory,
+    # and every context (the first of the process too) must plan the same tiles
+    cfg = workloads.scaled(workloads.c2_resnet18(), workloads.resnet18_cifar_layers()[:12] + [(64, 0)], rank=rank)
     runs = [GpuRun(cfg), GpuRun(cfg), GpuRun(cfg, timing=True)]
     try:
         sig = {}
@@ -243,6 +264,7 @@ def test_step_host_matches_step():
 
 
 def test_phase_timing():
+    # the phase kernels one by one (the fused step has one slot: test_gpu_fused.py)
     cfg = workloads.scaled(workloads.c2_resnet18(), [(128, 576), (9, 0)], rank=2)
     run = GpuRun(cfg, timing=True)
     try:

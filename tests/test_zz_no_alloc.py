@@ -62,10 +62,10 @@ def _noalloc_matches_context(n, m, r, W, seed):
             for w in range(W):
                 qw = Qw[w].double().cpu().numpy()
                 assert rel_fro(qw[:m], run.Qw(0, w)) <= TOL, (t, "Qw", w)
-                # new error E_w = B_w - Phat Q_w^T (B_w holds M_w after the call)
+                # new error E_w = B_w - Phat Q_w^T (B_w holds M_w after the call);
+                # every shape here has rank far above r, so E_w is not near zero
                 E = B[w].double().cpu().numpy()[:, :m] - got_P @ qw[:m].T
-                floor = 1e-2 * float(np.linalg.norm(grads[w][0]))
-                assert rel_fro(E, run.E(0, w), floor) <= TOL, (t, "E", w)
+                assert rel_fro(E, run.E(0, w)) <= TOL, (t, "E", w)
     finally:
         run.close()
 
@@ -76,6 +76,9 @@ def _noalloc_matches_context(n, m, r, W, seed):
     (1536, 1000, 4, 4),   # several row tiles in every phase
     (512, 4608, 2, 4),    # the largest ResNet-18 layer
     (257, 650, 8, 5),     # r = 8, odd worker count
+    (1000, 300, 16, 3),   # r = 16: the register-tiled project and decompress kernels
+    (511, 260, 32, 2),    # r = 32, ragged row tile
+    (63, 27, 1, 2),       # n r not a multiple of 4: the caller's Phat is not padded
 ])
 def test_noalloc_matches_context_two_calls(n, m, r, W):
     _noalloc_matches_context(n, m, r, W, seed=21)
