@@ -261,7 +261,7 @@ void build_tiles(psgd_ctx* c) {
   for (int li = 0; li < nm; ++li) {
     const LayerDev& L = c->hl[li];
     for (int rb = 0; rb < L.nrb; ++rb)
-      for (int s = 0; s < L.S; ++s) c->tiles[kProject].push_back({li, rb, s, 0});
+      for (int s = 0; s < L.s1; ++s) c->tiles[kProject].push_back({li, rb, s, 0});
     for (int t = 0; t < L.nph; ++t) c->tiles[kOrthonormalise].push_back({li, t, 0, 0});
     for (int rb = 0; rb < (int)ceil_div(L.n, L.ru); ++rb)
       for (int s = 0; s < L.S; ++s) c->tiles[kDecompress].push_back({li, rb, s, 0});
@@ -505,7 +505,10 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     delete c;
     return fail(PSGD_ERR_INVALID, "project_rows is fixed at %d rows for the tensor-core project tiles", c->ks->mma_rows);
   }
-  if (mma) tr.r1 = c->ks->mma_rows;
+  if (mma) {
+    tr.r1 = c->ks->mma_rows;
+    tr.pcols = c->ks->mma_cols;
+  }
   if (opt && opt->project_rows > 0) {
     if (opt->project_rows > c->ks->r1 || opt->project_rows % c->ks->rsb != 0) {
       delete c;
@@ -534,13 +537,13 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     L.q_off = c->q_total;
     c->q_total += c->ld[l] * rp;
     L.gram_off = c->gram_total;
-    c->gram_total += (int64_t)(L.nrb + L.g1 + L.nph) * NG;
+    c->gram_total += gram_slots(L.nrb, L.g1, L.nph) * NG;
     L.rinv_off = c->rinv_total;
     c->rinv_total += rinv_len(rp);
     L.qpart_off = c->qpart_total;
     c->qpart_total += (int64_t)L.t3r * c->W * c->ld[l] * rp;
     L.ppart_off = c->ppart_total;
-    if (L.S > 1) c->ppart_total += (int64_t)L.nrb * L.S * L.r1 * rp;
+    if (L.s1 > 1) c->ppart_total += (int64_t)L.nrb * L.s1 * L.r1 * rp;
     L.cnt_off = (int32_t)c->n_counters;
     c->n_counters += ncnt;
     L.f_off = (int32_t)c->n_flags;

@@ -32,8 +32,8 @@ struct KernelSet {
   // split step: the Gram factor of an all-reduced P over `tiles` row blocks
   cudaError_t (*launch_gram)(const StepArgs& a, int tiles, cudaStream_t s);
   // the project phase runs on the tensor cores (padded ranks 16, 32; not the
-  // unbiased variant): its tiles have mma_rows rows
-  int mma_rows;
+  // unbiased variant): its tiles have mma_rows rows and mma_cols columns
+  int mma_rows, mma_cols;
 };
 
 extern const KernelSet kKernelsR1, kKernelsR2, kKernelsR4, kKernelsR8, kKernelsR16, kKernelsR32;

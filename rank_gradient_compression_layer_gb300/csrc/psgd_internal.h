@@ -13,6 +13,15 @@ constexpr int kGramGroup = 32;    // project row blocks whose Gram partials one 
 // Rows of one orthonormalise tile (one thread per row): fewer at large r, so
 // that the tiles' float64 work (about r^2 per row) spreads over more SMs.
 constexpr int ph_rows(int rp) { return rp >= 32 ? 32 : (rp == 16 ? 64 : 128); }
+// Threads of an orthonormalise CTA: the row threads plus helpers for the
+// second pass's partial-Gram sums (whose cost is load latency, not rows).
+constexpr int kPhThreads = 128;
+// Groups of kGramGroup orthonormalise tiles whose second-pass Gram partials
+// one group sum takes.
+constexpr int64_t ph_groups(int64_t nph) { return (nph + kGramGroup - 1) / kGramGroup; }
+// Partial-Gram slots (NG doubles each) of a layer: project row blocks,
+// project groups, orthonormalise tiles, orthonormalise groups.
+constexpr int64_t gram_slots(int64_t nrb, int64_t g1, int64_t nph) { return nrb + g1 + nph + ph_groups(nph); }
 
 // Doubles per layer of the factor record: R of the first Cholesky-QR pass
 // (RP x RP, row-major) and 1 / diag R (RP); X = R2^-1 of the second pass
@@ -48,7 +57,7 @@ struct LayerDev {
   int64_t p_off;      // P and Phat: n x RP (16-byte aligned)
   int64_t q_off;      // Qbar: ld x RP; Q_w of worker w at w*q_total + q_off
   int64_t ppart_off;  // floats: nrb x S x R1 x RP partial P rows (S > 1)
-  int64_t gram_off;   // doubles: (nrb + g1 + nph) x NG partial Grams (P, then P1)
+  int64_t gram_off;   // doubles: gram_slots(nrb, g1, nph) x NG partial Grams (P, then P1)
   int64_t rinv_off;   // doubles: rinv_len(RP), the factor record
   int64_t qpart_off;  // floats: t3r x W x ld x RP partial Q_w
   int32_t cnt_off;    // first counter of the layer; the others sit at cnt_off + c_*
@@ -56,11 +65,13 @@ struct LayerDev {
   int32_t c_grp;      // row blocks done per Gram group (g1)
   int32_t c_qs;       // workers done per segment (S)
   int32_t c_p3;       // row tiles done per (segment, worker) (S x W)
-  int32_t c_rb;       // segments done per row block (nrb, when S > 1)
+  int32_t c_rb;       // project column blocks done per row block (nrb, when s1 > 1)
   int32_t nph;        // orthonormalise tiles (rph rows each)
-  int32_t c_ph;       // orthonormalise tiles done (1)
+  int32_t c_ph;       // orthonormalise tiles (one pass) or tile groups (two passes) done (1)
   int32_t f_off;      // fused step: first of the layer's 2 + S flags (R ready, X ready, Qbar per segment)
   int32_t rph;        // rows per orthonormalise tile (ph_rows)
+  int32_t s1;         // project tiles per row block (column blocks: segments, or half segments)
+  int32_t c_phg;      // orthonormalise tiles done per tile group, second pass (ph_groups(nph))
 };
 
 // The fused step runs every phase's tiles from one queue; an item is a Tile

@@ -51,6 +51,7 @@ struct Cfg {
   // RSB rows per pass
   static constexpr int RSB = RP <= 4 ? 4 : (RP == 8 ? 2 : 1);
   static constexpr int R1 = 32;
+  static constexpr int R1MAX = RP >= 16 ? 128 : R1;        // rows of a project row block at most (tensor-core tiles: 128)
   static constexpr int P1_WARPS = 8;                        // at most (more workers loop)
   static constexpr int P1_MINB = RP <= 2 ? 4 : (RP == 4 ? 3 : 1);          // 256-thread CTAs per SM the registers must allow
   // back-project: 8 warps over interleaved groups of UNR3 rows
@@ -426,14 +427,14 @@ template <int RP>
 __device__ __forceinline__ void p1_rows_done(const StepArgs& a, const LayerDev& L, const P1Tile& T, float* s_prow,
                                              double* s_gram, int* s_flag, unsigned* pub) {
   constexpr int R1 = Cfg<RP>::R1;
-  if (L.S > 1) {
-    float* pp = a.ppart + L.ppart_off + ((int64_t)T.rb * L.S + T.seg) * L.r1 * RP;
+  if (L.s1 > 1) {
+    float* pp = a.ppart + L.ppart_off + ((int64_t)T.rb * L.s1 + T.seg) * L.r1 * RP;
     for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) pp[idx] = s_prow[idx];
-    if (!cta_arrive_last(a.counters + L.cnt_off + L.c_rb + T.rb, (unsigned)L.S, s_flag)) return;
-    const float* pb = a.ppart + L.ppart_off + (int64_t)T.rb * L.S * L.r1 * RP;
+    if (!cta_arrive_last(a.counters + L.cnt_off + L.c_rb + T.rb, (unsigned)L.s1, s_flag)) return;
+    const float* pb = a.ppart + L.ppart_off + (int64_t)T.rb * L.s1 * L.r1 * RP;
     for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) {
       float s = 0.f;
-      for (int qq = 0; qq < L.S; ++qq) s += __ldcg(pb + (int64_t)qq * L.r1 * RP + idx);
+      for (int qq = 0; qq < L.s1; ++qq) s += __ldcg(pb + (int64_t)qq * L.r1 * RP + idx);
       s_prow[idx] = s;
     }
     __syncthreads();
@@ -523,18 +524,21 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
 // ----------------------------------------------------------------------------
 
 // One orthonormalise tile: rows chunk * NR .. + NR - 1 of layer L, NR =
-// ph_rows(RP), one thread per row (threads past NR, in a larger CTA, only
-// join the barriers).  P1 = P R^-1 by forward substitution in float64,
-// rounded to float32 and stored over P.  When the first pass was orthogonal
-// enough (the flag gram_tail set), that is the basis: at r >= 8 the tile also
-// stores it as Phat (at r <= 4 the back-project stages Phat from P1), and it
-// only counts itself done.  Otherwise the tile's rounded rows go to shared
-// memory and their Gram matrix (float64, each entry summed over the rows in
-// order) to the tile's partial slot; the CTA that completes the layer sums
-// the partials in order, factors the sum (Cholesky, R2) and stores
-// X = R2^-1, so that Phat = P1 X.  s_r: RP x RP + RP doubles; s_p1: NR x RP
-// floats; s_gram: RP x RP doubles.  pub (fused step only): the layer's X
-// flag, raised once the layer's tiles are done.
+// ph_rows(RP), one thread per row (the other threads of the CTA skip the row
+// work and only help with the sums).  P1 = P R^-1 by forward substitution in
+// float64, rounded to float32 and stored over P.  When the first pass was
+// orthogonal enough (the flag gram_tail set), that is the basis: at r >= 8
+// the tile also stores it as Phat (at r <= 4 the back-project stages Phat
+// from P1), and it only counts itself done.  Otherwise the tile's rounded
+// rows go to shared memory and their Gram matrix (float64, each entry summed
+// over the rows in order) to the tile's partial slot.  The partials are
+// summed in two levels, each in a fixed order: the last tile of each group
+// of kGramGroup tiles sums the group's partials, and the last group sums the
+// groups, factors the total (Cholesky, R2) and stores X = R2^-1, so that
+// Phat = P1 X.  (One CTA summing every tile's partial took one dependent L2
+// round trip per few loads and dominated the phase at r = 32.)  s_r: RP x RP
+// + RP doubles; s_p1: NR x RP floats; s_gram: RP x RP doubles.  pub (fused
+// step only): the layer's X flag, raised once the layer's tiles are done.
 template <int RP>
 __device__ __forceinline__ void ph_body(const StepArgs& a, const LayerDev& L, int chunk, double* s_r, float* s_p1,
                                         double* s_gram, int* s_flag, unsigned* pub) {
@@ -544,40 +548,43 @@ __device__ __forceinline__ void ph_body(const StepArgs& a, const LayerDev& L, in
   for (int e = threadIdx.x; e < RP * RP + RP; e += blockDim.x) s_r[e] = __ldcg(fr + e);
   const bool one_pass = __ldcg(fr + 2 * RP * RP + RP) != 0.0;
   __syncthreads();
-  const int row = chunk * NR + threadIdx.x;
-  const bool valid = threadIdx.x < NR && row < L.n;
-  float* prow = a.P + L.p_off + (int64_t)row * RP;
-  double x[RP];
+  if (threadIdx.x < NR) {  // whole warps (NR is a multiple of 32)
+    const int row = chunk * NR + threadIdx.x;
+    const bool valid = row < L.n;
+    float* prow = a.P + L.p_off + (int64_t)row * RP;
+    double x[RP];
 #pragma unroll
-  for (int k = 0; k < RP; ++k) x[k] = valid ? (double)__ldcg(prow + k) : 0.0;
+    for (int k = 0; k < RP; ++k) x[k] = valid ? (double)__ldcg(prow + k) : 0.0;
 #pragma unroll
-  for (int k = 0; k < RP; ++k) {
-    double s = x[k];
+    for (int k = 0; k < RP; ++k) {
+      double s = x[k];
 #pragma unroll
-    for (int j = 0; j < k; ++j) s = fma(-x[j], s_r[j * RP + k], s);
-    x[k] = s * s_r[RP * RP + k];
+      for (int j = 0; j < k; ++j) s = fma(-x[j], s_r[j * RP + k], s);
+      x[k] = s * s_r[RP * RP + k];
+    }
+    float xf[RP];
+#pragma unroll
+    for (int k = 0; k < RP; ++k) xf[k] = (float)x[k];
+    if (valid) {
+#pragma unroll
+      for (int k = 0; k < RP; ++k) prow[k] = xf[k];
+      if (RP >= 8 && one_pass)
+#pragma unroll
+        for (int k = 0; k < RP; ++k) a.Phat[L.p_off + (int64_t)row * RP + k] = xf[k];
+    }
+    if (!one_pass)
+#pragma unroll
+      for (int k = 0; k < RP; ++k) s_p1[threadIdx.x * RP + k] = valid ? xf[k] : 0.f;
   }
-  float xf[RP];
-#pragma unroll
-  for (int k = 0; k < RP; ++k) xf[k] = (float)x[k];
-  if (valid) {
-#pragma unroll
-    for (int k = 0; k < RP; ++k) prow[k] = xf[k];
-    if (RP >= 8 && one_pass)
-#pragma unroll
-      for (int k = 0; k < RP; ++k) a.Phat[L.p_off + (int64_t)row * RP + k] = xf[k];
-  }
+  unsigned* cnt = a.counters + L.cnt_off;
   if (one_pass) {
     // the layer is done once every tile has stored its rows
-    if (cta_arrive_last(a.counters + L.cnt_off + L.c_ph, (unsigned)L.nph, s_flag) && pub && threadIdx.x == 0)
+    if (cta_arrive_last(cnt + L.c_ph, (unsigned)L.nph, s_flag) && pub && threadIdx.x == 0)
       flag_raise(pub, a.epoch);
     return;
   }
-  if (threadIdx.x < NR)
-#pragma unroll
-    for (int k = 0; k < RP; ++k) s_p1[threadIdx.x * RP + k] = valid ? xf[k] : 0.f;
   __syncthreads();
-  double* gp = a.gram + L.gram_off + (int64_t)(L.nrb + L.g1) * NG;  // the P1 partials of the layer
+  double* gp = a.gram + L.gram_off + (int64_t)(L.nrb + L.g1) * NG;  // the P1 partials: tiles, then groups
   for (int e = threadIdx.x; e < NG; e += blockDim.x) {
     int i, j;
     tri_index(e, RP, i, j);
@@ -585,10 +592,23 @@ __device__ __forceinline__ void ph_body(const StepArgs& a, const LayerDev& L, in
     for (int rr = 0; rr < NR; ++rr) s = fma((double)s_p1[rr * RP + i], (double)s_p1[rr * RP + j], s);
     gp[(int64_t)chunk * NG + e] = s;
   }
-  if (!cta_arrive_last(a.counters + L.cnt_off + L.c_ph, (unsigned)L.nph, s_flag)) return;
+  const int grp = chunk / kGramGroup;
+  const int ngrp = (int)ph_groups(L.nph);
+  const int gsz = min(kGramGroup, L.nph - grp * kGramGroup);
+  if (!cta_arrive_last(cnt + L.c_phg + grp, (unsigned)gsz, s_flag)) return;
   for (int e = threadIdx.x; e < NG; e += blockDim.x) {
+    const double* src = gp + (int64_t)grp * kGramGroup * NG + e;
     double s = 0.0;
-    for (int c = 0; c < L.nph; ++c) s += __ldcg(gp + (int64_t)c * NG + e);
+#pragma unroll 8
+    for (int t = 0; t < gsz; ++t) s += __ldcg(src + (int64_t)t * NG);
+    gp[(int64_t)(L.nph + grp) * NG + e] = s;
+  }
+  if (!cta_arrive_last(cnt + L.c_ph, (unsigned)ngrp, s_flag)) return;
+  for (int e = threadIdx.x; e < NG; e += blockDim.x) {
+    const double* src = gp + (int64_t)L.nph * NG + e;
+    double s = 0.0;
+#pragma unroll 8
+    for (int g = 0; g < ngrp; ++g) s += __ldcg(src + (int64_t)g * NG);
     int i, j;
     tri_index(e, RP, i, j);
     s_gram[i * RP + j] = s;
@@ -607,7 +627,8 @@ __device__ __forceinline__ void ph_body(const StepArgs& a, const LayerDev& L, in
 }
 
 template <int RP>
-__global__ void __launch_bounds__(ph_rows(RP)) ph_kernel(const StepArgs a) {
+__global__ void __launch_bounds__(kPhThreads) ph_kernel(const StepArgs a) {
+  static_assert(ph_rows(RP) % 32 == 0 && ph_rows(RP) <= kPhThreads, "the row threads are whole warps of the CTA");
   __shared__ double s_r[RP * RP + RP];
   __shared__ float s_p1[ph_rows(RP) * RP];
   __shared__ double s_gram[RP * RP];
@@ -653,8 +674,7 @@ __global__ void __launch_bounds__(ph_rows(RP)) pf_kernel(const StepArgs a) {
 // the same Gram tail the project phase runs.
 template <int RP>
 __global__ void __launch_bounds__(kGramThreads) gram_kernel(const StepArgs a) {
-  constexpr int R1 = Cfg<RP>::R1;
-  __shared__ float s_prow[R1 * RP];
+  __shared__ float s_prow[Cfg<RP>::R1MAX * RP];
   __shared__ double s_gram[RP * RP];
   __shared__ int s_flag;
   pdl_enter();

@@ -64,7 +64,7 @@ __global__ void noalloc_tables_kernel(LayerDev L, int W, LayerDev* dL, Tile* t1,
   const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i0 == 0) *dL = L;
   for (int64_t i = i0; i < ncnt; i += stride) cnt[i] = 0u;
-  for (int64_t i = i0; i < n1; i += stride) t1[i] = Tile{0, (int32_t)(i / L.S), (int32_t)(i % L.S), 0};
+  for (int64_t i = i0; i < n1; i += stride) t1[i] = Tile{0, (int32_t)(i / L.s1), (int32_t)(i % L.s1), 0};
   for (int64_t i = i0; i < nph; i += stride) tph[i] = Tile{0, (int32_t)i, 0, 0};
   for (int64_t i = i0; i < nu; i += stride) tu[i] = Tile{0, (int32_t)(i / L.S), (int32_t)(i % L.S), 0};
   // back-project: last row tile and segment first (the rows project wrote last)
@@ -121,7 +121,10 @@ extern "C" int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers
   const std::vector<int64_t> nv{n}, mv{m};
   TileRows tr;
   if ((rc = choose_tile_rows(nv, mv, rp, W, *ks, dev, &tr))) return rc;
-  if (ks->mma_rows > 0) tr.r1 = ks->mma_rows;  // the tensor-core project tiles
+  if (ks->mma_rows > 0) {  // the tensor-core project tiles
+    tr.r1 = ks->mma_rows;
+    tr.pcols = ks->mma_cols;
+  }
   LayerDev L;
   std::memset(&L, 0, sizeof(L));
   ScratchPlan sp;
@@ -135,7 +138,7 @@ extern "C" int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers
   L.qpart_off = 0;
   L.ppart_off = 0;
   L.cnt_off = 0;
-  sp.ntiles[kProject] = (int)((int64_t)L.nrb * L.S);
+  sp.ntiles[kProject] = (int)((int64_t)L.nrb * L.s1);
   sp.ntiles[kOrthonormalise] = L.nph;
   sp.ntiles[kBackProject] = (int)((int64_t)L.t3r * L.S * W);
   sp.ntiles[kDecompress] = (int)(ceil_div(n, L.ru) * L.S);
@@ -150,9 +153,9 @@ extern "C" int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers
   for (int ph = 0; ph < kPhases; ++ph) sp.tiles[ph] = take((size_t)sp.ntiles[ph] * sizeof(Tile));
   sp.counters = take((size_t)sp.ncnt * sizeof(unsigned));
   sp.P = take((size_t)n * rp * sizeof(float));
-  sp.gram = take((size_t)(L.nrb + L.g1 + L.nph) * NG * sizeof(double));
+  sp.gram = take((size_t)gram_slots(L.nrb, L.g1, L.nph) * NG * sizeof(double));
   sp.rinv = take((size_t)rinv_len(rp) * sizeof(double));
-  sp.ppart = take(L.S > 1 ? (size_t)L.nrb * L.S * L.r1 * rp * sizeof(float) : 0);
+  sp.ppart = take(L.s1 > 1 ? (size_t)L.nrb * L.s1 * L.r1 * rp * sizeof(float) : 0);
   sp.qpart = take((size_t)L.t3r * W * ld * rp * sizeof(float));
   sp.total = pos;
   if (sp.total > kNoAllocScratchBytes)

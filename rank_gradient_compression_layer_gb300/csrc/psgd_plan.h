@@ -47,6 +47,7 @@ inline const KernelSet* kernels_for(int rp) {
 // Rows per tile of the project, back-project (least) and decompress phases.
 struct TileRows {
   int r1 = 32, r3min = 256, ru = 64;
+  int pcols = kSeg * 4;  // columns of a project tile
 };
 
 // The phase grids must hold several waves of resident CTAs, or the last,
@@ -78,8 +79,10 @@ inline int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp
   L.c_rb = L.c_p3 + L.S * W;
   L.rph = ph_rows(rp);
   L.nph = (int32_t)ceil_div(n, L.rph);
-  L.c_ph = L.c_rb + (L.S > 1 ? L.nrb : 0);
-  return (int64_t)L.c_ph + 1;
+  L.s1 = (int32_t)ceil_div(ld, tr.pcols);
+  L.c_ph = L.c_rb + (L.s1 > 1 ? L.nrb : 0);
+  L.c_phg = L.c_ph + 1;
+  return (int64_t)L.c_phg + ph_groups(L.nph);
 }
 
 // Chooses the tile rows of a layer set so that each phase grid is at least
@@ -126,7 +129,7 @@ inline int choose_tile_rows(const std::vector<int64_t>& n, const std::vector<int
 inline void layer_tiles(const LayerDev& L, int li, int W, std::vector<Tile> (&out)[kPhases]) {
   for (auto& v : out) v.clear();
   for (int rb = 0; rb < L.nrb; ++rb)
-    for (int s = 0; s < L.S; ++s) out[kProject].push_back({li, rb, s, 0});
+    for (int s = 0; s < L.s1; ++s) out[kProject].push_back({li, rb, s, 0});
   for (int t = 0; t < L.nph; ++t) out[kOrthonormalise].push_back({li, t, 0, 0});
   for (int rt = L.t3r - 1; rt >= 0; --rt)
     for (int s = L.S - 1; s >= 0; --s)

@@ -54,7 +54,7 @@ cudaError_t launch(int phase, const StepArgs& a, int tiles, cudaStream_t s) {
 #endif
     }
     case kOrthonormalise: {
-      cudaError_t e = launch_dependent(ph_kernel<kRP>, tiles, ph_rows(kRP), 0, s, a);
+      cudaError_t e = launch_dependent(ph_kernel<kRP>, tiles, kPhThreads, 0, s, a);
 #if PSGD_RP >= 8
       // the second pass's Phat rows, once per row (r <= 4: in the back-project)
       if (e == cudaSuccess) e = launch_dependent(pf_kernel<kRP>, tiles, ph_rows(kRP), 0, s, a);
@@ -117,7 +117,7 @@ cudaError_t occupancy(int phase, int W, int* ctas) {
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, u_kernel<kRP>, kUThreads, 0);
 #endif
     default:
-      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, ph_kernel<kRP>, ph_rows(kRP), 0);
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, ph_kernel<kRP>, kPhThreads, 0);
   }
 }
 
@@ -148,9 +148,9 @@ extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {
 #endif
     launch_gram,
 #if PSGD_RP >= 16
-    kMRows
+    kMRows, kMCols
 #else
-    0
+    0, 0
 #endif
 };
 

@@ -127,6 +127,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&f)[16]) {
   for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
 }
 
+// The same for 8 columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&f)[8]) {
+  uint32_t v[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "r"(taddr)
+               : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
+}
+
 // x = hi + lo, hi = x rounded to TF32 (round to nearest, ties away), lo exact.
 __device__ __forceinline__ void tf32_split(float x, float& hi, float& lo) {
   uint32_t h;
