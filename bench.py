@@ -59,7 +59,8 @@ NCU_TRAFFIC = {  # {(config, variant): (sources_sha256_prefix, bytes_per_launch)
 
 # the sources that define the phase kernels of a step and their launch
 # (the allocation-free entry point is not among them; rTop-k adds its own files)
-STEP_SOURCES = ("psgd_api.cu", "psgd_dispatch.h", "psgd_fused.cuh", "psgd_internal.h", "psgd_kernels.cuh", "psgd_plan.h",
+STEP_SOURCES = ("psgd_api.cu", "psgd_cluster.cuh", "psgd_dispatch.h", "psgd_fused.cuh", "psgd_internal.h",
+                "psgd_kernels.cuh", "psgd_mma.cuh", "psgd_plan.h", "psgd_umma.cuh",
                 "psgd_step_impl.cuh", "psgd_step_r1.cu", "psgd_step_r2.cu", "psgd_step_r4.cu", "psgd_step_r8.cu",
                 "psgd_step_r16.cu", "psgd_step_r32.cu")
 RTOPK_SOURCES = ("psgd_rtopk.cu", "psgd_rtopk.h")  # and STEP_SOURCES (the API and shared headers)
@@ -84,6 +85,11 @@ def config_of(name: str) -> workloads.Workload:
         base = workloads.c2_resnet18()
         return workloads.scaled(base, list(base.layers) * int(name[3:]), name=f"resnet18x{name[3:]}_r2_w4")
     return workloads.ALL[name]()
+
+
+def project_kernel_name(rp: int) -> str:
+    """The project phase's kernel at padded rank rp (PowerSGD, two passes)."""
+    return "p1m_kernel" if rp >= 16 else ("p1t_kernel" if rp >= 8 else "p1_kernel")
 
 
 def algorithmic_bytes(cfg: workloads.Workload, with_update: bool, momentum: bool = False) -> dict:
@@ -328,7 +334,8 @@ def run_ours(args, ws, rank, local):
     ctx = PowerSGD(cfg.layers, cfg.rank, cfg.workers, seed=cfg.seed, stream=stream, timing=True,
                    unbiased=args.unbiased, compressor="rtopk" if args.rtopk else "powersgd",
                    top_div=args.rtopk_top_div, sample_div=args.rtopk_sample_div,
-                   fused=args.fused, queue_lag_kb=args.queue_lag_kb, project_rows=args.project_rows)
+                   fused=args.fused, queue_lag_kb=args.queue_lag_kb, project_rows=args.project_rows,
+                   one_pass=args.one_pass)
     sets = 3
     grads = fill_gradients(ctx, cfg, sets, device)
     upd = ctx.empty_buffer()
@@ -421,7 +428,8 @@ def run_ours(args, ws, rank, local):
     h = kernel_sources_hash(rtopk=args.rtopk)
     traffic = None
     variant = "rtopk" if args.rtopk else (
-        ("powersgd_fused" if st["fused_step"] else "powersgd") if not (args.unbiased or args.momentum) else None)
+        ("powersgd_fused" if st["fused_step"] else ("powersgd_one_pass" if st["one_pass_project"] else "powersgd"))
+        if not (args.unbiased or args.momentum) else None)
     if (args.config, variant) in NCU_TRAFFIC and NCU_TRAFFIC[(args.config, variant)][0] == h:
         traffic = NCU_TRAFFIC[(args.config, variant)][1]
 
@@ -439,7 +447,8 @@ def run_ours(args, ws, rank, local):
                    "seed": cfg.seed, "out_update": not args.momentum,
                    "fused_momentum_update": bool(args.momentum),
                    "variant": "unbiased" if args.unbiased else (
-                       f"rtopk top 1/{args.rtopk_top_div}, sent 1/{args.rtopk_sample_div}" if args.rtopk else "powersgd"),
+                       f"rtopk top 1/{args.rtopk_top_div}, sent 1/{args.rtopk_sample_div}" if args.rtopk else
+                       "powersgd, one-pass project" if st["one_pass_project"] else "powersgd"),
                    "tile_rows": st["tile_rows"]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
@@ -450,7 +459,10 @@ def run_ours(args, ws, rank, local):
                                 f"psgd::fused_step_kernel<{st['kernel_rank']}> (the whole step: error add, E write, "
                                 "P = M Q, Gram-Schmidt, Q_w = M_w^T Phat, Qbar, U)" if st["fused_step"] else
                                 f"psgd::p1_kernel<{st['kernel_rank']}> (project: P = G Q)" if args.unbiased else
-                                f"psgd::p1_kernel<{st['kernel_rank']}> (project: error add, E write, P = M Q)"),
+                                f"psgd::p1c_kernel<{st['kernel_rank']}> (one-pass project on 8-CTA clusters: error "
+                                "add, E write, P = M Q, Y_w = M_w^T P)" if st["one_pass_project"] else
+                                f"psgd::{project_kernel_name(st['kernel_rank'])}<{st['kernel_rank']}> "
+                                "(project: error add, E write, P = M Q)"),
                      "algorithmic_bytes_per_launch": project_bytes, "launch_ms": round(project_ms, 5),
                      "launch_ms_source": "CUDA events around the kernel on the context's stream, "
                                          "averaged over a second pass of the timed steps with per-phase events",
@@ -549,6 +561,8 @@ def main():
     ap.add_argument("--fused", action="store_true",
                     help="time the fused step (one launch per step over a queue of every phase's tiles, r <= 4)")
     ap.add_argument("--queue-lag-kb", type=int, default=0, help="fused step: queue lag between a layer's phases")
+    ap.add_argument("--one-pass", action="store_true",
+                    help="time the one-pass project (Y_w = M_w^T P in the project phase; r <= 4)")
     ap.add_argument("--project-rows", type=int, default=0, help="rows per project tile (0: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unbiased", action="store_true",

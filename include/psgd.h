@@ -50,7 +50,24 @@
  * launched as a programmatic dependent of the one before; none waits on
  * another CTA.  At r >= 16 the project phase's products run on the tensor
  * cores (tcgen05, error-compensated TF32); a wait on them that runs out is
- * reported as PSGD_ERR_TIMEOUT.  With options.fused (padded rank 1, 2 or 4, one process) a step
+ * reported as PSGD_ERR_TIMEOUT.
+ *
+ * One-pass project (options.one_pass; psgd_step at padded rank 1, 2 or 4,
+ * every worker in this process): the project phase runs on clusters of
+ * 8 CTAs that together hold whole rows of a layer and exchange the row
+ * block's partial P rows through distributed shared memory, so each block's
+ * P rows are complete on chip; the CTAs then accumulate Y_w = M_w^T P from
+ * the M rows they just wrote (read back from L2).  Since Phat = P R^-1 after
+ * one Cholesky-QR pass, Q_w = M_w^T Phat = Y_w R^-1, and the back-project
+ * forms Q_w from Y without reading M from memory again -- for each layer
+ * whose P has kappa_F(R) <= 128 (the rounding of Y R^-1 grows with kappa);
+ * other layers' back-project reads M as in the two-pass form.  The kernels
+ * per step are the same four.  psgd_layer_flags tells which form a layer
+ * took.  A layer set whose widest layer needs more than 8 CTAs per row at
+ * the rank's thread limit (W x ceil(m / 4) > 8 x 256 x 16 / RP) keeps the
+ * two-pass form.
+ *
+ * With options.fused (padded rank 1, 2 or 4, one process) a step
  * is instead ONE launch whose CTAs take the tiles of all four phases from one
  * queue in dependency order; a tile whose inputs another CTA is still
  * producing waits for a flag.  Every such wait is bounded (options.wait_ms,
@@ -98,6 +115,8 @@ typedef struct {
   int32_t tile_rows[3];                 /* rows per tile: project, back-project (least), decompress */
   int32_t fused_step;                   /* 1: each step is one fused launch (see the header comment) */
   int64_t message_floats;               /* floats psgd_step_host writes to msg_host */
+  int32_t one_pass_project;             /* 1: psgd_step runs the one-pass project (see "Launches") */
+  int32_t reserved_;
 } psgd_stats;
 
 /* Optional knobs of psgd_create_ex (zero-initialise, then set what you need). */
@@ -117,6 +136,8 @@ typedef struct {
                            of matrix layer k - 1, so its later tiles wait until wait_ms */
   int32_t total_workers; /* workers over all processes when this context's num_workers are one
                             process's share (the split step below); 0: num_workers */
+  int32_t one_pass;     /* 1: the one-pass project where it applies (see "Launches");
+                           0: the back-project reads M again (two passes over M) */
 } psgd_options;
 
 enum { PSGD_POWERSGD = 0, PSGD_RTOPK = 1 };
@@ -311,6 +332,16 @@ int psgd_get_phase_times(psgd_ctx* ctx, float* ms);
  * and untimed steps run with the launches overlapped.
  */
 int psgd_set_timing(psgd_ctx* ctx, int on);
+
+/*
+ * How the last step treated matrix layer l (the stream is synchronised
+ * first): bit 0 of *flags set when one Cholesky-QR pass left Phat
+ * orthonormal to working precision (no second pass), bit 1 set when the
+ * back-project formed Q_w = (M_w^T P) R^-1 from the one-pass project's
+ * partials instead of reading M again (see "Launches").  0 before the first
+ * step.  PSGD_ERR_INVALID for a vector layer or a NULL argument.
+ */
+int psgd_layer_flags(psgd_ctx* ctx, int layer, int32_t* flags);
 
 /* Placement of layer l in a packed buffer: element offset, n, m, row stride. */
 int psgd_layer_info(const psgd_ctx* ctx, int layer, int64_t* offset, int64_t* n, int64_t* m,

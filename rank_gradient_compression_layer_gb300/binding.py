@@ -27,6 +27,7 @@ EXPORTS = (
     "psgd_layer_info", "psgd_plan_layout", "psgd_count_sent", "psgd_last_error", "psgd_version",
     "psgd_get_phase_times", "psgd_step_noalloc", "psgd_step_momentum", "psgd_set_timing", "psgd_get_sparse",
     "psgd_plan_queue", "psgd_exchange_sizes", "psgd_step_begin", "psgd_step_mid", "psgd_step_end",
+    "psgd_layer_flags",
 )
 
 PSGD_POWERSGD = 0
@@ -57,6 +58,8 @@ class Stats(ctypes.Structure):
         ("tile_rows", ctypes.c_int32 * 3),
         ("fused_step", ctypes.c_int32),
         ("message_floats", ctypes.c_int64),
+        ("one_pass_project", ctypes.c_int32),
+        ("reserved_", ctypes.c_int32),
     ]
 
 
@@ -65,7 +68,7 @@ class Options(ctypes.Structure):
                 ("compressor", ctypes.c_int32), ("rtopk_top_div", ctypes.c_int32),
                 ("rtopk_sample_div", ctypes.c_int32), ("fused", ctypes.c_int32), ("wait_ms", ctypes.c_int32),
                 ("queue_lag_kb", ctypes.c_int32), ("test_stall", ctypes.c_int32),
-                ("total_workers", ctypes.c_int32)]
+                ("total_workers", ctypes.c_int32), ("one_pass", ctypes.c_int32)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -99,6 +102,7 @@ def lib() -> ctypes.CDLL:
         "psgd_set_state": ([_P, ctypes.c_int, _P, ctypes.POINTER(_P)], ctypes.c_int),
         "psgd_get_stats": ([_P, ctypes.POINTER(Stats)], ctypes.c_int),
         "psgd_layer_info": ([_P, ctypes.c_int, _I64P, _I64P, _I64P, _I64P], ctypes.c_int),
+        "psgd_layer_flags": ([_P, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
         "psgd_plan_layout": ([ctypes.c_int, _I64P, _I64P, _I64P, _I64P, _I64P], ctypes.c_int),
         "psgd_count_sent": ([ctypes.c_int, _I64P, _I64P, ctypes.c_int, _I64P, _I64P], ctypes.c_int),
         "psgd_exchange_sizes": ([_P, _I64P, _I64P], ctypes.c_int),
@@ -199,7 +203,7 @@ class PowerSGD:
                  stream=None, timing: bool = False, project_rows: int = 0, unbiased: bool = False,
                  compressor: str = "powersgd", top_div: int = 100, sample_div: int = 4,
                  fused: bool = False, wait_ms: int = 0, queue_lag_kb: int = 0, test_stall: int = 0,
-                 total_workers: int = 0):
+                 total_workers: int = 0, one_pass: bool = False):
         import torch
 
         if not torch.cuda.is_available():
@@ -214,7 +218,7 @@ class PowerSGD:
         opt = Options(int(bool(timing)), int(project_rows), int(bool(unbiased)),
                       PSGD_RTOPK if compressor == "rtopk" else PSGD_POWERSGD, int(top_div), int(sample_div),
                       int(bool(fused)), int(wait_ms), int(queue_lag_kb), int(test_stall),
-                      int(total_workers))
+                      int(total_workers), int(bool(one_pass)))
         h = _P()
         _check(lib().psgd_create_ex(ctypes.byref(h), len(self.shapes), n, m, self.rank, self.workers,
                                     ctypes.c_uint64(self.seed), _stream_ptr(stream), ctypes.byref(opt)))
@@ -349,6 +353,14 @@ class PowerSGD:
         _check(lib().psgd_get_sparse(self._h, layer, worker, _ptr(idx), _ptr(val), None))
         return idx, val
 
+    def layer_flags(self, layer: int) -> dict:
+        """How the last step treated matrix layer ``layer``: ``one_pass_qr`` (one
+        Cholesky-QR pass sufficed) and ``q_from_y`` (Q_w formed from the one-pass
+        project's partials, M not read again)."""
+        f = ctypes.c_int32(0)
+        _check(lib().psgd_layer_flags(self._h, layer, ctypes.byref(f)))
+        return {"one_pass_qr": bool(f.value & 1), "q_from_y": bool(f.value & 2)}
+
     def get_Qw(self, layer: int, worker: int):
         import torch
         n, m = self._shape(layer)
@@ -397,6 +409,11 @@ class PowerSGD:
     def fused(self) -> bool:
         """True when each step is one fused launch."""
         return bool(self.stats()["fused_step"])
+
+    @property
+    def one_pass(self) -> bool:
+        """True when each step runs the one-pass project (no second read of M)."""
+        return bool(self.stats()["one_pass_project"])
 
     @property
     def message_floats(self) -> int:

@@ -221,6 +221,13 @@ struct psgd_ctx {
   Tile *d_gram_tiles = nullptr, *d_mat_u_tiles = nullptr;
   XEntry *d_xp = nullptr, *d_xq = nullptr;
   int64_t xp_floats = 0, xq_floats = 0;
+  // the one-pass project (psgd_step at padded rank <= 4): cluster items over
+  // the layers' row groups, and the Y partials they write
+  bool ypath = false;
+  std::vector<Tile> ytiles;
+  Tile* d_ytiles = nullptr;
+  float* ypart = nullptr;
+  int64_t y_total = 0;
   // stats
   int64_t steps = 0, sent_step = 0, unc_step = 0, mat_el = 0, vec_el = 0;
 };
@@ -231,7 +238,7 @@ void free_all(psgd_ctx* c) {
   void* ptrs[] = {c->B, c->P, c->Phat, c->Qbar, c->Qw, c->qpart, c->ppart, c->gram, c->rinv, c->counters,
                   c->d_layers, c->d_vecs, c->d_tiles[0], c->d_tiles[1], c->d_tiles[2], c->d_tiles[3], c->d_pack,
                   c->e_scratch, c->stage_G, c->stage_U, c->stage_msg, c->d_queue[0], c->d_queue[1], c->flags,
-                  c->sync_words, c->d_gram_tiles, c->d_mat_u_tiles, c->d_xp, c->d_xq};
+                  c->sync_words, c->d_gram_tiles, c->d_mat_u_tiles, c->d_xp, c->d_xq, c->d_ytiles, c->ypart};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   rtopk_destroy(c->rk);
@@ -250,6 +257,51 @@ int dalloc(T** p, int64_t count, const char* what) {
     return cuda_fail(e, what);
   }
   return PSGD_OK;
+}
+
+// Waves of resident CTAs the one-pass project's row groups aim for.
+constexpr int kYWaves = 4;
+
+// The one-pass project's plan: per layer the column split and the row
+// groups (sized so that the grid is about kYWaves waves of the resident
+// clusters), their counters, Gram and Y partial slots, and the cluster items
+// (kYClusterMax / cw row groups each), the largest layers first.  Leaves
+// c->ypath false when a layer does not fit or no cluster fits on the GPU.
+void plan_one_pass(psgd_ctx* c) {
+  for (LayerDev& L : c->hl)
+    if (!plan_ycols(L, c->rp, c->W, kYClusterMax)) c->ypath = false;
+  int clusters = 0;
+  if (c->ypath && (c->ks->occupancy_cluster(kYClusterMax, &clusters) != cudaSuccess || clusters <= 0)) {
+    cudaGetLastError();
+    c->ypath = false;
+  }
+  if (!c->ypath) {
+    for (LayerDev& L : c->hl) L.cw = L.yfc = 0;
+    return;
+  }
+  const int rp = c->rp, NG = rp * (rp + 1) / 2;
+  int64_t bytes = 0;
+  for (const LayerDev& L : c->hl) bytes += 12LL * L.n * L.ld * c->W;
+  const int64_t target = std::max<int64_t>(1, bytes / ((int64_t)clusters * kYClusterMax * kYWaves));
+  for (LayerDev& L : c->hl) {
+    plan_yrows(L, rp, c->W, target);
+    L.c_yg = (int32_t)(c->n_counters - L.cnt_off);
+    c->n_counters += ceil_div(L.nyg, kGramGroup);
+    L.ygram_off = c->gram_total;
+    c->gram_total += (L.nyg + ceil_div(L.nyg, kGramGroup)) * NG;
+    L.y_off = c->y_total;
+    c->y_total += (int64_t)L.nyg * c->W * L.ld * rp;
+  }
+  std::vector<int> order(c->hl.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+    return (int64_t)c->hl[x].n * c->hl[x].ld > (int64_t)c->hl[y].n * c->hl[y].ld;
+  });
+  for (int li : order) {
+    const LayerDev& L = c->hl[li];
+    const int sub = kYClusterMax / L.cw;
+    for (int g0 = 0; g0 < L.nyg; g0 += sub) c->ytiles.push_back({li, g0, 0, 0});
+  }
 }
 
 // Tiles of every phase.  Back-project walks the layers and rows in the
@@ -561,6 +613,11 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     c->unc_step += n[l] * m[l];
   }
   build_tiles(c);
+  // the one-pass project (options.one_pass): PowerSGD at padded rank <= 4,
+  // every worker in this process, four phase kernels
+  c->ypath = c->ks->launch_cluster && !c->unbiased && !rtopk && opt && opt->one_pass > 0 && !opt->fused &&
+             !c->hl.empty() && c->total_workers == c->W;
+  if (c->ypath) plan_one_pass(c);
   // the fused step: PowerSGD at padded rank <= 4 with at least one matrix
   c->fused = c->ks->launch_fused && !c->unbiased && !rtopk && opt && opt->fused && !c->hl.empty() &&
              c->total_workers == c->W;
@@ -622,6 +679,8 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
   ALLOC(d_xp, (int64_t)c->xp.size());
   ALLOC(d_xq, (int64_t)c->xq.size());
   ALLOC(sync_words, 4);
+  ALLOC(ypart, c->y_total);
+  ALLOC(d_ytiles, (int64_t)c->ytiles.size());
   if (c->fused) {
     ALLOC(d_queue[0], (int64_t)c->queue[0].size());
     ALLOC(d_queue[1], (int64_t)c->queue[1].size());
@@ -644,6 +703,7 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     CUDA_TRY(cudaMemsetAsync(c->Qbar, 0, (size_t)std::max<int64_t>(c->q_total, 1) * sizeof(float), s));
     CUDA_TRY(cudaMemsetAsync(c->Qw, 0, (size_t)std::max<int64_t>(W * c->q_total, 1) * sizeof(float), s));
     CUDA_TRY(cudaMemsetAsync(c->counters, 0, (size_t)std::max<int64_t>(c->n_counters, 1) * sizeof(unsigned), s));
+    CUDA_TRY(cudaMemsetAsync(c->rinv, 0, (size_t)std::max<int64_t>(c->rinv_total, 1) * sizeof(double), s));
     if (!c->hl.empty())
       CUDA_TRY(cudaMemcpyAsync(c->d_layers, c->hl.data(), c->hl.size() * sizeof(LayerDev),
                                cudaMemcpyHostToDevice, s));
@@ -664,6 +724,7 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     if (!rcu) rcu = up(c->d_mat_u_tiles, c->mat_u_tiles.data(), c->mat_u_tiles.size() * sizeof(Tile));
     if (!rcu) rcu = up(c->d_xp, c->xp.data(), c->xp.size() * sizeof(XEntry));
     if (!rcu) rcu = up(c->d_xq, c->xq.data(), c->xq.size() * sizeof(XEntry));
+    if (!rcu) rcu = up(c->d_ytiles, c->ytiles.data(), c->ytiles.size() * sizeof(Tile));
     if (rcu) return rcu;
     if (c->fused) {
       for (int q = 0; q < 2; ++q)
@@ -813,11 +874,21 @@ int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, flo
     c->steps += 1;
     return PSGD_OK;
   }
+  if (c->ypath) {
+    a.ypath = 1;
+    a.ypart = c->ypart;
+  }
   for (int ph = 0; ph < kPhases; ++ph) {
     const bool skip = c->unbiased && (ph == kOrthonormalise || ph == kBackProject);
     if (ph < phases && !skip) {
       a.tiles = c->d_tiles[ph];
-      cudaError_t e = c->ks->launch(ph, a, (int)c->tiles[ph].size(), c->stream);
+      cudaError_t e;
+      if (ph == kProject && c->ypath) {
+        a.tiles = c->d_ytiles;
+        e = c->ks->launch_cluster(a, (int)c->ytiles.size(), kYClusterMax, c->stream);
+      } else {
+        e = c->ks->launch(ph, a, (int)c->tiles[ph].size(), c->stream);
+      }
       if (e != cudaSuccess) {
         c->broken = true;
         return cuda_fail(e, "phase kernel launch");
@@ -1150,6 +1221,8 @@ int psgd_get_stats(const psgd_ctx* c, psgd_stats* out) {
   out->vector_elements = c->vec_el;
   out->buffer_elements = c->total;
   for (int ph = 0; ph < kPhases; ++ph) out->tiles[ph] = (int64_t)c->tiles[ph].size();
+  if (c->ypath) out->tiles[kProject] = (int64_t)c->ytiles.size() * kYClusterMax;
+  out->one_pass_project = c->ypath ? 1 : 0;
   out->kernel_rank = c->rp;
   for (int i = 0; i < 3; ++i) out->tile_rows[i] = c->tile_rows[i];
   out->launches_per_step = kPhases + (c->rp >= 8 ? 1 : 0);  // r >= 8: the second pass's Phat rows
@@ -1159,6 +1232,22 @@ int psgd_get_stats(const psgd_ctx* c, psgd_stats* out) {
   out->fused_step = c->fused ? 1 : 0;
   if (c->rk) out->launches_per_step = rtopk_launches(c->rk);
   out->message_floats = c->msg_floats;
+  return PSGD_OK;
+}
+
+int psgd_layer_flags(psgd_ctx* c, int layer, int32_t* flags) {
+  int rc = ctx_ok(c);
+  if (rc) return rc;
+  if (!flags) return fail(PSGD_ERR_INVALID, "flags must not be NULL");
+  const LayerDev* L = nullptr;
+  if ((rc = matrix_layer(c, layer, &L))) return rc;
+  *flags = 0;
+  if (c->steps == 0) return PSGD_OK;
+  double f[2] = {0.0, 0.0};
+  const int64_t at = L->rinv_off + 2 * (int64_t)c->rp * c->rp + c->rp;
+  CUDA_TRY(cudaMemcpyAsync(f, c->rinv + at, sizeof(f), cudaMemcpyDeviceToHost, c->stream));
+  CUDA_TRY(cudaStreamSynchronize(c->stream));
+  *flags = (f[0] != 0.0 ? 1 : 0) | (f[1] != 0.0 ? 2 : 0);
   return PSGD_OK;
 }
 

@@ -25,9 +25,23 @@ constexpr int64_t gram_slots(int64_t nrb, int64_t g1, int64_t nph) { return nrb 
 
 // Doubles per layer of the factor record: R of the first Cholesky-QR pass
 // (RP x RP, row-major) and 1 / diag R (RP); X = R2^-1 of the second pass
-// (RP x RP, upper triangular); a flag that is 1 when the first pass alone is
-// orthogonal enough (then Phat = P1 and X is not formed).
-constexpr int64_t rinv_len(int rp) { return 2 * (int64_t)rp * rp + rp + 1; }
+// (RP x RP, upper triangular) -- or, when the one-pass back-project applies,
+// R^-1; a flag that is 1 when the first pass alone is orthogonal enough
+// (then Phat = P1 and no second pass is formed); a flag that is 1 when the
+// project phase formed Y_w = M_w^T P and P is well enough conditioned that
+// Q_w = Y_w R^-1 (the back-project then reads no M).
+constexpr int64_t rinv_len(int rp) { return 2 * (int64_t)rp * rp + rp + 2; }
+
+// The one-pass project (padded rank <= 4): clusters of CTAs that together
+// cover whole rows of a layer, so that a row block's P rows are complete on
+// chip and Y_w = M_w^T P is accumulated in the same pass.
+constexpr int kYThreads = 256;     // threads of a CTA
+constexpr int kYClusterMax = 8;    // CTAs per cluster (portable cluster size)
+// kappa_F(R)^2 = ||R||_F^2 ||R^-1||_F^2 at most, for Q_w = Y_w R^-1: its
+// rounding error is about kappa times that of Q_w = M_w^T Phat.
+constexpr double kYKappa2 = 128.0 * 128.0;
+__host__ __device__ constexpr int y_rows(int rp) { return 16 / rp; }       // rows of a block
+__host__ __device__ constexpr int y_pairs_max(int rp) { return 16 / rp; }  // (float4 column, worker) pairs per thread
 
 // One tile of a phase kernel (one CTA).  Meaning of the fields per phase:
 //   project:        layer, row block, segment
@@ -72,6 +86,15 @@ struct LayerDev {
   int32_t rph;        // rows per orthonormalise tile (ph_rows)
   int32_t s1;         // project tiles per row block (column blocks: segments, or half segments)
   int32_t c_phg;      // orthonormalise tiles done per tile group, second pass (ph_groups(nph))
+  // one-pass project (cw = 0: the layer is not on it): cw CTAs across a row,
+  // yfc float4 columns each; row groups of ryg rows (nyg of them), one per
+  // group of cw CTAs; their Gram partials (nyg + ceil(nyg / kGramGroup)
+  // slots) and Y partials (nyg x W x ld x RP floats)
+  int32_t cw, yfc, ryg, nyg;
+  int32_t c_yg;       // row groups done per Gram group (ceil(nyg / kGramGroup))
+  int32_t ypad_;
+  int64_t ygram_off;  // doubles
+  int64_t y_off;      // floats
 };
 
 // The fused step runs every phase's tiles from one queue; an item is a Tile
@@ -139,6 +162,11 @@ struct StepArgs {
   // qbar_scale * sum over this process's workers of Q_w (1 / W in one process)
   int32_t split;
   float qbar_scale;
+  // one-pass project: the project phase runs the cluster kernel over the
+  // layers' row groups and writes Y partials here; the factor's last
+  // arriver decides per layer whether the back-project uses them
+  int32_t ypath;
+  float* ypart;
 };
 
 }  // namespace psgd

@@ -244,34 +244,30 @@ __device__ void warp_tri_inverse(const double* fr, double* X) {
   for (int j = 0; j < RP; ++j) X[k * RP + j] = x[j];
 }
 
-// CTA that completed row block rb of layer L (P rows in s_prow): Gram partial
-// of the rows, then the fixed-order group and layer sums, then the factor.
-// pub (fused step only): the layer's R flag, raised once R is stored.
+// The CTA has stored the Gram partial of slot `slot` (of nslots) at
+// gp + slot * NG.  The slots are summed in groups of kGramGroup (the group's
+// last arriver, counter cgrp[group]; the group sum goes to slot nslots +
+// group), then over the groups (the layer's last arriver); each sum in a
+// fixed order.  The layer's last arriver factors the total: R (Cholesky),
+// R^-1, and the flags of the factor record.  pub (fused step only): the
+// layer's R flag, raised once R is stored.
 template <int RP>
-__device__ void gram_tail(const StepArgs& a, const LayerDev& L, int rb, const float* s_prow, int nrows,
-                          double* s_gram, int* s_flag, unsigned* pub) {
+__device__ void gram_finish(const StepArgs& a, const LayerDev& L, double* gp, int slot, int nslots, unsigned* cgrp,
+                            double* s_gram, int* s_flag, unsigned* pub) {
   constexpr int NG = Cfg<RP>::NG;
-  unsigned* cnt = a.counters + L.cnt_off;
-  double* gp = a.gram + L.gram_off;
-  for (int e = threadIdx.x; e < NG; e += blockDim.x) {
-    int i, j;
-    tri_index(e, RP, i, j);
-    double s = 0.0;
-    for (int rr = 0; rr < nrows; ++rr) s = fma((double)s_prow[rr * RP + i], (double)s_prow[rr * RP + j], s);
-    gp[(int64_t)rb * NG + e] = s;
-  }
-  const int grp = rb / kGramGroup;
-  const int gsz = min(kGramGroup, L.nrb - grp * kGramGroup);
-  if (!cta_arrive_last(cnt + L.c_grp + grp, (unsigned)gsz, s_flag)) return;
+  const int grp = slot / kGramGroup;
+  const int ngrp = (nslots + kGramGroup - 1) / kGramGroup;
+  const int gsz = min(kGramGroup, nslots - grp * kGramGroup);
+  if (!cta_arrive_last(cgrp + grp, (unsigned)gsz, s_flag)) return;
   for (int e = threadIdx.x; e < NG; e += blockDim.x) {
     double s = 0.0;
     for (int t = 0; t < gsz; ++t) s += __ldcg(gp + (int64_t)(grp * kGramGroup + t) * NG + e);
-    gp[(int64_t)(L.nrb + grp) * NG + e] = s;
+    gp[(int64_t)(nslots + grp) * NG + e] = s;
   }
-  if (!cta_arrive_last(cnt + L.c_gram, (unsigned)L.g1, s_flag)) return;
+  if (!cta_arrive_last(a.counters + L.cnt_off + L.c_gram, (unsigned)ngrp, s_flag)) return;
   for (int e = threadIdx.x; e < NG; e += blockDim.x) {
     double s = 0.0;
-    for (int g = 0; g < L.g1; ++g) s += __ldcg(gp + (int64_t)(L.nrb + g) * NG + e);
+    for (int g = 0; g < ngrp; ++g) s += __ldcg(gp + (int64_t)(nslots + g) * NG + e);
     int i, j;
     tri_index(e, RP, i, j);
     s_gram[i * RP + j] = s;
@@ -298,12 +294,37 @@ __device__ void gram_tail(const StepArgs& a, const LayerDev& L, int rb, const fl
       r2 += __shfl_xor_sync(kFull, r2, o);
       x2 += __shfl_xor_sync(kFull, x2, o);
     }
-    if (threadIdx.x == 0) fr[2 * RP * RP + RP] = (r2 * x2 <= 1e6) ? 1.0 : 0.0;
+    // The one-pass back-project (Q_w = Y_w R^-1) when the project phase
+    // formed Y and P is well conditioned: R^-1 goes to the X slot.
+    const bool yk = a.ypath != 0 && r2 * x2 <= kYKappa2;
+    if (yk)
+      for (int e = threadIdx.x; e < RP * RP; e += 32) fr[RP * RP + RP + e] = s_gram[e];
+    if (threadIdx.x == 0) {
+      fr[2 * RP * RP + RP] = (r2 * x2 <= 1e6) ? 1.0 : 0.0;
+      fr[2 * RP * RP + RP + 1] = yk ? 1.0 : 0.0;
+    }
     if (pub) {
       __syncwarp();
       if (threadIdx.x == 0 && L.index != a.stall_layer) flag_raise(pub, a.epoch);
     }
   }
+}
+
+// CTA that completed row block rb of layer L (P rows in s_prow): Gram partial
+// of the rows, then gram_finish over the layer's row blocks.
+template <int RP>
+__device__ void gram_tail(const StepArgs& a, const LayerDev& L, int rb, const float* s_prow, int nrows,
+                          double* s_gram, int* s_flag, unsigned* pub) {
+  constexpr int NG = Cfg<RP>::NG;
+  double* gp = a.gram + L.gram_off;
+  for (int e = threadIdx.x; e < NG; e += blockDim.x) {
+    int i, j;
+    tri_index(e, RP, i, j);
+    double s = 0.0;
+    for (int rr = 0; rr < nrows; ++rr) s = fma((double)s_prow[rr * RP + i], (double)s_prow[rr * RP + j], s);
+    gp[(int64_t)rb * NG + e] = s;
+  }
+  gram_finish<RP>(a, L, gp, rb, L.nrb, a.counters + L.cnt_off + L.c_grp, s_gram, s_flag, pub);
 }
 
 // ----------------------------------------------------------------------------
@@ -527,9 +548,10 @@ __global__ void __launch_bounds__(32 * Cfg<RP>::P1_WARPS, Cfg<RP>::P1_MINB) p1_k
 // ph_rows(RP), one thread per row (the other threads of the CTA skip the row
 // work and only help with the sums).  P1 = P R^-1 by forward substitution in
 // float64, rounded to float32 and stored over P.  When the first pass was
-// orthogonal enough (the flag gram_tail set), that is the basis: at r >= 8
-// the tile also stores it as Phat (at r <= 4 the back-project stages Phat
-// from P1), and it only counts itself done.  Otherwise the tile's rounded
+// orthogonal enough (the flag gram_finish set), that is the basis: at r >= 8,
+// and at r <= 4 when the back-project forms Q_w from Y, the tile also stores
+// it as Phat (otherwise, at r <= 4, the back-project stages Phat from P1),
+// and it only counts itself done.  Otherwise the tile's rounded
 // rows go to shared memory and their Gram matrix (float64, each entry summed
 // over the rows in order) to the tile's partial slot.  The partials are
 // summed in two levels, each in a fixed order: the last tile of each group
@@ -547,6 +569,9 @@ __device__ __forceinline__ void ph_body(const StepArgs& a, const LayerDev& L, in
   double* fr = a.rinv + L.rinv_off;
   for (int e = threadIdx.x; e < RP * RP + RP; e += blockDim.x) s_r[e] = __ldcg(fr + e);
   const bool one_pass = __ldcg(fr + 2 * RP * RP + RP) != 0.0;
+  // Phat is stored here at r >= 8, and at r <= 4 when the back-project
+  // forms Q_w from Y (it then stages no Phat rows)
+  const bool store_phat = one_pass && (RP >= 8 || __ldcg(fr + 2 * RP * RP + RP + 1) != 0.0);
   __syncthreads();
   if (threadIdx.x < NR) {  // whole warps (NR is a multiple of 32)
     const int row = chunk * NR + threadIdx.x;
@@ -568,7 +593,7 @@ __device__ __forceinline__ void ph_body(const StepArgs& a, const LayerDev& L, in
     if (valid) {
 #pragma unroll
       for (int k = 0; k < RP; ++k) prow[k] = xf[k];
-      if (RP >= 8 && one_pass)
+      if (store_phat)
 #pragma unroll
         for (int k = 0; k < RP; ++k) a.Phat[L.p_off + (int64_t)row * RP + k] = xf[k];
     }
@@ -691,6 +716,9 @@ __global__ void __launch_bounds__(kGramThreads) gram_kernel(const StepArgs a) {
 // ----------------------------------------------------------------------------
 // back-project: partial Q_w = M_w^T Phat over a row tile; segment finalise
 // ----------------------------------------------------------------------------
+template <int RP>
+__device__ void qbar_segment(const StepArgs& a, const LayerDev& L, int seg, int* s_flag, unsigned* pub);
+
 // pub (fused step only): the segment's Qbar flag, raised once Qbar is stored.
 template <int RP>
 __device__ void qf_segment_worker(const StepArgs& a, const LayerDev& L, int seg, int w, int* s_flag, unsigned* pub) {
@@ -726,6 +754,17 @@ __device__ void qf_segment_worker(const StepArgs& a, const LayerDev& L, int seg,
     }
     reinterpret_cast<float4*>(qw)[q] = s;
   }
+  qbar_segment<RP>(a, L, seg, s_flag, pub);
+}
+
+// The CTA has stored Q_w of one worker over segment seg: the segment's last
+// worker forms Qbar = qbar_scale * sum_w Q_w (worker order).
+template <int RP>
+__device__ void qbar_segment(const StepArgs& a, const LayerDev& L, int seg, int* s_flag, unsigned* pub) {
+  const int col0 = seg * kSeg * 4;
+  const int col1 = min(L.ld, col0 + kSeg * 4);
+  const int n4 = (col1 - col0) * RP / 4;
+  const int64_t e0 = (int64_t)col0 * RP;
   if (!cta_arrive_last(a.counters + L.cnt_off + L.c_qs + seg, (unsigned)a.W, s_flag)) return;
   const float invw = a.qbar_scale;
   for (int q = threadIdx.x; q < n4; q += blockDim.x) {
@@ -743,6 +782,56 @@ __device__ void qf_segment_worker(const StepArgs& a, const LayerDev& L, int seg,
     __syncthreads();
     if (threadIdx.x == 0) flag_raise(pub, a.epoch);
   }
+}
+
+// One-pass back-project of worker w over segment seg: Y_w = sum over the
+// row groups of the Y partials (float64, group order), Q_w = Y_w R^-1
+// (float64, rounded), then Qbar as in the two-pass form.  s_x: RP x RP
+// doubles.
+template <int RP>
+__device__ void qy_segment_worker(const StepArgs& a, const LayerDev& L, int seg, int w, double* s_x, int* s_flag) {
+  const double* ri = a.rinv + L.rinv_off + RP * RP + RP;
+  for (int e = threadIdx.x; e < RP * RP; e += blockDim.x) s_x[e] = __ldg(ri + e);
+  __syncthreads();
+  const int col0 = seg * kSeg * 4;
+  const int col1 = min(L.ld, col0 + kSeg * 4);
+  const int64_t gstride = (int64_t)a.W * L.ld * RP;  // from one row group to the next
+  const float* yp = a.ypart + L.y_off + (int64_t)w * L.ld * RP;
+  float* qw = a.Qw + (int64_t)w * a.q_total + L.q_off;
+  for (int c = col0 + (int)threadIdx.x; c < col1; c += blockDim.x) {
+    double y[RP];
+#pragma unroll
+    for (int k = 0; k < RP; ++k) y[k] = 0.0;
+    const float* src = yp + (int64_t)c * RP;
+#pragma unroll 4
+    for (int g = 0; g < L.nyg; ++g) {
+      float v[RP];
+      if constexpr (RP == 4) {
+        const float4 x = __ldcs(reinterpret_cast<const float4*>(src + g * gstride));
+        v[0] = x.x;
+        v[1] = x.y;
+        v[2] = x.z;
+        v[3] = x.w;
+      } else if constexpr (RP == 2) {
+        const float2 x = __ldcs(reinterpret_cast<const float2*>(src + g * gstride));
+        v[0] = x.x;
+        v[1] = x.y;
+      } else {
+#pragma unroll
+        for (int k = 0; k < RP; ++k) v[k] = __ldcs(src + g * gstride + k);
+      }
+#pragma unroll
+      for (int k = 0; k < RP; ++k) y[k] += (double)v[k];
+    }
+#pragma unroll
+    for (int k = 0; k < RP; ++k) {
+      double q = 0.0;
+#pragma unroll
+      for (int j = 0; j <= k; ++j) q = fma(y[j], s_x[j * RP + k], q);
+      qw[(int64_t)c * RP + k] = (float)q;
+    }
+  }
+  qbar_segment<RP>(a, L, seg, s_flag, nullptr);
 }
 
 // Back-project: rank slices per row group (warps that read the same rows),
@@ -770,6 +859,12 @@ __device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, float*
   static_assert(p3_dyn_bytes(RP) >= (size_t)NW * UNR * RP * sizeof(float), "s_red holds every warp's P1 rows");
   const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
   const int rt = t.a, seg = t.b, w = t.c;
+  if (!FUSED && RP <= 4 && __ldg(a.rinv + L.rinv_off + 2 * RP * RP + RP + 1) != 0.0) {
+    // the project phase formed Y_w = M_w^T P: one tile per (segment, worker)
+    // forms Q_w from it, and no tile reads M
+    if (rt == 0) qy_segment_worker<RP>(a, L, seg, w, s_x, s_flag);
+    return;
+  }
   const int row0 = rt * L.r3;
   const int nrows = min(L.r3, L.n - row0);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

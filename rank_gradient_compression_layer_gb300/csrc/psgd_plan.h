@@ -85,6 +85,33 @@ inline int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp
   return (int64_t)L.c_phg + ph_groups(L.nph);
 }
 
+// One-pass project, columns: cw CTAs across a row (a power of two up to the
+// cluster size cs), the least that keeps a CTA at <= 2 pairs (float4 column
+// x worker) per thread, if any does; false when even cs CTAs would give a
+// thread more than y_pairs_max(rp) pairs.
+inline bool plan_ycols(LayerDev& L, int rp, int W, int cs) {
+  int cw = 1;
+  while (cw < cs && ceil_div(L.F, cw) * W > 2 * kYThreads) cw *= 2;
+  if (ceil_div(L.F, cw) * W > (int64_t)kYThreads * y_pairs_max(rp)) return false;
+  L.cw = cw;
+  L.yfc = (int32_t)ceil_div(L.F, cw);
+  return true;
+}
+
+// One-pass project, rows: row groups of about `target` bytes of traffic per
+// CTA (G and B read, B written), a multiple of the block rows, at least 8 r
+// rows (a group's Y partial, W x ld x r floats written and read once, stays
+// under 1 / 12 of its M traffic) and at most 64 r.
+inline void plan_yrows(LayerDev& L, int rp, int W, int64_t target) {
+  const int R = y_rows(rp);
+  const int64_t row_bytes = 48LL * L.yfc * W;
+  int64_t ryg = target / std::max<int64_t>(row_bytes, 1);
+  ryg = std::min<int64_t>(std::max<int64_t>(ryg, std::max(R, 8 * rp)), 64 * rp);
+  ryg = std::min<int64_t>(ceil_div(ryg, R) * R, ceil_div(L.n, R) * R);
+  L.ryg = (int32_t)ryg;
+  L.nyg = (int32_t)ceil_div(L.n, ryg);
+}
+
 // Chooses the tile rows of a layer set so that each phase grid is at least
 // kWaves waves of resident CTAs (or the rows reach their floor); decompress
 // tiles keep their size (their cost is the per-tile set-up, not the tail).

@@ -3,6 +3,7 @@
 #include "psgd_kernels.cuh"
 #if PSGD_RP <= 4
 #include "psgd_fused.cuh"
+#include "psgd_cluster.cuh"
 #endif
 #if PSGD_RP >= 16
 #include "psgd_mma.cuh"
@@ -94,6 +95,10 @@ cudaError_t prepare() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(p1m_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MmaCfg<kRP>::SMEM);
 #endif
+#if PSGD_RP <= 4
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(p1c_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)YCfg<kRP>::SMEM);
+#endif
   return e;
 }
 
@@ -135,6 +140,39 @@ cudaError_t launch_fused(const StepArgs& a, int ctas, cudaStream_t s) {
 cudaError_t occupancy_fused(int* ctas) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, fused_step_kernel<kRP>, kFThreads, 0);
 }
+
+// The one-pass project: `items` clusters of `cs` CTAs (one Tile each),
+// launched as a programmatic dependent like the phase kernels.
+cudaLaunchConfig_t cluster_config(int items, int cs, cudaStream_t s, cudaLaunchAttribute (&attr)[2], bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(items * cs));
+  cfg.blockDim = dim3((unsigned)kYThreads);
+  cfg.dynamicSmemBytes = YCfg<kRP>::SMEM;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cfg;
+}
+
+cudaError_t launch_cluster(const StepArgs& a, int items, int cs, cudaStream_t s) {
+  if (items <= 0) return cudaSuccess;
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = cluster_config(items, cs, s, attr, true);
+  return cudaLaunchKernelEx(&cfg, p1c_kernel<kRP>, a);
+}
+
+// Clusters of cs CTAs of the one-pass project that fit on the GPU at once.
+cudaError_t occupancy_cluster(int cs, int* clusters) {
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = cluster_config(1, cs, nullptr, attr, false);
+  return cudaOccupancyMaxActiveClusters(clusters, p1c_kernel<kRP>, &cfg);
+}
 #endif
 
 }  // namespace
@@ -148,9 +186,14 @@ extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {
 #endif
     launch_gram,
 #if PSGD_RP >= 16
-    kMRows, kMCols
+    kMRows, kMCols,
 #else
-    0, 0
+    0, 0,
+#endif
+#if PSGD_RP <= 4
+    launch_cluster, occupancy_cluster
+#else
+    nullptr, nullptr
 #endif
 };
 

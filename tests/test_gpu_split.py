@@ -3,7 +3,8 @@
 1. One process, the identity as all-reduce: the split step must give what a
    one-kernel-per-phase context gives (the same kernels on the same values:
    matrix layers bit for bit; vector means differ only in how the 1 / W
-   scale is applied, so to float32 rounding).
+   scale is applied, so to float32 rounding).  The split step has no
+   one-pass project: P is all-reduced before its rows are complete.
 2. Two processes sharing cuda:0, two workers each, with the all-reduces of
    P and of Q done by gloo (host copies): every process must match the
    oracle's single-process W = 4 step (PowerSGD review page, main findings,
