@@ -224,8 +224,10 @@ struct psgd_ctx {
   // the one-pass project (psgd_step at padded rank <= 4): cluster items over
   // the layers' row groups, and the Y partials they write
   bool ypath = false;
-  std::vector<Tile> ytiles;
+  std::vector<Tile> ytiles;  // y_clusters header tiles, then the segments
   Tile* d_ytiles = nullptr;
+  int y_clusters = 0;
+  size_t y_smem = 0;
   float* ypart = nullptr;
   int64_t y_total = 0;
   // stats
@@ -259,19 +261,21 @@ int dalloc(T** p, int64_t count, const char* what) {
   return PSGD_OK;
 }
 
-// Waves of resident CTAs the one-pass project's row groups aim for.
-constexpr int kYWaves = 4;
-
-// The one-pass project's plan: per layer the column split and the row
-// groups (sized so that the grid is about kYWaves waves of the resident
-// clusters), their counters, Gram and Y partial slots, and the cluster items
-// (kYClusterMax / cw row groups each), the largest layers first.  Leaves
-// c->ypath false when a layer does not fit or no cluster fits on the GPU.
+// The one-pass project's plan: per layer the column split; the dynamic
+// shared memory of the Y accumulators (the largest layer's need); the
+// clusters that fit on the GPU at once with it, each given an equal share of
+// the layers' row blocks (plan_yschedule); per layer the counters, Gram and Y
+// partial slots.  Leaves c->ypath false when a layer does not fit or no
+// cluster fits on the GPU.
 void plan_one_pass(psgd_ctx* c) {
-  for (LayerDev& L : c->hl)
-    if (!plan_ycols(L, c->rp, c->W, kYClusterMax)) c->ypath = false;
+  int64_t smem = 0;
+  for (LayerDev& L : c->hl) {
+    if (!plan_ycols(L, c->rp, c->W)) c->ypath = false;
+    else smem = std::max(smem, y_smem_bytes((int64_t)L.yfc * c->W, c->rp));
+  }
   int clusters = 0;
-  if (c->ypath && (c->ks->occupancy_cluster(kYClusterMax, &clusters) != cudaSuccess || clusters <= 0)) {
+  if (c->ypath &&
+      (c->ks->occupancy_cluster(kYClusterMax, (size_t)smem, &clusters) != cudaSuccess || clusters <= 0)) {
     cudaGetLastError();
     c->ypath = false;
   }
@@ -279,28 +283,17 @@ void plan_one_pass(psgd_ctx* c) {
     for (LayerDev& L : c->hl) L.cw = L.yfc = 0;
     return;
   }
+  c->y_smem = (size_t)smem;
+  c->y_clusters = clusters;
+  plan_yschedule(c->hl, c->rp, c->W, clusters, c->ytiles);
   const int rp = c->rp, NG = rp * (rp + 1) / 2;
-  int64_t bytes = 0;
-  for (const LayerDev& L : c->hl) bytes += 12LL * L.n * L.ld * c->W;
-  const int64_t target = std::max<int64_t>(1, bytes / ((int64_t)clusters * kYClusterMax * kYWaves));
   for (LayerDev& L : c->hl) {
-    plan_yrows(L, rp, c->W, target);
     L.c_yg = (int32_t)(c->n_counters - L.cnt_off);
-    c->n_counters += ceil_div(L.nyg, kGramGroup);
+    c->n_counters += ceil_div(L.nys, kGramGroup);
     L.ygram_off = c->gram_total;
-    c->gram_total += (L.nyg + ceil_div(L.nyg, kGramGroup)) * NG;
+    c->gram_total += (L.nys + ceil_div(L.nys, kGramGroup)) * NG;
     L.y_off = c->y_total;
-    c->y_total += (int64_t)L.nyg * c->W * L.ld * rp;
-  }
-  std::vector<int> order(c->hl.size());
-  for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
-  std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
-    return (int64_t)c->hl[x].n * c->hl[x].ld > (int64_t)c->hl[y].n * c->hl[y].ld;
-  });
-  for (int li : order) {
-    const LayerDev& L = c->hl[li];
-    const int sub = kYClusterMax / L.cw;
-    for (int g0 = 0; g0 < L.nyg; g0 += sub) c->ytiles.push_back({li, g0, 0, 0});
+    c->y_total += (int64_t)L.nys * c->W * L.ld * rp;
   }
 }
 
@@ -885,7 +878,8 @@ int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, flo
       cudaError_t e;
       if (ph == kProject && c->ypath) {
         a.tiles = c->d_ytiles;
-        e = c->ks->launch_cluster(a, (int)c->ytiles.size(), kYClusterMax, c->stream);
+        a.y_clusters = c->y_clusters;
+        e = c->ks->launch_cluster(a, c->y_clusters, kYClusterMax, c->y_smem, c->stream);
       } else {
         e = c->ks->launch(ph, a, (int)c->tiles[ph].size(), c->stream);
       }
@@ -1221,7 +1215,7 @@ int psgd_get_stats(const psgd_ctx* c, psgd_stats* out) {
   out->vector_elements = c->vec_el;
   out->buffer_elements = c->total;
   for (int ph = 0; ph < kPhases; ++ph) out->tiles[ph] = (int64_t)c->tiles[ph].size();
-  if (c->ypath) out->tiles[kProject] = (int64_t)c->ytiles.size() * kYClusterMax;
+  if (c->ypath) out->tiles[kProject] = (int64_t)c->y_clusters * kYClusterMax;
   out->one_pass_project = c->ypath ? 1 : 0;
   out->kernel_rank = c->rp;
   for (int i = 0; i < 3; ++i) out->tile_rows[i] = c->tile_rows[i];

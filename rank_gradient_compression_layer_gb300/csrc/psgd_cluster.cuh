@@ -12,21 +12,28 @@
 //
 // A layer's row is split over cw CTAs (column slices of yfc float4 columns,
 // all W workers each); cw is a power of two dividing the cluster size, and a
-// cluster of kYClusterMax CTAs holds kYClusterMax / cw such subgroups, each
-// on its own row group of ryg rows.  Per block of R rows a CTA
-//   1. streams G and B of its slice (128-bit loads), rebuilds E = B - Phat'
-//      Q_w'^T, stores M = G + E to B, and sums its share of the block's P rows
-//      (warp butterfly, then a fixed-order sum over the warps);
-//   2. pushes that share into every subgroup member's shared memory
-//      (st.shared::cluster) and arrives on the cluster barrier (release);
-//   3. streams the next block (step 1) while the barrier completes;
-//   4. waits (acquire), sums the members' shares in rank order -- every member
-//      gets the same P rows, bit for bit -- and re-reads its own M rows of the
-//      block (just written: an L2 hit) to accumulate Y in shared memory.
-// The subgroup's first CTA stores the P rows and keeps the block's float64
-// Gram sums.  At the end of the row group every CTA stores its slice of the
-// group's Y partial, and the first CTA runs the Gram tail (gram_finish) over
-// the layer's row groups.
+// cluster of kYClusterMax CTAs holds S = kYClusterMax / cw such subgroups.
+// The grid is persistent: one cluster per resident slot, each walking its own
+// run of segments (a layer's consecutive blocks of R rows; subgroup s takes
+// the segment's blocks s, s + S, ...), the runs cut for equal work.  Round i
+// of a segment, per CTA:
+//   1. for block i + 1: stream G and B of the slice (128-bit loads), rebuild
+//      E = B - Phat' Q_w'^T, store M = G + E to B, and sum this CTA's share
+//      of the block's P rows (warp butterfly, fixed-order sum over warps);
+//      interleaved with the same loop, for block i - 1 (whose P rows are
+//      known): re-read the M rows this thread stored two rounds before (L2
+//      hits) and accumulate Y_w += M_w^T P in shared memory -- the HBM
+//      stream and the L2 re-reads are in flight together;
+//   2. wait on the cluster barrier for block i's shares (pushed into every
+//      subgroup member's shared memory with st.shared::cluster, then a
+//      release arrive), sum them in rank order -- every member gets the same
+//      P rows, bit for bit -- and push block i + 1's share, arrive.
+// The subgroup's first CTA stores the P rows and keeps float64 Gram sums.
+// At the end of a segment the S subgroups' Y accumulators (same columns)
+// and Gram sums are added in subgroup order through distributed shared
+// memory, and the first subgroup stores the segment's Y partial (one slot)
+// and runs the Gram tail (gram_finish) over the layer's slots.  The result
+// does not depend on which cluster runs which segment.
 #pragma once
 
 #include "psgd_kernels.cuh"
@@ -36,13 +43,11 @@ namespace psgd {
 template <int RP>
 struct YCfg {
   static constexpr int R = y_rows(RP);         // rows of a block
-  static constexpr int PT = y_pairs_max(RP);   // (float4 column, worker) pairs per thread at most
-  static constexpr int RU = R < 4 ? R : 4;     // rows whose G and B loads are in flight together
+  static constexpr int RU = 2;                 // rows whose loads are in flight together
   static constexpr int NV = R * RP;            // P values of a block
   static constexpr int NW = kYThreads / 32;
-  // dynamic shared memory: the Y accumulators, PT x RP float4 per thread
-  static constexpr size_t SMEM = (size_t)PT * RP * kYThreads * sizeof(float4);
   static_assert(NV == 16, "a block's P values are one 16-value warp butterfly");
+  static_assert(R % RU == 0, "whole chunks of rows");
 };
 
 __device__ __forceinline__ unsigned cluster_ctarank() {
@@ -63,45 +68,78 @@ __device__ __forceinline__ unsigned cluster_index() {
 // cluster executes both, the same number of times.
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
+}
 
-// Stores v at the shared-memory location of `local` in the CTA of cluster rank `rank`.
-__device__ __forceinline__ void st_cluster_f32(const float* local, unsigned rank, float v) {
+// The shared::cluster address of `local` in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, unsigned rank) {
   const uint32_t a = (uint32_t)__cvta_generic_to_shared(local);
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(r), "f"(v) : "memory");
+  return r;
 }
 
-// The geometry of one CTA of the one-pass project.
+__device__ __forceinline__ void st_cluster_f32(const float* local, unsigned rank, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr(local, rank)), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(const float4* local, unsigned rank) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr(local, rank))
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ double ld_cluster_f64(const double* local, unsigned rank) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(cluster_addr(local, rank)) : "memory");
+  return v;
+}
+
+// The geometry of one CTA within a segment.
 struct YTile {
-  int sub, kl;              // subgroup of the cluster, rank within the subgroup
-  int g;                    // row group (>= nyg: an idle subgroup)
-  int row_begin, row_end;   // rows of the group (empty when idle)
-  int nblk;                 // blocks of R rows per group (the same in the whole cluster)
+  int sub, kl, S;           // subgroup, rank within it, subgroups of the cluster
+  int b0, b1;               // the segment's blocks [b0, b1)
+  int iters;                // rounds of S blocks (the same in the whole cluster)
   int f0, nf, ps;           // first float4 column, float4 columns and pairs of the slice
 };
 
-// Step 1 for block b: E, M (stored to B) and this thread's share of the
-// block's P values, pp[u * RP + k] (row u of the block, rank k).
+// The rows [r0, r1) of this subgroup's block in round i (empty outside the
+// segment's rounds and past its blocks).
 template <int RP>
-__device__ __forceinline__ void y_phase1(const StepArgs& a, const LayerDev& L, const YTile& Y, int b,
-                                         float (&pp)[YCfg<RP>::NV]) {
+__device__ __forceinline__ void y_block_rows(const LayerDev& L, const YTile& Y, int i, int& r0, int& r1) {
+  const int blk = Y.b0 + Y.sub + i * Y.S;
+  r0 = blk * L.yr;
+  r1 = (i >= 0 && i < Y.iters && blk < Y.b1) ? min(L.n, r0 + L.yr) : r0;
+}
+
+// One pass over this thread's pairs: step 1 for the rows [n0, n1) (E, M
+// stored to B, and this thread's share of their P values in pp[u * RP + k],
+// row n0 + u, rank k) and Y += M[rows]^T P[rows] for the rows [o0, o1),
+// whose P values are s_p (row o0 + u, rank k at u * RP + k).  s_y: RP float4
+// per pair, pair p = thread + j kYThreads at (j RP + k) kYThreads + thread.
+template <int RP>
+__device__ __forceinline__ void y_pass(const StepArgs& a, const LayerDev& L, const YTile& Y, int n0, int n1,
+                                       int o0, int o1, const float* s_p, float4* s_y, float (&pp)[YCfg<RP>::NV]) {
   using C = YCfg<RP>;
   constexpr int R = C::R, RU = C::RU;
 #pragma unroll
   for (int i = 0; i < C::NV; ++i) pp[i] = 0.f;
-  const int r0 = Y.row_begin + b * R;
+  const bool ph1 = n0 < n1, ph2 = o0 < o1;
+  if (!ph1 && !ph2) return;
   const bool prev = a.has_prev != 0;
-  const float* Pprev = a.Phat + L.p_off + (int64_t)r0 * RP;
-  for (int j = 0; j < C::PT; ++j) {
-    const int p = (int)threadIdx.x + j * kYThreads;
-    if (p >= Y.ps) break;
+  const float* Pprev = a.Phat + L.p_off + (int64_t)n0 * RP;
+  for (int p = (int)threadIdx.x, j = 0; p < Y.ps; p += kYThreads, ++j) {
     const int w = p / Y.nf, f = Y.f0 + p % Y.nf;
     const float* Gw = a.G[w] + L.off + 4 * f;
     float* Bw = a.B + (int64_t)w * a.total + L.off + 4 * f;
     // this pair's 4 rows of Q and of Q_w' (rows 4f .. 4f + 3 of ld x RP)
     float qv[4][RP], qw[4][RP];
-    {
+    if (ph1) {
       const float4* sq = reinterpret_cast<const float4*>(a.Qbar + L.q_off + (int64_t)(4 * f) * RP);
       const float4* sw = reinterpret_cast<const float4*>(a.Qw + (int64_t)w * a.q_total + L.q_off + (int64_t)(4 * f) * RP);
       float* fq = &qv[0][0];
@@ -120,25 +158,33 @@ __device__ __forceinline__ void y_phase1(const StepArgs& a, const LayerDev& L, c
         fw[4 * i + 3] = x.w;
       }
     }
+    float4 y[RP];
+    if (ph2)
+#pragma unroll
+      for (int k = 0; k < RP; ++k) y[k] = s_y[(j * RP + k) * kYThreads + threadIdx.x];
     const bool tailc = (f == L.F - 1) && (L.tail < 4);
 #pragma unroll
     for (int u0 = 0; u0 < R; u0 += RU) {
-      float4 gv[RU], bv[RU];
+      if (n0 + u0 >= n1 && o0 + u0 >= o1) break;  // blocks of fewer than R rows
+      float4 gv[RU], bv[RU], mv[RU];
 #pragma unroll
       for (int u = 0; u < RU; ++u) {
-        const int row = r0 + u0 + u;
-        if (row < Y.row_end) {
+        const int row = n0 + u0 + u;
+        if (row < n1) {
           gv[u] = __ldcs(reinterpret_cast<const float4*>(Gw + (int64_t)row * L.ld));
           bv[u] = __ldcs(reinterpret_cast<const float4*>(Bw + (int64_t)row * L.ld));
         } else {
           gv[u] = zero4();
           bv[u] = zero4();
         }
+        const int orow = o0 + u0 + u;
+        // this thread stored these M values two rounds before (program order)
+        mv[u] = orow < o1 ? __ldcg(reinterpret_cast<const float4*>(Bw + (int64_t)orow * L.ld)) : zero4();
       }
 #pragma unroll
       for (int u = 0; u < RU; ++u) {
-        const int row = r0 + u0 + u;
-        if (row < Y.row_end) {
+        const int row = n0 + u0 + u;
+        if (row < n1) {
           // E = B - Phat' Q_w'^T, k ascending (the chain of the error read-back)
           float e0 = bv[u].x, e1 = bv[u].y, e2 = bv[u].z, e3 = bv[u].w;
           if (prev) {
@@ -157,7 +203,7 @@ __device__ __forceinline__ void y_phase1(const StepArgs& a, const LayerDev& L, c
             if (L.tail < 3) m2 = 0.f;
             m3 = 0.f;
           }
-          // a plain store: the line stays in L2 for step 4's read
+          // a plain store: the line stays in L2 for the re-read two rounds on
           *reinterpret_cast<float4*>(Bw + (int64_t)row * L.ld) = make_float4(m0, m1, m2, m3);
 #pragma unroll
           for (int k = 0; k < RP; ++k) {
@@ -168,8 +214,21 @@ __device__ __forceinline__ void y_phase1(const StepArgs& a, const LayerDev& L, c
             pp[(u0 + u) * RP + k] += t;
           }
         }
+        if (o0 + u0 + u < o1) {
+#pragma unroll
+          for (int k = 0; k < RP; ++k) {
+            const float pv = s_p[(u0 + u) * RP + k];
+            y[k].x = fmaf(mv[u].x, pv, y[k].x);
+            y[k].y = fmaf(mv[u].y, pv, y[k].y);
+            y[k].z = fmaf(mv[u].z, pv, y[k].z);
+            y[k].w = fmaf(mv[u].w, pv, y[k].w);
+          }
+        }
       }
     }
+    if (ph2)
+#pragma unroll
+      for (int k = 0; k < RP; ++k) s_y[(j * RP + k) * kYThreads + threadIdx.x] = y[k];
   }
 }
 
@@ -196,128 +255,107 @@ __device__ __forceinline__ void y_push(const YTile& Y, int cw, const float* s_re
   for (int t = 0; t < cw; ++t) st_cluster_f32(dst, (unsigned)(Y.sub * cw + t), s);
 }
 
-// Step 4 for block b: Y += M[rows]^T P[rows] over this thread's pairs.
-// s_p: the block's P values (R x RP); s_y: PT x RP x kYThreads float4.
+// Shared memory of the one-pass project kernel besides the Y accumulators.
 template <int RP>
-__device__ __forceinline__ void y_phase2(const StepArgs& a, const LayerDev& L, const YTile& Y, int b,
-                                         const float* s_p, float4* s_y) {
-  using C = YCfg<RP>;
-  constexpr int R = C::R;
-  const int r0 = Y.row_begin + b * R;
-  for (int j = 0; j < C::PT; ++j) {
-    const int p = (int)threadIdx.x + j * kYThreads;
-    if (p >= Y.ps) break;
-    const int w = p / Y.nf, f = Y.f0 + p % Y.nf;
-    const float* Bw = a.B + (int64_t)w * a.total + L.off + 4 * f;
-    float4 m[R];
-#pragma unroll
-    for (int u = 0; u < R; ++u) {
-      const int row = r0 + u;
-      // this thread stored these M values in step 1 (program order)
-      m[u] = row < Y.row_end ? __ldcg(reinterpret_cast<const float4*>(Bw + (int64_t)row * L.ld)) : zero4();
-    }
-    float4 y[RP];
-#pragma unroll
-    for (int k = 0; k < RP; ++k) y[k] = s_y[(j * RP + k) * kYThreads + threadIdx.x];
-#pragma unroll
-    for (int u = 0; u < R; ++u) {
-#pragma unroll
-      for (int k = 0; k < RP; ++k) {
-        const float pv = s_p[u * RP + k];
-        y[k].x = fmaf(m[u].x, pv, y[k].x);
-        y[k].y = fmaf(m[u].y, pv, y[k].y);
-        y[k].z = fmaf(m[u].z, pv, y[k].z);
-        y[k].w = fmaf(m[u].w, pv, y[k].w);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < RP; ++k) s_y[(j * RP + k) * kYThreads + threadIdx.x] = y[k];
-  }
-}
+struct YShared {
+  float slot[2][kYClusterMax * YCfg<RP>::NV];  // the subgroup's shares of a block's P values
+  float red[2][YCfg<RP>::NW * YCfg<RP>::NV];   // the warps' shares
+  float prow[3][YCfg<RP>::NV];                 // P values of the last three blocks
+  double gacc[Cfg<RP>::NG];                    // the subgroup's Gram sums, at the end of a segment
+  double gram[RP * RP];
+  int flag;
+};
 
+// One segment of the cluster's run (every CTA of the cluster calls it).
 template <int RP>
-__global__ void __launch_bounds__(kYThreads, 2) p1c_kernel(const StepArgs a) {
+__device__ __forceinline__ void y_segment(const StepArgs& a, const Tile& sg, unsigned rank, float4* s_y,
+                                          YShared<RP>& sh) {
   using C = YCfg<RP>;
-  constexpr int R = C::R, NV = C::NV, NG = Cfg<RP>::NG;
-  extern __shared__ float4 s_y[];                   // the Y accumulators
-  __shared__ float s_slot[2][kYClusterMax * NV];    // the subgroup's shares of a block's P values
-  __shared__ float s_red[2][C::NW * NV];            // the warps' shares
-  __shared__ float s_prow[2][NV];                   // a block's P values
-  __shared__ double s_gram[RP * RP];
-  __shared__ int s_flag;
-  pdl_enter();
-  const Tile t = a.tiles[cluster_index()];
-  const LayerDev L = a.layers[t.layer];  // by value: stores to B cannot alias it
+  constexpr int NV = C::NV, NG = Cfg<RP>::NG, R = C::R;
+  const LayerDev L = a.layers[sg.layer];  // by value: stores to B cannot alias it
   const int cw = L.cw;
-  const unsigned rank = cluster_ctarank();
   YTile Y;
+  Y.S = kYClusterMax / cw;
   Y.sub = (int)rank / cw;
   Y.kl = (int)rank % cw;
-  Y.g = t.a + Y.sub;
-  Y.row_begin = Y.g * L.ryg;
-  Y.row_end = Y.g < L.nyg ? min(L.n, Y.row_begin + L.ryg) : Y.row_begin;
-  Y.nblk = (L.ryg + R - 1) / R;
+  Y.b0 = sg.a;
+  Y.b1 = sg.b;
+  Y.iters = (sg.b - sg.a + Y.S - 1) / Y.S;
   Y.f0 = Y.kl * L.yfc;
   Y.nf = max(0, min(L.F, Y.f0 + L.yfc) - Y.f0);
   Y.ps = Y.nf * a.W;
   const bool leader = Y.kl == 0;
-  for (int j = 0; j < C::PT; ++j)
+  // every CTA of the cluster is running, and done with the previous
+  // segment's shared memory (slots, Y and Gram sums), before this one
+  cluster_sync();
+  for (int p = (int)threadIdx.x, j = 0; p < Y.ps; p += kYThreads, ++j)
 #pragma unroll
     for (int k = 0; k < RP; ++k) s_y[(j * RP + k) * kYThreads + threadIdx.x] = zero4();
-  // every CTA of the cluster is running before any shared::cluster store
-  cluster_arrive();
-  cluster_wait();
 
   float pp[NV];
-  y_phase1<RP>(a, L, Y, 0, pp);
-  y_reduce_warps<RP>(pp, s_red[0]);
+  int r0, r1, n0, n1, o0, o1;
+  y_block_rows<RP>(L, Y, 0, n0, n1);
+  y_pass<RP>(a, L, Y, n0, n1, 0, 0, sh.prow[0], s_y, pp);
+  y_reduce_warps<RP>(pp, sh.red[0]);
   __syncthreads();
-  if (threadIdx.x < NV) y_push<RP>(Y, cw, s_red[0], s_slot[0]);
+  if (threadIdx.x < NV) y_push<RP>(Y, cw, sh.red[0], sh.slot[0]);
   cluster_arrive();
-  double gacc = 0.0;  // leader, thread e < NG: Gram entry e of the group
-  for (int b = 0; b < Y.nblk; ++b) {
-    const int par = b & 1;
-    const bool more = b + 1 < Y.nblk;
-    if (more) {
-      y_phase1<RP>(a, L, Y, b + 1, pp);
-      y_reduce_warps<RP>(pp, s_red[par ^ 1]);
-    }
-    cluster_wait();  // block b's shares are in s_slot[par]
+  double gacc = 0.0;  // leader, thread e < NG: Gram entry e of the subgroup's rows
+  for (int i = 0; i < Y.iters; ++i) {
+    const int par = i & 1;
+    const bool more = i + 1 < Y.iters;
+    y_block_rows<RP>(L, Y, i + 1, n0, n1);  // step 1 for the next block (empty in the last round)
+    y_block_rows<RP>(L, Y, i - 1, o0, o1);  // Y for the block before (empty in the first round)
+    y_pass<RP>(a, L, Y, n0, n1, o0, o1, sh.prow[(i + 2) % 3], s_y, pp);
+    if (more) y_reduce_warps<RP>(pp, sh.red[par ^ 1]);
+    cluster_wait();  // round i's shares are in slot[par]
     __syncthreads();
-    const int r0 = Y.row_begin + b * R;
+    y_block_rows<RP>(L, Y, i, r0, r1);
     if (threadIdx.x < NV) {
       const int v = threadIdx.x;
       float s = 0.f;
-      for (int q = 0; q < cw; ++q) s += s_slot[par][q * NV + v];
-      s_prow[par][v] = s;
+      for (int q = 0; q < cw; ++q) s += sh.slot[par][q * NV + v];
+      sh.prow[i % 3][v] = s;
       const int row = r0 + v / RP;
-      if (leader && row < Y.row_end) a.P[L.p_off + (int64_t)row * RP + v % RP] = s;
-      // the members read block b - 1's shares before arriving for block b, and
-      // every member has arrived for block b: s_slot[par ^ 1] is free
-      if (more) y_push<RP>(Y, cw, s_red[par ^ 1], s_slot[par ^ 1]);
+      if (leader && row < r1) a.P[L.p_off + (int64_t)row * RP + v % RP] = s;
+      // the members read round i - 1's shares before arriving for round i, and
+      // every member has arrived for round i: slot[par ^ 1] is free
+      if (more) y_push<RP>(Y, cw, sh.red[par ^ 1], sh.slot[par ^ 1]);
     }
     __syncthreads();
     if (leader && threadIdx.x < NG) {
-      int i, j;
-      tri_index(threadIdx.x, RP, i, j);
+      int ii, jj;
+      tri_index(threadIdx.x, RP, ii, jj);
 #pragma unroll
       for (int u = 0; u < R; ++u)
-        if (r0 + u < Y.row_end) gacc = fma((double)s_prow[par][u * RP + i], (double)s_prow[par][u * RP + j], gacc);
+        if (r0 + u < r1) gacc = fma((double)sh.prow[i % 3][u * RP + ii], (double)sh.prow[i % 3][u * RP + jj], gacc);
     }
-    y_phase2<RP>(a, L, Y, b, s_prow[par], s_y);
     if (more) cluster_arrive();
   }
-  // no shared::cluster access follows: every store into this CTA's slots
-  // preceded an arrival that the last wait covered
-  if (Y.g >= L.nyg) return;
-  float* yp = a.ypart + L.y_off + (int64_t)Y.g * a.W * L.ld * RP;
-  for (int j = 0; j < C::PT; ++j) {
-    const int p = (int)threadIdx.x + j * kYThreads;
-    if (p >= Y.ps) break;
+  y_block_rows<RP>(L, Y, Y.iters - 1, o0, o1);
+  y_pass<RP>(a, L, Y, 0, 0, o0, o1, sh.prow[(Y.iters - 1) % 3], s_y, pp);
+  if (leader && threadIdx.x < NG) sh.gacc[threadIdx.x] = gacc;
+  // every subgroup's Y and Gram sums are final
+  cluster_sync();
+  if (Y.sub != 0) return;
+  // the first subgroup adds the other subgroups' sums (the same columns) in
+  // subgroup order and stores the segment's slot
+  const int slot = sg.c;
+  float* yp = a.ypart + L.y_off + (int64_t)slot * a.W * L.ld * RP;
+  for (int p = (int)threadIdx.x, j = 0; p < Y.ps; p += kYThreads, ++j) {
     const int w = p / Y.nf, f = Y.f0 + p % Y.nf;
     float4 y[RP];
 #pragma unroll
     for (int k = 0; k < RP; ++k) y[k] = s_y[(j * RP + k) * kYThreads + threadIdx.x];
+    for (int s = 1; s < Y.S; ++s)
+#pragma unroll
+      for (int k = 0; k < RP; ++k) {
+        const float4 o = ld_cluster_f4(s_y + (j * RP + k) * kYThreads + threadIdx.x, (unsigned)(s * cw + Y.kl));
+        y[k].x += o.x;
+        y[k].y += o.y;
+        y[k].z += o.z;
+        y[k].w += o.w;
+      }
     // element (column 4f + c, rank k) at (4f + c) * RP + k
     float4* dst = reinterpret_cast<float4*>(yp + (int64_t)w * L.ld * RP + (int64_t)(4 * f) * RP);
     if constexpr (RP == 1) {
@@ -334,8 +372,27 @@ __global__ void __launch_bounds__(kYThreads, 2) p1c_kernel(const StepArgs a) {
   }
   if (!leader) return;
   double* gp = a.gram + L.ygram_off;
-  if (threadIdx.x < NG) gp[(int64_t)Y.g * NG + threadIdx.x] = gacc;
-  gram_finish<RP>(a, L, gp, Y.g, L.nyg, a.counters + L.cnt_off + L.c_yg, s_gram, &s_flag, nullptr);
+  if (threadIdx.x < NG) {
+    double g = sh.gacc[threadIdx.x];
+    for (int s = 1; s < Y.S; ++s) g += ld_cluster_f64(&sh.gacc[threadIdx.x], (unsigned)(s * cw));
+    gp[(int64_t)slot * NG + threadIdx.x] = g;
+  }
+  gram_finish<RP>(a, L, gp, slot, L.nys, a.counters + L.cnt_off + L.c_yg, sh.gram, &sh.flag, nullptr);
+}
+
+// The persistent grid: cluster c runs the segments of header tile c.  Every
+// CTA of a cluster runs the same segments and rounds, so the cluster barriers
+// match; no CTA waits on another cluster.
+template <int RP>
+__global__ void __launch_bounds__(kYThreads, 2) p1c_kernel(const StepArgs a) {
+  extern __shared__ float4 s_y[];  // the Y accumulators
+  __shared__ YShared<RP> sh;
+  pdl_enter();
+  const Tile hdr = a.tiles[cluster_index()];
+  const unsigned rank = cluster_ctarank();
+  for (int si = 0; si < hdr.b; ++si) y_segment<RP>(a, a.tiles[a.y_clusters + hdr.a + si], rank, s_y, sh);
+  // the first subgroup may still be reading this CTA's shared memory
+  cluster_sync();
 }
 
 }  // namespace psgd

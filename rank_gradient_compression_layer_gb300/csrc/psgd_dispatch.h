@@ -34,10 +34,11 @@ struct KernelSet {
   // the project phase runs on the tensor cores (padded ranks 16, 32; not the
   // unbiased variant): its tiles have mma_rows rows and mma_cols columns
   int mma_rows, mma_cols;
-  // the one-pass project (padded ranks <= 4; null above): `items` clusters
-  // of `cs` CTAs over a.tiles, and the clusters of cs CTAs resident at once
-  cudaError_t (*launch_cluster)(const StepArgs& a, int items, int cs, cudaStream_t s);
-  cudaError_t (*occupancy_cluster)(int cs, int* clusters);
+  // the one-pass project (padded ranks <= 4; null above): `clusters`
+  // clusters of `cs` CTAs with `smem` bytes of dynamic shared memory each
+  // over a.tiles, and the clusters of that shape resident at once
+  cudaError_t (*launch_cluster)(const StepArgs& a, int clusters, int cs, size_t smem, cudaStream_t s);
+  cudaError_t (*occupancy_cluster)(int cs, size_t smem, int* clusters);
 };
 
 extern const KernelSet kKernelsR1, kKernelsR2, kKernelsR4, kKernelsR8, kKernelsR16, kKernelsR32;

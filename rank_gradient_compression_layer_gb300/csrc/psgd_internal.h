@@ -37,11 +37,15 @@ constexpr int64_t rinv_len(int rp) { return 2 * (int64_t)rp * rp + rp + 2; }
 // chip and Y_w = M_w^T P is accumulated in the same pass.
 constexpr int kYThreads = 256;     // threads of a CTA
 constexpr int kYClusterMax = 8;    // CTAs per cluster (portable cluster size)
+constexpr int kYSmemMax = 64 * 1024;  // Y accumulators of a CTA at most (bytes), so 3 CTAs fit on an SM
+// M bytes a CTA writes per block at most (where a block of one row is not
+// larger): the rows are read back two blocks later, and the whole GPU's
+// blocks in between must stay in L2
+constexpr int kYBlockBytes = 64 * 1024;
 // kappa_F(R)^2 = ||R||_F^2 ||R^-1||_F^2 at most, for Q_w = Y_w R^-1: its
 // rounding error is about kappa times that of Q_w = M_w^T Phat.
 constexpr double kYKappa2 = 128.0 * 128.0;
-__host__ __device__ constexpr int y_rows(int rp) { return 16 / rp; }       // rows of a block
-__host__ __device__ constexpr int y_pairs_max(int rp) { return 16 / rp; }  // (float4 column, worker) pairs per thread
+__host__ __device__ constexpr int y_rows(int rp) { return 16 / rp; }       // rows of a block at most
 
 // One tile of a phase kernel (one CTA).  Meaning of the fields per phase:
 //   project:        layer, row block, segment
@@ -87,12 +91,13 @@ struct LayerDev {
   int32_t s1;         // project tiles per row block (column blocks: segments, or half segments)
   int32_t c_phg;      // orthonormalise tiles done per tile group, second pass (ph_groups(nph))
   // one-pass project (cw = 0: the layer is not on it): cw CTAs across a row,
-  // yfc float4 columns each; row groups of ryg rows (nyg of them), one per
-  // group of cw CTAs; their Gram partials (nyg + ceil(nyg / kGramGroup)
-  // slots) and Y partials (nyg x W x ld x RP floats)
-  int32_t cw, yfc, ryg, nyg;
-  int32_t c_yg;       // row groups done per Gram group (ceil(nyg / kGramGroup))
-  int32_t ypad_;
+  // yfc float4 columns each (a cluster holds kYClusterMax / cw such
+  // subgroups); nys partial slots, one per segment of the schedule, each
+  // with a Gram partial (nys + ceil(nys / kGramGroup) slots of NG doubles)
+  // and a Y partial (W x ld x RP floats)
+  int32_t cw, yfc, nys;
+  int32_t c_yg;       // slots done per Gram group (ceil(nys / kGramGroup))
+  int32_t yr;         // rows of a block (<= y_rows(RP)): a CTA's block of M stays about kYBlockBytes
   int64_t ygram_off;  // doubles
   int64_t y_off;      // floats
 };
@@ -162,10 +167,13 @@ struct StepArgs {
   // qbar_scale * sum over this process's workers of Q_w (1 / W in one process)
   int32_t split;
   float qbar_scale;
-  // one-pass project: the project phase runs the cluster kernel over the
-  // layers' row groups and writes Y partials here; the factor's last
-  // arriver decides per layer whether the back-project uses them
+  // one-pass project: the project phase runs the cluster kernel, one
+  // cluster per header tile (tiles[c] = {0, first segment, segments, 0}) over
+  // segment tiles (tiles[y_clusters + i] = {layer, first block, end block,
+  // first slot}), and writes Y partials here; the factor's last arriver
+  // decides per layer whether the back-project uses them
   int32_t ypath;
+  int32_t y_clusters;
   float* ypart;
 };
 

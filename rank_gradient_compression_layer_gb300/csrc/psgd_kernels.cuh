@@ -784,27 +784,31 @@ __device__ void qbar_segment(const StepArgs& a, const LayerDev& L, int seg, int*
   }
 }
 
-// One-pass back-project of worker w over segment seg: Y_w = sum over the
-// row groups of the Y partials (float64, group order), Q_w = Y_w R^-1
-// (float64, rounded), then Qbar as in the two-pass form.  s_x: RP x RP
-// doubles.
+// One-pass back-project of worker w over segment seg: Y_w = the sum of the
+// layer's Y partial slots (float64; the first half of the slots summed by
+// threads 0..127, the second by threads 128..255, each in slot order, then
+// first + second), Q_w = Y_w R^-1 (float64, rounded), then Qbar as in the
+// two-pass form.  A CTA of 256 threads; s_x: RP x RP doubles; s_half:
+// 128 x RP doubles.
 template <int RP>
-__device__ void qy_segment_worker(const StepArgs& a, const LayerDev& L, int seg, int w, double* s_x, int* s_flag) {
+__device__ void qy_segment_worker(const StepArgs& a, const LayerDev& L, int seg, int w, double* s_x, double* s_half,
+                                  int* s_flag) {
   const double* ri = a.rinv + L.rinv_off + RP * RP + RP;
   for (int e = threadIdx.x; e < RP * RP; e += blockDim.x) s_x[e] = __ldg(ri + e);
-  __syncthreads();
   const int col0 = seg * kSeg * 4;
   const int col1 = min(L.ld, col0 + kSeg * 4);
-  const int64_t gstride = (int64_t)a.W * L.ld * RP;  // from one row group to the next
-  const float* yp = a.ypart + L.y_off + (int64_t)w * L.ld * RP;
-  float* qw = a.Qw + (int64_t)w * a.q_total + L.q_off;
-  for (int c = col0 + (int)threadIdx.x; c < col1; c += blockDim.x) {
-    double y[RP];
+  const int c = col0 + (int)(threadIdx.x & 127);
+  const int h = (int)(threadIdx.x >> 7);
+  const int mid = (L.nys + 1) / 2;
+  const int g0 = h ? mid : 0, g1 = h ? L.nys : mid;
+  const int64_t gstride = (int64_t)a.W * L.ld * RP;  // from one slot to the next
+  double y[RP];
 #pragma unroll
-    for (int k = 0; k < RP; ++k) y[k] = 0.0;
-    const float* src = yp + (int64_t)c * RP;
-#pragma unroll 4
-    for (int g = 0; g < L.nyg; ++g) {
+  for (int k = 0; k < RP; ++k) y[k] = 0.0;
+  if (c < col1) {
+    const float* src = a.ypart + L.y_off + (int64_t)w * L.ld * RP + (int64_t)c * RP;
+#pragma unroll 8
+    for (int g = g0; g < g1; ++g) {
       float v[RP];
       if constexpr (RP == 4) {
         const float4 x = __ldcs(reinterpret_cast<const float4*>(src + g * gstride));
@@ -823,6 +827,15 @@ __device__ void qy_segment_worker(const StepArgs& a, const LayerDev& L, int seg,
 #pragma unroll
       for (int k = 0; k < RP; ++k) y[k] += (double)v[k];
     }
+  }
+  if (h)
+#pragma unroll
+    for (int k = 0; k < RP; ++k) s_half[(threadIdx.x & 127) * RP + k] = y[k];
+  __syncthreads();
+  if (!h && c < col1) {
+    float* qw = a.Qw + (int64_t)w * a.q_total + L.q_off;
+#pragma unroll
+    for (int k = 0; k < RP; ++k) y[k] += s_half[threadIdx.x * RP + k];
 #pragma unroll
     for (int k = 0; k < RP; ++k) {
       double q = 0.0;
@@ -862,7 +875,8 @@ __device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, float*
   if (!FUSED && RP <= 4 && __ldg(a.rinv + L.rinv_off + 2 * RP * RP + RP + 1) != 0.0) {
     // the project phase formed Y_w = M_w^T P: one tile per (segment, worker)
     // forms Q_w from it, and no tile reads M
-    if (rt == 0) qy_segment_worker<RP>(a, L, seg, w, s_x, s_flag);
+    static_assert(p3_dyn_bytes(RP) >= 128 * RP * sizeof(double), "s_red holds the second half's sums");
+    if (rt == 0) qy_segment_worker<RP>(a, L, seg, w, s_x, reinterpret_cast<double*>(s_red), s_flag);
     return;
   }
   const int row0 = rt * L.r3;

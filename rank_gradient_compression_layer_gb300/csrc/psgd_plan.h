@@ -85,31 +85,98 @@ inline int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp
   return (int64_t)L.c_phg + ph_groups(L.nph);
 }
 
-// One-pass project, columns: cw CTAs across a row (a power of two up to the
-// cluster size cs), the least that keeps a CTA at <= 2 pairs (float4 column
-// x worker) per thread, if any does; false when even cs CTAs would give a
-// thread more than y_pairs_max(rp) pairs.
-inline bool plan_ycols(LayerDev& L, int rp, int W, int cs) {
-  int cw = 1;
-  while (cw < cs && ceil_div(L.F, cw) * W > 2 * kYThreads) cw *= 2;
-  if (ceil_div(L.F, cw) * W > (int64_t)kYThreads * y_pairs_max(rp)) return false;
-  L.cw = cw;
-  L.yfc = (int32_t)ceil_div(L.F, cw);
+// Shared memory of a CTA's Y accumulators for `pairs` (float4 column,
+// worker) pairs: RP float4 per pair, in whole rounds of kYThreads pairs.
+inline int64_t y_smem_bytes(int64_t pairs, int rp) { return ceil_div(pairs, kYThreads) * kYThreads * rp * 16; }
+
+// One-pass project, columns of a layer: cw CTAs across a row (1, 2, 4 or 8).
+// A row's work is cw x ceil(pairs / kYThreads) rounds of (float4 column,
+// worker) pairs per thread, pairs = ceil(F / cw) x W; cw is the one with the
+// fewest rounds whose Y accumulators fit in kYSmemMax, ties going to the
+// larger cw (fewer Y partials).  False when none fits.
+inline bool plan_ycols(LayerDev& L, int rp, int W) {
+  int best = 0;
+  int64_t best_cost = 0;
+  for (int cw = kYClusterMax; cw >= 1; cw /= 2) {
+    const int64_t ps = ceil_div(L.F, cw) * W;
+    if (y_smem_bytes(ps, rp) > kYSmemMax) continue;
+    const int64_t cost = cw * ceil_div(ps, kYThreads);
+    if (!best || cost < best_cost) {
+      best = cw;
+      best_cost = cost;
+    }
+  }
+  if (!best) return false;
+  L.cw = best;
+  L.yfc = (int32_t)ceil_div(L.F, best);
+  // rows of a block: at most y_rows(rp) and kYBlockBytes of M per CTA; then
+  // as few as fill the same number of rounds of S blocks, so that the
+  // layer's last round has no idle subgroups where it can be avoided
+  const int64_t row_bytes = (int64_t)L.yfc * W * 16;
+  const int64_t yr_max = std::min<int64_t>(y_rows(rp), std::max<int64_t>(1, kYBlockBytes / row_bytes));
+  const int64_t S = kYClusterMax / best;
+  const int64_t rounds = ceil_div(ceil_div((int64_t)L.n, yr_max), S);
+  L.yr = (int32_t)ceil_div((int64_t)L.n, rounds * S);
   return true;
 }
 
-// One-pass project, rows: row groups of about `target` bytes of traffic per
-// CTA (G and B read, B written), a multiple of the block rows, at least 8 r
-// rows (a group's Y partial, W x ld x r floats written and read once, stays
-// under 1 / 12 of its M traffic) and at most 64 r.
-inline void plan_yrows(LayerDev& L, int rp, int W, int64_t target) {
-  const int R = y_rows(rp);
-  const int64_t row_bytes = 48LL * L.yfc * W;
-  int64_t ryg = target / std::max<int64_t>(row_bytes, 1);
-  ryg = std::min<int64_t>(std::max<int64_t>(ryg, std::max(R, 8 * rp)), 64 * rp);
-  ryg = std::min<int64_t>(ceil_div(ryg, R) * R, ceil_div(L.n, R) * R);
-  L.ryg = (int32_t)ryg;
-  L.nyg = (int32_t)ceil_div(L.n, ryg);
+// A block of yr rows in units of a cluster's time: kYClusterMax / cw blocks
+// run at once, each yr x ceil(pairs / kYThreads) rows of pair rounds long.
+inline int64_t y_block_cost(const LayerDev& L, int W) {
+  return (int64_t)L.cw * L.yr * ceil_div((int64_t)L.yfc * W, kYThreads);
+}
+
+// The one-pass project's persistent schedule for nc clusters: the layers'
+// blocks of yr rows, in layer order, cut into nc runs of about equal cost;
+// a run is a list of segments (layer, first block, end block, first slot),
+// cut after the whole number of rounds (S = kYClusterMax / cw blocks, one per
+// subgroup) nearest to each cluster's cumulative share of the total.
+// Subgroup s of a segment takes its blocks
+// s, s + S, ...; the segment's Y and Gram partials go to slot `first` (one
+// per segment).  tiles = nc header tiles {0, first segment, segments, 0}
+// followed by the segments.  Sets each layer's nys.
+inline void plan_yschedule(std::vector<LayerDev>& hl, int rp, int W, int nc, std::vector<Tile>& tiles) {
+  (void)rp;
+  // a segment of k blocks takes ceil(k / S) rounds of one block's cost
+  auto seg_cost = [&](const LayerDev& L, int64_t k) {
+    const int64_t S = kYClusterMax / L.cw;
+    return ceil_div(k, S) * S * y_block_cost(L, W);
+  };
+  int64_t total = 0;
+  for (const LayerDev& L : hl) total += seg_cost(L, ceil_div(L.n, L.yr));
+  std::vector<std::vector<Tile>> runs((size_t)nc);
+  int c = 0;
+  int64_t acc = 0;
+  for (int li = 0; li < (int)hl.size(); ++li) {
+    LayerDev& L = hl[li];
+    L.nys = 0;
+    const int64_t S = kYClusterMax / L.cw;
+    const int64_t nb = ceil_div(L.n, L.yr), rc = S * y_block_cost(L, W);
+    int64_t b = 0;
+    while (b < nb) {
+      int64_t k = nb - b;
+      if (c + 1 < nc) {
+        const int64_t room = total * (c + 1) / nc - acc;
+        const int64_t kr = room > 0 ? (room + rc / 2) / rc : 0;  // the nearest whole number of rounds
+        if (kr == 0) {
+          ++c;
+          continue;
+        }
+        k = std::min(k, kr * S);
+      }
+      runs[(size_t)c].push_back({li, (int32_t)b, (int32_t)(b + k), L.nys});
+      L.nys += 1;
+      acc += seg_cost(L, k);
+      b += k;
+    }
+  }
+  tiles.clear();
+  int32_t first = 0;
+  for (int i = 0; i < nc; ++i) {
+    tiles.push_back({0, first, (int32_t)runs[(size_t)i].size(), 0});
+    first += (int32_t)runs[(size_t)i].size();
+  }
+  for (const auto& r : runs) tiles.insert(tiles.end(), r.begin(), r.end());
 }
 
 // Chooses the tile rows of a layer set so that each phase grid is at least

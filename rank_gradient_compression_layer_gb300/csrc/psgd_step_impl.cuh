@@ -97,7 +97,7 @@ cudaError_t prepare() {
 #endif
 #if PSGD_RP <= 4
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(p1c_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)YCfg<kRP>::SMEM);
+    e = cudaFuncSetAttribute(p1c_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kYSmemMax);
 #endif
   return e;
 }
@@ -141,13 +141,15 @@ cudaError_t occupancy_fused(int* ctas) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, fused_step_kernel<kRP>, kFThreads, 0);
 }
 
-// The one-pass project: `items` clusters of `cs` CTAs (one Tile each),
-// launched as a programmatic dependent like the phase kernels.
-cudaLaunchConfig_t cluster_config(int items, int cs, cudaStream_t s, cudaLaunchAttribute (&attr)[2], bool pdl) {
+// The one-pass project: `clusters` clusters of `cs` CTAs, each with `smem`
+// bytes of dynamic shared memory, launched as a programmatic dependent like
+// the phase kernels.
+cudaLaunchConfig_t cluster_config(int clusters, int cs, size_t smem, cudaStream_t s, cudaLaunchAttribute (&attr)[2],
+                                  bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(items * cs));
+  cfg.gridDim = dim3((unsigned)(clusters * cs));
   cfg.blockDim = dim3((unsigned)kYThreads);
-  cfg.dynamicSmemBytes = YCfg<kRP>::SMEM;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cs;
@@ -160,17 +162,17 @@ cudaLaunchConfig_t cluster_config(int items, int cs, cudaStream_t s, cudaLaunchA
   return cfg;
 }
 
-cudaError_t launch_cluster(const StepArgs& a, int items, int cs, cudaStream_t s) {
-  if (items <= 0) return cudaSuccess;
+cudaError_t launch_cluster(const StepArgs& a, int clusters, int cs, size_t smem, cudaStream_t s) {
+  if (clusters <= 0) return cudaSuccess;
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = cluster_config(items, cs, s, attr, true);
+  const cudaLaunchConfig_t cfg = cluster_config(clusters, cs, smem, s, attr, true);
   return cudaLaunchKernelEx(&cfg, p1c_kernel<kRP>, a);
 }
 
 // Clusters of cs CTAs of the one-pass project that fit on the GPU at once.
-cudaError_t occupancy_cluster(int cs, int* clusters) {
+cudaError_t occupancy_cluster(int cs, size_t smem, int* clusters) {
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = cluster_config(1, cs, nullptr, attr, false);
+  const cudaLaunchConfig_t cfg = cluster_config(1, cs, smem, nullptr, attr, false);
   return cudaOccupancyMaxActiveClusters(clusters, p1c_kernel<kRP>, &cfg);
 }
 #endif
