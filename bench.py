@@ -452,6 +452,8 @@ def run_ours(args, ws, rank, local):
                    "tile_rows": st["tile_rows"]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "scope": "the dominant kernel alone (the whole step is step_roofline)"
+                     if not st["fused_step"] else "the whole step (one fused launch)",
                      "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
                      else "fallback 6.8 TB/s",
                      "kernel": ("psgd::rk_pass0_kernel (M = G + E written over E, top digit of |M|, U zeroed)"
@@ -470,6 +472,7 @@ def run_ours(args, ws, rank, local):
         "project_fp32": None if st["fused_step"] else project_fp32(cfg, args, project_ms, peaks, device),
         "timing": repeat_stats,
         "step_roofline": {"achieved": round(step_achieved, 1), "frac": round(step_achieved / peaks["hbm_gbs"], 4),
+                          "scope": "the whole step: all algorithmic bytes over ms_per_step",
                           "algorithmic_bytes_per_step": ab["total"],
                           "phase_ms": {k: round(v, 5) for k, v in phases.items()}},
         "e2e": e2e,

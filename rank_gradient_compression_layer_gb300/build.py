@@ -68,7 +68,7 @@ def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True) 
             if log.strip():
                 sys.stderr.write(log)
     tmp = LIB + ".tmp"
-    cmd = [nvcc(), "-shared"] + ARCH + ["-o", tmp] + objs
+    cmd = [nvcc(), "-shared"] + ARCH + ["-o", tmp] + objs + ["-ldl"]  # NVTX's tool loader
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError(f"link failed:\n{p.stderr}")

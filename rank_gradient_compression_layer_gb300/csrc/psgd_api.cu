@@ -8,6 +8,7 @@
 #define PSGD_SIDE_KERNELS 1
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -27,6 +28,15 @@ using namespace psgd;
 
 namespace {
 thread_local std::string g_err;
+
+// NVTX ranges on the host timeline, one per step and one per phase launch
+// (no-ops unless a profiling tool is attached).
+const char* const kPhaseRange[kPhases] = {"psgd project", "psgd orthonormalise", "psgd back-project",
+                                          "psgd decompress"};
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 }  // namespace
 
 namespace psgd {
@@ -294,6 +304,26 @@ void plan_one_pass(psgd_ctx* c) {
     c->gram_total += (L.nys + ceil_div(L.nys, kGramGroup)) * NG;
     L.y_off = c->y_total;
     c->y_total += (int64_t)L.nys * c->W * L.ld * rp;
+  }
+}
+
+// The project phase's last-written error rows, which the back-project
+// (whose tiles run in the reverse order) reads first: up to kL2KeepShare of
+// L2, counted from the end of the project order, are stored with an L2
+// evict-last policy so that they are still there.
+void plan_l2_keep(psgd_ctx* c) {
+  int l2 = 0;
+  if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, c->device) != cudaSuccess) {
+    cudaGetLastError();
+    l2 = 0;
+  }
+  int64_t room = (int64_t)(kL2KeepShare * (double)l2);
+  for (int li = (int)c->hl.size() - 1; li >= 0; --li) {
+    LayerDev& L = c->hl[li];
+    const int64_t row_bytes = (int64_t)c->W * L.ld * 4;
+    const int64_t rows = std::min<int64_t>(L.n, std::max<int64_t>(0, room / row_bytes));
+    L.l2row = (int32_t)(L.n - rows);
+    room -= rows * row_bytes;
   }
 }
 
@@ -606,6 +636,7 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     c->unc_step += n[l] * m[l];
   }
   build_tiles(c);
+  plan_l2_keep(c);
   // the one-pass project (options.one_pass): PowerSGD at padded rank <= 4,
   // every worker in this process, four phase kernels
   c->ypath = c->ks->launch_cluster && !c->unbiased && !rtopk && opt && opt->one_pass > 0 && !opt->fused &&
@@ -807,6 +838,7 @@ int make_args(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, Ste
 
 int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, float* X, float* Mom, float lr,
               float beta) {
+  const NvtxRange step_range("psgd step");
   int rc = ctx_ok(c);
   if (rc) return rc;
   if (c->total_workers != c->W)
@@ -874,6 +906,7 @@ int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, flo
   for (int ph = 0; ph < kPhases; ++ph) {
     const bool skip = c->unbiased && (ph == kOrthonormalise || ph == kBackProject);
     if (ph < phases && !skip) {
+      const NvtxRange phase_range(kPhaseRange[ph]);
       a.tiles = c->d_tiles[ph];
       cudaError_t e;
       if (ph == kProject && c->ypath) {

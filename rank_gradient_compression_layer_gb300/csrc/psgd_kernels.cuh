@@ -1,26 +1,29 @@
 // Device code of the PowerSGD compression step for sm_103a.
 //
-// A step is four stream-ordered kernels, each a plain grid of independent
-// tiles over ALL layers of the context (one launch per phase, not per layer):
+// A step is four stream-ordered phase kernels (a fifth at r >= 8), each a
+// plain grid of independent tiles over ALL layers of the context (one launch
+// per phase, not per layer):
 //
 //   project         M_w = G_w + (B_w - Phat' Q_w'^T): B holds M of the last
 //                   step, so the bracket is the error E_w; store B_w <- M_w;
 //                   P rows = (sum_w M_w) Q.  The CTA that completes a row
 //                   block writes its P rows and their Gram partial P^T P
 //                   (float64); the CTA that completes a layer sums the Gram
-//                   (fixed order), factors A = R^T R (Cholesky, float64) and
-//                   stores R: P R^-1 is the Gram-Schmidt basis of P.
-//   orthonormalise  Cholesky-QR2: rows P1 = P R^-1 by forward substitution
-//                   (float64, rounded to float32, stored over P); the CTA
-//                   that completes the layer factors the Gram matrix of P1
-//                   the same way and stores X = R2^-1, so Phat = P1 X.  The
-//                   second pass restores the orthogonality that one pass
-//                   loses when P is ill-conditioned (a warm-started Q whose
-//                   last columns carry little of M).
+//                   (fixed order), factors A = R^T R (Cholesky, float64),
+//                   stores R and decides whether one Cholesky-QR pass is
+//                   orthogonal enough (kappa_F(R) <= 1e3).  r >= 16: the
+//                   tensor-core tile of psgd_mma.cuh; options.one_pass
+//                   (r <= 4): the cluster kernel of psgd_cluster.cuh.
+//   orthonormalise  rows P1 = P R^-1 by forward substitution (float64,
+//                   rounded to float32, stored over P).  Where one pass is
+//                   not enough (Cholesky-QR2), the CTA that completes the
+//                   layer factors the Gram matrix of P1 the same way and
+//                   stores X = R2^-1, so Phat = P1 X; at r >= 8 a fifth kernel
+//                   stores those Phat rows once.
 //   back-project    partial Q_w = M_w^T Phat over a row tile of one segment
-//                   and one worker, with the Phat rows formed from P1 and X
-//                   as they are staged (one tile per row tile stores them);
-//                   the CTA that completes (segment, worker) sums the
+//                   and one worker (at r <= 4 with the Phat rows formed from
+//                   P1 and X as they are staged; one tile per row tile stores
+//                   them); the CTA that completes (segment, worker) sums the
 //                   partials (fixed order) into Q_w, and the one that
 //                   completes the segment forms Qbar = mean_w Q_w.
 //   decompress      U rows = Phat Qbar^T; vector layers U = mean_w G_w.
@@ -29,11 +32,12 @@
 // on the fly by the next step's project phase (r FMAs per element), which
 // saves a full read+write pass over every error buffer.
 //
-// The hot phases stream with 128-bit loads at high occupancy: on GB300 the
-// loaded HBM latency needs ~200 KB in flight per SM, which many resident
-// warps with a few independent loads each provide.  Every reduction runs in
-// a fixed order, so a step is bit-reproducible.  Data written by another CTA
-// of the same kernel is read with ld.global.cg (L2).
+// The hot phases stream with 128-bit loads at high occupancy: an SM's share
+// of GB300's HBM bandwidth (about 45 GB/s) over a loaded latency of one to two
+// microseconds needs 50-100 KB in flight per SM, which many resident warps
+// with a few independent loads each provide.  Every reduction runs in a fixed
+// order, so a step is bit-reproducible.  Data written by another CTA of the
+// same kernel is read with ld.global.cg (L2).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -73,6 +77,20 @@ constexpr unsigned kFull = 0xffffffffu;
 // ----------------------------------------------------------------------------
 
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+
+// An L2 cache policy under which the lines written are evicted last.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 16-byte store with an L2 cache policy.
+__device__ __forceinline__ void st_policy_f4(float* addr, float4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(addr), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w), "l"(pol)
+               : "memory");
+}
 
 __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
   unsigned old;
@@ -413,7 +431,14 @@ __device__ __forceinline__ void p1_rows(const LayerDev& L, const P1Tile& T, cons
         if (L.tail < 3) m2 = 0.f;
         m3 = 0.f;
       }
-      if (!T.ub) *reinterpret_cast<float4*>(Bw + (int64_t)(T.row0 + sb + i) * L.ld) = make_float4(m0, m1, m2, m3);
+      if (!T.ub) {
+        const int row = T.row0 + sb + i;
+        float* dst = Bw + (int64_t)row * L.ld;
+        if (row >= L.l2row)
+          st_policy_f4(dst, make_float4(m0, m1, m2, m3), l2_evict_last_policy());
+        else
+          *reinterpret_cast<float4*>(dst) = make_float4(m0, m1, m2, m3);
+      }
 #pragma unroll
       for (int k = 0; k < RP; ++k) {
         float t = m0 * qv[0][k];

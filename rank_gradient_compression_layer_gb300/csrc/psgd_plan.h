@@ -82,6 +82,7 @@ inline int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp
   L.s1 = (int32_t)ceil_div(ld, tr.pcols);
   L.c_ph = L.c_rb + (L.s1 > 1 ? L.nrb : 0);
   L.c_phg = L.c_ph + 1;
+  L.l2row = (int32_t)n;
   return (int64_t)L.c_phg + ph_groups(L.nph);
 }
 
