@@ -472,7 +472,6 @@ __device__ __forceinline__ void p1_reduce(const P1Tile& T, float (&acc)[Cfg<RP>:
 template <int RP>
 __device__ __forceinline__ void p1_rows_done(const StepArgs& a, const LayerDev& L, const P1Tile& T, float* s_prow,
                                              double* s_gram, int* s_flag, unsigned* pub) {
-  constexpr int R1 = Cfg<RP>::R1;
   if (L.s1 > 1) {
     float* pp = a.ppart + L.ppart_off + ((int64_t)T.rb * L.s1 + T.seg) * L.r1 * RP;
     for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) pp[idx] = s_prow[idx];

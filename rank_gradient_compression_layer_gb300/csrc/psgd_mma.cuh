@@ -18,9 +18,13 @@
 //
 // A CTA owns 128 rows x one segment (128 columns, the TMEM lanes) and loops
 // over the workers; worker w + 1's Q_w' rows are staged and its MMAs issued
-// while worker w's rows are combined (D in two TMEM buffers).  Every
-// wait on the tensor cores is bounded; one that runs out marks the step's
-// status word (the host reports it) and the tile is abandoned.
+// while worker w's rows are combined (D in two TMEM buffers).  G and B come
+// into shared memory by 16-byte asynchronous copies (cp.async.cg: 512 bytes
+// per warp request), a ring of NS chunks per row quarter (8 rows x the
+// segment's columns of G and of B), NS - 1 chunks ahead across the workers;
+// each thread then reads its own column from the chunk.  Every wait on the
+// tensor cores is bounded; one that runs out marks the step's status word
+// (the host reports it) and the tile is abandoned.
 #pragma once
 
 #include "psgd_kernels.cuh"
@@ -41,7 +45,18 @@ struct MmaCfg {
   static constexpr uint32_t OFF_Q = 2 * OP;                     // Q^T hi, lo (the P product's B operand)
   static constexpr uint32_t OFF_U = OFF_Q + 2 * OP;             // Q_w' buffers 0, 1 (hi, lo each), then Msum hi, lo
   static constexpr uint32_t U_BYTES = (4 * OP > 2 * MS) ? 4 * OP : 2 * MS;
-  static constexpr uint32_t SMEM = OFF_U + U_BYTES;
+  // the rings, after the Q_w' buffers, over Msum's space (Msum is formed
+  // after the worker loop): 4 row quarters x NS chunks of 8 rows x 128
+  // columns of G and of B, as many chunks as fit
+  static constexpr uint32_t CHUNK = 2u * 8 * kMCols * 4;
+  static constexpr uint32_t OFF_R = OFF_U + 4 * OP;
+  static constexpr int NS = (int)((227u * 1024 - 1024 - OFF_R) / (4 * CHUNK)) < 5
+                                ? (int)((227u * 1024 - 1024 - OFF_R) / (4 * CHUNK))
+                                : 5;
+  static_assert(NS >= 2, "a ring of at least two chunks");
+  static constexpr uint32_t RING = 4u * NS * CHUNK;
+  static constexpr uint32_t SMEM = (OFF_U + U_BYTES > OFF_R + RING) ? OFF_U + U_BYTES : OFF_R + RING;
+  static_assert(SMEM <= 227 * 1024, "fits the shared memory of one CTA");
   static constexpr uint32_t TMEM_COLS = 512;  // D of two workers (2 x 128) and the P tile (r)
   static_assert((uint32_t)kMRows * RP * 4 + RP * RP * 8 <= 2 * OP, "P rows and Gram scratch fit over the Phat' tile");
   static_assert(kMRows <= Cfg<RP>::R1MAX, "the split step's Gram tile holds a whole row block");
@@ -136,27 +151,36 @@ __global__ void __launch_bounds__(kMThreads, 1) p1m_kernel(const StepArgs a) {
   float msum[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) msum[i] = 0.f;
-  // G and B of 8 rows (row0 + r0 + 8 ch + k) of worker w at this thread's column
-  auto load8 = [&](int w, int ch, float (&g)[8], float (&b)[8]) {
-    const int rfirst = r0 + 8 * ch;
-    const int64_t o = (int64_t)(T.row0 + rfirst) * L.ld + L.off + col;
-    const float* gp = a.G[w] + o;
-    const float* bp = a.B + (int64_t)w * a.total + o;
-    const int nv = col_in ? min(8, T.rcnt - rfirst) : 0;  // rows of the chunk inside the tile
+  // Item i = chunk i % 4 (rows r0 + 8 (i % 4) .. + 7) of worker i / 4, in
+  // slot i % NS of this row quarter's ring: G rows [8][128] floats, then B
+  // rows.  The quarter's 128 threads copy it together (2 float4 of G and 2 of
+  // B each); thread (column cl) reads its column.
+  const int q = warp >> 2, jq = tid & 127;  // row quarter, thread within it
+  const int n_items = 4 * a.W;
+  auto slot_of = [&](int i) { return reinterpret_cast<float*>(sm + C::OFF_R + (uint32_t)(q * C::NS + i % C::NS) * C::CHUNK); };
+  auto chunk_rows = [&](int i) { return max(0, min(8, T.rcnt - (r0 + 8 * (i & 3)))); };
+  auto issue_item = [&](int i) {
+    if (i < n_items) {
+      const int w = i >> 2, nv = chunk_rows(i);
+      const int64_t o = (int64_t)(T.row0 + r0 + 8 * (i & 3)) * L.ld + L.off + (int64_t)T.seg * kMCols;
+      const float* gp = a.G[w] + o;
+      const float* bp = a.B + (int64_t)w * a.total + o;
+      float* dst = slot_of(i);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      g[k] = b[k] = 0.f;
-      if (k < nv) {
-        g[k] = __ldcs(gp);
-        b[k] = __ldcs(bp);
+      for (int h = 0; h < 2; ++h) {
+        const int e = jq + 128 * h;  // float4 e of the chunk: row e / 32, columns 4 (e % 32) ..
+        const int k = e >> 5, c4 = 4 * (e & 31);
+        if (k < nv && c4 < segcols) {
+          cp_async_16(dst + 128 * k + c4, gp + (int64_t)k * L.ld + c4);
+          cp_async_16(dst + 1024 + 128 * k + c4, bp + (int64_t)k * L.ld + c4);
+        }
       }
-      gp += L.ld;
-      bp += L.ld;
     }
+    cp_async_commit();  // one group per item (empty past the last one)
   };
-  float gc[8], bc[8], gn[8], bn[8];
+#pragma unroll
+  for (int i = 0; i < C::NS - 1; ++i) issue_item(i);
   for (int w = 0; w < a.W; ++w) {
-    load8(w, 0, gc, bc);
     if (prev && w + 1 < a.W) stage_qw(w + 1);  // its buffer's last reader, worker w - 1's MMA, is done
     fence_async_smem();
     tc_fence_before();
@@ -168,35 +192,38 @@ __global__ void __launch_bounds__(kMThreads, 1) p1m_kernel(const StepArgs a) {
       if (lane == 0 && a.sync) atomicCAS(a.sync + 2, 0u, 2u);
     }
     tc_fence_after();
-    if (!__syncthreads_and(ok ? 1 : 0)) {  // a tensor-core wait ran out: abandon the tile
+    if (!__syncthreads_and(ok ? 1 : 0)) {  // a wait ran out: abandon the tile
       ok = false;                          // (in every thread)
       break;
     }
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch) {
-      if (ch < 3) load8(w, ch + 1, gn, bn);
+      const int i = 4 * w + ch;
       float d[8];
       if (prev)
         tmem_ld8(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(w & 1) * kMRows + (uint32_t)(r0 + 8 * ch), d);
+      // this thread's copies of item i have landed; after the barrier every
+      // thread's have, and every thread is done with item i - 1's slot
+      cp_async_wait<C::NS - 2>();
+      named_barrier(1 + q, 128);
+      issue_item(i + C::NS - 1);  // into item i - 1's slot
       const int rfirst = r0 + 8 * ch;
-      const int nv = col_in ? min(8, T.rcnt - rfirst) : 0;
+      const int nv = col_in ? chunk_rows(i) : 0;
+      const float* sg = slot_of(i) + cl;
       float* bp = a.B + (int64_t)w * a.total + (int64_t)(T.row0 + rfirst) * L.ld + L.off + col;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        float m = prev ? gc[k] + (bc[k] - d[k]) : gc[k] + bc[k];
+        const float g = k < nv ? sg[128 * k] : 0.f;
+        const float b = k < nv ? sg[1024 + 128 * k] : 0.f;
+        float m = prev ? g + (b - d[k]) : g + b;
         if (col >= L.m) m = 0.f;  // the row padding stays zero
         if (k < nv) *bp = m;
         bp += L.ld;
         msum[8 * ch + k] += m;
       }
-      if (ch < 3)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          gc[k] = gn[k];
-          bc[k] = bn[k];
-        }
     }
   }
+  cp_async_wait<0>();  // no copy is in flight when the space is reused or the CTA leaves
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

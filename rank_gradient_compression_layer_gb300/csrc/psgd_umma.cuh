@@ -15,6 +15,7 @@
 //   * tcgen05.mma kind::tf32 (one thread), tcgen05.commit to an mbarrier,
 //     tcgen05.ld 32x32b.x32 (a warp reads 32 consecutive columns of its 32
 //     TMEM lanes), TMEM allocation by one warp.
+//   * Asynchronous copies global -> shared (cp.async) and their groups.
 //
 // float32 accuracy from TF32 products: x = hi + lo with hi = x rounded to
 // TF32 (cvt.rna) and lo = x - hi (exact); a b ~ hi_a hi_b + hi_a lo_b +
@@ -137,6 +138,27 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&f)[8]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
+}
+
+// Asynchronous 4-byte copy global -> shared (LDGSTS), and its groups: the
+// copies a thread issued before a commit form a group; wait_group<N> returns
+// once at most N of this thread's groups are still in flight.
+__device__ __forceinline__ void cp_async_f32(float* dst, const float* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// Asynchronous 16-byte copy global -> shared, cached in L2 only.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Barrier over the `threads` threads (whole warps) that use barrier `id` (1..15).
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // x = hi + lo, hi = x rounded to TF32 (round to nearest, ties away), lo exact.
