@@ -233,6 +233,7 @@ struct psgd_ctx {
   int64_t xp_floats = 0, xq_floats = 0;
   // the one-pass project (psgd_step at padded rank <= 4): cluster items over
   // the layers' row groups, and the Y partials they write
+  bool bmma = false;  // the back-project runs on the tensor cores (tiles without a worker)
   bool ypath = false;
   std::vector<Tile> ytiles;  // y_clusters header tiles, then the segments
   Tile* d_ytiles = nullptr;
@@ -345,7 +346,7 @@ void build_tiles(psgd_ctx* c) {
     const LayerDev& L = c->hl[li];
     for (int rt = L.t3r - 1; rt >= 0; --rt)
       for (int s = L.S - 1; s >= 0; --s)
-        for (int w = 0; w < c->W; ++w) c->tiles[kBackProject].push_back({li, rt, s, w});
+        for (int w = 0; w < (c->bmma ? 1 : c->W); ++w) c->tiles[kBackProject].push_back({li, rt, s, w});
   }
   for (int vi = 0; vi < (int)c->hv.size(); ++vi)
     for (int t = 0; t < (int)ceil_div(c->hv[vi].n, kVChunk); ++t) c->tiles[kDecompress].push_back({vi, t, 0, 1});
@@ -584,6 +585,11 @@ int psgd_create_ex(psgd_ctx** out, int num_layers, const int64_t* n, const int64
     tr.r1 = c->ks->mma_rows;
     tr.pcols = c->ks->mma_cols;
   }
+  // the back-project on the tensor cores (r = 32: at r = 16 the CUDA-core
+  // kernel is faster): every worker's D in TMEM (W r <= 512 columns), row
+  // tiles in whole chunks
+  c->bmma = bmma_applies(*c->ks, c->W) && !c->unbiased && !rtopk;
+  if (c->bmma) tr.r3mult = c->ks->bmma_rows;
   if (opt && opt->project_rows > 0) {
     if (opt->project_rows > c->ks->r1 || opt->project_rows % c->ks->rsb != 0) {
       delete c;
@@ -913,6 +919,8 @@ int step_impl(psgd_ctx* c, const float* const* grad_ptrs, float* out_update, flo
         a.tiles = c->d_ytiles;
         a.y_clusters = c->y_clusters;
         e = c->ks->launch_cluster(a, c->y_clusters, kYClusterMax, c->y_smem, c->stream);
+      } else if (ph == kBackProject && c->bmma) {
+        e = c->ks->launch_bmma(a, (int)c->tiles[ph].size(), c->stream);
       } else {
         e = c->ks->launch(ph, a, (int)c->tiles[ph].size(), c->stream);
       }
@@ -980,7 +988,9 @@ int xchg(psgd_ctx* c, const StepArgs& a, float* dense, float* padded, const std:
 
 int launch_phase(psgd_ctx* c, int phase, StepArgs& a, const Tile* tiles, int n) {
   a.tiles = tiles;
-  cudaError_t e = (phase < 0) ? c->ks->launch_gram(a, n, c->stream) : c->ks->launch(phase, a, n, c->stream);
+  cudaError_t e = (phase < 0)                           ? c->ks->launch_gram(a, n, c->stream)
+                  : (phase == kBackProject && c->bmma) ? c->ks->launch_bmma(a, n, c->stream)
+                                                        : c->ks->launch(phase, a, n, c->stream);
   if (e != cudaSuccess) {
     c->broken = true;
     return cuda_fail(e, "phase kernel launch");

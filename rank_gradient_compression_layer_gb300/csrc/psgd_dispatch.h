@@ -39,6 +39,10 @@ struct KernelSet {
   // over a.tiles, and the clusters of that shape resident at once
   cudaError_t (*launch_cluster)(const StepArgs& a, int clusters, int cs, size_t smem, cudaStream_t s);
   cudaError_t (*occupancy_cluster)(int cs, size_t smem, int* clusters);
+  // the back-project on the tensor cores (padded ranks 16, 32; null below):
+  // tiles of bmma_rows-row chunks over (row tile, segment) with every worker
+  cudaError_t (*launch_bmma)(const StepArgs& a, int tiles, cudaStream_t s);
+  int bmma_rows;
 };
 
 extern const KernelSet kKernelsR1, kKernelsR2, kKernelsR4, kKernelsR8, kKernelsR16, kKernelsR32;

@@ -38,6 +38,7 @@ constexpr int64_t rinv_len(int rp) { return 2 * (int64_t)rp * rp + rp + 2; }
 // The one-pass project (padded rank <= 4): clusters of CTAs that together
 // cover whole rows of a layer, so that a row block's P rows are complete on
 // chip and Y_w = M_w^T P is accumulated in the same pass.
+constexpr int kBmmaTmemCols = 512;  // tensor-core back-project: TMEM columns for every worker's D (W r)
 constexpr int kYThreads = 256;     // threads of a CTA
 constexpr int kYClusterMax = 8;    // CTAs per cluster (portable cluster size)
 constexpr int kYSmemMax = 64 * 1024;  // Y accumulators of a CTA at most (bytes), so 3 CTAs fit on an SM

@@ -303,4 +303,193 @@ __global__ void __launch_bounds__(kMThreads, 1) p1m_kernel(const StepArgs a) {
   p1_rows_done<RP>(a, L, T, s_prow, s_gram, &s_flag, nullptr);
 }
 
+// ----------------------------------------------------------------------------
+// back-project on the tensor cores (r >= 16)
+// ----------------------------------------------------------------------------
+//
+// Q_w (partial over a row tile) = M_w^T Phat: per 128-row chunk and worker,
+// D_w (128 columns x r, TMEM; lane = column) += M_w[chunk]^T Phat[chunk] in
+// error-compensated TF32, D_w accumulating over the tile's chunks in TMEM
+// columns w r.  The A operand (M_w^T: the segment's 128 columns x 128 rows,
+// K-major) is written by the CUDA cores, transposed: a warp loads 4 rows x
+// 32 columns (float4 per lane, 128-byte rows) and stores each value's hi and
+// lo parts; its 8-column core-matrix groups are BSBO bytes apart, 16 more
+// than packed, so that those scattered 4-byte stores hit 32 distinct banks.
+// The B operand is the chunk's Phat rows (r x 128, K-major).  Each thread
+// loads its 8 float4 of the next (chunk, worker) while the tensor cores run
+// the current one.  At the end every worker's D is read from TMEM as the
+// tile's partial Q_w; the row tiles' partials are summed as in the CUDA-core
+// back-project (last arriver per segment and worker, then Qbar).
+constexpr int kBThreads = 512;    // 16 warps
+constexpr int kBRows = 128;       // rows of a chunk: the K of one round of MMAs
+
+template <int RP>
+struct BmmaCfg {
+  static_assert(RP == 16 || RP == 32, "tensor-core back-project tiles are for padded ranks 16 and 32");
+  static constexpr uint32_t SBO = (kBRows / 4) * 128 + 16;       // A: 8-column groups apart (padded)
+  static constexpr uint32_t A_BYTES = (kMCols / 8) * SBO;        // one copy (hi or lo) of A
+  static constexpr uint32_t B_SBO = (kBRows / 4) * 128;          // B: 8-rank groups apart
+  static constexpr uint32_t B_BYTES = (uint32_t)(RP / 8) * B_SBO;  // one copy of B (r x 128)
+  static constexpr uint32_t OFF_A = 0;                             // A hi, then lo
+  static constexpr uint32_t OFF_B = 2 * A_BYTES;                   // B hi, then lo
+  static constexpr uint32_t SMEM = OFF_B + 2 * B_BYTES;
+  static_assert(SMEM <= 227 * 1024, "fits the shared memory of one CTA");
+  static_assert(A_BYTES % 16 == 0 && B_BYTES % 16 == 0, "operands start on 16-byte boundaries");
+};
+
+// Byte offset of element (m, k) of the padded K-major A operand (K = 128).
+template <int RP>
+__device__ __forceinline__ uint32_t bmma_a_off(int m, int k) {
+  return (uint32_t)(m >> 3) * BmmaCfg<RP>::SBO + (uint32_t)(k >> 2) * 128 + (uint32_t)(m & 7) * 16 + (uint32_t)(k & 3) * 4;
+}
+
+template <int RP>
+__global__ void __launch_bounds__(kBThreads, 1) p3m_kernel(const StepArgs a) {
+  using C = BmmaCfg<RP>;
+  extern __shared__ __align__(1024) unsigned char sm[];
+  __shared__ __align__(8) uint64_t s_mbar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_flag;
+  pdl_enter();
+  const Tile t = a.tiles[blockIdx.x];
+  const LayerDev L = a.layers[t.layer];  // by value: stores cannot alias it
+  const int rt = t.a, seg = t.b;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row0 = rt * L.r3;
+  const int nrows = min(L.r3, L.n - row0);
+  const int nchunks = (nrows + kBRows - 1) / kBRows;
+  const int segcols = min(kMCols, L.ld - seg * kMCols);
+  const uint32_t base = smem_u32(sm);
+  if (warp == 0) tmem_alloc(&s_tmem, kBmmaTmemCols);
+  if (tid == 0) mbar_init(&s_mbar);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  // this thread's 8 float4 of a chunk: rows 8 warp + 4 (u & 1) + lane / 8,
+  // float4 column 8 (u / 2) + lane % 8, u = 0..7
+  const int n_it = nchunks * a.W;  // iteration it = chunk it / W, worker it % W
+  float4 v[8];
+  auto load_it = [&](int it) {
+    const int c = it / a.W, w = it - c * a.W;
+    const float* bw = a.B + (int64_t)w * a.total + L.off + (int64_t)seg * kMCols;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int r = 8 * warp + 4 * (u & 1) + (lane >> 3);
+      const int c4 = 4 * (8 * (u >> 1) + (lane & 7));
+      const int row = c * kBRows + r;
+      v[u] = (row < nrows && c4 < segcols)
+                 ? __ldcs(reinterpret_cast<const float4*>(bw + (int64_t)(row0 + row) * L.ld + c4))
+                 : zero4();
+    }
+  };
+  auto store_a = [&]() {
+    unsigned char* ahi = sm + C::OFF_A;
+    unsigned char* alo = ahi + C::A_BYTES;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int r = 8 * warp + 4 * (u & 1) + (lane >> 3);
+      const int m0 = 4 * (8 * (u >> 1) + (lane & 7));
+      const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float h, l;
+        tf32_split(x[j], h, l);
+        const uint32_t o = bmma_a_off<RP>(m0 + j, r);
+        *reinterpret_cast<float*>(ahi + o) = h;
+        *reinterpret_cast<float*>(alo + o) = l;
+      }
+    }
+  };
+  // the chunk's Phat rows as the B operand (rank n, row k), hi and lo
+  auto stage_b = [&](int c) {
+    constexpr int K4 = RP / 4;
+    const float* ph = a.Phat + L.p_off + (int64_t)(row0 + c * kBRows) * RP;
+    const int rows = min(kBRows, nrows - c * kBRows);
+    for (int e = tid; e < kBRows * K4; e += kBThreads) {
+      const int k = e / K4, n4 = e - k * K4;
+      const float4 p = k < rows ? __ldg(reinterpret_cast<const float4*>(ph + (int64_t)k * RP) + n4) : zero4();
+      const float x[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float h, l;
+        tf32_split(x[j], h, l);
+        const int n = 4 * n4 + j;
+        const uint32_t o = (uint32_t)(n >> 3) * C::B_SBO + (uint32_t)(k >> 2) * 128 + (uint32_t)(n & 7) * 16 + (uint32_t)(k & 3) * 4;
+        *reinterpret_cast<float*>(sm + C::OFF_B + o) = h;
+        *reinterpret_cast<float*>(sm + C::OFF_B + C::B_BYTES + o) = l;
+      }
+    }
+  };
+
+  bool ok = true;
+  if (n_it > 0) load_it(0);
+  for (int it = 0; it < n_it; ++it) {
+    const int c = it / a.W, w = it - c * a.W;
+    // the tensor cores are done with the operands of iteration it - 1
+    if (it > 0 && !mbar_wait(&s_mbar, (uint32_t)((it - 1) & 1))) {
+      ok = false;
+      if (lane == 0 && a.sync) atomicCAS(a.sync + 2, 0u, 2u);
+    }
+    tc_fence_after();
+    if (!__syncthreads_and(ok ? 1 : 0)) {
+      ok = false;
+      break;
+    }
+    if (w == 0) stage_b(c);
+    store_a();
+    if (it + 1 < n_it) load_it(it + 1);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+      constexpr uint32_t id = umma_idesc_tf32(kMCols, RP);
+      const uint32_t d = tmem + (uint32_t)(w * RP);
+      const uint32_t ahi = base + C::OFF_A, alo = ahi + C::A_BYTES;
+      const uint32_t bhi = base + C::OFF_B, blo = bhi + C::B_BYTES;
+#pragma unroll 1
+      for (int ks = 0; ks < kBRows / 8; ++ks) {
+        const uint32_t o = (uint32_t)ks * 256;
+        const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
+        umma_tf32(d, umma_sdesc_los(ahi + o, 128, C::SBO), umma_sdesc_los(bhi + o, 128, C::B_SBO), id, acc);
+        umma_tf32(d, umma_sdesc_los(ahi + o, 128, C::SBO), umma_sdesc_los(blo + o, 128, C::B_SBO), id, 1u);
+        umma_tf32(d, umma_sdesc_los(alo + o, 128, C::SBO), umma_sdesc_los(bhi + o, 128, C::B_SBO), id, 1u);
+      }
+      umma_commit(&s_mbar);
+    }
+  }
+  if (ok && n_it > 0 && !mbar_wait(&s_mbar, (uint32_t)((n_it - 1) & 1))) {
+    ok = false;
+    if (tid == 0 && a.sync) atomicCAS(a.sync + 2, 0u, 2u);
+  }
+  tc_fence_after();
+  // every worker's D: the tile's partial Q_w (TMEM lane = column)
+  if (ok) {
+    const int g = warp & 3, cl = 32 * g + lane;
+    for (int w = warp >> 2; w < a.W; w += 4) {
+      float q[RP];
+      if constexpr (RP == 32) {
+        tmem_ld32(tmem + ((uint32_t)(32 * g) << 16) + (uint32_t)(w * RP), q);
+      } else {
+        tmem_ld16(tmem + ((uint32_t)(32 * g) << 16) + (uint32_t)(w * RP), q);
+      }
+      if (cl < segcols) {
+        float4* dst = reinterpret_cast<float4*>(a.qpart + L.qpart_off +
+                                                ((int64_t)(rt * a.W + w) * L.ld + seg * kMCols + cl) * RP);
+#pragma unroll
+        for (int k4 = 0; k4 < RP / 4; ++k4) dst[k4] = make_float4(q[4 * k4], q[4 * k4 + 1], q[4 * k4 + 2], q[4 * k4 + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_free(tmem, kBmmaTmemCols);
+  if (!__syncthreads_and(ok ? 1 : 0)) return;
+  for (int w = 0; w < a.W; ++w)
+    if (cta_arrive_last(a.counters + L.cnt_off + L.c_p3 + seg * a.W + w, (unsigned)L.t3r, &s_flag))
+      qf_segment_worker<RP>(a, L, seg, w, &s_flag, nullptr);
+}
+
 }  // namespace psgd

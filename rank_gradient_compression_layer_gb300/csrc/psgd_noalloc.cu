@@ -58,7 +58,9 @@ struct ScratchPlan {
 // Writes the layer record and the tile lists (same order as a context's
 // tiles for a one-layer set) and clears the counters, which must start at
 // zero.  Grid-stride over every entry.
-__global__ void noalloc_tables_kernel(LayerDev L, int W, LayerDev* dL, Tile* t1, int n1, Tile* tph, int nph,
+// W3: back-project tiles per (row tile, segment): W, or 1 when one tile takes
+// every worker (the tensor-core back-project).
+__global__ void noalloc_tables_kernel(LayerDev L, int W3, LayerDev* dL, Tile* t1, int n1, Tile* tph, int nph,
                                       Tile* t3, int n3, Tile* tu, int nu, unsigned* cnt, int ncnt) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -68,9 +70,9 @@ __global__ void noalloc_tables_kernel(LayerDev L, int W, LayerDev* dL, Tile* t1,
   for (int64_t i = i0; i < nph; i += stride) tph[i] = Tile{0, (int32_t)i, 0, 0};
   for (int64_t i = i0; i < nu; i += stride) tu[i] = Tile{0, (int32_t)(i / L.S), (int32_t)(i % L.S), 0};
   // back-project: last row tile and segment first (the rows project wrote last)
-  const int64_t sw = (int64_t)L.S * W;
+  const int64_t sw = (int64_t)L.S * W3;
   for (int64_t i = i0; i < n3; i += stride)
-    t3[i] = Tile{0, (int32_t)(L.t3r - 1 - i / sw), (int32_t)(L.S - 1 - (i / W) % L.S), (int32_t)(i % W)};
+    t3[i] = Tile{0, (int32_t)(L.t3r - 1 - i / sw), (int32_t)(L.S - 1 - (i / W3) % L.S), (int32_t)(i % W3)};
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -125,6 +127,8 @@ extern "C" int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers
     tr.r1 = ks->mma_rows;
     tr.pcols = ks->mma_cols;
   }
+  const bool bmma = bmma_applies(*ks, W);  // the tensor-core back-project, as a context would
+  if (bmma) tr.r3mult = ks->bmma_rows;
   LayerDev L;
   std::memset(&L, 0, sizeof(L));
   ScratchPlan sp;
@@ -140,7 +144,7 @@ extern "C" int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers
   L.cnt_off = 0;
   sp.ntiles[kProject] = (int)((int64_t)L.nrb * L.s1);
   sp.ntiles[kOrthonormalise] = L.nph;
-  sp.ntiles[kBackProject] = (int)((int64_t)L.t3r * L.S * W);
+  sp.ntiles[kBackProject] = (int)((int64_t)L.t3r * L.S * (bmma ? 1 : W));
   sp.ntiles[kDecompress] = (int)(ceil_div(n, L.ru) * L.S);
   const int NG = rp * (rp + 1) / 2;
   size_t pos = 0;
@@ -170,7 +174,7 @@ extern "C" int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers
   Tile* dt[kPhases];
   for (int ph = 0; ph < kPhases; ++ph) dt[ph] = reinterpret_cast<Tile*>(base + sp.tiles[ph]);
   unsigned* cnt = reinterpret_cast<unsigned*>(base + sp.counters);
-  noalloc_tables_kernel<<<64, 256, 0, s>>>(L, W, dL, dt[kProject], sp.ntiles[kProject], dt[kOrthonormalise],
+  noalloc_tables_kernel<<<64, 256, 0, s>>>(L, bmma ? 1 : W, dL, dt[kProject], sp.ntiles[kProject], dt[kOrthonormalise],
                                            sp.ntiles[kOrthonormalise], dt[kBackProject], sp.ntiles[kBackProject],
                                            dt[kDecompress], sp.ntiles[kDecompress], cnt, sp.ncnt);
   CUDA_TRY(cudaGetLastError());
@@ -197,7 +201,10 @@ extern "C" int psgd_step_noalloc(int64_t n, int64_t m, int rank, int num_workers
   for (int ph = 0; ph < phases; ++ph) {
     if (sp.ntiles[ph] == 0) continue;
     a.tiles = dt[ph];
-    CUDA_TRY(ks->launch(ph, a, sp.ntiles[ph], s));
+    if (ph == kBackProject && bmma)
+      CUDA_TRY(ks->launch_bmma(a, sp.ntiles[ph], s));
+    else
+      CUDA_TRY(ks->launch(ph, a, sp.ntiles[ph], s));
   }
   return PSGD_OK;
 }

@@ -45,9 +45,18 @@ inline const KernelSet* kernels_for(int rp) {
 }
 
 // Rows per tile of the project, back-project (least) and decompress phases.
+// Whether the back-project runs on the tensor cores: padded rank 32 (at 16
+// the CUDA-core kernel is faster: the tensor-core tile is bound by its shared
+// memory traffic, hi and lo copies of M written and read three times), and
+// every worker's D fits in TMEM.
+inline bool bmma_applies(const KernelSet& ks, int W) {
+  return ks.launch_bmma != nullptr && ks.rp == 32 && W * ks.rp <= kBmmaTmemCols;
+}
+
 struct TileRows {
   int r1 = 32, r3min = 256, ru = 64;
   int pcols = kSeg * 4;  // columns of a project tile
+  int r3mult = 1;        // back-project rows per tile: a multiple of this (tensor-core chunks)
 };
 
 // The phase grids must hold several waves of resident CTAs, or the last,
@@ -69,7 +78,7 @@ inline int64_t plan_matrix(LayerDev& L, int64_t n, int64_t m, int64_t ld, int rp
   L.ru = tr.ru;
   L.g1 = (int32_t)ceil_div(L.nrb, kGramGroup);
   // back-project: at most 16 row tiles (the Q partial sums stay short)
-  const int64_t r3 = std::max<int64_t>(std::max(tr.r3min, 8 * rp), ceil_div(n, 16));
+  const int64_t r3 = ceil_div(std::max<int64_t>(std::max(tr.r3min, 8 * rp), ceil_div(n, 16)), tr.r3mult) * tr.r3mult;
   L.r3 = (int32_t)std::min<int64_t>(n, r3);
   L.t3r = (int32_t)ceil_div(n, L.r3);
   L.c_gram = 0;

@@ -94,6 +94,8 @@ cudaError_t prepare() {
 #if PSGD_RP >= 16
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(p1m_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MmaCfg<kRP>::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(p3m_kernel<kRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BmmaCfg<kRP>::SMEM);
 #endif
 #if PSGD_RP <= 4
   if (e == cudaSuccess)
@@ -125,6 +127,13 @@ cudaError_t occupancy(int phase, int W, int* ctas) {
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, ph_kernel<kRP>, kPhThreads, 0);
   }
 }
+
+#if PSGD_RP >= 16
+cudaError_t launch_bmma(const StepArgs& a, int tiles, cudaStream_t s) {
+  if (tiles <= 0) return cudaSuccess;
+  return launch_dependent(p3m_kernel<kRP>, tiles, kBThreads, BmmaCfg<kRP>::SMEM, s, a);
+}
+#endif
 
 cudaError_t launch_gram(const StepArgs& a, int tiles, cudaStream_t s) {
   if (tiles <= 0) return cudaSuccess;
@@ -193,9 +202,14 @@ extern const KernelSet PSGD_CAT(kKernelsR, PSGD_RP) = {
     0, 0,
 #endif
 #if PSGD_RP <= 4
-    launch_cluster, occupancy_cluster
+    launch_cluster, occupancy_cluster,
 #else
-    nullptr, nullptr
+    nullptr, nullptr,
+#endif
+#if PSGD_RP >= 16
+    launch_bmma, kBRows
+#else
+    nullptr, 0
 #endif
 };
 
