@@ -426,6 +426,21 @@ int psgd_count_sent(int num_layers, const int64_t* n, const int64_t* m, int rank
                     int64_t* compressed, int64_t* uncompressed);
 
 /*
+ * The one-pass project's plan for a layer set (host only, no GPU), for
+ * `clusters` resident clusters of 8 CTAs: per matrix layer (counting matrix
+ * layers only) 4 int32 in layer_plan -- cw (CTAs across a row), yfc (float4
+ * columns per CTA), yr (rows per block), nys (partial slots); and in tiles,
+ * 4 int32 each, `clusters` header tiles (0, first segment, segments, 0)
+ * followed by the segments (matrix index, first block, end block, slot).
+ * With tiles == NULL only *count (header tiles + segments) is set.  Padded
+ * rank 1, 2 or 4; PSGD_ERR_INVALID when a layer does not fit the one-pass
+ * project (see "Launches").  For checking the plan: every block of every
+ * layer belongs to exactly one segment, and the runs are of about equal work.
+ */
+int psgd_plan_one_pass(int num_layers, const int64_t* n, const int64_t* m, int rank, int num_workers,
+                       int clusters, int32_t* layer_plan, int32_t* tiles, int64_t* count);
+
+/*
  * The fused step's queue for a layer set (host only, no GPU): the items a
  * context with these layers would run, in order, 4 int32 each -- (phase << 24
  * | matrix index, a, b, c) with phase 0 project (a = row block, b = segment),

@@ -27,7 +27,7 @@ EXPORTS = (
     "psgd_layer_info", "psgd_plan_layout", "psgd_count_sent", "psgd_last_error", "psgd_version",
     "psgd_get_phase_times", "psgd_step_noalloc", "psgd_step_momentum", "psgd_set_timing", "psgd_get_sparse",
     "psgd_plan_queue", "psgd_exchange_sizes", "psgd_step_begin", "psgd_step_mid", "psgd_step_end",
-    "psgd_layer_flags",
+    "psgd_layer_flags", "psgd_plan_one_pass",
 )
 
 PSGD_POWERSGD = 0
@@ -109,6 +109,8 @@ def lib() -> ctypes.CDLL:
         "psgd_step_begin": ([_P, ctypes.POINTER(_P), _P], ctypes.c_int),
         "psgd_step_mid": ([_P, _P, _P], ctypes.c_int),
         "psgd_step_end": ([_P, _P, _P], ctypes.c_int),
+        "psgd_plan_one_pass": ([ctypes.c_int, _I64P, _I64P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), _I64P], ctypes.c_int),
         "psgd_plan_queue": ([ctypes.c_int, _I64P, _I64P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                              ctypes.c_int, ctypes.POINTER(ctypes.c_int32), _I64P], ctypes.c_int),
         "psgd_last_error": ([], ctypes.c_char_p),
@@ -176,6 +178,27 @@ def psgd_plan_queue(shapes: Sequence[Tuple[int, int]], rank: int, workers: int, 
         lay, a, b, c = buf[4 * i:4 * i + 4]
         out.append((lay >> 24, lay & 0xFFFFFF, a, b, c))
     return out
+
+
+def psgd_plan_one_pass(shapes: Sequence[Tuple[int, int]], rank: int, workers: int, clusters: int):
+    """The one-pass project's plan for a layer set, needs no GPU (see
+    psgd_plan_one_pass in include/psgd.h): (per matrix layer (cw, yfc, yr,
+    nys), per cluster its segments [(matrix index, first block, end block,
+    slot), ...])."""
+    n, m = _shapes(shapes)
+    mats = sum(1 for _, b in shapes if b)
+    cnt = ctypes.c_int64()
+    _check(lib().psgd_plan_one_pass(len(shapes), n, m, rank, workers, clusters, None, None, ctypes.byref(cnt)))
+    plan = (ctypes.c_int32 * (4 * max(mats, 1)))()
+    buf = (ctypes.c_int32 * (4 * cnt.value))()
+    _check(lib().psgd_plan_one_pass(len(shapes), n, m, rank, workers, clusters, plan, buf, ctypes.byref(cnt)))
+    layers = [tuple(plan[4 * i:4 * i + 4]) for i in range(mats)]
+    tiles = [tuple(buf[4 * i:4 * i + 4]) for i in range(cnt.value)]
+    runs = []
+    for c in range(clusters):
+        _, first, segs, _ = tiles[c]
+        runs.append(tiles[clusters + first:clusters + first + segs])
+    return layers, runs
 
 
 def _stream_ptr(stream) -> Optional[int]:

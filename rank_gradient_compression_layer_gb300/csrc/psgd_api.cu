@@ -452,6 +452,50 @@ int psgd_count_sent(int num_layers, const int64_t* n, const int64_t* m, int rank
   return PSGD_OK;
 }
 
+int psgd_plan_one_pass(int num_layers, const int64_t* n, const int64_t* m, int rank, int num_workers,
+                       int clusters, int32_t* layer_plan, int32_t* tiles, int64_t* count) {
+  int rc = check_layers(num_layers, n, m);
+  if (rc) return rc;
+  if (rank < 1 || rank > 4) return fail(PSGD_ERR_INVALID, "the one-pass project is for ranks 1..4 (got %d)", rank);
+  if (num_workers < 1 || num_workers > kMaxWorkers)
+    return fail(PSGD_ERR_INVALID, "num_workers must be in [1, %d] (got %d)", kMaxWorkers, num_workers);
+  if (clusters < 1) return fail(PSGD_ERR_INVALID, "clusters must be >= 1 (got %d)", clusters);
+  if (!count) return fail(PSGD_ERR_INVALID, "count must not be NULL");
+  const int rp = padded_rank(rank);
+  std::vector<int64_t> off(num_layers), ld(num_layers);
+  int64_t total = 0;
+  layout(num_layers, n, m, off.data(), ld.data(), &total);
+  std::vector<LayerDev> hl;
+  for (int l = 0; l < num_layers; ++l) {
+    if (m[l] == 0) continue;
+    LayerDev L;
+    std::memset(&L, 0, sizeof(L));
+    L.n = (int32_t)n[l];
+    L.F = (int32_t)(ld[l] / 4);
+    L.ld = (int32_t)ld[l];
+    if (!plan_ycols(L, rp, num_workers)) return fail(PSGD_ERR_INVALID, "layer %d does not fit the one-pass project", l);
+    hl.push_back(L);
+  }
+  std::vector<Tile> t;
+  plan_yschedule(hl, rp, num_workers, clusters, t);
+  *count = (int64_t)t.size();
+  if (layer_plan)
+    for (size_t i = 0; i < hl.size(); ++i) {
+      layer_plan[4 * i] = hl[i].cw;
+      layer_plan[4 * i + 1] = hl[i].yfc;
+      layer_plan[4 * i + 2] = hl[i].yr;
+      layer_plan[4 * i + 3] = hl[i].nys;
+    }
+  if (tiles)
+    for (size_t i = 0; i < t.size(); ++i) {
+      tiles[4 * i] = t[i].layer;
+      tiles[4 * i + 1] = t[i].a;
+      tiles[4 * i + 2] = t[i].b;
+      tiles[4 * i + 3] = t[i].c;
+    }
+  return PSGD_OK;
+}
+
 int psgd_plan_queue(int num_layers, const int64_t* n, const int64_t* m, int rank, int num_workers,
                     int project_rows, int64_t lag_bytes, int with_update, int32_t* items, int64_t* count) {
   int rc = check_layers(num_layers, n, m);
