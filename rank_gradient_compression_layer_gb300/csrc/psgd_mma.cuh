@@ -44,7 +44,13 @@ struct MmaCfg {
   static constexpr uint32_t OFF_P = 0;                          // Phat' tile hi, lo; later the P rows, Gram scratch
   static constexpr uint32_t OFF_Q = 2 * OP;                     // Q^T hi, lo (the P product's B operand)
   static constexpr uint32_t OFF_U = OFF_Q + 2 * OP;             // Q_w' buffers 0, 1 (hi, lo each), then Msum hi, lo
-  static constexpr uint32_t U_BYTES = (4 * OP > 2 * MS) ? 4 * OP : 2 * MS;
+  // Msum as the P product's A operand (128 rows x K = 128 columns, K-major):
+  // its K-adjacent core matrices 144 bytes apart, 16 more than packed, so that
+  // a warp's stores of one row's 32 columns hit 32 distinct banks
+  static constexpr uint32_t M_LBO = 144;
+  static constexpr uint32_t M_SBO = (kMCols / 4) * M_LBO;
+  static constexpr uint32_t MS_P = (kMRows / 8) * M_SBO;  // one copy of the padded Msum
+  static constexpr uint32_t U_BYTES = (4 * OP > 2 * MS_P) ? 4 * OP : 2 * MS_P;
   // the rings, after the Q_w' buffers, over Msum's space (Msum is formed
   // after the worker loop): 4 row quarters x NS chunks of 8 rows x 128
   // columns of G and of B, as many chunks as fit
@@ -235,12 +241,14 @@ __global__ void __launch_bounds__(kMThreads, 1) p1m_kernel(const StepArgs a) {
   // over the Q_w' buffers) and Q^T (hi, lo) as the B operand
   {
     unsigned char* mhi = sm + C::OFF_U;
-    unsigned char* mlo = mhi + C::MS;
+    unsigned char* mlo = mhi + C::MS_P;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       float h, l;
       tf32_split(msum[i], h, l);
-      const uint32_t o = umma_off(r0 + i, cl, kMCols);
+      const int r = r0 + i;
+      const uint32_t o = (uint32_t)(r >> 3) * C::M_SBO + (uint32_t)(cl >> 2) * C::M_LBO + (uint32_t)(r & 7) * 16 +
+                         (uint32_t)(cl & 3) * 4;
       *reinterpret_cast<float*>(mhi + o) = h;
       *reinterpret_cast<float*>(mlo + o) = l;
     }
@@ -267,14 +275,14 @@ __global__ void __launch_bounds__(kMThreads, 1) p1m_kernel(const StepArgs a) {
   if (tid == 0) {
     constexpr uint32_t id = umma_idesc_tf32(kMRows, RP);
     const uint32_t d = tmem + 2u * kMRows;
-    const uint32_t ahi = base + C::OFF_U, alo = ahi + C::MS;
+    const uint32_t ahi = base + C::OFF_U, alo = ahi + C::MS_P;
     const uint32_t bhi = base + C::OFF_Q, blo = bhi + C::OP;
 #pragma unroll 1
     for (int ks = 0; ks < kMCols / 8; ++ks) {
-      const uint32_t o = (uint32_t)ks * 256;
-      umma_tf32(d, umma_sdesc(ahi + o, kMCols), umma_sdesc(bhi + o, kMCols), id, ks > 0 ? 1u : 0u);
-      umma_tf32(d, umma_sdesc(ahi + o, kMCols), umma_sdesc(blo + o, kMCols), id, 1u);
-      umma_tf32(d, umma_sdesc(alo + o, kMCols), umma_sdesc(bhi + o, kMCols), id, 1u);
+      const uint32_t oa = (uint32_t)ks * 2 * C::M_LBO, ob = (uint32_t)ks * 256;
+      umma_tf32(d, umma_sdesc_los(ahi + oa, C::M_LBO, C::M_SBO), umma_sdesc(bhi + ob, kMCols), id, ks > 0 ? 1u : 0u);
+      umma_tf32(d, umma_sdesc_los(ahi + oa, C::M_LBO, C::M_SBO), umma_sdesc(blo + ob, kMCols), id, 1u);
+      umma_tf32(d, umma_sdesc_los(alo + oa, C::M_LBO, C::M_SBO), umma_sdesc(bhi + ob, kMCols), id, 1u);
     }
     umma_commit(&s_mbar[2]);
   }

@@ -54,7 +54,7 @@ inline bool bmma_applies(const KernelSet& ks, int W) {
 }
 
 struct TileRows {
-  int r1 = 32, r3min = 256, ru = 64;
+  int r1 = 32, r3min = 512, ru = 64;
   int pcols = kSeg * 4;  // columns of a project tile
   int r3mult = 1;        // back-project rows per tile: a multiple of this (tensor-core chunks)
 };
