@@ -51,9 +51,13 @@ UNIT = "GB/s"
 # from a one-kernel ncu capture, valid only for the kernel sources whose hash
 # is recorded with it.
 NCU_TRAFFIC = {  # {(config, variant): (sources_sha256_prefix, bytes_per_launch)}
-    # ResNet-18 set, rTop-k, W = 4: ncu capture of three pass-0 launches, DRAM
-    # 363.0 MB read + 177.2 MB written per launch
-    ("c2", "rtopk"): ("f06f8d79ceb1a692", 540190976),
+    # ResNet-18 set, r = 2, W = 4: ncu capture of two project launches, DRAM
+    # 361.6 MB read + 104.1 MB written per launch (the rest of the error write
+    # is still in L2 when the kernel ends)
+    ("c2", "powersgd"): ("015a0b92d69c6dcd", 465662720),
+    # ResNet-18 set, rTop-k, W = 4: ncu capture of two pass-0 launches, DRAM
+    # 363.0 MB read + 177.9 MB written per launch
+    ("c2", "rtopk"): ("f019056e5ded52ed", 540920576),
 }
 
 
