@@ -130,12 +130,15 @@ static __device__ __forceinline__ void fused_back(const StepArgs& a, const Tile&
   float* s_red = reinterpret_cast<float*>(s_buf);  // p3_dyn_bytes, 16-byte aligned
   double* s_x = reinterpret_cast<double*>(s_red + p3_dyn_bytes(RP) / 4);
   float* s_ph = reinterpret_cast<float*>(s_x + RP * RP);
-  p3_body<RP, C::UNR, true>(a, t, s_ph, s_x, s_red, s_flag, pub);
+  const LayerDev L = a.layers[t.layer];  // by value: stores to B cannot alias it
+  p3_body<RP, C::UNR, true>(a, t, L, s_ph, s_x, s_red, s_flag, pub);
 }
 
 template <int RP>
 static __device__ __forceinline__ void fused_decomp(const StepArgs& a, const Tile& t, unsigned char* s_buf) {
-  u_body<RP, true>(a, t, reinterpret_cast<float*>(s_buf));
+  LayerDev L{};  // by value: stores to U cannot alias it (matrix tiles only)
+  if (t.c != 1) L = a.layers[t.layer];
+  u_body<RP, true>(a, t, L, reinterpret_cast<float*>(s_buf));
 }
 
 // Thread 0: the next queue position (n_items once the step was abandoned).

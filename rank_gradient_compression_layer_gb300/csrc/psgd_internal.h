@@ -12,7 +12,7 @@ constexpr int kSeg = 32;          // float4 columns per segment (one warp width)
 constexpr int kGramGroup = 32;    // project row blocks whose Gram partials one group sums
 // Share of L2 the project phase's last-written error rows may hold with an
 // evict-last policy, for the back-project's first tiles to read.
-constexpr double kL2KeepShare = 0.5;
+constexpr double kL2KeepShare = 0.3;
 // Rows of one orthonormalise tile (one thread per row): fewer at large r, so
 // that the tiles' float64 work (about r^2 per row) spreads over more SMs.
 constexpr int ph_rows(int rp) { return rp >= 32 ? 32 : (rp == 16 ? 64 : 128); }

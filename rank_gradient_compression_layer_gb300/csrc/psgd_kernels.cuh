@@ -58,8 +58,12 @@ struct Cfg {
   static constexpr int R1MAX = RP >= 16 ? 128 : R1;        // rows of a project row block at most (tensor-core tiles: 128)
   static constexpr int P1_WARPS = 8;                        // at most (more workers loop)
   static constexpr int P1_MINB = RP <= 2 ? 4 : (RP == 4 ? 3 : 1);          // 256-thread CTAs per SM the registers must allow
-  // back-project: 8 warps over interleaved groups of UNR3 rows
-  static constexpr int UNR3 = RP <= 2 ? 16 : 8;  // rows a warp loads at once (r = 4: 8 is faster)
+  // back-project: 8 warps over interleaved groups of UNR3 rows a warp loads
+  // at once, and the CTAs per SM the registers must allow (more CTAs hide
+  // each other's start-up and closing sums; two at r >= 16, whose
+  // accumulators take the most registers)
+  static constexpr int UNR3 = 8;
+  static constexpr int P3_MINB = RP <= 2 ? 4 : (RP <= 8 ? 3 : 2);
   // decompress: RU rows x one segment per CTA of 256 threads
   static constexpr int RU = 128;
 };
@@ -77,6 +81,33 @@ constexpr unsigned kFull = 0xffffffffu;
 // ----------------------------------------------------------------------------
 
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+
+// A phase kernel's tile and layer record, staged in shared memory by the
+// first warp before the programmatic-dependent wait, so that their two
+// dependent round trips overlap the end of the phase before.  The tables are
+// written before the step's first phase (by the host, or by a kernel the
+// project phase waited for), so only a later phase may read them early, and
+// it reads them through L2 (ld.global.cg): one request per table row and
+// CTA, as lane i loads word i of the record (every thread loading the whole
+// record would send the grid's requests for one layer to one L2 slice).
+// The caller's barrier after the wait publishes them to the CTA.
+struct EarlyTables {
+  Tile t;
+  LayerDev L;
+};
+
+__device__ __forceinline__ void stage_tables_early(const StepArgs& a, EarlyTables* s, bool vector_tiles) {
+  static_assert(sizeof(Tile) == 16 && sizeof(LayerDev) % 8 == 0 && sizeof(LayerDev) / 8 <= 32,
+                "a tile is one 16-byte word and a layer record at most 32 8-byte words");
+  if (threadIdx.x >= 32) return;
+  const int4 v = __ldcg(reinterpret_cast<const int4*>(a.tiles + blockIdx.x));
+  const Tile t{v.x, v.y, v.z, v.w};
+  if (threadIdx.x == 0) s->t = t;
+  if (vector_tiles && t.c == 1) return;  // a vector tile: no layer record
+  const int lane = (int)threadIdx.x;
+  if (lane < (int)(sizeof(LayerDev) / 8))
+    reinterpret_cast<long long*>(&s->L)[lane] = __ldcg(reinterpret_cast<const long long*>(a.layers + t.layer) + lane);
+}
 
 // An L2 cache policy under which the lines written are evicted last.
 __device__ __forceinline__ uint64_t l2_evict_last_policy() {
@@ -627,9 +658,10 @@ __device__ __forceinline__ void ph_body(const StepArgs& a, const LayerDev& L, in
   }
   unsigned* cnt = a.counters + L.cnt_off;
   if (one_pass) {
-    // the layer is done once every tile has stored its rows
-    if (cta_arrive_last(cnt + L.c_ph, (unsigned)L.nph, s_flag) && pub && threadIdx.x == 0)
-      flag_raise(pub, a.epoch);
+    // the layer is done once every tile has stored its rows (the fused step
+    // raises its X flag then; the phase kernels need no count: the
+    // back-project waits for the whole grid)
+    if (pub && cta_arrive_last(cnt + L.c_ph, (unsigned)L.nph, s_flag) && threadIdx.x == 0) flag_raise(pub, a.epoch);
     return;
   }
   __syncthreads();
@@ -682,10 +714,12 @@ __global__ void __launch_bounds__(kPhThreads) ph_kernel(const StepArgs a) {
   __shared__ float s_p1[ph_rows(RP) * RP];
   __shared__ double s_gram[RP * RP];
   __shared__ int s_flag;
+  __shared__ EarlyTables s_tab;
+  stage_tables_early(a, &s_tab, false);
   pdl_enter();
-  const Tile t = a.tiles[blockIdx.x];
-  const LayerDev L = a.layers[t.layer];  // by value: stores to P cannot alias it
-  ph_body<RP>(a, L, t.a, s_r, s_p1, s_gram, &s_flag, nullptr);
+  __syncthreads();
+  const LayerDev L = s_tab.L;  // a copy: stores to P cannot alias it
+  ph_body<RP>(a, L, s_tab.t.a, s_r, s_p1, s_gram, &s_flag, nullptr);
 }
 
 // r >= 8, second pass: Phat rows = P1 X (float64 products, rounded), once per
@@ -877,15 +911,16 @@ constexpr int p3_slices(int rp) { return rp >= 32 ? 2 : 1; }
 constexpr size_t p3_dyn_bytes(int rp) { return (size_t)(kP3Threads / 32 / p3_slices(rp)) * 32 * 4 * rp * sizeof(float); }
 
 
-// One back-project tile (kP3Threads threads), UNR rows per warp group.
+// One back-project tile (kP3Threads threads) of layer L, UNR rows per warp
+// group.
 // FUSED: the tile runs inside the fused step, where B, P1 and X were written
 // by other CTAs of the same launch, so they are read through L2 only
 // (ld.global.cg; an L1 line of this SM could be stale); pub is then the
 // segment's Qbar flag.  s_ph: warps x UNR x RH floats; s_x: RP x RP doubles;
 // s_red: p3_dyn_bytes(RP) bytes.
 template <int RP, int UNR, bool FUSED>
-__device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, float* s_ph, double* s_x, float* s_red,
-                                        int* s_flag, unsigned* pub) {
+__device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, const LayerDev& L, float* s_ph, double* s_x,
+                                        float* s_red, int* s_flag, unsigned* pub) {
   constexpr int NW = kP3Threads / 32;
   // r = 32: the ranks are split over warp pairs that read the same rows (the
   // second read hits in cache), so a warp holds 4 x RP / 2 accumulators and
@@ -894,9 +929,8 @@ __device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, float*
   constexpr int RH = RP / HS;        // ranks per warp
   constexpr int NG = NW / HS;        // row groups in flight
   static_assert(p3_dyn_bytes(RP) >= (size_t)NW * UNR * RP * sizeof(float), "s_red holds every warp's P1 rows");
-  const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
   const int rt = t.a, seg = t.b, w = t.c;
-  if (!FUSED && RP <= 4 && __ldg(a.rinv + L.rinv_off + 2 * RP * RP + RP + 1) != 0.0) {
+  if (!FUSED && RP <= 4 && a.ypath && __ldg(a.rinv + L.rinv_off + 2 * RP * RP + RP + 1) != 0.0) {
     // the project phase formed Y_w = M_w^T P: one tile per (segment, worker)
     // forms Q_w from it, and no tile reads M
     static_assert(p3_dyn_bytes(RP) >= 128 * RP * sizeof(double), "s_red holds the second half's sums");
@@ -918,6 +952,17 @@ __device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, float*
   const float* P1 = (kForm ? a.P : a.Phat) + L.p_off + (int64_t)row0 * RP;
   float* Pout = (kForm && seg == 0 && w == 0) ? a.Phat + L.p_off + (int64_t)row0 * RP : nullptr;
   const double* X = a.rinv + L.rinv_off + RP * RP + RP;
+  float4 bv[UNR];
+  auto load_rows = [&](int i0) {
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const float4* src = reinterpret_cast<const float4*>(Bw + (int64_t)(row0 + i0 + u) * L.ld);
+      bv[u] = (act && i0 + u < nrows) ? (FUSED ? __ldcg(src) : (HS > 1 ? __ldg(src) : __ldcs(src))) : zero4();
+    }
+  };
+  // r <= 4: the first group's rows go out before the X flag is known (they
+  // need only the layer record), so the flag's load overlaps them
+  if (kForm) load_rows(grp * UNR);
   const bool ident = !kForm || (FUSED ? __ldcg(X + RP * RP) : __ldg(X + RP * RP)) != 0.0;
   if (!ident) {
     for (int e = threadIdx.x; e < RP * RP; e += blockDim.x) s_x[e] = FUSED ? __ldcg(X + e) : __ldg(X + e);
@@ -931,13 +976,15 @@ __device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, float*
 #pragma unroll
     for (int k = 0; k < RH; ++k) acc[j][k] = 0.f;
   // row groups of UNR rows interleaved over the NG groups; each warp stages
-  // its own slice of the group's Phat rows (warp barriers only)
+  // its own slice of the group's Phat rows (warp barriers only) while the
+  // group's B rows are in flight
   for (int i0 = grp * UNR; i0 < nrows; i0 += NG * UNR) {
     const int nr = min(UNR, nrows - i0);
     __syncwarp();  // the previous group's rows are no longer read
+    if (!kForm || i0 != grp * UNR) load_rows(i0);
     if (!ident) {
       // Phat = P1 X (j ascending): the group's P1 rows (all ranks), then the
-      // product, before the B loads so that their registers are not live
+      // product
       for (int e = lane; e < nr * RP; e += 32)
         s_p1[e] = FUSED ? __ldcg(P1 + (int64_t)i0 * RP + e) : __ldg(P1 + (int64_t)i0 * RP + e);
       __syncwarp();
@@ -952,14 +999,7 @@ __device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, float*
         s_mine[e] = (float)v;
         if (Pout) Pout[(int64_t)(i0 + u) * RP + k] = (float)v;
       }
-    }
-    float4 bv[UNR];
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const float4* src = reinterpret_cast<const float4*>(Bw + (int64_t)(row0 + i0 + u) * L.ld);
-      bv[u] = (act && i0 + u < nrows) ? (FUSED ? __ldcg(src) : (HS > 1 ? __ldg(src) : __ldcs(src))) : zero4();
-    }
-    if (ident) {  // Phat = P1, staged while the B loads are in flight
+    } else {  // Phat = P1
       for (int e = lane; e < nr * RH; e += 32) {
         const int64_t o = (int64_t)(i0 + e / RH) * RP + hs * RH + e % RH;
         const float v = FUSED ? __ldcg(P1 + o) : __ldg(P1 + o);
@@ -990,8 +1030,13 @@ __device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, float*
 #pragma unroll
     for (int k = 0; k < RH; ++k) mine[j * RP + k] = acc[j][k];
   __syncthreads();
+  // a layer of one row tile: the tile's sum is Q_w itself (the same value
+  // the sum over one partial gives), stored without the partial's round
+  // trip through L2
+  const bool direct = L.t3r == 1;
   {
-    float* part = a.qpart + L.qpart_off + ((int64_t)rt * a.W + w) * L.ld * RP;
+    float* part = direct ? a.Qw + (int64_t)w * a.q_total + L.q_off
+                         : a.qpart + L.qpart_off + ((int64_t)rt * a.W + w) * L.ld * RP;
     const int ncol4 = min(kSeg, L.F - seg * kSeg);
     for (int idx = threadIdx.x; idx < ncol4 * 4 * RP; idx += blockDim.x) {
       const int ln = idx / (4 * RP), jk = idx % (4 * RP);
@@ -1001,20 +1046,27 @@ __device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, float*
       part[(int64_t)(seg * kSeg + ln) * 4 * RP + jk] = s;
     }
   }
-  if (cta_arrive_last(a.counters + L.cnt_off + L.c_p3 + seg * a.W + w, (unsigned)L.t3r, s_flag))
+  if (direct)
+    qbar_segment<RP>(a, L, seg, s_flag, pub);
+  else if (cta_arrive_last(a.counters + L.cnt_off + L.c_p3 + seg * a.W + w, (unsigned)L.t3r, s_flag))
     qf_segment_worker<RP>(a, L, seg, w, s_flag, pub);
 }
 
 template <int RP>
-__global__ void __launch_bounds__(kP3Threads) p3_kernel(const StepArgs a) {
+__global__ void __launch_bounds__(kP3Threads, Cfg<RP>::P3_MINB) p3_kernel(const StepArgs a) {
   constexpr int UNR = Cfg<RP>::UNR3;
   constexpr int RH = RP / p3_slices(RP);
   __shared__ float s_ph[(kP3Threads / 32) * UNR * RH];  // each warp's Phat values of its current group
   __shared__ double s_x[RP * RP];                       // X = R2^-1 (when it is not the identity)
   extern __shared__ __align__(16) float s_red[];        // the cross-warp reduction; first each warp's P1 rows
   __shared__ int s_flag;
+  __shared__ EarlyTables s_tab;
+  stage_tables_early(a, &s_tab, false);
   pdl_enter();
-  p3_body<RP, UNR, false>(a, a.tiles[blockIdx.x], s_ph, s_x, s_red, &s_flag, nullptr);
+  __syncthreads();
+  const Tile t = s_tab.t;
+  const LayerDev L = s_tab.L;  // a copy: stores to B cannot alias it
+  p3_body<RP, UNR, false>(a, t, L, s_ph, s_x, s_red, &s_flag, nullptr);
 }
 
 // ----------------------------------------------------------------------------
@@ -1041,11 +1093,11 @@ __device__ __forceinline__ void momentum4(float* X, float* Mom, int64_t p, float
   __stcs(reinterpret_cast<float4*>(X + p), x);
   __stcs(reinterpret_cast<float4*>(Mom + p), m);
 }
-// One decompress tile (kUThreads threads).  FUSED: Phat and Qbar were
-// written by other CTAs of the same launch and are read through L2 only.
-// s_ph: RU x RP floats.
+// One decompress tile (kUThreads threads): of layer L, or (t.c == 1) of the
+// vector layers, L unused.  FUSED: Phat and Qbar were written by other CTAs
+// of the same launch and are read through L2 only.  s_ph: RU x RP floats.
 template <int RP, bool FUSED>
-__device__ __forceinline__ void u_body(const StepArgs& a, const Tile& t, float* s_ph) {
+__device__ __forceinline__ void u_body(const StepArgs& a, const Tile& t, const LayerDev& L, float* s_ph) {
   constexpr int RU = Cfg<RP>::RU;
   if (t.c == 1) {  // vector layer: U = mean_w G_w
     const VecDev V = a.vecs[t.layer];
@@ -1065,7 +1117,6 @@ __device__ __forceinline__ void u_body(const StepArgs& a, const Tile& t, float* 
     }
     return;
   }
-  const LayerDev L = a.layers[t.layer];  // by value: stores to B, U cannot alias it
   const int row0 = t.a * L.ru, seg = t.b;
   const int rcnt = min(L.ru, L.n - row0);
   const float* Psrc = (a.unbiased ? a.P : a.Phat) + L.p_off + (int64_t)row0 * RP;
@@ -1121,8 +1172,13 @@ __device__ __forceinline__ void u_body(const StepArgs& a, const Tile& t, float* 
 template <int RP>
 __global__ void __launch_bounds__(kUThreads) u_kernel(const StepArgs a) {
   __shared__ float s_ph[Cfg<RP>::RU * RP];
+  __shared__ EarlyTables s_tab;
+  stage_tables_early(a, &s_tab, true);
   pdl_enter();
-  u_body<RP, false>(a, a.tiles[blockIdx.x], s_ph);
+  __syncthreads();
+  const Tile t = s_tab.t;
+  const LayerDev L = s_tab.L;  // a copy (matrix tiles only): stores to U cannot alias it
+  u_body<RP, false>(a, t, L, s_ph);
 }
 
 // ----------------------------------------------------------------------------
@@ -1328,8 +1384,11 @@ template <int RP>
 __global__ void __launch_bounds__(kSeg * 4) ut_kernel(const StepArgs a) {
   constexpr int RU = Cfg<RP>::RU;
   __shared__ __align__(16) float s_ph[RU * RP];
+  __shared__ EarlyTables s_tab;
+  stage_tables_early(a, &s_tab, true);
   pdl_enter();
-  const Tile t = a.tiles[blockIdx.x];
+  __syncthreads();
+  const Tile t = s_tab.t;
   if (t.c == 1) {  // vector layer: U = mean_w G_w
     const VecDev V = a.vecs[t.layer];
     const int base = t.a * kVChunk;
@@ -1348,7 +1407,7 @@ __global__ void __launch_bounds__(kSeg * 4) ut_kernel(const StepArgs a) {
     }
     return;
   }
-  const LayerDev L = a.layers[t.layer];  // by value
+  const LayerDev L = s_tab.L;  // a copy: stores to U cannot alias it
   const int row0 = t.a * L.ru, seg = t.b;
   const int rcnt = min(L.ru, L.n - row0);
   const float* Psrc = a.unbiased ? a.P : a.Phat;
