@@ -308,6 +308,19 @@ void plan_one_pass(psgd_ctx* c) {
   }
 }
 
+// The project phase's order of the matrix layers: largest first (stable),
+// so that the grid ends on short tiles of small layers and the long closing
+// sums of the large layers (their row blocks' segment and Gram partials)
+// overlap other layers' streaming instead of trailing the phase.
+std::vector<int> project_order(const psgd_ctx* c) {
+  std::vector<int> order(c->hl.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+    return (int64_t)c->hl[x].n * c->hl[x].ld > (int64_t)c->hl[y].n * c->hl[y].ld;
+  });
+  return order;
+}
+
 // The project phase's last-written error rows, which the back-project
 // (whose tiles run in the reverse order) reads first: up to kL2KeepShare of
 // L2, counted from the end of the project order, are stored with an L2
@@ -319,8 +332,9 @@ void plan_l2_keep(psgd_ctx* c) {
     l2 = 0;
   }
   int64_t room = (int64_t)(kL2KeepShare * (double)l2);
-  for (int li = (int)c->hl.size() - 1; li >= 0; --li) {
-    LayerDev& L = c->hl[li];
+  const std::vector<int> order = project_order(c);
+  for (auto it = order.rbegin(); it != order.rend(); ++it) {
+    LayerDev& L = c->hl[*it];
     const int64_t row_bytes = (int64_t)c->W * L.ld * 4;
     const int64_t rows = std::min<int64_t>(L.n, std::max<int64_t>(0, room / row_bytes));
     L.l2row = (int32_t)(L.n - rows);
@@ -334,15 +348,20 @@ void plan_l2_keep(psgd_ctx* c) {
 void build_tiles(psgd_ctx* c) {
   for (auto& v : c->tiles) v.clear();
   const int nm = (int)c->hl.size();
-  for (int li = 0; li < nm; ++li) {
+  const std::vector<int> order = project_order(c);
+  for (int li : order) {
     const LayerDev& L = c->hl[li];
     for (int rb = 0; rb < L.nrb; ++rb)
       for (int s = 0; s < L.s1; ++s) c->tiles[kProject].push_back({li, rb, s, 0});
+  }
+  for (int li = 0; li < nm; ++li) {
+    const LayerDev& L = c->hl[li];
     for (int t = 0; t < L.nph; ++t) c->tiles[kOrthonormalise].push_back({li, t, 0, 0});
     for (int rb = 0; rb < (int)ceil_div(L.n, L.ru); ++rb)
       for (int s = 0; s < L.S; ++s) c->tiles[kDecompress].push_back({li, rb, s, 0});
   }
-  for (int li = nm - 1; li >= 0; --li) {
+  for (auto it = order.rbegin(); it != order.rend(); ++it) {
+    const int li = *it;
     const LayerDev& L = c->hl[li];
     for (int rt = L.t3r - 1; rt >= 0; --rt)
       for (int s = L.S - 1; s >= 0; --s)

@@ -510,6 +510,7 @@ __device__ __forceinline__ void p1_rows_done(const StepArgs& a, const LayerDev& 
     const float* pb = a.ppart + L.ppart_off + (int64_t)T.rb * L.s1 * L.r1 * RP;
     for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) {
       float s = 0.f;
+#pragma unroll 12
       for (int qq = 0; qq < L.s1; ++qq) s += __ldcg(pb + (int64_t)qq * L.r1 * RP + idx);
       s_prow[idx] = s;
     }
