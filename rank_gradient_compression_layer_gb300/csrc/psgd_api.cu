@@ -308,11 +308,12 @@ void plan_one_pass(psgd_ctx* c) {
   }
 }
 
-// The project phase's order of the matrix layers: largest first (stable),
-// so that the grid ends on short tiles of small layers and the long closing
-// sums of the large layers (their row blocks' segment and Gram partials)
-// overlap other layers' streaming instead of trailing the phase.
-std::vector<int> project_order(const psgd_ctx* c) {
+// The order of the matrix layers in the project and back-project phases:
+// largest first (stable), so that each grid ends on the short tiles of small
+// layers, and the long closing sums of the large layers (their row blocks'
+// segment and Gram partials, their segments' Q_w sums) overlap other
+// layers' streaming instead of trailing the phase.
+std::vector<int> layer_order(const psgd_ctx* c) {
   std::vector<int> order(c->hl.size());
   for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
   std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
@@ -321,10 +322,10 @@ std::vector<int> project_order(const psgd_ctx* c) {
   return order;
 }
 
-// The project phase's last-written error rows, which the back-project
-// (whose tiles run in the reverse order) reads first: up to kL2KeepShare of
-// L2, counted from the end of the project order, are stored with an L2
-// evict-last policy so that they are still there.
+// The error rows the back-project reads first (the first layers' last rows:
+// it takes each layer's row tiles from the last): up to kL2KeepShare of L2,
+// counted from the start of the layer order, are stored by the project phase
+// with an L2 evict-last policy so that they are still there.
 void plan_l2_keep(psgd_ctx* c) {
   int l2 = 0;
   if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, c->device) != cudaSuccess) {
@@ -332,9 +333,8 @@ void plan_l2_keep(psgd_ctx* c) {
     l2 = 0;
   }
   int64_t room = (int64_t)(kL2KeepShare * (double)l2);
-  const std::vector<int> order = project_order(c);
-  for (auto it = order.rbegin(); it != order.rend(); ++it) {
-    LayerDev& L = c->hl[*it];
+  for (int li : layer_order(c)) {
+    LayerDev& L = c->hl[li];
     const int64_t row_bytes = (int64_t)c->W * L.ld * 4;
     const int64_t rows = std::min<int64_t>(L.n, std::max<int64_t>(0, room / row_bytes));
     L.l2row = (int32_t)(L.n - rows);
@@ -342,13 +342,13 @@ void plan_l2_keep(psgd_ctx* c) {
   }
 }
 
-// Tiles of every phase.  Back-project walks the layers and rows in the
-// reverse of the project order, so it first reads the error buffers the
-// project phase wrote last, while they are still in L2.
+// Tiles of every phase.  Project and back-project take the layers in
+// layer_order; the back-project takes a layer's row tiles from the last, so
+// it starts on rows the project phase kept in L2.
 void build_tiles(psgd_ctx* c) {
   for (auto& v : c->tiles) v.clear();
   const int nm = (int)c->hl.size();
-  const std::vector<int> order = project_order(c);
+  const std::vector<int> order = layer_order(c);
   for (int li : order) {
     const LayerDev& L = c->hl[li];
     for (int rb = 0; rb < L.nrb; ++rb)
@@ -360,8 +360,7 @@ void build_tiles(psgd_ctx* c) {
     for (int rb = 0; rb < (int)ceil_div(L.n, L.ru); ++rb)
       for (int s = 0; s < L.S; ++s) c->tiles[kDecompress].push_back({li, rb, s, 0});
   }
-  for (auto it = order.rbegin(); it != order.rend(); ++it) {
-    const int li = *it;
+  for (int li : order) {
     const LayerDev& L = c->hl[li];
     for (int rt = L.t3r - 1; rt >= 0; --rt)
       for (int s = L.S - 1; s >= 0; --s)

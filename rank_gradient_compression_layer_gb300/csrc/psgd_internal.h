@@ -10,8 +10,8 @@ namespace psgd {
 constexpr int kMaxWorkers = 64;   // W limit (pointer table passed by value)
 constexpr int kSeg = 32;          // float4 columns per segment (one warp width)
 constexpr int kGramGroup = 32;    // project row blocks whose Gram partials one group sums
-// Share of L2 the project phase's last-written error rows may hold with an
-// evict-last policy, for the back-project's first tiles to read.
+// Share of L2 the error rows the back-project reads first may hold, stored
+// by the project phase with an evict-last policy.
 constexpr double kL2KeepShare = 0.3;
 // Rows of one orthonormalise tile (one thread per row): fewer at large r, so
 // that the tiles' float64 work (about r^2 per row) spreads over more SMs.
@@ -95,7 +95,7 @@ struct LayerDev {
   int32_t s1;         // project tiles per row block (column blocks: segments, or half segments)
   int32_t c_phg;      // orthonormalise tiles done per tile group, second pass (ph_groups(nph))
   int32_t l2row;      // project: rows >= l2row store M to B with an L2 evict-last policy (the
-                      // back-project, in reverse order, reads them first, from L2); n: none
+                      // back-project reads them first, from L2); n: none
   // one-pass project (cw = 0: the layer is not on it): cw CTAs across a row,
   // yfc float4 columns each (a cluster holds kYClusterMax / cw such
   // subgroups); nys partial slots, one per segment of the schedule, each
