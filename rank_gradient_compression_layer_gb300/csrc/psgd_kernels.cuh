@@ -510,7 +510,10 @@ __device__ __forceinline__ void p1_rows_done(const StepArgs& a, const LayerDev& 
     const float* pb = a.ppart + L.ppart_off + (int64_t)T.rb * L.s1 * L.r1 * RP;
     for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) {
       float s = 0.f;
-#pragma unroll 12
+      // loads batched at r <= 4 (at r >= 16 the unrolled loads push the
+      // tensor-core tile's registers into spills)
+      constexpr int kBatch = RP <= 4 ? 12 : 1;
+#pragma unroll kBatch
       for (int qq = 0; qq < L.s1; ++qq) s += __ldcg(pb + (int64_t)qq * L.r1 * RP + idx);
       s_prow[idx] = s;
     }
@@ -1061,13 +1064,22 @@ __global__ void __launch_bounds__(kP3Threads, Cfg<RP>::P3_MINB) p3_kernel(const 
   __shared__ double s_x[RP * RP];                       // X = R2^-1 (when it is not the identity)
   extern __shared__ __align__(16) float s_red[];        // the cross-warp reduction; first each warp's P1 rows
   __shared__ int s_flag;
-  __shared__ EarlyTables s_tab;
-  stage_tables_early(a, &s_tab, false);
-  pdl_enter();
-  __syncthreads();
-  const Tile t = s_tab.t;
-  const LayerDev L = s_tab.L;  // a copy: stores to B cannot alias it
-  p3_body<RP, UNR, false>(a, t, L, s_ph, s_x, s_red, &s_flag, nullptr);
+  if constexpr (RP >= 16) {
+    // two CTAs per SM of 27 or more waves: the early staging's barrier costs
+    // more than the first wave's round trips it saves
+    pdl_enter();
+    const Tile t = a.tiles[blockIdx.x];
+    const LayerDev L = a.layers[t.layer];  // by value: stores to B cannot alias it
+    p3_body<RP, UNR, false>(a, t, L, s_ph, s_x, s_red, &s_flag, nullptr);
+  } else {
+    __shared__ EarlyTables s_tab;
+    stage_tables_early(a, &s_tab, false);
+    pdl_enter();
+    __syncthreads();
+    const Tile t = s_tab.t;
+    const LayerDev L = s_tab.L;  // a copy: stores to B cannot alias it
+    p3_body<RP, UNR, false>(a, t, L, s_ph, s_x, s_red, &s_flag, nullptr);
+  }
 }
 
 // ----------------------------------------------------------------------------
