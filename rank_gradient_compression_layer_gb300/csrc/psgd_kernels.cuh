@@ -510,11 +510,14 @@ __device__ __forceinline__ void p1_rows_done(const StepArgs& a, const LayerDev& 
     const float* pb = a.ppart + L.ppart_off + (int64_t)T.rb * L.s1 * L.r1 * RP;
     for (int idx = threadIdx.x; idx < T.rcnt * RP; idx += blockDim.x) {
       float s = 0.f;
-      // loads batched at r <= 4 (at r >= 16 the unrolled loads push the
-      // tensor-core tile's registers into spills)
-      constexpr int kBatch = RP <= 4 ? 12 : 1;
-#pragma unroll kBatch
-      for (int qq = 0; qq < L.s1; ++qq) s += __ldcg(pb + (int64_t)qq * L.r1 * RP + idx);
+      if constexpr (RP <= 4) {
+        // loads batched (at r >= 16 this pushes the tensor-core tile's
+        // registers into spills)
+#pragma unroll 12
+        for (int qq = 0; qq < L.s1; ++qq) s += __ldcg(pb + (int64_t)qq * L.r1 * RP + idx);
+      } else {
+        for (int qq = 0; qq < L.s1; ++qq) s += __ldcg(pb + (int64_t)qq * L.r1 * RP + idx);
+      }
       s_prow[idx] = s;
     }
     __syncthreads();

@@ -60,8 +60,12 @@ struct TileRows {
 };
 
 // The phase grids must hold several waves of resident CTAs, or the last,
-// partly filled wave leaves HBM idle.
+// partly filled wave leaves HBM idle.  The back-project needs fewer: its
+// tiles end in a cross-warp sum and a count, whose barriers cost more than
+// the tail of fewer, taller tiles (two waves measured faster than four or
+// eight on the ResNet-18 set).
 constexpr int kWaves = 4;
+constexpr int kBackWaves = 2;
 
 // Tiling of one matrix layer for padded rank rp and W workers.  Returns the
 // number of counters the layer needs and sets its counter offsets relative
@@ -189,9 +193,10 @@ inline void plan_yschedule(std::vector<LayerDev>& hl, int rp, int W, int nc, std
   for (const auto& r : runs) tiles.insert(tiles.end(), r.begin(), r.end());
 }
 
-// Chooses the tile rows of a layer set so that each phase grid is at least
-// kWaves waves of resident CTAs (or the rows reach their floor); decompress
-// tiles keep their size (their cost is the per-tile set-up, not the tail).
+// Chooses the tile rows of a layer set so that the project grid is at least
+// kWaves waves of resident CTAs and the back-project grid kBackWaves (or the
+// rows reach their floor); decompress tiles keep their size (their cost is
+// the per-tile set-up, not the tail).
 inline int choose_tile_rows(const std::vector<int64_t>& n, const std::vector<int64_t>& m, int rp, int W,
                             const KernelSet& ks, int device, TileRows* tr) {
   int sms = 0, c1 = 0, c3 = 0, cu = 0;
@@ -219,7 +224,7 @@ inline int choose_tile_rows(const std::vector<int64_t>& n, const std::vector<int
     r.r1 /= 2;
     count(r.r1, r.r3min, r.ru, &t1, &t3, &tu);
   }
-  while (t3 < (int64_t)kWaves * c3 * sms && r.r3min > 32) {
+  while (t3 < (int64_t)kBackWaves * c3 * sms && r.r3min > 32) {
     r.r3min /= 2;
     count(r.r1, r.r3min, r.ru, &t1, &t3, &tu);
   }
