@@ -52,12 +52,12 @@ UNIT = "GB/s"
 # is recorded with it.
 NCU_TRAFFIC = {  # {(config, variant): (sources_sha256_prefix, bytes_per_launch)}
     # ResNet-18 set, r = 2, W = 4: ncu capture of two project launches, DRAM
-    # 361.6 MB read + 104.1 MB written per launch (the rest of the error write
+    # 361.1 MB read + 101.1 MB written per launch (the rest of the error write
     # is still in L2 when the kernel ends)
-    ("c2", "powersgd"): ("015a0b92d69c6dcd", 465662720),
+    ("c2", "powersgd"): ("e199a6f86b9e344f", 462178688),
     # ResNet-18 set, rTop-k, W = 4: ncu capture of two pass-0 launches, DRAM
     # 363.0 MB read + 177.9 MB written per launch
-    ("c2", "rtopk"): ("f019056e5ded52ed", 540920576),
+    ("c2", "rtopk"): ("46d59ec3e9470943", 540897792),
 }
 
 
