@@ -629,6 +629,13 @@ __device__ __forceinline__ void ph_body(const StepArgs& a, const LayerDev& L, in
   constexpr int NG = Cfg<RP>::NG;
   constexpr int NR = ph_rows(RP);
   double* fr = a.rinv + L.rinv_off;
+  // the row thread's P row is requested first, with the factor's loads
+  const int row = chunk * NR + (int)threadIdx.x;
+  const bool valid = threadIdx.x < NR && row < L.n;
+  float* prow = a.P + L.p_off + (int64_t)row * RP;
+  double x[RP];
+#pragma unroll
+  for (int k = 0; k < RP; ++k) x[k] = valid ? (double)__ldcg(prow + k) : 0.0;
   for (int e = threadIdx.x; e < RP * RP + RP; e += blockDim.x) s_r[e] = __ldcg(fr + e);
   const bool one_pass = __ldcg(fr + 2 * RP * RP + RP) != 0.0;
   // Phat is stored here at r >= 8, and at r <= 4 when the back-project
@@ -636,12 +643,6 @@ __device__ __forceinline__ void ph_body(const StepArgs& a, const LayerDev& L, in
   const bool store_phat = one_pass && (RP >= 8 || __ldcg(fr + 2 * RP * RP + RP + 1) != 0.0);
   __syncthreads();
   if (threadIdx.x < NR) {  // whole warps (NR is a multiple of 32)
-    const int row = chunk * NR + threadIdx.x;
-    const bool valid = row < L.n;
-    float* prow = a.P + L.p_off + (int64_t)row * RP;
-    double x[RP];
-#pragma unroll
-    for (int k = 0; k < RP; ++k) x[k] = valid ? (double)__ldcg(prow + k) : 0.0;
 #pragma unroll
     for (int k = 0; k < RP; ++k) {
       double s = x[k];
@@ -968,8 +969,15 @@ __device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, const 
     }
   };
   // r <= 4: the first group's rows go out before the X flag is known (they
-  // need only the layer record), so the flag's load overlaps them
+  // need only the layer record), so the flag's load overlaps them; outside
+  // the fused step so does the lane's value of the group's P1 rows, which
+  // is Phat when one pass was enough (UNR x RH <= 32: one value a lane)
+  constexpr bool kEarly = !FUSED && RP <= 4;
+  static_assert(!kEarly || UNR * RH <= 32, "one early P1 value per lane");
   if (kForm) load_rows(grp * UNR);
+  float p_early = 0.f;
+  if (kEarly && grp * UNR < nrows && lane < min(UNR, nrows - grp * UNR) * RH)
+    p_early = __ldg(P1 + (int64_t)(grp * UNR + lane / RH) * RP + hs * RH + lane % RH);
   const bool ident = !kForm || (FUSED ? __ldcg(X + RP * RP) : __ldg(X + RP * RP)) != 0.0;
   if (!ident) {
     for (int e = threadIdx.x; e < RP * RP; e += blockDim.x) s_x[e] = FUSED ? __ldcg(X + e) : __ldg(X + e);
@@ -1009,7 +1017,7 @@ __device__ __forceinline__ void p3_body(const StepArgs& a, const Tile& t, const 
     } else {  // Phat = P1
       for (int e = lane; e < nr * RH; e += 32) {
         const int64_t o = (int64_t)(i0 + e / RH) * RP + hs * RH + e % RH;
-        const float v = FUSED ? __ldcg(P1 + o) : __ldg(P1 + o);
+        const float v = (kEarly && i0 == grp * UNR) ? p_early : (FUSED ? __ldcg(P1 + o) : __ldg(P1 + o));
         s_mine[e] = v;
         if (Pout) Pout[o] = v;
       }
@@ -1136,13 +1144,11 @@ __device__ __forceinline__ void u_body(const StepArgs& a, const Tile& t, const L
   const int row0 = t.a * L.ru, seg = t.b;
   const int rcnt = min(L.ru, L.n - row0);
   const float* Psrc = (a.unbiased ? a.P : a.Phat) + L.p_off + (int64_t)row0 * RP;
-  for (int i = threadIdx.x; i < rcnt * RP; i += blockDim.x) s_ph[i] = FUSED ? __ldcg(Psrc + i) : __ldg(Psrc + i);
-  __syncthreads();
   const int lane = threadIdx.x & 31, sub = threadIdx.x >> 5;  // 8 rows in flight per pass
   const int c = seg * kSeg + lane;
-  if (c >= L.F) return;
+  // the lane's Qbar rows are requested with the Phat rows, before the barrier
   float qv[4][RP];
-  {
+  if (c < L.F) {
     const float* qs = a.Qbar + L.q_off + (int64_t)(4 * c) * RP;
     float* flat = &qv[0][0];
     if constexpr (RP % 4 == 0) {
@@ -1160,6 +1166,9 @@ __device__ __forceinline__ void u_body(const StepArgs& a, const Tile& t, const L
       for (int i = 0; i < 4 * RP; ++i) flat[i] = FUSED ? __ldcg(qs + i) : __ldg(qs + i);
     }
   }
+  for (int i = threadIdx.x; i < rcnt * RP; i += blockDim.x) s_ph[i] = FUSED ? __ldcg(Psrc + i) : __ldg(Psrc + i);
+  __syncthreads();
+  if (c >= L.F) return;
   const int valid = (c == L.F - 1) ? L.tail : 4;
   const int64_t col = L.off + 4 * c;
 #pragma unroll 4
