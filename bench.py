@@ -52,12 +52,12 @@ UNIT = "GB/s"
 # is recorded with it.
 NCU_TRAFFIC = {  # {(config, variant): (sources_sha256_prefix, bytes_per_launch)}
     # ResNet-18 set, r = 2, W = 4: ncu capture of two project launches, DRAM
-    # 361.1 MB read + 101.1 MB written per launch (the rest of the error write
+    # 361.2 MB read + 102.2 MB written per launch (the rest of the error write
     # is still in L2 when the kernel ends)
-    ("c2", "powersgd"): ("e199a6f86b9e344f", 462178688),
+    ("c2", "powersgd"): ("46e00040e0fc3a25", 463434368),
     # ResNet-18 set, rTop-k, W = 4: ncu capture of two pass-0 launches, DRAM
     # 363.0 MB read + 177.9 MB written per launch
-    ("c2", "rtopk"): ("46d59ec3e9470943", 540897792),
+    ("c2", "rtopk"): ("8d88d16b3e14d2cc", 540944128),
 }
 
 
