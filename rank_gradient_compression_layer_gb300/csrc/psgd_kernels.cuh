@@ -184,7 +184,9 @@ __device__ __forceinline__ void tri_index(int e, int rp, int& i, int& j) {
 // of the kernel before them in the stream): wait until that kernel has
 // completed and its writes are visible -- a no-op for a normal launch -- then
 // let the next kernel's CTAs be scheduled while this grid runs, so they are
-// resident and waiting when it ends.  Every phase kernel calls this first.
+// resident and waiting when it ends.  Every phase kernel calls this before it
+// reads anything a kernel of the step writes (the later phases stage their
+// tile and layer record first: stage_tables_early).
 __device__ __forceinline__ void pdl_enter() {
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");

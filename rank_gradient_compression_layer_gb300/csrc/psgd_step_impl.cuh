@@ -24,7 +24,9 @@ constexpr size_t kP1TDyn = (size_t)(2 * kRP * kP1TRow + Cfg<kRP>::R1 * kRP) * si
 #endif
 
 // A phase kernel launched as a programmatic dependent of the kernel before it
-// in the stream (the kernels wait for it in pdl_enter before touching data).
+// in the stream (the kernels wait for it in pdl_enter before reading anything
+// a kernel of the step writes; only the later phases' tile and layer tables,
+// written before the step, are read earlier).
 cudaError_t launch_dependent(void (*kernel)(StepArgs), int tiles, int threads, size_t smem, cudaStream_t s,
                              const StepArgs& a) {
   cudaLaunchConfig_t cfg = {};

@@ -54,3 +54,11 @@ def test_source_hashes_per_variant_and_traffic_keys():
     for key, (h, nbytes) in bench.NCU_TRAFFIC.items():
         assert isinstance(key, tuple) and key[1] in ("powersgd", "rtopk")
         assert len(h) == 16 and nbytes > 0
+
+
+def test_source_hash_ignores_comments_only():
+    # comments and blank lines are left out; code, and a // inside it, is kept
+    src = "int a; // note\n/* block\n   comment */\n\nint b = 2;  /* x */ int c;\n"
+    assert bench._code_only(src) == "int a;\nint b = 2;   int c;"
+    assert bench._code_only(src) == bench._code_only(src.replace("note", "another note"))
+    assert bench._code_only(src) != bench._code_only(src.replace("b = 2", "b = 3"))
