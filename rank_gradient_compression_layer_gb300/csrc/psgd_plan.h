@@ -62,10 +62,10 @@ struct TileRows {
 // The phase grids must hold several waves of resident CTAs, or the last,
 // partly filled wave leaves HBM idle.  The back-project needs fewer: its
 // tiles end in a cross-warp sum and a count, whose barriers cost more than
-// the tail of fewer, taller tiles (two waves measured faster than four or
-// eight on the ResNet-18 set).
+// the tail of fewer, taller tiles (one wave of 512-row tiles measured faster
+// than two, four or eight waves on the ResNet-18 set).
 constexpr int kWaves = 4;
-constexpr int kBackWaves = 2;
+constexpr int kBackWaves = 1;
 
 // Tiling of one matrix layer for padded rank rp and W workers.  Returns the
 // number of counters the layer needs and sets its counter offsets relative
