@@ -53,12 +53,12 @@ UNIT = "GB/s"
 # (of their code, comments left out) is recorded with it.
 NCU_TRAFFIC = {  # {(config, variant): (sources_sha256_prefix, bytes_per_launch)}
     # ResNet-18 set, r = 2, W = 4: ncu capture of two project launches, DRAM
-    # 361.2 MB read + 101.1 MB written per launch (the rest of the error write
+    # 359.5 MB read + 101.0 MB written per launch (the rest of the error write
     # is still in L2 when the kernel ends)
-    ("c2", "powersgd"): ("5e436fbd4daf60f8", 462237952),
+    ("c2", "powersgd"): ("3034e04c68da275f", 460501376),
     # ResNet-18 set, rTop-k, W = 4: ncu capture of two pass-0 launches, DRAM
     # 363.0 MB read + 177.9 MB written per launch
-    ("c2", "rtopk"): ("81af32f32b57ceb8", 540918016),
+    ("c2", "rtopk"): ("a761099234848755", 540899968),
 }
 
 

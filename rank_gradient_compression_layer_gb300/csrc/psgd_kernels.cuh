@@ -465,12 +465,14 @@ __device__ __forceinline__ void p1_rows(const LayerDev& L, const P1Tile& T, cons
         m3 = 0.f;
       }
       if (!T.ub) {
+        // rows the back-project reads first stay in L2 (evict-last); the
+        // rest stream out (evict-first), leaving L2 to the loads in flight
         const int row = T.row0 + sb + i;
         float* dst = Bw + (int64_t)row * L.ld;
         if (row >= L.l2row)
           st_policy_f4(dst, make_float4(m0, m1, m2, m3), l2_evict_last_policy());
         else
-          *reinterpret_cast<float4*>(dst) = make_float4(m0, m1, m2, m3);
+          __stcs(reinterpret_cast<float4*>(dst), make_float4(m0, m1, m2, m3));
       }
 #pragma unroll
       for (int k = 0; k < RP; ++k) {
